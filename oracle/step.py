@@ -1,0 +1,108 @@
+"""The whole step (append, then decode) on a synthetic problem, in fp64.
+
+TEST INFRASTRUCTURE (same rule as mla_oracle): used by the tests, the smoke check and
+the benchmark's CPU baseline only. It takes any object with the attributes the seeded
+generator's `Problem` has (wl, q, pool, page_table, rows_per_seq, positions, seq_lens,
+norm_w, kv_b, kva_rows | x, w_kva) and reads nothing but those arrays.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from . import mla_oracle as O
+
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest bf16 (8 significant bits), ties to even.
+    Used once, where the cache stores the finished row in bf16."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)                      # x = m * 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.rint(m * 256.0) / 256.0, e)
+
+
+def store(x: np.ndarray, act: str) -> np.ndarray:
+    """The value a cache of dtype `act` holds for x (one rounding)."""
+    if act == "bf16":
+        return round_to_bf16(x)
+    return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
+def decode_act(a: np.ndarray, act: str) -> np.ndarray:
+    return O.bf16_to_f64(a) if act == "bf16" else O.f32_to_f64(a)
+
+
+def kv_b_f64(prob) -> np.ndarray:
+    wl = prob.wl
+    if wl.kv_b == "q8_0":
+        return O.q8_0_to_f64(prob.kv_b, wl.C)
+    return decode_act(prob.kv_b, wl.kv_b)
+
+
+def tables(wl):
+    """(inv_freq, softmax scale) for a workload's RoPE / YaRN parameters."""
+    inv = O.yarn_inv_freq(wl.R, wl.rope_theta, wl.yarn_factor, wl.yarn_orig_max_pos,
+                          wl.yarn_beta_fast, wl.yarn_beta_slow)
+    ms = O.yarn_mscale(wl.yarn_factor, wl.yarn_mscale_coeff)
+    return inv, O.softmax_scale(wl.N, wl.R, ms)
+
+
+def appended_rows(prob) -> np.ndarray:
+    """[B, C+R] float64: the finished rows the append writes, before storage rounding."""
+    wl = prob.wl
+    inv, _ = tables(wl)
+    if prob.kva_rows is not None:
+        kva = np.asarray(prob.kva_rows, dtype=np.float64)
+    else:
+        kva = O.kv_a_rows(O.bf16_to_f64(prob.x), O.bf16_to_f64(prob.w_kva))
+    return O.append_rows(kva, prob.norm_w.astype(np.float64), prob.positions, inv,
+                         wl.C, wl.rms_eps)
+
+
+def sequence_rows(prob, b: int, new_row=None) -> np.ndarray:
+    """[L_b, C+R] float64 rows sequence b attends, in logical order. With `new_row` the
+    row at positions[b] is replaced by it (the cache state after the append)."""
+    wl = prob.wl
+    L = int(prob.seq_lens[b])
+    phys = O.physical_row(b, np.arange(L), prob.page_table, wl.page_size, prob.rows_per_seq)
+    rows = decode_act(prob.pool[phys], wl.act)
+    if new_row is not None:
+        rows[int(prob.positions[b])] = new_row
+    return rows
+
+
+def run_step(prob, seqs=None, heads=None, with_append: bool = True):
+    """Append (when `with_append`) then decode. Returns (appended rows as stored
+    [B, C+R] float64, out [nb, nh, V], lse [nb, nh]) over the chosen sequences/heads."""
+    wl = prob.wl
+    inv, scale = tables(wl)
+    q = decode_act(prob.q, wl.act)
+    kvb = kv_b_f64(prob)
+    W_UK, W_UV = O.split_kv_b(kvb, wl.H, wl.N, wl.V)
+    seqs = range(wl.B) if seqs is None else list(seqs)
+    heads = np.arange(wl.H) if heads is None else np.asarray(heads)
+    new = store(appended_rows(prob), wl.act) if with_append else None
+    out = np.empty((len(seqs), len(heads), wl.V))
+    lse = np.empty((len(seqs), len(heads)))
+    for i, b in enumerate(seqs):
+        rows = sequence_rows(prob, b, None if new is None else new[b])
+        out[i], lse[i] = O.decode_one(q[b, heads], W_UK[heads], W_UV[heads], rows,
+                                      int(prob.positions[b]), inv, scale, wl.C)
+    return new, out, lse
+
+
+def rows_per_second_sample(prob, seconds: float = 10.0, max_reps: int = 1000):
+    """Time whole oracle steps on the host until `seconds` elapse; returns
+    (cache rows per second, repetitions, elapsed seconds)."""
+    import time
+    rows = int(np.sum(prob.seq_lens))
+    t0 = time.perf_counter()
+    reps = 0
+    while reps < max_reps:
+        run_step(prob)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return rows * reps / dt, reps, dt

@@ -1,0 +1,337 @@
+"""Pins for the fp64 oracle: each test checks it against something other than itself
+(a closed form, an identity of the mathematics, or the pages' own fixture), chosen so
+that a plausible slip (dropped term, wrong sign or index, transposed operand, swapped
+kv_b blocks, wrong RoPE pairing, wrong ramp direction) fails at least one of them."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import mla_oracle as O
+from oracle import step as OS
+
+RNG = np.random.default_rng(12345)
+
+
+def rand_problem(H, C, N, R, V, L, rng=RNG):
+    q = rng.standard_normal((H, N + R))
+    kv_b = rng.standard_normal((H * (N + V), C)) / math.sqrt(C)
+    rows = rng.standard_normal((L, C + R))
+    inv = O.yarn_inv_freq(R, 10000.0, 1.0, 4096, 32.0, 1.0)
+    return q, kv_b, rows, inv
+
+
+# ----------------------------------------------------------------------------------------
+# absorbed == unabsorbed (plain MHA with decompressed K and V)
+# ----------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("H,C,N,R,V,L,pos", [
+    (1, 8, 4, 2, 3, 1, 0),
+    (2, 16, 6, 4, 5, 7, 3),
+    (3, 32, 8, 8, 12, 33, 100),
+    (16, 64, 32, 16, 32, 65, 64),
+    (4, 24, 10, 6, 7, 129, 5000),
+])
+def test_absorbed_equals_unabsorbed(H, C, N, R, V, L, pos):
+    q, kv_b, rows, inv = rand_problem(H, C, N, R, V, L)
+    W_UK, W_UV = O.split_kv_b(kv_b, H, N, V)
+    scale = O.softmax_scale(N, R, 1.0)
+    o1, l1 = O.decode_one(q, W_UK, W_UV, rows, pos, inv, scale, C)
+    o2, l2 = O.decode_unabsorbed_one(q, W_UK, W_UV, rows, pos, inv, scale, C)
+    assert np.max(np.abs(o1 - o2)) <= 1e-12 * max(1.0, np.max(np.abs(o2)))
+    assert np.max(np.abs(l1 - l2)) <= 1e-12 * max(1.0, np.max(np.abs(l2)))
+
+
+def test_scale_changes_result():
+    # the scale enters the scores: a different scale must change out (guards a dropped scale)
+    q, kv_b, rows, inv = rand_problem(2, 16, 6, 4, 5, 9)
+    W_UK, W_UV = O.split_kv_b(kv_b, 2, 6, 5)
+    o1, _ = O.decode_one(q, W_UK, W_UV, rows, 2, inv, 0.2, 16)
+    o2, _ = O.decode_one(q, W_UK, W_UV, rows, 2, inv, 0.4, 16)
+    assert np.max(np.abs(o1 - o2)) > 1e-6
+
+
+# ----------------------------------------------------------------------------------------
+# T = 1, identical rows, zero query: closed forms
+# ----------------------------------------------------------------------------------------
+
+def _kv_b_from_blocks(W_UK, W_UV):
+    """Assemble kv_b from per-head blocks in the documented order (nope rows, then v rows)."""
+    H = W_UK.shape[0]
+    return np.concatenate([np.concatenate([W_UK[h], W_UV[h]], axis=0) for h in range(H)], axis=0)
+
+
+def test_single_row_gives_up_projected_latent():
+    rng = np.random.default_rng(1)
+    H, C, N, R, V = 3, 16, 5, 4, 6
+    W_UK = rng.standard_normal((H, N, C))
+    W_UV = rng.standard_normal((H, V, C))
+    kv_b = _kv_b_from_blocks(W_UK, W_UV)
+    q = rng.standard_normal((H, N + R))
+    rows = rng.standard_normal((1, C + R))
+    inv = O.yarn_inv_freq(R, 10000.0, 1.0, 4096, 32.0, 1.0)
+    uk, uv = O.split_kv_b(kv_b, H, N, V)
+    out, _ = O.decode_one(q, uk, uv, rows, 7, inv, 0.3, C)
+    for h in range(H):
+        np.testing.assert_allclose(out[h], W_UV[h] @ rows[0, :C], rtol=1e-13, atol=1e-13)
+
+
+def test_zero_query_gives_lse_zero_and_mean_value():
+    # q = 0 -> all scores 0 -> lse = ln L, uniform weights -> out = W_UV mean(lat)
+    rng = np.random.default_rng(2)
+    H, C, N, R, V, L = 2, 8, 3, 2, 4, 11
+    W_UK = rng.standard_normal((H, N, C))
+    W_UV = rng.standard_normal((H, V, C))
+    kv_b = _kv_b_from_blocks(W_UK, W_UV)
+    uk, uv = O.split_kv_b(kv_b, H, N, V)
+    rows = rng.standard_normal((L, C + R))
+    inv = O.yarn_inv_freq(R, 10000.0, 1.0, 4096, 32.0, 1.0)
+    out, lse = O.decode_one(np.zeros((H, N + R)), uk, uv, rows, 3, inv, 0.5, C)
+    np.testing.assert_allclose(lse, np.full(H, math.log(L)), rtol=0, atol=1e-14)
+    for h in range(H):
+        np.testing.assert_allclose(out[h], W_UV[h] @ rows[:, :C].mean(axis=0), rtol=1e-12, atol=1e-13)
+
+
+def test_identical_rows_lse_adds_log_count():
+    rng = np.random.default_rng(3)
+    H, C, N, R, V = 2, 8, 3, 2, 4
+    q, kv_b, row, inv = rand_problem(H, C, N, R, V, 1, rng)
+    uk, uv = O.split_kv_b(kv_b, H, N, V)
+    o1, l1 = O.decode_one(q, uk, uv, row, 9, inv, 0.25, C)
+    rows = np.repeat(row, 37, axis=0)
+    o2, l2 = O.decode_one(q, uk, uv, rows, 9, inv, 0.25, C)
+    np.testing.assert_allclose(o2, o1, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(l2, l1 + math.log(37), rtol=0, atol=1e-12)
+
+
+def test_kv_b_block_order_pins_w_uk_rows():
+    # zero W_UK (the nope rows of each head) and zero q_pe: scores are all zero, so out must
+    # be W_UV applied to the mean latent. A split that took the v rows as W_UK would give
+    # nonzero scores and a different out.
+    rng = np.random.default_rng(4)
+    H, C, N, R, V, L = 2, 8, 3, 2, 5, 13
+    W_UK = np.zeros((H, N, C))
+    W_UV = rng.standard_normal((H, V, C))
+    kv_b = _kv_b_from_blocks(W_UK, W_UV)
+    uk, uv = O.split_kv_b(kv_b, H, N, V)
+    q = rng.standard_normal((H, N + R))
+    q[:, N:] = 0.0
+    rows = rng.standard_normal((L, C + R))
+    inv = O.yarn_inv_freq(R, 10000.0, 1.0, 4096, 32.0, 1.0)
+    out, lse = O.decode_one(q, uk, uv, rows, 3, inv, 0.7, C)
+    np.testing.assert_allclose(lse, np.full(H, math.log(L)), atol=1e-14)
+    for h in range(H):
+        np.testing.assert_allclose(out[h], W_UV[h] @ rows[:, :C].mean(axis=0), rtol=1e-12, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------------------
+# softmax and split / merge
+# ----------------------------------------------------------------------------------------
+
+def test_softmax_rows_sum_to_one_and_shift_invariant():
+    s = RNG.standard_normal((5, 40)) * 3
+    p, lse = O.softmax_lse(s)
+    np.testing.assert_allclose(p.sum(axis=1), 1.0, atol=1e-15)
+    p2, lse2 = O.softmax_lse(s + 123.0)
+    np.testing.assert_allclose(p2, p, atol=1e-15)
+    np.testing.assert_allclose(lse2, lse + 123.0, atol=1e-12)
+    # lse against the unshifted definition on small scores
+    np.testing.assert_allclose(lse, np.log(np.exp(s).sum(axis=1)), rtol=1e-14)
+
+
+@pytest.mark.parametrize("cuts", [[5], [1, 2, 3], [10, 11], [1, 30, 31, 60]])
+def test_split_merge_equals_one_pass(cuts):
+    H, C, R, L = 4, 16, 4, 64
+    q_abs = RNG.standard_normal((H, C + R))
+    rows = RNG.standard_normal((L, C + R))
+    O1, l1 = O.partial_attention(q_abs, rows, 0.3, C)
+    edges = [0] + cuts + [L]
+    parts = [O.partial_attention(q_abs, rows[a:b], 0.3, C) for a, b in zip(edges[:-1], edges[1:])]
+    O2, l2 = O.lse_merge(parts)
+    np.testing.assert_allclose(O2, O1, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(l2, l1, rtol=0, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------------------
+# RoPE: consecutive pairs, pure rotation
+# ----------------------------------------------------------------------------------------
+
+INV16 = O.yarn_inv_freq(16, 10000.0, 1.0, 4096, 32.0, 1.0)
+
+
+def test_rope_identity_at_position_zero():
+    x = RNG.standard_normal((3, 16))
+    np.testing.assert_array_equal(O.rope_pairs(x, 0, INV16), x)
+
+
+def test_rope_preserves_each_pair_norm():
+    x = RNG.standard_normal((5, 16))
+    y = O.rope_pairs(x, 977, INV16)
+    np.testing.assert_allclose(np.hypot(y[:, 0::2], y[:, 1::2]), np.hypot(x[:, 0::2], x[:, 1::2]),
+                               rtol=1e-14)
+
+
+@pytest.mark.parametrize("i", [0, 3, 7])
+def test_rope_pairs_consecutive_elements(i):
+    # e_{2i} rotates into index 2i+1 only: the (i, i + d/2) pairing would move it to i + d/2
+    x = np.zeros(16)
+    x[2 * i] = 1.0
+    pos = 5
+    y = O.rope_pairs(x, pos, INV16)
+    a = pos * INV16[i]
+    expect = np.zeros(16)
+    expect[2 * i] = math.cos(a)
+    expect[2 * i + 1] = math.sin(a)
+    np.testing.assert_allclose(y, expect, atol=1e-15)
+
+
+def test_rope_equals_complex_multiplication():
+    # pair (x0, x1) as x0 + i x1, multiplied by exp(i * pos * inv_freq)
+    x = RNG.standard_normal((4, 16))
+    pos = 4097
+    z = (x[:, 0::2] + 1j * x[:, 1::2]) * np.exp(1j * pos * INV16)
+    y = O.rope_pairs(x, pos, INV16)
+    np.testing.assert_allclose(y[:, 0::2], z.real, atol=1e-12)
+    np.testing.assert_allclose(y[:, 1::2], z.imag, atol=1e-12)
+
+
+def test_rope_composition_and_relative_position():
+    x = RNG.standard_normal(16)
+    k = RNG.standard_normal(16)
+    np.testing.assert_allclose(O.rope_pairs(O.rope_pairs(x, 30, INV16), 12, INV16),
+                               O.rope_pairs(x, 42, INV16), atol=1e-12)
+    d1 = O.rope_pairs(x, 100, INV16) @ O.rope_pairs(k, 60, INV16)
+    d2 = O.rope_pairs(x, 40, INV16) @ k
+    assert abs(d1 - d2) < 1e-12
+
+
+# ----------------------------------------------------------------------------------------
+# YaRN table and scales
+# ----------------------------------------------------------------------------------------
+
+def test_yarn_factor_one_is_plain_rope():
+    for d in (16, 64):
+        inv = O.yarn_inv_freq(d, 10000.0, 1.0, 4096, 32.0, 1.0)
+        np.testing.assert_allclose(inv, [10000.0 ** (-2.0 * i / d) for i in range(d // 2)], rtol=1e-15)
+
+
+def test_yarn_ramp_limits(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "yarn_rope64_theta1e4_factor40.json")))
+    d = g["rope_dim"]
+    inv = O.yarn_inv_freq(d, g["theta"], g["factor"], g["orig_max_pos"], g["beta_fast"], g["beta_slow"])
+    base = np.array([g["theta"] ** (-2.0 * i / d) for i in range(d // 2)])
+    lo, hi = g["ramp_lo"], g["ramp_hi"]
+    # pairs at or below the fast correction dim keep the base frequency (high frequencies)
+    np.testing.assert_allclose(inv[:lo + 1], base[:lo + 1], rtol=1e-15)
+    # pairs at or above the slow correction dim are fully interpolated: base / factor
+    np.testing.assert_allclose(inv[hi:], base[hi:] / g["factor"], rtol=1e-15)
+    # in between, the interpolation weight rises linearly: ratio base/inv moves from 1 to factor
+    ramp = (np.arange(lo, hi + 1) - lo) / (hi - lo)
+    np.testing.assert_allclose(inv[lo:hi + 1] / base[lo:hi + 1], 1 - ramp + ramp / g["factor"], rtol=1e-14)
+
+
+def test_mscale_and_softmax_scale(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "yarn_rope64_theta1e4_factor40.json")))
+    assert abs(O.yarn_mscale(40.0, 1.0) - g["mscale"]) < 1e-15
+    assert O.yarn_mscale(1.0, 1.0) == 1.0
+    assert abs(O.softmax_scale(128, 64, O.yarn_mscale(40.0)) - g["softmax_scale_nope128_rope64"]) < 1e-13
+    assert abs(O.softmax_scale(32, 16, 1.0) - g["softmax_scale_plain_nope32_rope16"]) < 1e-16
+    assert abs(O.softmax_scale(128, 64, 1.0) - g["softmax_scale_plain_nope128_rope64"]) < 1e-16
+
+
+# ----------------------------------------------------------------------------------------
+# RMSNorm
+# ----------------------------------------------------------------------------------------
+
+def test_rms_norm_unit_rms_and_scale_invariance():
+    x = RNG.standard_normal((3, 64)) * 5
+    w = np.ones(64)
+    y = O.rms_norm(x, w, 0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=1)), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(O.rms_norm(7.5 * x, w, 0.0), y, rtol=1e-14)
+    wv = RNG.uniform(0.5, 1.5, 64)
+    np.testing.assert_allclose(O.rms_norm(x, wv, 0.0) / wv, y, rtol=1e-14)
+
+
+def test_rms_norm_eps_closed_form():
+    # constant input c: mean square = c^2, so y = c / sqrt(c^2 + eps)
+    c, eps = 1e-3, 1e-6
+    y = O.rms_norm(np.full(8, c), np.full(8, 2.0), eps)
+    np.testing.assert_allclose(y, 2.0 * c / math.sqrt(c * c + eps), rtol=1e-15)
+
+
+# ----------------------------------------------------------------------------------------
+# Q8_0
+# ----------------------------------------------------------------------------------------
+
+def test_q8_0_golden_blocks(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "q8_0_blocks.json")))
+    raw = bytearray()
+    expect = []
+    for blk in g["blocks"]:
+        raw += int(blk["d_f16_bits"]).to_bytes(2, "little")
+        raw += bytes((c & 0xFF) for c in blk["codes"])
+        expect += blk["values"]
+    blob = np.frombuffer(bytes(raw), dtype=np.uint8).reshape(1, -1)
+    got = O.q8_0_to_f64(blob, 64)
+    np.testing.assert_array_equal(got[0], np.array(expect))
+
+
+def test_q8_0_validation_fixture(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "q8_0_kv_b_validation.json")))
+    args = (g["heads"], g["nope"], g["kv_lora"], g["v_dim"])
+    v = g["valid"]
+    assert O.q8_0_validate(v["dtype"], v["shape"], v["size_bytes"], *args) is None
+    for r in g["rejects"]:
+        assert O.q8_0_validate(r["dtype"], r["shape"], r["size_bytes"], *args) is not None, r["why"]
+    # a width that does not tile 32-element blocks
+    assert O.q8_0_validate("q8_0", (12, 48), 12 * 2 * 34, 4, 2, 48, 1) is not None
+
+
+# ----------------------------------------------------------------------------------------
+# cache addressing, append, storage rounding
+# ----------------------------------------------------------------------------------------
+
+def test_physical_row_paged_and_contiguous():
+    pt = np.array([[3, 1, -1], [0, 2, 4]], dtype=np.int32)
+    assert O.physical_row(0, 0, pt, 64, 0) == 192
+    assert O.physical_row(0, 70, pt, 64, 0) == 70          # page 1 -> rows 64..127
+    assert O.physical_row(1, 5, pt, 64, 0) == 5
+    assert O.physical_row(1, 130, pt, 64, 0) == 4 * 64 + 2
+    assert O.physical_row(2, 17, None, 0, 100) == 217
+
+
+def test_append_rows_norm_and_rope_parts():
+    rng = np.random.default_rng(5)
+    C, R, B = 32, 8, 3
+    kva = rng.standard_normal((B, C + R)) * 3
+    w = rng.uniform(0.5, 1.5, C)
+    inv = O.yarn_inv_freq(R, 10000.0, 1.0, 4096, 32.0, 1.0)
+    pos = [0, 17, 4096]
+    rows = O.append_rows(kva, w, pos, inv, C, 0.0)
+    # latent: unit RMS once the weight is divided out
+    np.testing.assert_allclose(np.sqrt(np.mean((rows[:, :C] / w) ** 2, axis=1)), 1.0, rtol=1e-14)
+    # k_pe: untouched at position 0, rotated (not normed) elsewhere
+    np.testing.assert_array_equal(rows[0, C:], kva[0, C:])
+    for b in range(B):
+        z = (kva[b, C::2] + 1j * kva[b, C + 1::2]) * np.exp(1j * pos[b] * inv)
+        np.testing.assert_allclose(rows[b, C::2], z.real, atol=1e-12)
+        np.testing.assert_allclose(rows[b, C + 1::2], z.imag, atol=1e-12)
+
+
+def test_round_to_bf16_matches_ieee_rounding_on_float32_grid():
+    # for values already on the fp32 grid, bf16 RNE rounding is the fp32->bf16 rounding
+    import torch
+    x = np.concatenate([RNG.standard_normal(5000).astype(np.float32),
+                        np.array([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -1.0 - 2 ** -8, 0.0], np.float32)])
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(OS.round_to_bf16(x.astype(np.float64)), ref)
+
+
+def test_kv_a_projection_is_matvec():
+    x = RNG.standard_normal((2, 12))
+    w = RNG.standard_normal((5, 12))
+    np.testing.assert_allclose(O.kv_a_rows(x, w)[1], [sum(w[r, i] * x[1, i] for i in range(12)) for r in range(5)],
+                               rtol=1e-13)
