@@ -1,0 +1,502 @@
+#!/usr/bin/env python3
+"""Benchmark of one MLA decode step (cache append + absorbed decode) on GB300.
+
+A step is one pass of the whole path over one batch: mla_cache_append (new row per sequence)
+then mla_decode_attn (absorb, split attention over every cached row, combine + W_UV
+up-projection). The default workload is the DeepSeek-V2-Lite-shaped single-sequence decode
+(B=1, H=16, kv_lora 512, rope 64, 4096 rows, bf16). Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Timing: inputs resident in HBM; each step uses the next of R rotating input copies whose total
+exceeds 2x L2, so no step reads another's data from L2; the timed K steps are replayed as CUDA
+graphs with CUDA events on the launching stream; the attention kernel is bracketed by events
+inside the graphs (every step). N > 1 (torchrun) runs independent replicas per GPU (the
+sequences are independent: no data-path collective) and reports the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "MLA decode: KV-cache rows/s, achieved TFLOP/s & HBM GB/s vs roofline"
+DEFAULT_WORKLOAD = "v2lite_b1_t4096"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ------------------------------------------------------------------------------------------------
+# algorithmic work of one step
+# ------------------------------------------------------------------------------------------------
+
+def step_work(prob):
+    """Algorithmic FLOPs and bytes of one step, and of the attention stage alone.
+
+    FLOPs: absorb 2HNC per sequence, attention (QK over the C+R row and PV over the C latent)
+    rows*H*(2(C+R)+2C), up-projection 2HCV per sequence, plus the kv_a GEMV when the append
+    projects. Bytes: every attended cache row once (shared by all heads), kv_b once, q, out,
+    lse, page table, append input and output (and W_kva, x when projecting)."""
+    wl = prob.wl
+    B, H, C, N, R, V = wl.B, wl.H, wl.C, wl.N, wl.R, wl.V
+    e = 2 if wl.act == "bf16" else 4
+    rows = int(np.sum(prob.seq_lens))
+    if wl.kv_b == "q8_0":
+        kvb = H * (N + V) * (C // 32) * 34
+    else:
+        kvb = H * (N + V) * C * (2 if wl.kv_b == "bf16" else 4)
+    attn_flops = rows * H * (2 * (C + R) + 2 * C)
+    attn_bytes = rows * (C + R) * e
+    flops = B * 2 * H * N * C + attn_flops + B * 2 * H * C * V
+    pages = 0 if prob.page_table is None else int(np.sum((prob.seq_lens + wl.page_size - 1) // wl.page_size))
+    byts = attn_bytes + kvb + B * H * (N + R) * e + B * H * (V + 1) * 4 + 4 * (pages + 2 * B)
+    if wl.append == "gemv":
+        flops += B * 2 * (C + R) * wl.hidden
+        byts += (C + R) * wl.hidden * e + B * wl.hidden * e
+    else:
+        byts += B * (C + R) * 4
+    byts += B * (C + R) * e  # the appended rows
+    return dict(rows=rows, flops=flops, bytes=byts, attn_flops=attn_flops, attn_bytes=attn_bytes)
+
+
+def input_bytes(prob):
+    n = prob.pool.nbytes + prob.kv_b.nbytes + prob.q.nbytes
+    for a in (prob.kva_rows, prob.x, prob.w_kva, prob.page_table):
+        if a is not None:
+            n += a.nbytes
+    return n
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------------------
+
+_SMI_FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, uuid: str):
+        self.uuid = uuid
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={_SMI_FIELDS}", "--format=csv,noheader",
+                                       "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+        self.f.flush()
+
+    def samples(self, t0: float, t1: float):
+        out = []
+        try:
+            lines = open(self.f.name).read().strip().splitlines()
+        except OSError:
+            return out
+        for ln in lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm = float(parts[2].split()[0])
+                smax = float(parts[3].split()[0])
+            except ValueError:
+                continue
+            if t0 <= ts <= t1:
+                out.append(dict(uuid=parts[1], sm=sm, smax=smax, hw=parts[6], hwt=parts[7], swt=parts[8],
+                                pcap=parts[9]))
+        mine = [s for s in out if s["uuid"] == self.uuid]
+        if mine or len({s["uuid"] for s in out}) > 1:
+            return mine
+        return out  # only one GPU visible to nvidia-smi: it is ours
+
+
+def summarize_clocks(samples, window):
+    if not samples:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": window}
+    reasons = set()
+    for s in samples:
+        for k, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                        ("pcap", "sw_power_cap")):
+            if s[k].lower() == "active":
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(s["sm"] for s in samples), "sm_max_mhz": max(s["smax"] for s in samples),
+            "reasons": sorted(reasons), "samples": len(samples), "window": window}
+
+
+# ------------------------------------------------------------------------------------------------
+# events that can live inside a CUDA graph
+# ------------------------------------------------------------------------------------------------
+
+def graph_event(torch):
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError as e:  # very old torch: no external events
+        raise RuntimeError("torch.cuda.Event(external=True) is required for in-graph timing") from e
+
+
+# ------------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------------
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def kernel_source_sha(kernel: int) -> str:
+    f = os.path.join(ROOT, "mla_latent_cache_absorb_gb300", "csrc", "attn_tc.cu" if kernel == 1 else "attn_simt.cu")
+    return hashlib.sha256(open(f, "rb").read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel: int, workload: str):
+    """DRAM bytes per launch of the attention kernel from the committed ncu summary, if it
+    was taken on the current kernel source."""
+    try:
+        d = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    except (OSError, ValueError):
+        return None
+    ent = d.get(f"{'attn_tc' if kernel == 1 else 'attn_simt'}:{workload}")
+    if not ent or ent.get("source_sha") != kernel_source_sha(kernel):
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def run_ours(args, rank, world, device):
+    import torch
+
+    from mla_latent_cache_absorb_gb300 import binding as L
+    from mla_latent_cache_absorb_gb300 import synth
+    from mla_latent_cache_absorb_gb300.runner import DeviceStep
+
+    wl = synth.WORKLOADS[args.workload]
+    prob = synth.make_problem(wl)
+    work = step_work(prob)
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 129 * 2 ** 20)
+    per_copy = input_bytes(prob)
+    R = max(1, min(64, math.ceil(2.2 * l2 / per_copy)))
+    stream = torch.cuda.Stream(device=device)
+    steps = [DeviceStep(prob, device=device, stream=stream)]
+    for _ in range(R - 1):
+        steps.append(DeviceStep(prob, device=device, stream=stream))
+    st, plan = L.mla_decode_plan(steps[0].cfg, wl.B)
+    L.check(st, "mla_decode_plan")
+    launches_per_step = (2 if wl.append == "gemv" else 1) + 3
+
+    def one_step(ds, s, ev=None):
+        L.check(ds.append(s), "mla_cache_append")
+        L.check(ds.absorb(s), "mla_decode_absorb")
+        if ev is not None:
+            ev[0].record(s)
+        L.check(ds.partial(s), "mla_decode_partial")
+        if ev is not None:
+            ev[1].record(s)
+        L.check(ds.combine(s), "mla_decode_combine")
+
+    # graphs of G steps (one pass over the R copies), two of them to double-buffer the
+    # in-graph attention events, plus a tail graph for K mod G steps
+    K, W = args.steps, args.warmup
+    G = R if R > 1 else max(1, min(64, K))
+    torch.cuda.synchronize(device)
+
+    def capture(n, with_events):
+        g = torch.cuda.CUDAGraph()
+        evs = [(graph_event(torch), graph_event(torch)) for _ in range(n)] if with_events else None
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            s = torch.cuda.current_stream(device)
+            for i in range(n):
+                one_step(steps[i % R], s, evs[i] if evs else None)
+        return g, evs
+
+    with torch.cuda.stream(stream):
+        # eager warm-up (W steps) also checks every call once outside capture
+        for i in range(W):
+            one_step(steps[i % R], stream)
+        torch.cuda.synchronize(device)
+        for ds in steps:
+            for ws in (ds.ws_append, ds.ws_decode):
+                e, seq = L.mla_get_device_error(ws, stream)
+                L.check(e, f"device error (seq {seq})")
+        gA, evA = capture(G, True)
+        gB, evB = capture(G, True)
+        tail = K % G
+        gT, evT = capture(tail, True) if tail else (None, None)
+        n_full = K // G
+
+        sampler = ClockSampler(str(props.uuid) if hasattr(props, "uuid") else "")
+        if not str(sampler.uuid).startswith("GPU-") and sampler.uuid:
+            sampler.uuid = "GPU-" + sampler.uuid
+        sampler.start()
+        time.sleep(0.3)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(device)
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        wall0 = time.time()
+        t_start.record(stream)
+        attn_ms = []
+        pending = []
+        graphs = [(gA, evA), (gB, evB)]
+        for r in range(n_full):
+            g, ev = graphs[r % 2]
+            if len(pending) == 2:  # reuse of this graph's events: read the previous replay first
+                ev_old = pending.pop(0)
+                ev_old[-1][1].synchronize()
+                attn_ms.extend(a.elapsed_time(b) for a, b in ev_old)
+            g.replay()
+            pending.append(ev)
+        if gT is not None:
+            gT.replay()
+            pending.append(evT)
+        t_end.record(stream)
+        for ev in pending:
+            ev[-1][1].synchronize()
+            attn_ms.extend(a.elapsed_time(b) for a, b in ev)
+        t_end.synchronize()
+        wall1 = time.time()
+        if world > 1:
+            torch.distributed.barrier()
+        total_ms = t_start.elapsed_time(t_end)
+        clk = sampler.samples(wall0, wall1)
+        window = "timed"
+        if len(clk) < 3:
+            # the timed region was shorter than the sampler's period: sample the same graphs
+            # for about a second right after it (untimed) and say so
+            wa = time.time()
+            while time.time() - wa < 1.2:
+                gA.replay()
+                gB.replay()
+                torch.cuda.synchronize(device)
+            clk = sampler.samples(wa, time.time())
+            window = "adjacent"
+        sampler.stop()
+        clocks = summarize_clocks(clk, window)
+
+        # end to end through the public calls: pinned host inputs in, results out, every step
+        e2e = None
+        if not args.no_e2e:
+            e2e = run_e2e(torch, L, steps, prob, stream, device, K, W, work)
+
+    # aggregate over ranks: max time, every rank's rows
+    tmax = total_ms
+    if world > 1:
+        t = torch.tensor([total_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        tmax = float(t.item())
+    ms_per_step = tmax / K
+    value = world * work["rows"] * K / (tmax / 1e3)
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+    hbm, tf_burst, tf_sust, src = peaks()
+    attn_gbs = work["attn_bytes"] / (attn_avg_ms / 1e3) / 1e9
+    step_s = ms_per_step / 1e3
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": wl.act, "data": "synthetic (seeded generator; random-init kv_b)",
+        "config": {
+            "workload": wl.name, "B": wl.B, "H": wl.H, "kv_lora": wl.C, "qk_nope": wl.N, "qk_rope": wl.R,
+            "v_head": wl.V, "rows_per_step": work["rows"], "kv_b": wl.kv_b,
+            "paged": bool(wl.page_size), "append": wl.append,
+            "l2": f"rotating {R} input copies ({R * per_copy / 2 ** 20:.0f} MB, L2 {l2 / 2 ** 20:.0f} MB)",
+            "timing": f"CUDA graphs of {G} steps, events on the launching stream",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "attention_kernel": "tcgen05" if plan.kernel == 1 else "cuda-core",
+            "splits": plan.splits, "rows_per_split": plan.rows_per_split,
+        },
+        "tflops": work["flops"] / step_s / 1e12,
+        "hbm_gbs": work["bytes"] / step_s / 1e9,
+        "step_roofline_frac": max(work["flops"] / (tf_burst * 1e12), work["bytes"] / (hbm * 1e9)) / step_s,
+        "roofline": {
+            "kernel": "attn_tc (split attention)" if plan.kernel == 1 else "attn_simt (split attention)",
+            "bound": "hbm", "achieved": attn_gbs, "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm,
+            "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback",
+            "bytes_per_launch": work["attn_bytes"], "avg_launch_us": attn_avg_ms * 1e3,
+            "traffic": ncu_traffic(plan.kernel, wl.name),
+            "tensor_tflops": work["attn_flops"] / (attn_avg_ms / 1e3) / 1e12,
+        },
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    return line
+
+
+def run_e2e(torch, L, steps, prob, stream, device, K, W, work):
+    """Same metric through the public calls with host buffers: every step copies its inputs
+    from pinned host memory, calls mla_cache_append + mla_decode_attn, and copies out + lse
+    back; launched eagerly (no graph)."""
+    R = len(steps)
+    ds0 = steps[0]
+    host_in = {"q": ds0.q.cpu().pin_memory(), "kv_in": ds0.kv_in.cpu().pin_memory(),
+               "positions": ds0.positions.cpu().pin_memory(), "len_before": ds0.len_before.cpu().pin_memory(),
+               "seq_lens": ds0.seq_lens.cpu().pin_memory()}
+    host_out = {"out": torch.empty_like(ds0.out, device="cpu").pin_memory(),
+                "lse": torch.empty_like(ds0.lse, device="cpu").pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def one(ds):
+        for k, t in host_in.items():
+            getattr(ds, k).copy_(t, non_blocking=True)
+        L.check(ds.append(stream), "mla_cache_append")
+        L.check(ds.decode(stream), "mla_decode_attn")
+        host_out["out"].copy_(ds.out, non_blocking=True)
+        host_out["lse"].copy_(ds.lse, non_blocking=True)
+
+    for i in range(W):
+        one(steps[i % R])
+    torch.cuda.synchronize(device)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(K):
+        one(steps[i % R])
+    b.record(stream)
+    b.synchronize()
+    ms = a.elapsed_time(b)
+    return {"value": work["rows"] * K / (ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms / K, "launch": "eager, one call each per step"}
+
+
+# ------------------------------------------------------------------------------------------------
+# the CPU oracle: cpu_baseline leg and the reference arm
+# ------------------------------------------------------------------------------------------------
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(prob, seconds):
+    from oracle import step as OS
+    rps, n, rows, dt = OS.rows_per_second_sample(prob, seconds=seconds)
+    return {"value": rps, "unit": "rows/s", "cores": host_cores(), "kind": "oracle",
+            "sample": f"{n} oracle sequence-steps (append + decode of one sequence, all {prob.wl.H} heads), "
+                      f"{rows:.0f} rows in {dt:.1f} s, fp64 numpy on the host"}
+
+
+def run_reference(args, budget_s=150.0):
+    """The oracle as it stands, timed on the host cores. Each step is a bounded sample of the
+    workload: one sequence's whole step (append + decode) with all heads when that fits the
+    time budget (budget_s over all warm-up and timed steps), else with its first heads only;
+    rows are credited in proportion to the heads computed."""
+    from mla_latent_cache_absorb_gb300 import synth
+    from oracle import step as OS
+    wl = synth.WORKLOADS[args.workload]
+    prob = synth.make_problem(wl)
+    t0 = time.perf_counter()
+    OS.run_step(prob, seqs=[0])
+    t_one = time.perf_counter() - t0
+    per_step = budget_s / (args.steps + args.warmup)
+    hs = wl.H if t_one <= per_step else max(1, int(wl.H * per_step / t_one))
+    heads = np.arange(hs)
+
+    def sample(k):
+        b = k % wl.B
+        OS.run_step(prob, seqs=[b], heads=heads)
+        return float(prob.seq_lens[b]) * hs / wl.H
+
+    for k in range(args.warmup):
+        sample(k)
+    rows = 0.0
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        rows += sample(k)
+    dt = time.perf_counter() - t0
+    value = rows / dt
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded generator)",
+        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "kv_lora": wl.C,
+                   "rows_per_step": int(np.sum(prob.seq_lens))},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "kind": "oracle", "cores": host_cores(),
+                         "sample": f"{args.steps} oracle sequence-steps ({hs} of {wl.H} heads, append + decode) "
+                                   f"after {args.warmup} warm-up, {rows:.0f} rows credited in {dt:.1f} s"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ------------------------------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if args.steps is None:
+            args.steps = 20
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    import torch
+    if args.steps is None:
+        args.steps = 20000 if args.workload == DEFAULT_WORKLOAD else 200
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    line = run_ours(args, rank, world, device)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from mla_latent_cache_absorb_gb300 import synth
+        line["cpu_baseline"] = cpu_baseline(synth.make_problem(synth.WORKLOADS[args.workload]), args.cpu_seconds)
+    else:
+        line["cpu_baseline"] = None
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

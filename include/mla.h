@@ -1,0 +1,246 @@
+/*
+ * mla.h -- C ABI for one decode step of Multi-head Latent Attention (MLA) over a
+ * compressed latent KV cache, on an NVIDIA GB300 (sm_103a).
+ *
+ * Two calls carry the method:
+ *   mla_cache_append  writes each sequence's new compressed row [kv_lat ; k_pe] into the
+ *                     cache: optional kv_a projection, RMSNorm over the latent part,
+ *                     consecutive-pair YaRN RoPE over the k_pe tail.
+ *   mla_decode_attn   absorbs q_nope through W_UK into latent space, attends over every
+ *                     cached row with all heads sharing each row (split over the sequence),
+ *                     merges the splits by log-sum-exp and up-projects through W_UV.
+ *
+ * Sources (docs.rs source pages):
+ *   moeflux 0.1.0-pre.3, src/riir/attn/mla_attn_forward.rs -- mla_attn_layer_forward_gpu:
+ *     KV chain, YaRN RoPE of q_pe and k_pe, cache append, folded SDPA chain
+ *     (q_prime -> mla_sdpa_folded -> out_per_head), softmax scale, error set.
+ *   turbospark-runtime 0.3.0, src/families/deepseek2/attn.rs -- encode_mla_attention_block:
+ *     the fused cache row, in-place norm and RoPE, absorb, MQA attention over compressed
+ *     rows, v-combine; validate_q8_0_matrix.
+ *
+ * Conventions for every call:
+ *   - Dimensions: H heads, C = kv_lora, N = qk_nope, R = qk_rope, V = v_head, a cache row
+ *     holds C+R elements: [kv_lat (C) ; k_pe (R)].
+ *   - Pointers marked "device" are CUDA device (or managed) pointers on the current device;
+ *     "host" pointers are plain host memory. The caller owns every buffer; the library
+ *     allocates no device memory and keeps no per-call state.
+ *   - Calls marked "async" only validate on the host and enqueue kernels on `stream`;
+ *     they return before the GPU work ends and never synchronise. Errors found on the
+ *     host return before anything is enqueued. Conditions only the GPU can see (a bad
+ *     length, a position that does not match the cache length, a page id out of range)
+ *     set a sticky error word in the call's workspace; the affected sequence's outputs
+ *     are written as NaN and the other sequences are unaffected. Read it with
+ *     mla_get_device_error. Kernels never trap.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (same handle as cudaStream_t / CUstream). NULL = the legacy default stream. */
+typedef struct CUstream_st* mla_stream_t;
+
+typedef enum mla_status {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,   /* null pointer, bad dimension, misaligned pointer, B < 1 */
+  MLA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (dtype / dimension combination) */
+  MLA_ERR_POS_MISMATCH = 3,  /* device: append position != the sequence's current length */
+  MLA_ERR_CACHE_FULL = 4,    /* device: append position beyond the cache's capacity */
+  MLA_ERR_WORKSPACE = 5,     /* workspace NULL, misaligned or smaller than required */
+  MLA_ERR_TIMEOUT = 6,       /* device: a bounded wait inside a kernel ran out */
+  MLA_ERR_CUDA = 7,          /* a CUDA runtime call failed (launch, attribute, no device) */
+  MLA_ERR_BAD_SEQ_LEN = 8,   /* device: seq_len < 1 or above the cache's capacity */
+  MLA_ERR_BAD_PAGE = 9,      /* device: page-table entry outside [0, n_physical_rows/page_size) */
+  MLA_ERR_BAD_KV_B = 10      /* kv_b dtype / shape / byte size contract broken */
+} mla_status;
+
+typedef enum mla_dtype {
+  MLA_F32 = 0,
+  MLA_BF16 = 1,
+  /* Q8_0: 34-byte blocks of 32 elements along a row: an fp16 scale d (little endian)
+   * then 32 int8 codes q; element value d*q. Weights only (kv_b). */
+  MLA_Q8_0 = 2
+} mla_dtype;
+
+typedef struct mla_config {
+  int32_t n_heads;            /* H >= 1 */
+  int32_t kv_lora;            /* C >= 1 (a multiple of 32 when kv_b is Q8_0) */
+  int32_t qk_nope;            /* N >= 1 */
+  int32_t qk_rope;            /* R >= 2, even */
+  int32_t v_head;             /* V >= 1 */
+  int32_t act_dtype;          /* mla_dtype, F32 or BF16: q and the cache rows */
+  int32_t kv_b_dtype;         /* mla_dtype, F32, BF16 or Q8_0 */
+  float softmax_scale;        /* mscale^2 / sqrt(N+R); see mla_softmax_scale */
+  float rms_eps;              /* RMSNorm epsilon of the latent norm (append only) */
+  int32_t page_size;          /* 0: contiguous rows per sequence; else rows per page (>= 1) */
+  int32_t max_pages_per_seq;  /* paged: width of a page-table row */
+  int64_t rows_per_seq;       /* contiguous: rows reserved per sequence (its capacity) */
+  const double* rope_inv_freq;/* device [R/2] float64 per-pair inverse frequencies,
+                                 e.g. from mla_yarn_inv_freq; may be NULL only for a
+                                 decode call whose q_pe is already rotated */
+} mla_config;
+
+/* The cache: physical rows plus, when paged, the page table.
+ * Contiguous: logical row t of sequence b is physical row b*rows_per_seq + t.
+ * Paged: logical row t of sequence b is physical row
+ *        page_table[b*max_pages_per_seq + t/page_size]*page_size + t%page_size. */
+typedef struct mla_cache {
+  void* rows;                 /* device [n_physical_rows, C+R] in act_dtype, row-major,
+                                 16-byte aligned; rows are C+R contiguous elements */
+  const int32_t* page_table;  /* device [B, max_pages_per_seq] int32, or NULL (contiguous) */
+  int64_t n_physical_rows;    /* rows in `rows` (bounds every address the kernels form) */
+} mla_cache;
+
+/* ---- host-only helpers (no GPU needed) ------------------------------------------------ */
+
+/* Human-readable name of a status. Never NULL. */
+const char* mla_status_string(mla_status s);
+
+/* ABI revision of this header (bumped on any incompatible change). */
+int32_t mla_abi_version(void);
+
+/* YaRN per-pair inverse frequencies, float64, into out_host[rope_dim/2].
+ * moeflux mla_attn_forward.rs, MlaYarnTables::new (table from rope_dim, theta, factor,
+ * original max position, beta_fast, beta_slow); turbospark gptoss attn.rs module doc
+ * (a per-pair table, because the ramp is not one theta). Pair i has base frequency
+ * theta^(-2i/rope_dim); for factor > 1 pairs below the beta_fast correction dimension
+ * keep it, pairs above the beta_slow one are divided by factor, linear ramp between
+ * (YaRN's NTK-by-parts). factor <= 1 gives plain RoPE.
+ * Errors: INVALID_ARG for rope_dim < 2 or odd, theta <= 1, orig_max_pos < 1, NULL out. */
+mla_status mla_yarn_inv_freq(int32_t rope_dim, double theta, double factor,
+                             int32_t orig_max_pos, double beta_fast, double beta_slow,
+                             double* out_host);
+
+/* YaRN magnitude scale: 1 + 0.1*coeff*ln(factor) for factor > 1, else 1.
+ * turbospark deepseek2 attn.rs, attention scale comment. */
+double mla_yarn_mscale(double factor, double coeff);
+
+/* Softmax scale mscale^2 / sqrt(qk_nope + qk_rope) (moeflux mla_attn_forward.rs,
+ * folded SDPA chain: 1/sqrt(qk_head_dim) * mscale * mscale). Returns 0 on bad dims. */
+float mla_softmax_scale(int32_t qk_nope, int32_t qk_rope, double mscale);
+
+/* The kv_b contract (turbospark deepseek2 attn.rs, validate_q8_0_matrix, generalised to
+ * all three weight dtypes): shape must be (heads*(nope+v_dim), kv_lora); for Q8_0
+ * kv_lora must be a non-zero multiple of 32; size_bytes must equal the packed size,
+ * computed with overflow-checked multiplies. Returns OK, BAD_KV_B or INVALID_ARG. */
+mla_status mla_validate_kv_b(int32_t dtype, int64_t rows, int64_t cols, uint64_t size_bytes,
+                             int32_t heads, int32_t nope, int32_t kv_lora, int32_t v_dim);
+
+/* Bytes of a kv_b tensor for cfg (0 on invalid cfg or overflow). kv_b is row-major
+ * [H*(N+V), C]: per head its N rows of W_UK then its V rows of W_UV
+ * (moeflux mla_attn_forward.rs: kv_b_per_head = nope + v_head_dim; out_per_head skips
+ * the nope rows). */
+uint64_t mla_kv_b_bytes(const mla_config* cfg);
+
+/* ---- workspace sizing (needs a CUDA device: the split plan depends on its SM count) ---- */
+
+/* Bytes of device workspace mla_cache_append needs for B sequences (with or without the
+ * kv_a projection). Writes *bytes; returns INVALID_ARG / CUDA on failure. */
+mla_status mla_append_workspace_size(const mla_config* cfg, int32_t B, size_t* bytes);
+
+/* Bytes of device workspace mla_decode_attn (and its three stages) needs for B sequences
+ * on the current device. The split plan is fixed by (cfg, B, device), so a workspace sized
+ * here fits every call with the same cfg and B. */
+mla_status mla_decode_workspace_size(const mla_config* cfg, int32_t B, size_t* bytes);
+
+/* The split plan mla_decode_attn uses for (cfg, B) on the current device. */
+typedef struct mla_plan_info {
+  int32_t kernel;          /* attention kernel: 0 = CUDA-core (any dims, f32 or bf16),
+                              1 = tcgen05 tensor-core (bf16 rows of 576 = 512 + 64) */
+  int32_t heads_per_cta;   /* heads that share each staged row tile */
+  int32_t head_groups;     /* ceil(H / heads_per_cta) */
+  int32_t splits;          /* row splits per sequence (partials kept in the workspace) */
+  int64_t rows_per_split;  /* rows each split covers (a multiple of the row tile) */
+  int64_t capacity;        /* most rows one sequence can attend */
+} mla_plan_info;
+
+/* Fills *info with the plan for (cfg, B). Host-only query; needs a CUDA device. */
+mla_status mla_decode_plan(const mla_config* cfg, int32_t B, mla_plan_info* info);
+
+/* ---- the method ----------------------------------------------------------------------- */
+
+/* Append one new row per sequence, in place (async).
+ * turbospark deepseek2 attn.rs, encode_mla_attention_block: kv_a straight into the cache
+ * row, RMSNorm over kv_lora in place, RoPE of the pe tail in place with the q pairing;
+ * moeflux mla_attn_forward.rs: KV-A chain, kv_a_layernorm, YaRN RoPE of k_pe, append of
+ * row[pos], guards PosMismatch and CacheFull.
+ *   kv_in      device. w_kva == NULL: [B, C+R] float32 kv_a rows (the projection's output).
+ *              w_kva != NULL: [B, hidden] hidden states in act_dtype.
+ *   w_kva      device [C+R, hidden] in act_dtype, row-major, or NULL.
+ *   hidden     columns of w_kva (ignored when w_kva == NULL; a multiple of 8 otherwise).
+ *   norm_w     device [C] float32 RMSNorm weight.
+ *   positions  device [B] int32: the row index each sequence writes and the RoPE position.
+ *   seq_lens   device [B] int32 current lengths, or NULL. When given, positions[b] must
+ *              equal seq_lens[b] (device error POS_MISMATCH otherwise). The call never
+ *              changes lengths: the caller advances them.
+ * For each b the finished row is y[0:C] = x[0:C]/sqrt(mean(x[0:C]^2)+eps)*norm_w and
+ * y[C:C+R] = RoPE(x[C:C+R], positions[b]) with pairs (2i, 2i+1), x = kv_in row or
+ * W_kva*x_b, computed in float32 and rounded once to act_dtype. No other row changes.
+ * Device errors: CACHE_FULL (position outside capacity), BAD_PAGE, POS_MISMATCH. */
+mla_status mla_cache_append(const mla_config* cfg, const mla_cache* cache,
+                            const void* kv_in, const void* w_kva, int32_t hidden,
+                            const float* norm_w, const int32_t* positions,
+                            const int32_t* seq_lens, int32_t B,
+                            void* workspace, size_t ws_bytes, mla_stream_t stream);
+
+/* One absorbed decode step for B sequences (async): the three stages below, in order.
+ * moeflux mla_attn_forward.rs, folded SDPA chain; turbospark deepseek2 attn.rs, absorb ->
+ * MQA attention over compressed rows -> v-combine.
+ *   q          device [B, H, N+R] act_dtype; each head [q_nope (N) ; q_pe (R)].
+ *   kv_b       device kv_b in kv_b_dtype (see mla_kv_b_bytes), 16-byte aligned.
+ *   seq_lens   device [B] int32 rows to attend (1 <= seq_lens[b] <= capacity).
+ *   positions  device [B] int32 RoPE position of each query's q_pe, or NULL when q_pe
+ *              is already rotated.
+ *   out        device [B, H, V] float32: out[b,h] = W_UV,h * sum_t p_t kv_lat_t.
+ *   lse        device [B, H] float32 natural-log sum-exp of the scaled scores, or NULL.
+ * Scores are s_t = softmax_scale * ([q' ; q_pe] . row_t) with q' = W_UK,h^T q_nope.
+ * Device errors: BAD_SEQ_LEN, BAD_PAGE (that sequence's out/lse become NaN). */
+mla_status mla_decode_attn(const mla_config* cfg, const void* q, const void* kv_b,
+                           const mla_cache* cache, const int32_t* seq_lens,
+                           const int32_t* positions, float* out, float* lse, int32_t B,
+                           void* workspace, size_t ws_bytes, mla_stream_t stream);
+
+/* Stage 1 of mla_decode_attn (async): RoPE of q_pe at positions[b] and the absorb
+ * q'[b,h,:] = W_UK,h^T q_nope[b,h,:], written as the fused query rows [q' ; q_pe] in
+ * act_dtype into the workspace (moeflux q_prime; turbospark encode_mla_absorb_q). */
+mla_status mla_decode_absorb(const mla_config* cfg, const void* q, const void* kv_b,
+                             const int32_t* positions, int32_t B,
+                             void* workspace, size_t ws_bytes, mla_stream_t stream);
+
+/* Stage 2 (async): split attention over the cache rows with all heads of a sequence
+ * sharing each row. Each split writes its softmax-normalised latent sum O_s [H, C] and
+ * its log-sum-exp lse_s [H] into the workspace (moeflux mla_sdpa_folded; turbospark
+ * encode_mla_attention_decode, V = the row's first kv_lora values). */
+mla_status mla_decode_partial(const mla_config* cfg, const mla_cache* cache,
+                              const int32_t* seq_lens, int32_t B,
+                              void* workspace, size_t ws_bytes, mla_stream_t stream);
+
+/* Stage 3 (async): merge the splits (lse = log sum_s exp(lse_s), vc = sum_s
+ * exp(lse_s - lse) O_s) and up-project out[b,h] = W_UV,h vc (moeflux out_per_head;
+ * turbospark encode_mla_v_combine; the split + combine structure of turbospark
+ * gptoss attn.rs). */
+mla_status mla_decode_combine(const mla_config* cfg, const void* kv_b,
+                              const int32_t* seq_lens, float* out, float* lse, int32_t B,
+                              void* workspace, size_t ws_bytes, mla_stream_t stream);
+
+/* ---- device error word ------------------------------------------------------------------ */
+
+/* Synchronises `stream`, then reads the workspace's sticky error word: returns the first
+ * device error any call using this workspace recorded since the last clear (MLA_OK if
+ * none), and writes the sequence index it concerns to *seq_out when seq_out != NULL. */
+mla_status mla_get_device_error(const void* workspace, int32_t* seq_out, mla_stream_t stream);
+
+/* Clears the workspace's error word (async, on `stream`). A fresh workspace must be
+ * cleared once (or zero-filled) before its first use. */
+mla_status mla_clear_device_error(void* workspace, mla_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

@@ -1,0 +1,147 @@
+// Cache append: optional kv_a projection, RMSNorm over the latent, consecutive-pair YaRN
+// RoPE over the k_pe tail, one rounding into the cache row.
+//
+// turbospark-runtime 0.3.0, src/families/deepseek2/attn.rs, encode_mla_attention_block:
+// kv_a straight into the compressed row [latent ; k_pe], norm over kv_lora in place, RoPE of
+// the pe tail in place with the same (consecutive-element) pairing as q.
+// moeflux 0.1.0-pre.3, src/riir/attn/mla_attn_forward.rs, mla_attn_layer_forward_gpu: KV-A
+// chain, kv_a_layernorm, YaRN RoPE of k_pe, append of row[pos]; PosMismatch / CacheFull guards.
+//
+// Here the finished row is produced in registers (float32) and written once, so the cache
+// never holds a half-finished row and the value is rounded to the cache dtype only once.
+#include "common.cuh"
+
+namespace mla {
+
+// ---- kv_a projection: kva[b, r] = sum_k x[b, k] * W[r, k] ------------------------------------
+// One warp per output row r, all B sequences at once (W is read once, 16-byte vectors);
+// x is small and stays in L1/L2.
+constexpr int GEMV_WARPS = 8;
+constexpr int GEMV_BMAX = 8;   // sequences per register pass
+
+template <int DT>
+__global__ void __launch_bounds__(GEMV_WARPS * 32)
+append_gemv_kernel(const typename Act<DT>::T* __restrict__ x, const typename Act<DT>::T* __restrict__ w,
+                   int hidden, int rows, int B, float* __restrict__ kva) {
+  using T = typename Act<DT>::T;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * GEMV_WARPS + warp;
+  if (r >= rows) return;
+  constexpr int VEC = 16 / sizeof(T);  // elements per 16-byte load
+  const T* wr = w + (int64_t)r * hidden;
+  for (int b0 = 0; b0 < B; b0 += GEMV_BMAX) {
+    const int nb = min(GEMV_BMAX, B - b0);
+    float acc[GEMV_BMAX];
+#pragma unroll
+    for (int j = 0; j < GEMV_BMAX; ++j) acc[j] = 0.f;
+    for (int k = lane * VEC; k < hidden; k += 32 * VEC) {
+      uint4 wv = *reinterpret_cast<const uint4*>(wr + k);
+      const T* we = reinterpret_cast<const T*>(&wv);
+#pragma unroll
+      for (int j = 0; j < GEMV_BMAX; ++j) {
+        if (j < nb) {
+          uint4 xv = *reinterpret_cast<const uint4*>(x + (int64_t)(b0 + j) * hidden + k);
+          const T* xe = reinterpret_cast<const T*>(&xv);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e)
+            acc[j] = fmaf(Act<DT>::load(we, e), Act<DT>::load(xe, e), acc[j]);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < GEMV_BMAX; ++j) {
+      float v = warp_sum(acc[j]);
+      if (lane == 0 && j < nb) kva[(int64_t)(b0 + j) * rows + r] = v;
+    }
+  }
+}
+
+cudaError_t launch_append_gemv(const mla_config& cfg, const void* x, const void* w, int hidden,
+                               float* kva_out, int B, cudaStream_t st) {
+  const int rows = cfg.kv_lora + cfg.qk_rope;
+  dim3 grid((rows + GEMV_WARPS - 1) / GEMV_WARPS);
+  if (cfg.act_dtype == MLA_BF16)
+    append_gemv_kernel<MLA_BF16><<<grid, GEMV_WARPS * 32, 0, st>>>(
+        static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(w), hidden, rows, B, kva_out);
+  else
+    append_gemv_kernel<MLA_F32><<<grid, GEMV_WARPS * 32, 0, st>>>(
+        static_cast<const float*>(x), static_cast<const float*>(w), hidden, rows, B, kva_out);
+  return cudaGetLastError();
+}
+
+// ---- finish: norm + rope + store, one CTA per sequence ---------------------------------------
+constexpr int FIN_THREADS = 128;
+constexpr int FIN_MAX_PER_THREAD = 16;   // row elements per thread: C+R <= 2048
+
+template <int DT>
+__global__ void __launch_bounds__(FIN_THREADS)
+append_finish_kernel(mla_config cfg, RowMap map, typename Act<DT>::T* __restrict__ rows_out,
+                     const float* __restrict__ kva, const float* __restrict__ norm_w,
+                     const int32_t* __restrict__ positions, const int32_t* __restrict__ seq_lens,
+                     WsHeader* hdr) {
+  const int b = blockIdx.x;
+  const int C = cfg.kv_lora, R = cfg.qk_rope, row = C + R;
+  const int pos = positions[b];
+  if (seq_lens != nullptr && seq_lens[b] != pos) {
+    if (threadIdx.x == 0) set_error(hdr, MLA_ERR_POS_MISMATCH, b);
+    return;
+  }
+  if (pos < 0 || (int64_t)pos >= map.capacity()) {
+    if (threadIdx.x == 0) set_error(hdr, MLA_ERR_CACHE_FULL, b);
+    return;
+  }
+  const int64_t pr = map.phys(b, pos);
+  if (pr < 0 || pr >= map.n_phys) {
+    if (threadIdx.x == 0) set_error(hdr, MLA_ERR_BAD_PAGE, b);
+    return;
+  }
+
+  __shared__ float red[FIN_THREADS / 32];
+  float v[FIN_MAX_PER_THREAD];
+  float ss = 0.f;
+  const float* src = kva + (int64_t)b * row;
+#pragma unroll
+  for (int k = 0; k < FIN_MAX_PER_THREAD; ++k) {
+    const int i = threadIdx.x + k * FIN_THREADS;
+    v[k] = (i < row) ? src[i] : 0.f;
+    if (i < C) ss = fmaf(v[k], v[k], ss);
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < FIN_THREADS / 32; ++w) tot += red[w];
+  const float inv_rms = 1.0f / sqrtf(tot / static_cast<float>(C) + cfg.rms_eps);
+
+  typename Act<DT>::T* dst = rows_out + pr * row;
+#pragma unroll
+  for (int k = 0; k < FIN_MAX_PER_THREAD; ++k) {
+    const int i = threadIdx.x + k * FIN_THREADS;
+    if (i < C) Act<DT>::store(dst, i, v[k] * inv_rms * norm_w[i]);
+  }
+  // RoPE over the pe tail: one thread per pair (2i, 2i+1)
+  for (int i = threadIdx.x; i < R / 2; i += FIN_THREADS) {
+    float c, s;
+    rope_cs(cfg.rope_inv_freq, i, pos, &c, &s);
+    const float x0 = src[C + 2 * i], x1 = src[C + 2 * i + 1];
+    Act<DT>::store(dst, C + 2 * i, x0 * c - x1 * s);
+    Act<DT>::store(dst, C + 2 * i + 1, x0 * s + x1 * c);
+  }
+}
+
+cudaError_t launch_append_finish(const mla_config& cfg, const mla_cache& cache, const float* kva,
+                                 const float* norm_w, const int32_t* positions,
+                                 const int32_t* seq_lens, int B, WsHeader* hdr, cudaStream_t st) {
+  RowMap map{cache.page_table, cfg.page_size, cfg.max_pages_per_seq, cfg.rows_per_seq,
+             cache.n_physical_rows};
+  if (cfg.act_dtype == MLA_BF16)
+    append_finish_kernel<MLA_BF16><<<B, FIN_THREADS, 0, st>>>(
+        cfg, map, static_cast<uint16_t*>(cache.rows), kva, norm_w, positions, seq_lens, hdr);
+  else
+    append_finish_kernel<MLA_F32><<<B, FIN_THREADS, 0, st>>>(
+        cfg, map, static_cast<float*>(cache.rows), kva, norm_w, positions, seq_lens, hdr);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

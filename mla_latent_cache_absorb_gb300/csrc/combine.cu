@@ -1,0 +1,121 @@
+// Combine + up-project: merge the splits of each (sequence, head) by log-sum-exp, then
+// out[b,h,:] = W_UV,h * vc[b,h,:].
+//
+// moeflux 0.1.0-pre.3, src/riir/attn/mla_attn_forward.rs, out_per_head (v_combine through the
+// v rows of kv_b, skipping the nope rows). turbospark-runtime 0.3.0,
+// src/families/deepseek2/attn.rs, encode_mla_v_combine (Q8_0 W_UV). The split + COMBINE pass
+// structure follows turbospark-runtime 0.3.0, src/families/gptoss/attn.rs.
+//
+// Grid (head, 32-wide slice of V, block of sequences). Each CTA merges the splits of its
+// sequences for its head into float32 latent vectors in shared memory, stages its slice of
+// W_UV (dequantised), and forms the dot products.
+#include "common.cuh"
+
+#include <math_constants.h>
+
+namespace mla {
+
+constexpr int CMB_THREADS = 256;
+constexpr int CMB_VJ = 32;      // V outputs per CTA
+constexpr int CMB_BC = 16;      // sequences per CTA
+
+struct CombineArgs {
+  const void* kv_b;
+  const int32_t* seq_lens;
+  const float* part_o;
+  const float* part_lse;
+  float* out;
+  float* lse;
+  int kv_b_dtype;
+  int H, C, N, V, S, B;
+  int64_t chunk, capacity;
+};
+
+__global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
+  extern __shared__ float sm[];
+  const int h = blockIdx.x;
+  const int j0 = blockIdx.y * CMB_VJ;
+  const int b0 = blockIdx.z * CMB_BC;
+  const int nb = min(CMB_BC, a.B - b0);
+  const int nj = min(CMB_VJ, a.V - j0);
+  const int Cp = a.C + 1;                  // padded W row: conflict-free across j
+  float* w_s = sm;                         // [CMB_VJ][C+1]
+  float* vc_s = w_s + CMB_VJ * Cp;         // [CMB_BC][C]
+  float* wt_s = vc_s + CMB_BC * a.C;       // [CMB_BC][S] split weights
+  float* lse_s = wt_s + CMB_BC * a.S;      // [CMB_BC]
+
+  const int64_t wrow0 = (int64_t)h * (a.N + a.V) + a.N + j0;
+  for (int i = threadIdx.x; i < CMB_VJ * a.C; i += CMB_THREADS) {
+    const int j = i / a.C, c = i % a.C;
+    w_s[j * Cp + c] = (j < nj) ? kv_b_load(a.kv_b, a.kv_b_dtype, wrow0 + j, c, a.C) : 0.f;
+  }
+
+  // split weights: one warp per sequence
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int bb = warp; bb < nb; bb += CMB_THREADS / 32) {
+    const int b = b0 + bb;
+    const int64_t L = a.seq_lens[b];
+    const bool ok = (L >= 1 && L <= a.capacity);
+    const int ns = ok ? (int)((L + a.chunk - 1) / a.chunk) : 0;
+    float mx = -CUDART_INF_F;
+    for (int s = lane; s < ns; s += 32)
+      mx = fmaxf(mx, a.part_lse[((int64_t)b * a.S + s) * a.H + h]);
+    mx = warp_max(mx);
+    float tot = 0.f;
+    for (int s = lane; s < ns; s += 32)
+      tot += expf(a.part_lse[((int64_t)b * a.S + s) * a.H + h] - mx);
+    tot = warp_sum(tot);
+    const float l = ok ? mx + logf(tot) : CUDART_NAN_F;
+    for (int s = lane; s < a.S; s += 32)
+      wt_s[bb * a.S + s] = (s < ns) ? expf(a.part_lse[((int64_t)b * a.S + s) * a.H + h] - l) : 0.f;
+    if (lane == 0) lse_s[bb] = l;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < nb * a.C; i += CMB_THREADS) {
+    const int bb = i / a.C, c = i % a.C;
+    const int b = b0 + bb;
+    float v = 0.f;
+    if (isnan(lse_s[bb])) {
+      v = CUDART_NAN_F;
+    } else {
+      const int64_t L = a.seq_lens[b];
+      const int ns = (int)((L + a.chunk - 1) / a.chunk);
+      for (int s = 0; s < ns; ++s)
+        v = fmaf(wt_s[bb * a.S + s], a.part_o[(((int64_t)b * a.S + s) * a.H + h) * a.C + c], v);
+    }
+    vc_s[bb * a.C + c] = v;
+  }
+  __syncthreads();
+  // out[b, h, j0 + j]: one warp per sequence, lane = j
+  for (int bb = warp; bb < nb; bb += CMB_THREADS / 32) {
+    if (lane < nj) {
+      float acc = 0.f;
+      const float* wr = w_s + lane * Cp;
+      const float* vr = vc_s + bb * a.C;
+      for (int c = 0; c < a.C; ++c) acc = fmaf(wr[c], vr[c], acc);
+      a.out[((int64_t)(b0 + bb) * a.H + h) * a.V + j0 + lane] = acc;
+    }
+  }
+  if (blockIdx.y == 0 && a.lse != nullptr)
+    for (int bb = threadIdx.x; bb < nb; bb += CMB_THREADS) a.lse[(int64_t)(b0 + bb) * a.H + h] = lse_s[bb];
+}
+
+cudaError_t launch_combine(const mla_config& cfg, const DecodePlan& plan, const void* kv_b,
+                           const int32_t* seq_lens, const float* part_o, const float* part_lse,
+                           float* out, float* lse, int B, WsHeader* hdr, cudaStream_t st) {
+  (void)hdr;
+  CombineArgs a;
+  a.kv_b = kv_b; a.seq_lens = seq_lens; a.part_o = part_o; a.part_lse = part_lse;
+  a.out = out; a.lse = lse; a.kv_b_dtype = cfg.kv_b_dtype;
+  a.H = cfg.n_heads; a.C = cfg.kv_lora; a.N = cfg.qk_nope; a.V = cfg.v_head;
+  a.S = plan.splits; a.B = B; a.chunk = plan.chunk_rows; a.capacity = plan.capacity;
+  dim3 grid(cfg.n_heads, (cfg.v_head + CMB_VJ - 1) / CMB_VJ, (B + CMB_BC - 1) / CMB_BC);
+  const size_t smem = sizeof(float) * ((size_t)CMB_VJ * (cfg.kv_lora + 1) + (size_t)CMB_BC * cfg.kv_lora +
+                                       (size_t)CMB_BC * plan.splits + CMB_BC);
+  cudaError_t e = ensure_smem((const void*)combine_kernel, (int)smem);
+  if (e != cudaSuccess) return e;
+  combine_kernel<<<grid, CMB_THREADS, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,134 @@
+// Shared device helpers and the internal launch interface of libmla.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+// ---- workspace header (first 256 bytes of every workspace) ---------------------------------
+struct WsHeader {
+  int32_t code;   // first device error recorded (mla_status), 0 = none
+  int32_t seq;    // sequence index it concerns
+  int32_t pad[62];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+__device__ __forceinline__ void set_error(WsHeader* hdr, int code, int seq) {
+  if (atomicCAS(&hdr->code, 0, code) == 0) atomicExch(&hdr->seq, seq);
+}
+
+// ---- element access -------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+template <int DT> struct Act;
+template <> struct Act<MLA_F32> {
+  using T = float;
+  static __device__ __forceinline__ float load(const T* p, int64_t i) { return p[i]; }
+  static __device__ __forceinline__ void store(T* p, int64_t i, float v) { p[i] = v; }
+};
+template <> struct Act<MLA_BF16> {
+  using T = uint16_t;
+  static __device__ __forceinline__ float load(const T* p, int64_t i) { return bf16_bits_to_f32(p[i]); }
+  static __device__ __forceinline__ void store(T* p, int64_t i, float v) {
+    __nv_bfloat16 h = __float2bfloat16_rn(v);
+    p[i] = *reinterpret_cast<uint16_t*>(&h);
+  }
+};
+
+// One kv_b element (row r, column c) in any weight dtype. Q8_0: fp16 scale then 32 codes
+// per 34-byte block; value = scale * code (exact in float32).
+__device__ __forceinline__ float kv_b_load(const void* kv_b, int dtype, int64_t r, int c, int C) {
+  if (dtype == MLA_BF16) {
+    return bf16_bits_to_f32(static_cast<const uint16_t*>(kv_b)[r * C + c]);
+  } else if (dtype == MLA_F32) {
+    return static_cast<const float*>(kv_b)[r * C + c];
+  } else {
+    const uint8_t* blk = static_cast<const uint8_t*>(kv_b) + r * (int64_t)(C / 32) * 34 + (c / 32) * 34;
+    uint16_t dbits = static_cast<uint16_t>(blk[0]) | (static_cast<uint16_t>(blk[1]) << 8);
+    float d = __half2float(__ushort_as_half(dbits));
+    return d * static_cast<float>(static_cast<int8_t>(blk[2 + (c & 31)]));
+  }
+}
+
+// Logical row t of sequence b -> physical row, or -1 when the page id is out of range.
+struct RowMap {
+  const int32_t* page_table;
+  int32_t page_size;
+  int32_t max_pages;
+  int64_t rows_per_seq;
+  int64_t n_phys;
+  __device__ __forceinline__ int64_t phys(int b, int64_t t) const {
+    if (page_size == 0) return (int64_t)b * rows_per_seq + t;
+    int32_t pg = page_table[(int64_t)b * max_pages + t / page_size];
+    if (pg < 0 || (int64_t)(pg + 1) * page_size > n_phys) return -1;
+    return (int64_t)pg * page_size + t % page_size;
+  }
+  __host__ __device__ __forceinline__ int64_t capacity() const {
+    return page_size == 0 ? rows_per_seq : (int64_t)max_pages * page_size;
+  }
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// RoPE angle for pair i at position pos, reduced in float64 so that large positions keep
+// their accuracy; returns cos and sin as float.
+__device__ __forceinline__ void rope_cs(const double* inv_freq, int i, int pos, float* c, float* s) {
+  double a = static_cast<double>(pos) * inv_freq[i];
+  double sd, cd;
+  sincos(a, &sd, &cd);
+  *c = static_cast<float>(cd);
+  *s = static_cast<float>(sd);
+}
+
+// ---- decode plan: how the rows of a sequence are split, and the workspace layout -------------
+struct DecodePlan {
+  int path;              // PATH_SIMT or PATH_TC
+  int heads_per_cta;     // heads sharing one staged row tile in one CTA
+  int n_groups;          // ceil(H / heads_per_cta)
+  int splits;            // S: row splits per sequence (workspace slots)
+  int64_t chunk_rows;    // rows per split (a multiple of the row tile)
+  int64_t capacity;      // maximum rows a sequence can attend
+  size_t off_qabs, off_po, off_plse, total;
+};
+enum { PATH_SIMT = 0, PATH_TC = 1 };
+
+// Raise a kernel's dynamic shared memory limit once per (kernel, device), so that repeated
+// launches (and launches under stream capture) make no attribute calls.
+cudaError_t ensure_smem(const void* func, int bytes);
+
+// host launchers (defined in the kernel files)
+cudaError_t launch_append_gemv(const mla_config& cfg, const void* x, const void* w, int hidden,
+                               float* kva_out, int B, cudaStream_t st);
+cudaError_t launch_append_finish(const mla_config& cfg, const mla_cache& cache, const float* kva,
+                                 const float* norm_w, const int32_t* positions,
+                                 const int32_t* seq_lens, int B, WsHeader* hdr, cudaStream_t st);
+cudaError_t launch_absorb(const mla_config& cfg, const void* q, const void* kv_b,
+                          const int32_t* positions, void* q_abs, int B, cudaStream_t st);
+cudaError_t launch_attn_simt(const mla_config& cfg, const mla_cache& cache, const DecodePlan& plan,
+                             const int32_t* seq_lens, const void* q_abs, float* part_o,
+                             float* part_lse, int B, WsHeader* hdr, cudaStream_t st);
+cudaError_t launch_attn_tc(const mla_config& cfg, const mla_cache& cache, const DecodePlan& plan,
+                           const int32_t* seq_lens, const void* q_abs, float* part_o,
+                           float* part_lse, int B, WsHeader* hdr, cudaStream_t st);
+bool attn_tc_supported(const mla_config& cfg);
+cudaError_t launch_combine(const mla_config& cfg, const DecodePlan& plan, const void* kv_b,
+                           const int32_t* seq_lens, const float* part_o, const float* part_lse,
+                           float* out, float* lse, int B, WsHeader* hdr, cudaStream_t st);
+
+}  // namespace mla

@@ -1,0 +1,400 @@
+// The C ABI of libmla: host validation, workspace layout, split plan and kernel launches.
+// Every entry point validates on the host before enqueueing anything; kernels report what
+// only the GPU can see through the workspace's error word.
+#include <cmath>
+#include <cstring>
+#include <limits>
+
+#include "common.cuh"
+
+namespace mla {
+
+static bool checked_mul(uint64_t a, uint64_t b, uint64_t* out) {
+  if (a != 0 && b > std::numeric_limits<uint64_t>::max() / a) return false;
+  *out = a * b;
+  return true;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static size_t act_size(int dt) { return dt == MLA_BF16 ? 2 : 4; }
+
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Dimensions and dtypes shared by every call.
+static mla_status check_cfg(const mla_config* cfg) {
+  if (cfg == nullptr) return MLA_ERR_INVALID_ARG;
+  if (cfg->n_heads < 1 || cfg->kv_lora < 1 || cfg->qk_nope < 1 || cfg->qk_rope < 2 ||
+      (cfg->qk_rope & 1) || cfg->v_head < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (cfg->act_dtype != MLA_F32 && cfg->act_dtype != MLA_BF16) return MLA_ERR_INVALID_ARG;
+  if (cfg->kv_b_dtype != MLA_F32 && cfg->kv_b_dtype != MLA_BF16 && cfg->kv_b_dtype != MLA_Q8_0)
+    return MLA_ERR_INVALID_ARG;
+  if (cfg->kv_b_dtype == MLA_Q8_0 && (cfg->kv_lora % 32) != 0) return MLA_ERR_BAD_KV_B;
+  if (cfg->page_size < 0) return MLA_ERR_INVALID_ARG;
+  if (cfg->page_size == 0 && cfg->rows_per_seq < 1) return MLA_ERR_INVALID_ARG;
+  if (cfg->page_size > 0 && cfg->max_pages_per_seq < 1) return MLA_ERR_INVALID_ARG;
+  if (!(cfg->softmax_scale > 0.f) || !std::isfinite(cfg->softmax_scale)) return MLA_ERR_INVALID_ARG;
+  // implementation limits of the kernels (row staged per thread / per CTA)
+  if (cfg->kv_lora + cfg->qk_rope > 2048 || cfg->qk_nope > 512 || cfg->kv_lora > 4096)
+    return MLA_ERR_UNSUPPORTED;
+  // row stride must keep 16-byte alignment for vectorised row access
+  if (((int64_t)(cfg->kv_lora + cfg->qk_rope) * (int64_t)act_size(cfg->act_dtype)) % 16 != 0)
+    return MLA_ERR_UNSUPPORTED;
+  return MLA_OK;
+}
+
+static mla_status check_cache(const mla_config* cfg, const mla_cache* cache, int B) {
+  if (cache == nullptr || cache->rows == nullptr || cache->n_physical_rows < 1) return MLA_ERR_INVALID_ARG;
+  if (!aligned(cache->rows, 16)) return MLA_ERR_INVALID_ARG;
+  if (cfg->page_size > 0) {
+    if (cache->page_table == nullptr) return MLA_ERR_INVALID_ARG;
+  } else {
+    uint64_t need;
+    if (!checked_mul((uint64_t)B, (uint64_t)cfg->rows_per_seq, &need)) return MLA_ERR_INVALID_ARG;
+    if ((uint64_t)cache->n_physical_rows < need) return MLA_ERR_INVALID_ARG;
+  }
+  return MLA_OK;
+}
+
+static int device_sms() {
+  static int cached[64] = {0};
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+int simt_heads_per_cta(const mla_config& cfg);
+
+// The split plan: how many row splits per sequence, how many rows each, and where the
+// workspace keeps the fused query rows and the per-split partials.
+static mla_status make_plan(const mla_config& cfg, int B, DecodePlan* p) {
+  const int sms = device_sms();
+  if (sms <= 0) return MLA_ERR_CUDA;
+  std::memset(p, 0, sizeof(*p));
+  p->capacity = cfg.page_size == 0 ? cfg.rows_per_seq : (int64_t)cfg.max_pages_per_seq * cfg.page_size;
+  int64_t tile;
+  int target;
+  if (attn_tc_supported(cfg)) {
+    p->path = PATH_TC;
+    p->heads_per_cta = cfg.n_heads <= 64 ? cfg.n_heads : 64;
+    tile = 128;
+    target = sms;
+  } else {
+    p->path = PATH_SIMT;
+    p->heads_per_cta = simt_heads_per_cta(cfg);
+    tile = 16;
+    target = 2 * sms;
+  }
+  p->n_groups = (cfg.n_heads + p->heads_per_cta - 1) / p->heads_per_cta;
+  const int64_t per_seq_ctas = (int64_t)B * p->n_groups;
+  int64_t want = (target + per_seq_ctas - 1) / per_seq_ctas;
+  if (want < 1) want = 1;
+  if (want > 64) want = 64;
+  int64_t chunk = (p->capacity + want - 1) / want;
+  chunk = ((chunk + tile - 1) / tile) * tile;
+  p->chunk_rows = chunk;
+  p->splits = (int)((p->capacity + chunk - 1) / chunk);
+
+  const size_t row = (size_t)(cfg.kv_lora + cfg.qk_rope);
+  size_t off = sizeof(WsHeader);
+  p->off_qabs = off;
+  off = align256(off + (size_t)B * cfg.n_heads * row * act_size(cfg.act_dtype));
+  p->off_po = off;
+  off = align256(off + (size_t)B * p->splits * cfg.n_heads * cfg.kv_lora * sizeof(float));
+  p->off_plse = off;
+  off = align256(off + (size_t)B * p->splits * cfg.n_heads * sizeof(float));
+  p->total = off;
+  return MLA_OK;
+}
+
+cudaError_t ensure_smem(const void* func, int bytes) {
+  struct Entry { const void* f; int dev; int bytes; };
+  static Entry table[128];
+  static int n = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < n; ++i)
+    if (table[i].f == func && table[i].dev == dev && table[i].bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < n; ++i)
+    if (table[i].f == func && table[i].dev == dev) { table[i].bytes = bytes; return cudaSuccess; }
+  if (n < 128) table[n++] = Entry{func, dev, bytes};
+  return cudaSuccess;
+}
+
+static mla_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+static mla_status check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (ws == nullptr || !aligned(ws, 256)) return MLA_ERR_WORKSPACE;
+  if (ws_bytes < need) return MLA_ERR_WORKSPACE;
+  return MLA_OK;
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+const char* mla_status_string(mla_status s) {
+  switch (s) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MLA_ERR_POS_MISMATCH: return "append position does not match the sequence length";
+    case MLA_ERR_CACHE_FULL: return "append position beyond the cache capacity";
+    case MLA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MLA_ERR_TIMEOUT: return "a bounded device wait timed out";
+    case MLA_ERR_CUDA: return "CUDA runtime error";
+    case MLA_ERR_BAD_SEQ_LEN: return "sequence length below 1 or above the cache capacity";
+    case MLA_ERR_BAD_PAGE: return "page-table entry out of range";
+    case MLA_ERR_BAD_KV_B: return "kv_b dtype, shape or size does not match the configuration";
+  }
+  return "unknown status";
+}
+
+int32_t mla_abi_version(void) { return 1; }
+
+mla_status mla_yarn_inv_freq(int32_t rope_dim, double theta, double factor, int32_t orig_max_pos,
+                             double beta_fast, double beta_slow, double* out_host) {
+  if (out_host == nullptr || rope_dim < 2 || (rope_dim & 1) || !(theta > 1.0) || orig_max_pos < 1)
+    return MLA_ERR_INVALID_ARG;
+  const int half = rope_dim / 2;
+  const double d = static_cast<double>(rope_dim);
+  double lo = 0, hi = 1;
+  const bool yarn = factor > 1.0;
+  if (yarn) {
+    if (!(beta_fast > 0) || !(beta_slow > 0)) return MLA_ERR_INVALID_ARG;
+    const double two_pi = 6.283185307179586476925286766559;
+    // correction dimension: the pair index whose wavelength fits n_rot turns into the
+    // original context
+    auto corr = [&](double n_rot) {
+      return d * std::log(static_cast<double>(orig_max_pos) / (n_rot * two_pi)) / (2.0 * std::log(theta));
+    };
+    lo = std::floor(corr(beta_fast));
+    hi = std::ceil(corr(beta_slow));
+    if (lo < 0) lo = 0;
+    if (hi > d - 1) hi = d - 1;
+    if (lo == hi) hi += 0.001;
+  }
+  for (int i = 0; i < half; ++i) {
+    const double base = std::pow(theta, -2.0 * i / d);
+    if (!yarn) {
+      out_host[i] = base;
+      continue;
+    }
+    double r = (i - lo) / (hi - lo);
+    r = r < 0 ? 0 : (r > 1 ? 1 : r);
+    out_host[i] = base / factor * r + base * (1.0 - r);
+  }
+  return MLA_OK;
+}
+
+double mla_yarn_mscale(double factor, double coeff) {
+  return factor <= 1.0 ? 1.0 : 1.0 + 0.1 * coeff * std::log(factor);
+}
+
+float mla_softmax_scale(int32_t qk_nope, int32_t qk_rope, double mscale) {
+  if (qk_nope < 0 || qk_rope < 0 || qk_nope + qk_rope < 1) return 0.f;
+  return static_cast<float>(mscale * mscale / std::sqrt(static_cast<double>(qk_nope + qk_rope)));
+}
+
+mla_status mla_validate_kv_b(int32_t dtype, int64_t rows, int64_t cols, uint64_t size_bytes,
+                             int32_t heads, int32_t nope, int32_t kv_lora, int32_t v_dim) {
+  if (heads < 1 || nope < 1 || kv_lora < 1 || v_dim < 1) return MLA_ERR_INVALID_ARG;
+  if (dtype != MLA_F32 && dtype != MLA_BF16 && dtype != MLA_Q8_0) return MLA_ERR_BAD_KV_B;
+  uint64_t exp_rows;
+  if (!checked_mul((uint64_t)heads, (uint64_t)nope + (uint64_t)v_dim, &exp_rows)) return MLA_ERR_BAD_KV_B;
+  if (rows < 0 || cols < 0 || (uint64_t)rows != exp_rows || cols != kv_lora) return MLA_ERR_BAD_KV_B;
+  uint64_t row_bytes;
+  if (dtype == MLA_Q8_0) {
+    if (kv_lora % 32 != 0) return MLA_ERR_BAD_KV_B;
+    if (!checked_mul((uint64_t)(kv_lora / 32), 34u, &row_bytes)) return MLA_ERR_BAD_KV_B;
+  } else {
+    if (!checked_mul((uint64_t)kv_lora, dtype == MLA_BF16 ? 2u : 4u, &row_bytes)) return MLA_ERR_BAD_KV_B;
+  }
+  uint64_t total;
+  if (!checked_mul(exp_rows, row_bytes, &total)) return MLA_ERR_BAD_KV_B;
+  return total == size_bytes ? MLA_OK : MLA_ERR_BAD_KV_B;
+}
+
+uint64_t mla_kv_b_bytes(const mla_config* cfg) {
+  if (cfg == nullptr || cfg->n_heads < 1 || cfg->qk_nope < 1 || cfg->v_head < 1 || cfg->kv_lora < 1) return 0;
+  uint64_t rows, row_bytes, total;
+  if (!checked_mul((uint64_t)cfg->n_heads, (uint64_t)cfg->qk_nope + (uint64_t)cfg->v_head, &rows)) return 0;
+  if (cfg->kv_b_dtype == MLA_Q8_0) {
+    if (cfg->kv_lora % 32) return 0;
+    row_bytes = (uint64_t)(cfg->kv_lora / 32) * 34u;
+  } else if (cfg->kv_b_dtype == MLA_BF16) {
+    row_bytes = (uint64_t)cfg->kv_lora * 2u;
+  } else if (cfg->kv_b_dtype == MLA_F32) {
+    row_bytes = (uint64_t)cfg->kv_lora * 4u;
+  } else {
+    return 0;
+  }
+  if (!checked_mul(rows, row_bytes, &total)) return 0;
+  return total;
+}
+
+mla_status mla_append_workspace_size(const mla_config* cfg, int32_t B, size_t* bytes) {
+  mla_status st = check_cfg(cfg);
+  if (st != MLA_OK) return st;
+  if (B < 1 || bytes == nullptr) return MLA_ERR_INVALID_ARG;
+  *bytes = align256(sizeof(WsHeader) + (size_t)B * (cfg->kv_lora + cfg->qk_rope) * sizeof(float));
+  return MLA_OK;
+}
+
+mla_status mla_decode_workspace_size(const mla_config* cfg, int32_t B, size_t* bytes) {
+  mla_status st = check_cfg(cfg);
+  if (st != MLA_OK) return st;
+  if (B < 1 || bytes == nullptr) return MLA_ERR_INVALID_ARG;
+  DecodePlan p;
+  st = make_plan(*cfg, B, &p);
+  if (st != MLA_OK) return st;
+  *bytes = p.total;
+  return MLA_OK;
+}
+
+mla_status mla_decode_plan(const mla_config* cfg, int32_t B, mla_plan_info* info) {
+  mla_status st = check_cfg(cfg);
+  if (st != MLA_OK) return st;
+  if (B < 1 || info == nullptr) return MLA_ERR_INVALID_ARG;
+  DecodePlan p;
+  st = make_plan(*cfg, B, &p);
+  if (st != MLA_OK) return st;
+  info->kernel = p.path;
+  info->heads_per_cta = p.heads_per_cta;
+  info->head_groups = p.n_groups;
+  info->splits = p.splits;
+  info->rows_per_split = p.chunk_rows;
+  info->capacity = p.capacity;
+  return MLA_OK;
+}
+
+mla_status mla_cache_append(const mla_config* cfg, const mla_cache* cache, const void* kv_in,
+                            const void* w_kva, int32_t hidden, const float* norm_w,
+                            const int32_t* positions, const int32_t* seq_lens, int32_t B,
+                            void* workspace, size_t ws_bytes, mla_stream_t stream) {
+  mla_status st = check_cfg(cfg);
+  if (st != MLA_OK) return st;
+  if (B < 1 || kv_in == nullptr || norm_w == nullptr || positions == nullptr) return MLA_ERR_INVALID_ARG;
+  if (cfg->rope_inv_freq == nullptr) return MLA_ERR_INVALID_ARG;
+  st = check_cache(cfg, cache, B);
+  if (st != MLA_OK) return st;
+  if (w_kva != nullptr) {
+    const int vec = 16 / (int)act_size(cfg->act_dtype);
+    if (hidden < 1 || hidden % vec != 0 || !aligned(kv_in, 16) || !aligned(w_kva, 16))
+      return MLA_ERR_INVALID_ARG;
+  }
+  size_t need;
+  st = mla_append_workspace_size(cfg, B, &need);
+  if (st != MLA_OK) return st;
+  st = check_ws(workspace, ws_bytes, need);
+  if (st != MLA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  WsHeader* hdr = static_cast<WsHeader*>(workspace);
+  const float* kva = static_cast<const float*>(kv_in);
+  if (w_kva != nullptr) {
+    float* kva_ws = reinterpret_cast<float*>(static_cast<char*>(workspace) + sizeof(WsHeader));
+    st = cuda_status(launch_append_gemv(*cfg, kv_in, w_kva, hidden, kva_ws, B, s));
+    if (st != MLA_OK) return st;
+    kva = kva_ws;
+  }
+  return cuda_status(launch_append_finish(*cfg, *cache, kva, norm_w, positions, seq_lens, B, hdr, s));
+}
+
+static mla_status decode_prologue(const mla_config* cfg, int32_t B, void* workspace, size_t ws_bytes,
+                                  DecodePlan* plan) {
+  mla_status st = check_cfg(cfg);
+  if (st != MLA_OK) return st;
+  if (B < 1) return MLA_ERR_INVALID_ARG;
+  st = make_plan(*cfg, B, plan);
+  if (st != MLA_OK) return st;
+  return check_ws(workspace, ws_bytes, plan->total);
+}
+
+mla_status mla_decode_absorb(const mla_config* cfg, const void* q, const void* kv_b,
+                             const int32_t* positions, int32_t B, void* workspace, size_t ws_bytes,
+                             mla_stream_t stream) {
+  DecodePlan plan;
+  mla_status st = decode_prologue(cfg, B, workspace, ws_bytes, &plan);
+  if (st != MLA_OK) return st;
+  if (q == nullptr || kv_b == nullptr) return MLA_ERR_INVALID_ARG;
+  if (positions != nullptr && cfg->rope_inv_freq == nullptr) return MLA_ERR_INVALID_ARG;
+  void* q_abs = static_cast<char*>(workspace) + plan.off_qabs;
+  return cuda_status(launch_absorb(*cfg, q, kv_b, positions, q_abs, B,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mla_status mla_decode_partial(const mla_config* cfg, const mla_cache* cache, const int32_t* seq_lens,
+                              int32_t B, void* workspace, size_t ws_bytes, mla_stream_t stream) {
+  DecodePlan plan;
+  mla_status st = decode_prologue(cfg, B, workspace, ws_bytes, &plan);
+  if (st != MLA_OK) return st;
+  if (seq_lens == nullptr) return MLA_ERR_INVALID_ARG;
+  st = check_cache(cfg, cache, B);
+  if (st != MLA_OK) return st;
+  char* ws = static_cast<char*>(workspace);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  float* po = reinterpret_cast<float*>(ws + plan.off_po);
+  float* pl = reinterpret_cast<float*>(ws + plan.off_plse);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (plan.path == PATH_TC)
+    return cuda_status(launch_attn_tc(*cfg, *cache, plan, seq_lens, ws + plan.off_qabs, po, pl, B, hdr, s));
+  return cuda_status(launch_attn_simt(*cfg, *cache, plan, seq_lens, ws + plan.off_qabs, po, pl, B, hdr, s));
+}
+
+mla_status mla_decode_combine(const mla_config* cfg, const void* kv_b, const int32_t* seq_lens,
+                              float* out, float* lse, int32_t B, void* workspace, size_t ws_bytes,
+                              mla_stream_t stream) {
+  DecodePlan plan;
+  mla_status st = decode_prologue(cfg, B, workspace, ws_bytes, &plan);
+  if (st != MLA_OK) return st;
+  if (kv_b == nullptr || seq_lens == nullptr || out == nullptr) return MLA_ERR_INVALID_ARG;
+  char* ws = static_cast<char*>(workspace);
+  return cuda_status(launch_combine(*cfg, plan, kv_b, seq_lens,
+                                    reinterpret_cast<const float*>(ws + plan.off_po),
+                                    reinterpret_cast<const float*>(ws + plan.off_plse), out, lse, B,
+                                    reinterpret_cast<WsHeader*>(ws), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mla_status mla_decode_attn(const mla_config* cfg, const void* q, const void* kv_b, const mla_cache* cache,
+                           const int32_t* seq_lens, const int32_t* positions, float* out, float* lse,
+                           int32_t B, void* workspace, size_t ws_bytes, mla_stream_t stream) {
+  // validate everything before the first launch, so a bad argument enqueues nothing
+  DecodePlan plan;
+  mla_status st = decode_prologue(cfg, B, workspace, ws_bytes, &plan);
+  if (st != MLA_OK) return st;
+  if (q == nullptr || kv_b == nullptr || seq_lens == nullptr || out == nullptr) return MLA_ERR_INVALID_ARG;
+  if (positions != nullptr && cfg->rope_inv_freq == nullptr) return MLA_ERR_INVALID_ARG;
+  st = check_cache(cfg, cache, B);
+  if (st != MLA_OK) return st;
+  st = mla_decode_absorb(cfg, q, kv_b, positions, B, workspace, ws_bytes, stream);
+  if (st != MLA_OK) return st;
+  st = mla_decode_partial(cfg, cache, seq_lens, B, workspace, ws_bytes, stream);
+  if (st != MLA_OK) return st;
+  return mla_decode_combine(cfg, kv_b, seq_lens, out, lse, B, workspace, ws_bytes, stream);
+}
+
+mla_status mla_get_device_error(const void* workspace, int32_t* seq_out, mla_stream_t stream) {
+  if (workspace == nullptr) return MLA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
+  int32_t h[2];
+  if (cudaMemcpy(h, workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
+  if (seq_out != nullptr) *seq_out = h[1];
+  return static_cast<mla_status>(h[0]);
+}
+
+mla_status mla_clear_device_error(void* workspace, mla_stream_t stream) {
+  if (workspace == nullptr) return MLA_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(workspace, 0, sizeof(WsHeader), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

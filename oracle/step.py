@@ -92,17 +92,24 @@ def run_step(prob, seqs=None, heads=None, with_append: bool = True):
     return new, out, lse
 
 
-def rows_per_second_sample(prob, seconds: float = 10.0, max_reps: int = 1000):
-    """Time whole oracle steps on the host until `seconds` elapse; returns
-    (cache rows per second, repetitions, elapsed seconds)."""
+def rows_per_second_sample(prob, seconds: float = 10.0, heads=None):
+    """Time the oracle on the host over a bounded sample of a workload: whole steps for one
+    sequence at a time (all or `heads` of its heads), cycling through the sequences, until
+    `seconds` elapse (at least one). Returns (rows per second, counting a row once per full
+    set of heads; sequence-steps run; rows credited; elapsed seconds)."""
     import time
-    rows = int(np.sum(prob.seq_lens))
+    H = prob.wl.H
+    hs = None if heads is None else np.arange(min(int(heads), H))
+    frac = 1.0 if hs is None else len(hs) / H
     t0 = time.perf_counter()
-    reps = 0
-    while reps < max_reps:
-        run_step(prob)
-        reps += 1
+    n = 0
+    rows = 0.0
+    while True:
+        b = n % prob.wl.B
+        run_step(prob, seqs=[b], heads=hs)
+        rows += float(prob.seq_lens[b]) * frac
+        n += 1
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
-    return rows * reps / dt, reps, dt
+    return rows / dt, n, rows, dt
