@@ -192,6 +192,19 @@ def ncu_traffic(kernel: int, workload: str):
     return ent.get("dram_bytes_per_launch")
 
 
+def aggregate_over_ranks(total_ms, world, rows_per_step, steps, device):
+    """Whole-job throughput: every rank processed rows_per_step * steps rows; the job took
+    as long as the slowest rank. Returns (max time in ms, rows per second)."""
+    tmax = float(total_ms)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([tmax], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tmax = float(t.item())
+    return tmax, world * rows_per_step * steps / (tmax / 1e3)
+
+
 def run_ours(args, rank, world, device):
     import torch
 
@@ -291,11 +304,11 @@ def run_ours(args, rank, world, device):
         total_ms = t_start.elapsed_time(t_end)
         clk = sampler.samples(wall0, wall1)
         window = "timed"
-        if len(clk) < 3:
+        if len(clk) < 3 and args.clock_window_s > 0:
             # the timed region was shorter than the sampler's period: sample the same graphs
             # for about a second right after it (untimed) and say so
             wa = time.time()
-            while time.time() - wa < 1.2:
+            while time.time() - wa < args.clock_window_s:
                 gA.replay()
                 gB.replay()
                 torch.cuda.synchronize(device)
@@ -309,14 +322,8 @@ def run_ours(args, rank, world, device):
         if not args.no_e2e:
             e2e = run_e2e(torch, L, steps, prob, stream, device, K, W, work)
 
-    # aggregate over ranks: max time, every rank's rows
-    tmax = total_ms
-    if world > 1:
-        t = torch.tensor([total_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        tmax = float(t.item())
+    tmax, value = aggregate_over_ranks(total_ms, world, work["rows"], K, device)
     ms_per_step = tmax / K
-    value = world * work["rows"] * K / (tmax / 1e3)
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
     hbm, tf_burst, tf_sust, src = peaks()
     attn_gbs = work["attn_bytes"] / (attn_avg_ms / 1e3) / 1e9
@@ -464,6 +471,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--clock-window-s", type=float, default=1.2,
+                    help="seconds of untimed replays to sample clocks when the timed region is too short")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

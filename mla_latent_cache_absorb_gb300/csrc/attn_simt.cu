@@ -25,6 +25,7 @@ struct SimtArgs {
   const void* q_abs;
   float* part_o;
   float* part_lse;
+  int32_t* meta;
   WsHeader* hdr;
   int H, C, R, hpb, S;
   int64_t chunk;
@@ -40,10 +41,14 @@ __global__ void __launch_bounds__(SIMT_THREADS) attn_simt_kernel(SimtArgs a) {
   const int h0 = g * a.hpb;
   const int nh = min(a.hpb, a.H - h0);
   const int64_t L = a.seq_lens[b];
-  if (L < 1 || L > a.map.capacity()) {
-    if (threadIdx.x == 0 && s == 0 && g == 0) set_error(a.hdr, MLA_ERR_BAD_SEQ_LEN, b);
-    return;  // the combine stage writes NaN for this sequence
+  const bool len_ok = (L >= 1 && L <= a.map.capacity());
+  if (threadIdx.x == 0 && s == 0 && g == 0) {
+    // slots of sequence b for the combine stage: b*S .. b*S + ceil(L/chunk) - 1
+    a.meta[2 * b] = b * a.S;
+    a.meta[2 * b + 1] = len_ok ? (int)((L + a.chunk - 1) / a.chunk) : 0;
+    if (!len_ok) set_error(a.hdr, MLA_ERR_BAD_SEQ_LEN, b);
   }
+  if (!len_ok) return;  // the combine stage writes NaN for this sequence
   const int64_t t0 = (int64_t)s * a.chunk;
   const int64_t t1 = min(L, t0 + a.chunk);
   float* po = a.part_o + (((int64_t)b * a.S + s) * a.H + h0) * a.C;
@@ -152,7 +157,7 @@ size_t simt_smem_bytes(const mla_config& cfg, int hpb) {
 
 cudaError_t launch_attn_simt(const mla_config& cfg, const mla_cache& cache, const DecodePlan& plan,
                              const int32_t* seq_lens, const void* q_abs, float* part_o,
-                             float* part_lse, int B, WsHeader* hdr, cudaStream_t st) {
+                             float* part_lse, int32_t* meta, int B, WsHeader* hdr, cudaStream_t st) {
   SimtArgs a;
   a.map = RowMap{cache.page_table, cfg.page_size, cfg.max_pages_per_seq, cfg.rows_per_seq,
                  cache.n_physical_rows};
@@ -161,6 +166,7 @@ cudaError_t launch_attn_simt(const mla_config& cfg, const mla_cache& cache, cons
   a.q_abs = q_abs;
   a.part_o = part_o;
   a.part_lse = part_lse;
+  a.meta = meta;
   a.hdr = hdr;
   a.H = cfg.n_heads; a.C = cfg.kv_lora; a.R = cfg.qk_rope;
   a.hpb = plan.heads_per_cta;

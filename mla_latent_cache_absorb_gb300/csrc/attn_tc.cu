@@ -1,16 +1,623 @@
-// tcgen05 split attention (bf16 rows, tensor cores). Not built yet: the CUDA-core path runs.
+// Split attention over compressed bf16 cache rows on the 5th-generation tensor cores (tcgen05).
+//
+// turbospark-runtime 0.3.0, src/families/deepseek2/attn.rs, MQA attention over the compressed
+// rows (key = whole row [kv_lat ; k_pe], value = its first kv_lora elements, all heads read the
+// same rows); moeflux 0.1.0-pre.3, src/riir/attn/mla_attn_forward.rs, mla_sdpa_folded.
+//
+// Shape: rows of 576 = 512 latent + 64 rope, bf16. One CTA per SM streams 128-row tiles of the
+// cache through shared memory with TMA and computes, for 64 heads at once,
+//     S^T = K_tile . Q^T          (M = 128 rows, N = 64 heads, K = 576)    K-major operands
+//     O^T += V_tile^T . P^T       (M = 4 x 128 latent, N = 64 heads, K = 128 rows)  MN-major
+// with both accumulators in TMEM (S^T 2 x 64 columns, O^T 4 x 64 columns). The row tile is the
+// A operand of both products, so every staged row is shared by all 64 heads and read from
+// shared memory twice. The tile's nine 64-column blocks live in nine 16 KB slots; the rope slot
+// is reused for P^T once QK^T has read it, and each pair of latent slots is handed back to the
+// TMA producer as soon as its 128-column chunk of PV has completed, so the next tile streams in
+// while this one finishes.
+//
+// Softmax (four warps, one thread per tile row) runs in the log2 domain with a per-head running
+// maximum that is only raised when a score exceeds it by more than 2^8: the exact column max
+// (a cross-thread reduction) and the rescale of O^T in TMEM happen on the first tile of a
+// segment and on those rare tiles only. Each thread keeps per-head partial sums of p; they are
+// reduced once per segment.
+//
+// Work split: the tiles of all sequences form one list per 64-head group; CTA k of a group takes
+// the k-th equal share of it (crossing sequence boundaries), so every SM gets the same number of
+// tiles whatever the length mix. Each (CTA, sequence) piece writes a partial (O normalised, lse)
+// into slot k + b, and the combine stage merges the slots of a sequence.
+//
+// Roles: warp 0 issues TMA loads, warp 1 owns TMEM and issues the MMAs (one thread), warps 2-5
+// do the softmax and the epilogue. Every mbarrier wait is bounded; on a timeout the CTA records
+// MLA_ERR_TIMEOUT, every role stops, and TMEM is freed before exit.
 #include "common.cuh"
+#include "tc_ptx.cuh"
+
+#include <cudaTypedefs.h>
+#include <math_constants.h>
 
 namespace mla {
 
-bool attn_tc_supported(const mla_config& cfg) {
-  (void)cfg;
+namespace {
+
+constexpr int TC_HG = 64;          // heads per CTA (MMA N)
+constexpr int TC_TILE = 128;       // rows per tile (MMA M)
+constexpr int TC_KB = 9;           // 64-column blocks per row (576 / 64)
+constexpr int TC_LAT_KB = 8;       // latent blocks (512 / 64)
+constexpr int TC_SLOT_BYTES = TC_TILE * 128;   // 16 KB
+constexpr int TC_QBLK_BYTES = TC_HG * 128;     // 8 KB
+constexpr int TC_THREADS = 192;
+constexpr int TC_SMEM_DYN = TC_KB * TC_SLOT_BYTES + TC_KB * TC_QBLK_BYTES + 1024;
+constexpr uint32_t TC_TMEM_COLS = 512;
+constexpr uint32_t TC_O_COL = 0;       // O^T chunks at columns [0, 256)
+constexpr uint32_t TC_S_COL = 256;     // S^T buffers at [256, 320) and [320, 384)
+constexpr uint32_t WAIT_LIMIT = 1u << 21;
+constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: p may reach 2^8 before a rescale
+
+struct TcArgs {
+  RowMap map;
+  const int32_t* seq_lens;
+  float* part_o;          // [G][n_slots][64][C]
+  float* part_lse;        // [G][n_slots][64]
+  int32_t* meta;          // [B][2]: first slot, slot count
+  WsHeader* hdr;
+  int B, H, G, ncg, n_slots;
+  float scale_log2;
+};
+
+struct Smem {
+  uint64_t full[TC_KB], empty[TC_KB];
+  uint64_t q_full, q_empty;
+  uint64_t s_full[2], s_empty[2];
+  uint64_t p_full, o_done, o_empty, mma_fin;
+  uint32_t tmem_base;
+  int abort;
+  int seg_b0;
+  long long seg_p0;
+  int bad_page[2];        // per segment parity: the producer runs at most one segment ahead
+  float red[4][TC_HG];
+  float m2[TC_HG];        // running max per head, log2 units
+  float alpha[TC_HG];     // rescale factors (then 1/l in the epilogue)
+  long long scan[TC_THREADS];
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// OR of `v` over the 128 softmax threads (named barrier 1), returned to all of them.
+__device__ __forceinline__ bool softmax_vote_or(bool v) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, 1, 128, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(out)
+      : "r"((uint32_t)v)
+      : "memory");
+  return out != 0;
+}
+
+__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Tiles a sequence contributes (0 for an invalid length).
+__device__ __forceinline__ long long seq_tiles(const TcArgs& a, int b) {
+  const long long L = a.seq_lens[b];
+  if (L < 1 || L > a.map.capacity()) return 0;
+  return (L + TC_TILE - 1) / TC_TILE;
+}
+
+// Tile range [r0, r1) of CTA k among ncg CTAs sharing T tiles.
+__device__ __forceinline__ void cta_range(long long T, int k, int ncg, long long* r0, long long* r1) {
+  *r0 = (T * k) / ncg;
+  *r1 = (T * (k + 1)) / ncg;
+}
+
+// A bounded wait that also gives up once another role has aborted.
+__device__ __forceinline__ bool wait_bar(Smem& s, uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 63 && *reinterpret_cast<volatile int*>(&s.abort)) return false;
+  }
   return false;
 }
 
-cudaError_t launch_attn_tc(const mla_config&, const mla_cache&, const DecodePlan&, const int32_t*,
-                           const void*, float*, float*, int, WsHeader*, cudaStream_t) {
-  return cudaErrorNotSupported;
+// Softmax-side wait: one thread polls, then all 128 softmax threads agree on the outcome, so
+// they always leave (or stay in) their loops together and never strand a named barrier.
+__device__ __forceinline__ bool softmax_wait(Smem& s, uint64_t* bar, uint32_t parity, int sidx) {
+  bool ok = true;
+  if (sidx == 0) ok = wait_bar(s, bar, parity);
+  return !softmax_vote_or(!ok);
+}
+
+__device__ __forceinline__ void fail(Smem& s, WsHeader* hdr, int b) {
+  if (atomicExch(&s.abort, 1) == 0) set_error(hdr, MLA_ERR_TIMEOUT, b);
+}
+
+// Segment iterator: walks the (sequence, tile range) pieces of this CTA's share.
+struct SegIter {
+  int b;
+  long long p;      // first global tile of sequence b
+  long long r0, r1; // this CTA's range
+  __device__ bool next(const TcArgs& a, int* sb, int* t_lo, int* t_hi) {
+    while (b < a.B && p < r1) {
+      const long long n = seq_tiles(a, b);
+      const long long lo = max(r0, p), hi = min(r1, p + n);
+      const int cur = b;
+      const long long pb = p;
+      ++b;
+      p += n;
+      if (hi > lo) {
+        *sb = cur;
+        *t_lo = (int)(lo - pb);
+        *t_hi = (int)(hi - pb);
+        return true;
+      }
+    }
+    return false;
+  }
+};
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_constant__ CUtensorMap q_map,
+               TcArgs a) {
+  extern __shared__ uint8_t dyn_raw[];
+  __shared__ Smem s;
+  uint8_t* dyn = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* slots = dyn;                                 // 9 x 16 KB
+  uint8_t* qs = dyn + TC_KB * TC_SLOT_BYTES;            // 9 x 8 KB
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = blockIdx.x % a.G;
+  const int k = blockIdx.x / a.G;
+
+  // ---- every thread: total tile count (block scan over per-thread chunks of sequences) ----------
+  const int chunk = (a.B + TC_THREADS - 1) / TC_THREADS;
+  const int cb0 = min(a.B, tid * chunk), cb1 = min(a.B, cb0 + chunk);
+  long long mine = 0;
+  for (int b = cb0; b < cb1; ++b) mine += seq_tiles(a, b);
+  s.scan[tid] = mine;
+  if (tid == 0) {
+    s.abort = 0;
+    s.seg_b0 = a.B;
+    s.seg_p0 = 0;
+    s.bad_page[0] = 0;
+    s.bad_page[1] = 0;
+  }
+  __syncthreads();
+  long long before = 0, T = 0;
+  for (int i = 0; i < TC_THREADS; ++i) {   // 192 smem reads, broadcast
+    const long long v = s.scan[i];
+    if (i < tid) before += v;
+    T += v;
+  }
+  long long r0, r1;
+  cta_range(T, k, a.ncg, &r0, &r1);
+  // the thread whose chunk holds tile r0 finds the first sequence of this CTA's share
+  if (r0 < r1 && before <= r0 && r0 < before + mine) {
+    long long p = before;
+    for (int b = cb0; b < cb1; ++b) {
+      const long long n = seq_tiles(a, b);
+      if (r0 < p + n) {
+        s.seg_b0 = b;
+        s.seg_p0 = p;
+        break;
+      }
+      p += n;
+    }
+  }
+  // CTA 0 of group 0 publishes, per sequence, which partial slots the combine must merge
+  if (blockIdx.x == 0) {
+    long long p = before;
+    for (int b = cb0; b < cb1; ++b) {
+      const long long n = seq_tiles(a, b);
+      int first = 0, count = 0;
+      if (n > 0) {
+        // covering CTAs: smallest k with r1_k > p, largest k with r0_k < p + n
+        const long long kf = ((p + 1) * a.ncg + T - 1) / T - 1;
+        const long long kl = ((p + n) * a.ncg + T - 1) / T - 1;
+        first = (int)(kf + b);
+        count = (int)(kl - kf + 1);
+      } else {
+        set_error(a.hdr, MLA_ERR_BAD_SEQ_LEN, b);
+      }
+      a.meta[2 * b] = first;
+      a.meta[2 * b + 1] = count;
+      p += n;
+    }
+  }
+  if (r0 >= r1) return;   // uniform: no share for this CTA
+
+  if (tid == 0) {
+    for (int i = 0; i < TC_KB; ++i) {
+      tc::mbar_init(&s.full[i], 1);
+      tc::mbar_init(&s.empty[i], 1);
+    }
+    tc::mbar_init(&s.q_full, 1);
+    tc::mbar_init(&s.q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&s.s_full[i], 1);
+      tc::mbar_init(&s.s_empty[i], 128);
+    }
+    tc::mbar_init(&s.p_full, 128);
+    tc::mbar_init(&s.o_done, 1);
+    tc::mbar_init(&s.o_empty, 128);
+    tc::mbar_init(&s.mma_fin, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&s.tmem_base, TC_TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::tma_prefetch_desc(&rows_map);
+    tc::tma_prefetch_desc(&q_map);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+  SegIter it{s.seg_b0, s.seg_p0, r0, r1};
+
+  if (warp == 0) {
+    // ================================ TMA producer ================================
+    if (lane == 0) {
+      int sb = 0, tlo, thi;
+      int seg = 0;
+      long long n = 0;            // global tile counter of this CTA
+      long long last_n[TC_KB];    // last tile loaded into each slot (for the abort drain)
+      for (int kb = 0; kb < TC_KB; ++kb) last_n[kb] = -1;
+      int q_loaded = -1;
+      bool ok = true;
+      while (ok && it.next(a, &sb, &tlo, &thi)) {
+        if (seg > 0 && !wait_bar(s, &s.q_empty, (seg - 1) & 1)) { ok = false; break; }
+        tc::mbar_arrive_expect_tx(&s.q_full, TC_KB * TC_QBLK_BYTES);
+        const int qrow = sb * a.H + g * TC_HG;
+        for (int kb = 0; kb < TC_KB; ++kb) tc::tma_load_2d(qs + kb * TC_QBLK_BYTES, &q_map, kb * 64, qrow, &s.q_full);
+        q_loaded = seg;
+        const long long L = a.seq_lens[sb];
+        for (int t = tlo; t < thi && ok; ++t) {
+          const long long t0 = (long long)t * TC_TILE;
+          // physical first row of each 64-row half; halves past the sequence are skipped
+          int y[2];
+          uint32_t bytes = 0;
+          for (int j = 0; j < 2; ++j) {
+            const long long lt = t0 + 64 * j;
+            y[j] = -1;
+            if (lt < L) {
+              int64_t pr = a.map.phys(sb, lt);
+              if (pr < 0) {   // out-of-range page id: load a valid row, flag the segment
+                atomicExch(&s.bad_page[seg & 1], 1);
+                set_error(a.hdr, MLA_ERR_BAD_PAGE, sb);
+                pr = 0;
+              }
+              y[j] = (int)pr;
+              bytes += 64 * 128;
+            }
+          }
+          for (int i = 0; i < TC_KB; ++i) {
+            const int kb = (i < TC_LAT_KB) ? i : TC_LAT_KB;   // latent blocks first, rope last
+            if (n > 0 && !wait_bar(s, &s.empty[kb], (uint32_t)((n - 1) & 1))) { ok = false; break; }
+            tc::mbar_arrive_expect_tx(&s.full[kb], bytes);
+            for (int j = 0; j < 2; ++j)
+              if (y[j] >= 0)
+                tc::tma_load_2d(slots + kb * TC_SLOT_BYTES + j * 64 * 128, &rows_map, kb * 64, y[j], &s.full[kb]);
+            last_n[kb] = n;
+          }
+          if (ok) ++n;
+        }
+        if (ok) ++seg;
+      }
+      if (!ok) {
+        fail(s, a.hdr, sb);
+        // wait (bounded) for every copy already issued, so none lands after the CTA exits
+        for (int kb = 0; kb < TC_KB; ++kb)
+          if (last_n[kb] >= 0) tc::mbar_wait(&s.full[kb], (uint32_t)(last_n[kb] & 1), WAIT_LIMIT);
+        if (q_loaded >= 0) tc::mbar_wait(&s.q_full, (uint32_t)(q_loaded & 1), WAIT_LIMIT);
+      }
+    }
+  } else if (warp == 1) {
+    // ================================ MMA issuer ================================
+    if (lane == 0) {
+      const uint32_t idesc_qk = tc::idesc_bf16_f32(TC_TILE, TC_HG, 0, 0);
+      const uint32_t idesc_pv = tc::idesc_bf16_f32(128, TC_HG, 1, 1);
+      const uint32_t slot0 = tc::smem_u32(slots), q0 = tc::smem_u32(qs);
+      int sb = 0, tlo, thi;
+      int seg = 0;
+      long long n = 0;
+      bool ok = true;
+      while (ok && it.next(a, &sb, &tlo, &thi)) {
+        if (!wait_bar(s, &s.q_full, seg & 1)) { ok = false; break; }
+        tc::tc_fence_after();
+        for (int t = tlo; t < thi; ++t, ++n) {
+          const int sbuf = (int)(n & 1);
+          const uint32_t s_tmem = tmem + TC_S_COL + sbuf * TC_HG;
+          if (n >= 2 && !wait_bar(s, &s.s_empty[sbuf], (uint32_t)(((n >> 1) - 1) & 1))) { ok = false; break; }
+          tc::tc_fence_after();
+          for (int i = 0; i < TC_KB; ++i) {
+            const int kb = (i < TC_LAT_KB) ? i : TC_LAT_KB;
+            if (!wait_bar(s, &s.full[kb], (uint32_t)(n & 1))) { ok = false; break; }
+            tc::tc_fence_after();
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = tc::sdesc_sw128(slot0 + kb * TC_SLOT_BYTES + kk * 32, 16, 1024);
+              const uint64_t bd = tc::sdesc_sw128(q0 + kb * TC_QBLK_BYTES + kk * 32, 16, 1024);
+              tc::mma_f16_ss(s_tmem, ad, bd, idesc_qk, (i | kk) != 0);
+            }
+          }
+          if (!ok) break;
+          tc::mma_commit(&s.s_full[sbuf]);
+          if (t + 1 == thi) tc::mma_commit(&s.q_empty);
+          // PV needs P^T (slot 8) and, on a segment's first tile, the previous O^T read out
+          if (!wait_bar(s, &s.p_full, (uint32_t)(n & 1))) { ok = false; break; }
+          if (t == tlo && seg > 0 && !wait_bar(s, &s.o_empty, (uint32_t)((seg - 1) & 1))) { ok = false; break; }
+          tc::tc_fence_after();
+          const uint32_t p_addr = slot0 + TC_LAT_KB * TC_SLOT_BYTES;
+          for (int cc = 0; cc < 4; ++cc) {
+            const uint32_t a_base = slot0 + (2 * cc) * TC_SLOT_BYTES;
+            for (int j = 0; j < TC_TILE / 16; ++j) {
+              const uint64_t ad = tc::sdesc_sw128(a_base + j * 2048, TC_SLOT_BYTES, 1024);
+              const uint64_t bd = tc::sdesc_sw128(p_addr + j * 2048, TC_SLOT_BYTES, 1024);
+              tc::mma_f16_ss(tmem + TC_O_COL + cc * TC_HG, ad, bd, idesc_pv, !(t == tlo && j == 0));
+            }
+            tc::mma_commit(&s.empty[2 * cc]);
+            tc::mma_commit(&s.empty[2 * cc + 1]);
+          }
+          tc::mma_commit(&s.empty[TC_LAT_KB]);
+          tc::mma_commit(&s.o_done);
+        }
+        ++seg;
+      }
+      if (!ok) fail(s, a.hdr, sb);
+      // every MMA issued must finish before TMEM is released
+      tc::mma_commit(&s.mma_fin);
+      tc::mbar_wait(&s.mma_fin, 0, WAIT_LIMIT);
+    }
+  } else {
+    // ================================ softmax + epilogue ================================
+    const int q = warp & 3;                  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;           // tile row (and O^T latent row within a chunk)
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    const int sidx = tid - 64;               // 0..127
+    int sb = 0, tlo, thi;
+    int seg = 0;
+    long long n = 0;
+    bool ok = true;
+    float lp[TC_HG];                         // this row's share of each head's sum of p
+    uint8_t* prow = slots + TC_LAT_KB * TC_SLOT_BYTES;   // P^T lives in the rope slot
+    while (ok && it.next(a, &sb, &tlo, &thi)) {
+      const long long L = a.seq_lens[sb];
+#pragma unroll
+      for (int h = 0; h < TC_HG; ++h) lp[h] = 0.f;
+      if (sidx < TC_HG) s.m2[sidx] = -CUDART_INF_F;
+      for (int t = tlo; t < thi; ++t, ++n) {
+        const int sbuf = (int)(n & 1);
+        const uint32_t s_addr = tmem + lane_base + TC_S_COL + sbuf * TC_HG;
+        if (!softmax_wait(s, &s.s_full[sbuf], (uint32_t)((n >> 1) & 1), sidx)) { ok = false; break; }
+        tc::tc_fence_after();
+        const bool valid = (long long)t * TC_TILE + row < L;
+        const bool first = (t == tlo);
+        // PV of the previous tile has completed (its commit preceded this tile's QK commit);
+        // waiting keeps the o_done phases in step for every softmax thread
+        if (n > 0 && !softmax_wait(s, &s.o_done, (uint32_t)((n - 1) & 1), sidx)) { ok = false; break; }
+        tc::tc_fence_after();
+        // pass 1: does any score exceed its head's running max by more than the threshold?
+        bool need = first;
+        if (valid) {
+          for (int half = 0; half < 2; ++half) {
+            uint32_t r[32];
+            tc::tmem_ld32(s_addr + half * 32, r);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              need |= fmaf(__uint_as_float(r[j]), a.scale_log2, -s.m2[half * 32 + j]) > RESCALE_THRESHOLD;
+          }
+        }
+        if (softmax_vote_or(need)) {
+          // exact per-head maximum over the tile's valid rows; raise the running max
+          for (int half = 0; half < 2; ++half) {
+            uint32_t r[32];
+            tc::tmem_ld32(s_addr + half * 32, r);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              float v = valid ? __uint_as_float(r[j]) * a.scale_log2 : -CUDART_INF_F;
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+              if (lane == 0) s.red[q][half * 32 + j] = v;
+            }
+          }
+          softmax_bar();
+          if (sidx < TC_HG) {
+            const float mt = fmaxf(fmaxf(s.red[0][sidx], s.red[1][sidx]), fmaxf(s.red[2][sidx], s.red[3][sidx]));
+            const float mo = s.m2[sidx];
+            const float mn = fmaxf(mo, mt);
+            s.alpha[sidx] = first ? 0.f : ex2(mo - mn);
+            s.m2[sidx] = mn;
+          }
+          softmax_bar();
+#pragma unroll
+          for (int h = 0; h < TC_HG; ++h) lp[h] *= s.alpha[h];
+          if (!first) {
+            // rescale the four O^T chunks this thread's TMEM lane holds (PV of the previous
+            // tile has completed, see the o_done wait above)
+            for (int cc = 0; cc < 4; ++cc) {
+              for (int half = 0; half < 2; ++half) {
+                uint32_t r[32];
+                const uint32_t ta = tmem + lane_base + TC_O_COL + cc * TC_HG + half * 32;
+                tc::tmem_ld32(ta, r);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  r[j] = __float_as_uint(__uint_as_float(r[j]) * s.alpha[half * 32 + j]);
+                tc::tmem_st32(ta, r);
+              }
+            }
+            tc::tmem_wait_st();
+          }
+        }
+        // pass 2: probabilities, partial sums, and this row of P^T (MN-major, 128-byte swizzle)
+        // into the rope slot, which TMA (async proxy) wrote and QK^T has finished reading
+        tc::fence_proxy_async_smem();
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[32];
+          tc::tmem_ld32(s_addr + half * 32, r);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = c4 * 8 + 2 * e;
+              const int h = half * 32 + j;
+              float p0 = 0.f, p1 = 0.f;
+              if (valid) {
+                p0 = ex2(fmaf(__uint_as_float(r[j]), a.scale_log2, -s.m2[h]));
+                p1 = ex2(fmaf(__uint_as_float(r[j + 1]), a.scale_log2, -s.m2[h + 1]));
+              }
+              lp[h] += p0;
+              lp[h + 1] += p1;
+              w[e] = pack_bf16x2(p0, p1);
+            }
+            *reinterpret_cast<uint4*>(prow + tc::sw128_offset(row, half * 4 + c4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        // S^T of this tile is fully read: the MMA warp may reuse the buffer
+        tc::tc_fence_before();
+        tc::mbar_arrive(&s.s_empty[sbuf]);
+        if (!valid) {
+          // rows past the sequence: zero their latent so 0 * (stale or NaN) cannot reach O^T
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          for (int kb = 0; kb < TC_LAT_KB; ++kb)
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8)
+              *reinterpret_cast<uint4*>(slots + kb * TC_SLOT_BYTES + row * 128 + c8 * 16) = z;
+        }
+        tc::fence_proxy_async_smem();
+        tc::tc_fence_before();
+        tc::mbar_arrive(&s.p_full);
+      }
+      if (!ok) break;
+      // ---- epilogue of the segment: wait for its last PV, normalise, write the partial ----
+      if (!softmax_wait(s, &s.o_done, (uint32_t)((n - 1) & 1), sidx)) { ok = false; break; }
+      tc::tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < TC_HG; ++h) {
+        float v = lp[h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) s.red[q][h] = v;
+      }
+      softmax_bar();
+      const int slot = k + sb;
+      const int nh = min(TC_HG, a.H - g * TC_HG);
+      if (sidx < TC_HG) {
+        const float l = s.red[0][sidx] + s.red[1][sidx] + s.red[2][sidx] + s.red[3][sidx];
+        s.alpha[sidx] = 1.0f / l;
+        if (sidx < nh) {
+          const bool bad = *reinterpret_cast<volatile int*>(&s.bad_page[seg & 1]) != 0;
+          a.part_lse[(size_t)(g * a.n_slots + slot) * TC_HG + sidx] =
+              bad ? CUDART_NAN_F : (s.m2[sidx] + __log2f(l)) * 0.69314718055994530942f;
+        }
+      }
+      softmax_bar();
+      float* po = a.part_o + ((size_t)(g * a.n_slots + slot) * TC_HG) * 512;
+      for (int cc = 0; cc < 4; ++cc) {
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[32];
+          tc::tmem_ld32(tmem + lane_base + TC_O_COL + cc * TC_HG + half * 32, r);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int h = half * 32 + j;
+            if (h < nh) po[(size_t)h * 512 + cc * 128 + row] = __uint_as_float(r[j]) * s.alpha[h];
+          }
+        }
+      }
+      tc::tc_fence_before();
+      softmax_bar();   // s.red, s.alpha and s.m2 free; every thread has read bad_page
+      if (sidx == 0) s.bad_page[seg & 1] = 0;
+      tc::mbar_arrive(&s.o_empty);
+      ++seg;
+    }
+    if (!ok) fail(s, a.hdr, sb);
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, TC_TMEM_COLS);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2D bf16 map over `rows` rows of 576 elements, boxes of 64 columns x 64 rows, 128-byte swizzle.
+bool make_rows_map(CUtensorMap* m, const void* base, uint64_t rows) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {576, rows};
+  cuuint64_t strides[1] = {576 * 2};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool attn_tc_supported(const mla_config& cfg) {
+  return cfg.act_dtype == MLA_BF16 && cfg.kv_lora == 512 && cfg.qk_rope == 64 &&
+         (cfg.page_size == 0 || cfg.page_size % 64 == 0) && encode_fn() != nullptr;
+}
+
+int tc_heads_per_cta() { return TC_HG; }
+
+
+cudaError_t launch_attn_tc(const mla_config& cfg, const mla_cache& cache, const DecodePlan& plan,
+                           const int32_t* seq_lens, const void* q_abs, float* part_o, float* part_lse,
+                           int32_t* meta, int B, WsHeader* hdr, cudaStream_t st) {
+  if (cache.n_physical_rows >= (int64_t(1) << 31) || (int64_t)B * cfg.n_heads >= (int64_t(1) << 31))
+    return cudaErrorInvalidValue;
+  CUtensorMap rows_map, q_map;
+  if (!make_rows_map(&rows_map, cache.rows, (uint64_t)cache.n_physical_rows)) return cudaErrorInvalidValue;
+  if (!make_rows_map(&q_map, q_abs, (uint64_t)B * cfg.n_heads)) return cudaErrorInvalidValue;
+  TcArgs a;
+  a.map = RowMap{cache.page_table, cfg.page_size, cfg.max_pages_per_seq, cfg.rows_per_seq, cache.n_physical_rows};
+  a.seq_lens = seq_lens;
+  a.part_o = part_o;
+  a.part_lse = part_lse;
+  a.meta = meta;
+  a.hdr = hdr;
+  a.B = B;
+  a.H = cfg.n_heads;
+  a.G = plan.n_groups;
+  a.ncg = plan.ctas_per_group;
+  a.n_slots = plan.n_slots;
+  a.scale_log2 = cfg.softmax_scale * 1.4426950408889634f;
+  cudaError_t e = ensure_smem((const void*)attn_tc_kernel, TC_SMEM_DYN);
+  if (e != cudaSuccess) return e;
+  attn_tc_kernel<<<plan.n_groups * plan.ctas_per_group, TC_THREADS, TC_SMEM_DYN, st>>>(rows_map, q_map, a);
+  return cudaGetLastError();
 }
 
 }  // namespace mla

@@ -21,14 +21,14 @@ constexpr int CMB_BC = 16;      // sequences per CTA
 
 struct CombineArgs {
   const void* kv_b;
-  const int32_t* seq_lens;
-  const float* part_o;
-  const float* part_lse;
+  const int32_t* meta;      // [B][2]: first partial slot, slot count (0 = invalid sequence)
+  const float* part_o;      // [groups][n_slots][hpg][C]
+  const float* part_lse;    // [groups][n_slots][hpg]
   float* out;
   float* lse;
   int kv_b_dtype;
-  int H, C, N, V, S, B;
-  int64_t chunk, capacity;
+  int H, C, N, V, B;
+  int hpg, n_slots, max_slots;
 };
 
 __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
@@ -41,8 +41,13 @@ __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
   const int Cp = a.C + 1;                  // padded W row: conflict-free across j
   float* w_s = sm;                         // [CMB_VJ][C+1]
   float* vc_s = w_s + CMB_VJ * Cp;         // [CMB_BC][C]
-  float* wt_s = vc_s + CMB_BC * a.C;       // [CMB_BC][S] split weights
-  float* lse_s = wt_s + CMB_BC * a.S;      // [CMB_BC]
+  float* wt_s = vc_s + CMB_BC * a.C;       // [CMB_BC][max_slots] split weights
+  float* lse_s = wt_s + CMB_BC * a.max_slots;  // [CMB_BC]
+  int* first_s = reinterpret_cast<int*>(lse_s + CMB_BC);  // [CMB_BC]
+  int* cnt_s = first_s + CMB_BC;                           // [CMB_BC]
+  const int pg = h / a.hpg, hh = h % a.hpg;
+  // partial (slot, head) -> element offsets
+  auto lse_at = [&](int slot) { return ((int64_t)pg * a.n_slots + slot) * a.hpg + hh; };
 
   const int64_t wrow0 = (int64_t)h * (a.N + a.V) + a.N + j0;
   for (int i = threadIdx.x; i < CMB_VJ * a.C; i += CMB_THREADS) {
@@ -54,34 +59,31 @@ __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int bb = warp; bb < nb; bb += CMB_THREADS / 32) {
     const int b = b0 + bb;
-    const int64_t L = a.seq_lens[b];
-    const bool ok = (L >= 1 && L <= a.capacity);
-    const int ns = ok ? (int)((L + a.chunk - 1) / a.chunk) : 0;
+    const int first = a.meta[2 * b];
+    const int ns = min(a.meta[2 * b + 1], a.max_slots);
     float mx = -CUDART_INF_F;
-    for (int s = lane; s < ns; s += 32)
-      mx = fmaxf(mx, a.part_lse[((int64_t)b * a.S + s) * a.H + h]);
+    for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, a.part_lse[lse_at(first + s)]);
     mx = warp_max(mx);
     float tot = 0.f;
-    for (int s = lane; s < ns; s += 32)
-      tot += expf(a.part_lse[((int64_t)b * a.S + s) * a.H + h] - mx);
+    for (int s = lane; s < ns; s += 32) tot += expf(a.part_lse[lse_at(first + s)] - mx);
     tot = warp_sum(tot);
-    const float l = ok ? mx + logf(tot) : CUDART_NAN_F;
-    for (int s = lane; s < a.S; s += 32)
-      wt_s[bb * a.S + s] = (s < ns) ? expf(a.part_lse[((int64_t)b * a.S + s) * a.H + h] - l) : 0.f;
-    if (lane == 0) lse_s[bb] = l;
+    const float l = (ns > 0) ? mx + logf(tot) : CUDART_NAN_F;
+    for (int s = lane; s < ns; s += 32) wt_s[bb * a.max_slots + s] = expf(a.part_lse[lse_at(first + s)] - l);
+    if (lane == 0) {
+      lse_s[bb] = l;
+      first_s[bb] = first;
+      cnt_s[bb] = ns;
+    }
   }
   __syncthreads();
   for (int i = threadIdx.x; i < nb * a.C; i += CMB_THREADS) {
     const int bb = i / a.C, c = i % a.C;
-    const int b = b0 + bb;
     float v = 0.f;
     if (isnan(lse_s[bb])) {
       v = CUDART_NAN_F;
     } else {
-      const int64_t L = a.seq_lens[b];
-      const int ns = (int)((L + a.chunk - 1) / a.chunk);
-      for (int s = 0; s < ns; ++s)
-        v = fmaf(wt_s[bb * a.S + s], a.part_o[(((int64_t)b * a.S + s) * a.H + h) * a.C + c], v);
+      for (int s = 0; s < cnt_s[bb]; ++s)
+        v = fmaf(wt_s[bb * a.max_slots + s], a.part_o[lse_at(first_s[bb] + s) * a.C + c], v);
     }
     vc_s[bb * a.C + c] = v;
   }
@@ -101,17 +103,18 @@ __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
 }
 
 cudaError_t launch_combine(const mla_config& cfg, const DecodePlan& plan, const void* kv_b,
-                           const int32_t* seq_lens, const float* part_o, const float* part_lse,
-                           float* out, float* lse, int B, WsHeader* hdr, cudaStream_t st) {
-  (void)hdr;
+                           const int32_t* meta, const float* part_o, const float* part_lse,
+                           float* out, float* lse, int B, cudaStream_t st) {
   CombineArgs a;
-  a.kv_b = kv_b; a.seq_lens = seq_lens; a.part_o = part_o; a.part_lse = part_lse;
+  a.kv_b = kv_b; a.meta = meta; a.part_o = part_o; a.part_lse = part_lse;
   a.out = out; a.lse = lse; a.kv_b_dtype = cfg.kv_b_dtype;
-  a.H = cfg.n_heads; a.C = cfg.kv_lora; a.N = cfg.qk_nope; a.V = cfg.v_head;
-  a.S = plan.splits; a.B = B; a.chunk = plan.chunk_rows; a.capacity = plan.capacity;
+  a.H = cfg.n_heads; a.C = cfg.kv_lora; a.N = cfg.qk_nope; a.V = cfg.v_head; a.B = B;
+  a.hpg = plan.part_hpg; a.n_slots = plan.n_slots;
+  // most slots one sequence can span: splits (CUDA-core path) or CTAs per group (tensor path)
+  a.max_slots = plan.path == PATH_TC ? plan.ctas_per_group : plan.splits;
   dim3 grid(cfg.n_heads, (cfg.v_head + CMB_VJ - 1) / CMB_VJ, (B + CMB_BC - 1) / CMB_BC);
   const size_t smem = sizeof(float) * ((size_t)CMB_VJ * (cfg.kv_lora + 1) + (size_t)CMB_BC * cfg.kv_lora +
-                                       (size_t)CMB_BC * plan.splits + CMB_BC);
+                                       (size_t)CMB_BC * a.max_slots + 3 * CMB_BC);
   cudaError_t e = ensure_smem((const void*)combine_kernel, (int)smem);
   if (e != cudaSuccess) return e;
   combine_kernel<<<grid, CMB_THREADS, smem, st>>>(a);

@@ -101,10 +101,14 @@ struct DecodePlan {
   int path;              // PATH_SIMT or PATH_TC
   int heads_per_cta;     // heads sharing one staged row tile in one CTA
   int n_groups;          // ceil(H / heads_per_cta)
-  int splits;            // S: row splits per sequence (workspace slots)
-  int64_t chunk_rows;    // rows per split (a multiple of the row tile)
+  int splits;            // CUDA-core path: row splits per sequence
+  int64_t chunk_rows;    // CUDA-core path: rows per split (a multiple of its row tile)
   int64_t capacity;      // maximum rows a sequence can attend
-  size_t off_qabs, off_po, off_plse, total;
+  int ctas_per_group;    // tensor-core path: CTAs sharing one head group's tile list
+  // partials: part_o[g][slot][hh][C], part_lse[g][slot][hh] for part_groups x n_slots slots of
+  // part_hpg heads; meta[b] = {first slot, slot count} of sequence b (count 0: invalid length)
+  int part_groups, part_hpg, n_slots;
+  size_t off_qabs, off_po, off_plse, off_meta, total;
 };
 enum { PATH_SIMT = 0, PATH_TC = 1 };
 
@@ -122,13 +126,14 @@ cudaError_t launch_absorb(const mla_config& cfg, const void* q, const void* kv_b
                           const int32_t* positions, void* q_abs, int B, cudaStream_t st);
 cudaError_t launch_attn_simt(const mla_config& cfg, const mla_cache& cache, const DecodePlan& plan,
                              const int32_t* seq_lens, const void* q_abs, float* part_o,
-                             float* part_lse, int B, WsHeader* hdr, cudaStream_t st);
+                             float* part_lse, int32_t* meta, int B, WsHeader* hdr, cudaStream_t st);
 cudaError_t launch_attn_tc(const mla_config& cfg, const mla_cache& cache, const DecodePlan& plan,
                            const int32_t* seq_lens, const void* q_abs, float* part_o,
-                           float* part_lse, int B, WsHeader* hdr, cudaStream_t st);
+                           float* part_lse, int32_t* meta, int B, WsHeader* hdr, cudaStream_t st);
 bool attn_tc_supported(const mla_config& cfg);
+int tc_heads_per_cta();
 cudaError_t launch_combine(const mla_config& cfg, const DecodePlan& plan, const void* kv_b,
-                           const int32_t* seq_lens, const float* part_o, const float* part_lse,
-                           float* out, float* lse, int B, WsHeader* hdr, cudaStream_t st);
+                           const int32_t* meta, const float* part_o, const float* part_lse,
+                           float* out, float* lse, int B, cudaStream_t st);
 
 }  // namespace mla

@@ -76,37 +76,47 @@ static mla_status make_plan(const mla_config& cfg, int B, DecodePlan* p) {
   if (sms <= 0) return MLA_ERR_CUDA;
   std::memset(p, 0, sizeof(*p));
   p->capacity = cfg.page_size == 0 ? cfg.rows_per_seq : (int64_t)cfg.max_pages_per_seq * cfg.page_size;
-  int64_t tile;
-  int target;
   if (attn_tc_supported(cfg)) {
+    // tensor-core path: one CTA per SM, each head group's tile list split evenly over its CTAs
     p->path = PATH_TC;
-    p->heads_per_cta = cfg.n_heads <= 64 ? cfg.n_heads : 64;
-    tile = 128;
-    target = sms;
+    p->heads_per_cta = tc_heads_per_cta();
+    p->n_groups = (cfg.n_heads + p->heads_per_cta - 1) / p->heads_per_cta;
+    p->ctas_per_group = sms / p->n_groups > 0 ? sms / p->n_groups : 1;
+    p->splits = p->ctas_per_group;
+    p->chunk_rows = 0;
+    p->part_groups = p->n_groups;
+    p->part_hpg = p->heads_per_cta;
+    p->n_slots = p->ctas_per_group + B - 1;
   } else {
+    // CUDA-core path: grid (split, sequence, head group) with equal row splits
     p->path = PATH_SIMT;
     p->heads_per_cta = simt_heads_per_cta(cfg);
-    tile = 16;
-    target = 2 * sms;
+    p->n_groups = (cfg.n_heads + p->heads_per_cta - 1) / p->heads_per_cta;
+    const int64_t tile = 16;
+    const int64_t per_seq_ctas = (int64_t)B * p->n_groups;
+    int64_t want = (2 * sms + per_seq_ctas - 1) / per_seq_ctas;
+    if (want < 1) want = 1;
+    if (want > 64) want = 64;
+    int64_t chunk = (p->capacity + want - 1) / want;
+    chunk = ((chunk + tile - 1) / tile) * tile;
+    p->chunk_rows = chunk;
+    p->splits = (int)((p->capacity + chunk - 1) / chunk);
+    p->part_groups = 1;
+    p->part_hpg = cfg.n_heads;
+    p->n_slots = B * p->splits;
   }
-  p->n_groups = (cfg.n_heads + p->heads_per_cta - 1) / p->heads_per_cta;
-  const int64_t per_seq_ctas = (int64_t)B * p->n_groups;
-  int64_t want = (target + per_seq_ctas - 1) / per_seq_ctas;
-  if (want < 1) want = 1;
-  if (want > 64) want = 64;
-  int64_t chunk = (p->capacity + want - 1) / want;
-  chunk = ((chunk + tile - 1) / tile) * tile;
-  p->chunk_rows = chunk;
-  p->splits = (int)((p->capacity + chunk - 1) / chunk);
 
   const size_t row = (size_t)(cfg.kv_lora + cfg.qk_rope);
+  const size_t n_part = (size_t)p->part_groups * p->n_slots * p->part_hpg;
   size_t off = sizeof(WsHeader);
   p->off_qabs = off;
   off = align256(off + (size_t)B * cfg.n_heads * row * act_size(cfg.act_dtype));
   p->off_po = off;
-  off = align256(off + (size_t)B * p->splits * cfg.n_heads * cfg.kv_lora * sizeof(float));
+  off = align256(off + n_part * cfg.kv_lora * sizeof(float));
   p->off_plse = off;
-  off = align256(off + (size_t)B * p->splits * cfg.n_heads * sizeof(float));
+  off = align256(off + n_part * sizeof(float));
+  p->off_meta = off;
+  off = align256(off + (size_t)B * 2 * sizeof(int32_t));
   p->total = off;
   return MLA_OK;
 }
@@ -272,7 +282,7 @@ mla_status mla_decode_plan(const mla_config* cfg, int32_t B, mla_plan_info* info
   info->heads_per_cta = p.heads_per_cta;
   info->head_groups = p.n_groups;
   info->splits = p.splits;
-  info->rows_per_split = p.chunk_rows;
+  info->rows_per_split = p.chunk_rows;   // 0: tiles are balanced across CTAs instead
   info->capacity = p.capacity;
   return MLA_OK;
 }
@@ -344,10 +354,11 @@ mla_status mla_decode_partial(const mla_config* cfg, const mla_cache* cache, con
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   float* po = reinterpret_cast<float*>(ws + plan.off_po);
   float* pl = reinterpret_cast<float*>(ws + plan.off_plse);
+  int32_t* meta = reinterpret_cast<int32_t*>(ws + plan.off_meta);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (plan.path == PATH_TC)
-    return cuda_status(launch_attn_tc(*cfg, *cache, plan, seq_lens, ws + plan.off_qabs, po, pl, B, hdr, s));
-  return cuda_status(launch_attn_simt(*cfg, *cache, plan, seq_lens, ws + plan.off_qabs, po, pl, B, hdr, s));
+    return cuda_status(launch_attn_tc(*cfg, *cache, plan, seq_lens, ws + plan.off_qabs, po, pl, meta, B, hdr, s));
+  return cuda_status(launch_attn_simt(*cfg, *cache, plan, seq_lens, ws + plan.off_qabs, po, pl, meta, B, hdr, s));
 }
 
 mla_status mla_decode_combine(const mla_config* cfg, const void* kv_b, const int32_t* seq_lens,
@@ -356,12 +367,13 @@ mla_status mla_decode_combine(const mla_config* cfg, const void* kv_b, const int
   DecodePlan plan;
   mla_status st = decode_prologue(cfg, B, workspace, ws_bytes, &plan);
   if (st != MLA_OK) return st;
-  if (kv_b == nullptr || seq_lens == nullptr || out == nullptr) return MLA_ERR_INVALID_ARG;
+  if (kv_b == nullptr || out == nullptr) return MLA_ERR_INVALID_ARG;
+  (void)seq_lens;   // the partial stage recorded each sequence's slots (and validity) in meta
   char* ws = static_cast<char*>(workspace);
-  return cuda_status(launch_combine(*cfg, plan, kv_b, seq_lens,
+  return cuda_status(launch_combine(*cfg, plan, kv_b, reinterpret_cast<const int32_t*>(ws + plan.off_meta),
                                     reinterpret_cast<const float*>(ws + plan.off_po),
                                     reinterpret_cast<const float*>(ws + plan.off_plse), out, lse, B,
-                                    reinterpret_cast<WsHeader*>(ws), reinterpret_cast<cudaStream_t>(stream)));
+                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mla_status mla_decode_attn(const mla_config* cfg, const void* q, const void* kv_b, const mla_cache* cache,
