@@ -233,7 +233,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
       p += n;
     }
   }
-  if (r0 >= r1) return;   // uniform: no share for this CTA
+  if (r0 >= r1) {
+    // No share. If the empty range sits strictly inside a sequence, this CTA's slot lies in
+    // that sequence's slot interval: mark it empty (lse = -inf, weight 0 in the combine).
+    if (before <= r0 && r0 < before + mine) {
+      long long p = before;
+      for (int b = cb0; b < cb1; ++b) {
+        const long long n = seq_tiles(a, b);
+        if (r0 < p + n) {
+          if (p < r0) {
+            float* pl = a.part_lse + (size_t)(g * a.n_slots + k + b) * TC_HG;
+            for (int h = 0; h < TC_HG; ++h) pl[h] = -CUDART_INF_F;
+          }
+          break;
+        }
+        p += n;
+      }
+    }
+    return;   // uniform: every thread computed the same range
+  }
 
   if (tid == 0) {
     for (int i = 0; i < TC_KB; ++i) {
@@ -557,6 +575,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
   }
 }
 
+}  // namespace
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (fn == nullptr) {
@@ -570,20 +590,27 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+namespace {
+
 // 2D bf16 map over `rows` rows of 576 elements, boxes of 64 columns x 64 rows, 128-byte swizzle.
 bool make_rows_map(CUtensorMap* m, const void* base, uint64_t rows) {
+  return make_map_2d_bf16(m, base, 576, rows, 64, 64);
+}
+
+}  // namespace
+
+bool make_map_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                      uint32_t box_rows) {
   auto enc = encode_fn();
   if (enc == nullptr) return false;
-  cuuint64_t dims[2] = {576, rows};
-  cuuint64_t strides[1] = {576 * 2};
-  cuuint32_t box[2] = {64, 64};
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-}  // namespace
 
 bool attn_tc_supported(const mla_config& cfg) {
   return cfg.act_dtype == MLA_BF16 && cfg.kv_lora == 512 && cfg.qk_rope == 64 &&

@@ -82,8 +82,10 @@ __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
     if (isnan(lse_s[bb])) {
       v = CUDART_NAN_F;
     } else {
-      for (int s = 0; s < cnt_s[bb]; ++s)
-        v = fmaf(wt_s[bb * a.max_slots + s], a.part_o[lse_at(first_s[bb] + s) * a.C + c], v);
+      for (int s = 0; s < cnt_s[bb]; ++s) {
+        const float w = wt_s[bb * a.max_slots + s];
+        if (w != 0.f) v = fmaf(w, a.part_o[lse_at(first_s[bb] + s) * a.C + c], v);   // empty slots: skip
+      }
     }
     vc_s[bb * a.C + c] = v;
   }

@@ -1,6 +1,7 @@
 // Shared device helpers and the internal launch interface of libmla.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -86,14 +87,15 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// RoPE angle for pair i at position pos, reduced in float64 so that large positions keep
-// their accuracy; returns cos and sin as float.
+// RoPE angle for pair i at position pos. The angle pos * inv_freq[i] is formed in float64 and
+// reduced to [-pi, pi] there (a - 2*pi*round(a / 2*pi)), so positions in the hundreds of
+// thousands keep full accuracy; the reduced angle then goes to the float sincos.
 __device__ __forceinline__ void rope_cs(const double* inv_freq, int i, int pos, float* c, float* s) {
-  double a = static_cast<double>(pos) * inv_freq[i];
-  double sd, cd;
-  sincos(a, &sd, &cd);
-  *c = static_cast<float>(cd);
-  *s = static_cast<float>(sd);
+  const double two_pi = 6.283185307179586476925286766559;
+  const double a = static_cast<double>(pos) * inv_freq[i];
+  const double turns = rint(a * (1.0 / two_pi));
+  const float r = static_cast<float>(fma(-turns, two_pi, a));
+  sincosf(r, s, c);
 }
 
 // ---- decode plan: how the rows of a sequence are split, and the workspace layout -------------
@@ -111,6 +113,12 @@ struct DecodePlan {
   size_t off_qabs, off_po, off_plse, off_meta, total;
 };
 enum { PATH_SIMT = 0, PATH_TC = 1 };
+
+// 2D bf16 TMA map over a row-major [rows, inner] tensor (inner elements contiguous) with
+// boxes of box_inner x box_rows and the 128-byte swizzle. False when the driver entry point
+// is unavailable or the encoding is rejected.
+bool make_map_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                      uint32_t box_rows);
 
 // Raise a kernel's dynamic shared memory limit once per (kernel, device), so that repeated
 // launches (and launches under stream capture) make no attribute calls.
@@ -132,6 +140,13 @@ cudaError_t launch_attn_tc(const mla_config& cfg, const mla_cache& cache, const 
                            float* part_lse, int32_t* meta, int B, WsHeader* hdr, cudaStream_t st);
 bool attn_tc_supported(const mla_config& cfg);
 int tc_heads_per_cta();
+bool absorb_tc_supported(const mla_config& cfg, int B);
+bool combine_tc_supported(const mla_config& cfg, int B);
+cudaError_t launch_absorb_tc(const mla_config& cfg, const void* q, const void* kv_b, const int32_t* positions,
+                             void* q_abs, int B, WsHeader* hdr, cudaStream_t st);
+cudaError_t launch_combine_tc(const mla_config& cfg, const DecodePlan& plan, const void* kv_b,
+                              const int32_t* meta, const float* part_o, const float* part_lse, float* out,
+                              float* lse, int B, WsHeader* hdr, cudaStream_t st);
 cudaError_t launch_combine(const mla_config& cfg, const DecodePlan& plan, const void* kv_b,
                            const int32_t* meta, const float* part_o, const float* part_lse,
                            float* out, float* lse, int B, cudaStream_t st);

@@ -1,0 +1,354 @@
+// Tensor-core absorb and up-projection for bf16 kv_b with kv_lora 512 and nope / v_head 128.
+//
+// moeflux 0.1.0-pre.3, src/riir/attn/mla_attn_forward.rs, folded SDPA chain: q_prime (the nope
+// rows of kv_b, per head) and out_per_head (the v rows, skipping nope); turbospark-runtime 0.3.0,
+// src/families/deepseek2/attn.rs, absorb into fused [q' ; q_pe] rows and v-combine.
+//
+// Both stages are, per head, a GEMM whose cost is reading the head's 128 KB slice of kv_b once:
+//   absorb:  q'^T[c, b]  = W_UK,h^T[c, n] . q_nope^T[n, b]   (M = 2 x 128 latent, N = batch, K = 128)
+//   combine: out^T[j, b] = W_UV,h[j, c]   . vc^T[c, b]       (M = 128, N = batch, K = 512)
+// The weight slice arrives by TMA in the 128-byte swizzle layout and is the A operand (MN-major
+// for W_UK^T, K-major for W_UV); the batch is the N dimension (padded to 16), so one CTA per head
+// (and batch chunk) issues a handful of tcgen05 MMAs with the fp32 accumulator in TMEM.
+// The combine first merges the split partials into vc (float32) and feeds it as two bf16 terms
+// (hi + lo), so the up-projection keeps close to float32 accuracy on the bf16 tensor path.
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+#include <math_constants.h>
+
+namespace mla {
+
+namespace {
+
+constexpr int G_THREADS = 128;
+constexpr uint32_t G_WAIT = 1u << 21;
+constexpr int ABS_TC_BCHUNK = 64;
+constexpr int CMB_TC_BCHUNK = 32;
+constexpr int ABS_TC_SMEM = 4 * 16384 + 2 * 8192 + 1024;
+constexpr int CMB_TC_WSMEM = 8 * 16384 + 2 * 8 * 4096;   // W_UV + vc hi/lo
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float v) {
+  __nv_bfloat16 h = __float2bfloat16_rn(v);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+
+struct AbsorbTcArgs {
+  const uint16_t* q;        // [B][H][N+R] bf16
+  uint16_t* q_abs;          // [B][H][C+R] bf16
+  const int32_t* positions;
+  const double* inv_freq;
+  WsHeader* hdr;
+  int B, H, N, R, V, C;
+};
+
+// grid (H, 2 latent halves, batch chunks of 64); 128 threads
+__global__ void __launch_bounds__(G_THREADS, 1)
+absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
+  extern __shared__ uint8_t dyn_raw[];
+  __shared__ uint64_t bar_w, bar_mma;
+  __shared__ uint32_t tmem_base;
+  __shared__ int failed;
+  uint8_t* dyn = align1024(dyn_raw);
+  uint8_t* ws = dyn;                 // 4 blocks [128 n rows x 64 latent] (MN-major A)
+  uint8_t* qs = dyn + 4 * 16384;     // 2 blocks [64 b rows x 64 n] (K-major B)
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.x, lh = blockIdx.y, b0 = blockIdx.z * ABS_TC_BCHUNK;
+  const int nb = min(ABS_TC_BCHUNK, a.B - b0);
+  const int NB = (nb + 15) & ~15;
+  const int qrow = a.N + a.R, arow = a.C + a.R;
+
+  if (tid == 0) {
+    failed = 0;
+    tc::mbar_init(&bar_w, 1);
+    tc::mbar_init(&bar_mma, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(&tmem_base, 128);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  if (tid == 0) {
+    tc::mbar_arrive_expect_tx(&bar_w, 4 * 16384);
+    for (int cb = 0; cb < 4; ++cb)
+      tc::tma_load_2d(ws + cb * 16384, &w_map, 256 * lh + 64 * cb, h * (a.N + a.V), &bar_w);
+  }
+  // q_nope rows of this batch chunk, 128-byte swizzled, zero rows past the batch
+  for (int i = tid; i < ABS_TC_BCHUNK * 16; i += G_THREADS) {
+    const int r = i >> 4, ch = i & 15, kb = ch >> 3, c8 = ch & 7;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < nb) v = *reinterpret_cast<const uint4*>(a.q + ((size_t)(b0 + r) * a.H + h) * qrow + kb * 64 + c8 * 8);
+    *reinterpret_cast<uint4*>(qs + kb * 8192 + tc::sw128_offset(r, c8)) = v;
+  }
+  tc::fence_proxy_async_smem();
+  __syncthreads();
+  if (tid == 0) {
+    if (!tc::mbar_wait(&bar_w, 0, G_WAIT)) {
+      failed = 1;
+      set_error(a.hdr, MLA_ERR_TIMEOUT, b0);
+    } else {
+      tc::tc_fence_after();
+      const uint32_t idesc = tc::idesc_bf16_f32(128, NB, 1, 0);
+      const uint32_t w0 = tc::smem_u32(ws), q0 = tc::smem_u32(qs);
+      for (int mc = 0; mc < 2; ++mc)
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = tc::sdesc_sw128(w0 + (2 * mc) * 16384 + kk * 2048, 16384, 1024);
+          const uint64_t bd = tc::sdesc_sw128(q0 + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+          tc::mma_f16_ss(tmem + mc * 64, ad, bd, idesc, kk > 0);
+        }
+    }
+    tc::mma_commit(&bar_mma);   // arrives once every MMA issued above has completed
+  }
+  __syncwarp();
+  const bool ok = tc::mbar_wait(&bar_mma, 0, G_WAIT) && !*reinterpret_cast<volatile int*>(&failed);
+  tc::tc_fence_after();
+  if (ok) {
+    for (int mc = 0; mc < 2; ++mc) {
+      const int c = 256 * lh + 128 * mc + 32 * warp + lane;
+      for (int col0 = 0; col0 < NB; col0 += 32) {
+        uint32_t r[32];
+        tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + mc * 64 + col0, r);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int b = col0 + j;
+          if (b < nb) a.q_abs[((size_t)(b0 + b) * a.H + h) * arow + c] = bf16_bits(__uint_as_float(r[j]));
+        }
+      }
+    }
+  }
+  // rotated q_pe into the row's tail (once per head and batch chunk)
+  if (lh == 0) {
+    for (int i = tid; i < nb * (a.R / 2); i += G_THREADS) {
+      const int bb = i / (a.R / 2), p = i % (a.R / 2);
+      const size_t qi = ((size_t)(b0 + bb) * a.H + h) * qrow + a.N + 2 * p;
+      const size_t ai = ((size_t)(b0 + bb) * a.H + h) * arow + a.C + 2 * p;
+      const float x0 = bf16_bits_to_f32(a.q[qi]), x1 = bf16_bits_to_f32(a.q[qi + 1]);
+      float y0 = x0, y1 = x1;
+      if (a.positions != nullptr) {
+        float c, s;
+        rope_cs(a.inv_freq, p, a.positions[b0 + bb], &c, &s);
+        y0 = x0 * c - x1 * s;
+        y1 = x0 * s + x1 * c;
+      }
+      a.q_abs[ai] = bf16_bits(y0);
+      a.q_abs[ai + 1] = bf16_bits(y1);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 128);
+  }
+}
+
+struct CombineTcArgs {
+  const int32_t* meta;
+  const float* part_o;
+  const float* part_lse;
+  float* out;
+  float* lse;
+  WsHeader* hdr;
+  int H, C, N, V, B, hpg, n_slots, max_slots;
+};
+
+// grid (H, batch chunks of 32); 128 threads
+__global__ void __launch_bounds__(G_THREADS, 1)
+combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
+  extern __shared__ uint8_t dyn_raw[];
+  __shared__ uint64_t bar_w, bar_mma;
+  __shared__ uint32_t tmem_base;
+  __shared__ int failed;
+  __shared__ float lse_s[CMB_TC_BCHUNK];
+  __shared__ int first_s[CMB_TC_BCHUNK], cnt_s[CMB_TC_BCHUNK];
+  uint8_t* dyn = align1024(dyn_raw);
+  uint8_t* wu = dyn;                           // 8 blocks [128 j rows x 64 c] (K-major A)
+  uint8_t* vh = dyn + 8 * 16384;               // 8 blocks [32 b rows x 64 c] (K-major B), hi
+  uint8_t* vl = vh + 8 * 4096;                 // same, lo
+  float* wt_s = reinterpret_cast<float*>(vl + 8 * 4096);   // [32][max_slots]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.x, b0 = blockIdx.y * CMB_TC_BCHUNK;
+  const int nb = min(CMB_TC_BCHUNK, a.B - b0);
+  const int NB = (nb + 15) & ~15;
+  const int pg = h / a.hpg, hh = h % a.hpg;
+  auto lse_at = [&](int slot) { return ((int64_t)pg * a.n_slots + slot) * a.hpg + hh; };
+
+  if (tid == 0) {
+    failed = 0;
+    tc::mbar_init(&bar_w, 1);
+    tc::mbar_init(&bar_mma, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(&tmem_base, 32);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  if (tid == 0) {
+    tc::mbar_arrive_expect_tx(&bar_w, 8 * 16384);
+    for (int kb = 0; kb < 8; ++kb)
+      tc::tma_load_2d(wu + kb * 16384, &w_map, 64 * kb, h * (a.N + a.V) + a.N, &bar_w);
+  }
+  // split weights, one warp per sequence
+  for (int bb = warp; bb < CMB_TC_BCHUNK; bb += G_THREADS / 32) {
+    int first = 0, ns = 0;
+    if (bb < nb) {
+      first = a.meta[2 * (b0 + bb)];
+      ns = min(a.meta[2 * (b0 + bb) + 1], a.max_slots);
+    }
+    float mx = -CUDART_INF_F;
+    for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, a.part_lse[lse_at(first + s)]);
+    mx = warp_max(mx);
+    float tot = 0.f;
+    for (int s = lane; s < ns; s += 32) tot += expf(a.part_lse[lse_at(first + s)] - mx);
+    tot = warp_sum(tot);
+    const float l = (ns > 0) ? mx + logf(tot) : CUDART_NAN_F;
+    for (int s = lane; s < ns; s += 32) wt_s[bb * a.max_slots + s] = expf(a.part_lse[lse_at(first + s)] - l);
+    if (lane == 0) {
+      lse_s[bb] = l;
+      first_s[bb] = first;
+      cnt_s[bb] = ns;
+    }
+  }
+  __syncthreads();
+  // vc = sum_s w_s O_s as bf16 hi + lo, 8 latent columns per item, 128-byte swizzled
+  for (int i = tid; i < CMB_TC_BCHUNK * 64; i += G_THREADS) {
+    const int bb = i >> 6, ch = i & 63, kb = ch >> 3, c8 = ch & 7;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    if (bb < nb) {
+      if (isnan(lse_s[bb])) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = CUDART_NAN_F;
+      } else {
+        for (int s = 0; s < cnt_s[bb]; ++s) {
+          const float w = wt_s[bb * a.max_slots + s];
+          if (w == 0.f) continue;   // empty slot
+          const float4* src = reinterpret_cast<const float4*>(a.part_o + lse_at(first_s[bb] + s) * a.C + ch * 8);
+          const float4 u = src[0], v = src[1];
+          acc[0] = fmaf(w, u.x, acc[0]); acc[1] = fmaf(w, u.y, acc[1]);
+          acc[2] = fmaf(w, u.z, acc[2]); acc[3] = fmaf(w, u.w, acc[3]);
+          acc[4] = fmaf(w, v.x, acc[4]); acc[5] = fmaf(w, v.y, acc[5]);
+          acc[6] = fmaf(w, v.z, acc[6]); acc[7] = fmaf(w, v.w, acc[7]);
+        }
+      }
+    }
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint16_t h0 = bf16_bits(acc[2 * e]), h1 = bf16_bits(acc[2 * e + 1]);
+      const uint16_t l0 = bf16_bits(acc[2 * e] - bf16_bits_to_f32(h0));
+      const uint16_t l1 = bf16_bits(acc[2 * e + 1] - bf16_bits_to_f32(h1));
+      hi[e] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+      lo[e] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+    }
+    *reinterpret_cast<uint4*>(vh + kb * 4096 + tc::sw128_offset(bb, c8)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(vl + kb * 4096 + tc::sw128_offset(bb, c8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  }
+  tc::fence_proxy_async_smem();
+  __syncthreads();
+  if (tid == 0) {
+    if (!tc::mbar_wait(&bar_w, 0, G_WAIT)) {
+      failed = 1;
+      set_error(a.hdr, MLA_ERR_TIMEOUT, b0);
+    } else {
+      tc::tc_fence_after();
+      const uint32_t idesc = tc::idesc_bf16_f32(128, NB, 0, 0);
+      const uint32_t w0 = tc::smem_u32(wu), h0 = tc::smem_u32(vh), l0 = tc::smem_u32(vl);
+      for (int kb = 0; kb < 8; ++kb)
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t ad = tc::sdesc_sw128(w0 + kb * 16384 + kk * 32, 16, 1024);
+          tc::mma_f16_ss(tmem, ad, tc::sdesc_sw128(h0 + kb * 4096 + kk * 32, 16, 1024), idesc, (kb | kk) != 0);
+          tc::mma_f16_ss(tmem, ad, tc::sdesc_sw128(l0 + kb * 4096 + kk * 32, 16, 1024), idesc, 1);
+        }
+    }
+    tc::mma_commit(&bar_mma);
+  }
+  __syncwarp();
+  const bool ok = tc::mbar_wait(&bar_mma, 0, G_WAIT) && !*reinterpret_cast<volatile int*>(&failed);
+  tc::tc_fence_after();
+  if (ok) {
+    uint32_t r[32];
+    tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16), r);
+    tc::tmem_wait_ld();
+    const int j = 32 * warp + lane;
+#pragma unroll
+    for (int b = 0; b < 32; ++b)
+      if (b < nb) a.out[((size_t)(b0 + b) * a.H + h) * a.V + j] = __uint_as_float(r[b]);
+  }
+  if (a.lse != nullptr)
+    for (int bb = tid; bb < nb; bb += G_THREADS) a.lse[(size_t)(b0 + bb) * a.H + h] = lse_s[bb];
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 32);
+  }
+}
+
+}  // namespace
+
+// The tensor-core absorb / combine take bf16 kv_b with kv_lora 512 and 128-row W_UK / W_UV
+// blocks, and batches large enough to fill an MMA's N dimension.
+bool absorb_tc_supported(const mla_config& cfg, int B) {
+  return cfg.act_dtype == MLA_BF16 && cfg.kv_b_dtype == MLA_BF16 && cfg.kv_lora == 512 && cfg.qk_nope == 128 &&
+         B >= 8 && (int64_t)cfg.n_heads * (cfg.qk_nope + cfg.v_head) < (int64_t(1) << 31);
+}
+
+bool combine_tc_supported(const mla_config& cfg, int B) {
+  return cfg.kv_b_dtype == MLA_BF16 && cfg.kv_lora == 512 && cfg.v_head == 128 && B >= 8 &&
+         (int64_t)cfg.n_heads * (cfg.qk_nope + cfg.v_head) < (int64_t(1) << 31);
+}
+
+cudaError_t launch_absorb_tc(const mla_config& cfg, const void* q, const void* kv_b, const int32_t* positions,
+                             void* q_abs, int B, WsHeader* hdr, cudaStream_t st) {
+  CUtensorMap w_map;
+  if (!make_map_2d_bf16(&w_map, kv_b, 512, (uint64_t)cfg.n_heads * (cfg.qk_nope + cfg.v_head), 64, 128))
+    return cudaErrorInvalidValue;
+  AbsorbTcArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.q_abs = static_cast<uint16_t*>(q_abs);
+  a.positions = positions;
+  a.inv_freq = cfg.rope_inv_freq;
+  a.hdr = hdr;
+  a.B = B; a.H = cfg.n_heads; a.N = cfg.qk_nope; a.R = cfg.qk_rope; a.V = cfg.v_head; a.C = cfg.kv_lora;
+  cudaError_t e = ensure_smem((const void*)absorb_tc_kernel, ABS_TC_SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid(cfg.n_heads, 2, (B + ABS_TC_BCHUNK - 1) / ABS_TC_BCHUNK);
+  absorb_tc_kernel<<<grid, G_THREADS, ABS_TC_SMEM, st>>>(w_map, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_tc(const mla_config& cfg, const DecodePlan& plan, const void* kv_b,
+                              const int32_t* meta, const float* part_o, const float* part_lse, float* out,
+                              float* lse, int B, WsHeader* hdr, cudaStream_t st) {
+  CUtensorMap w_map;
+  if (!make_map_2d_bf16(&w_map, kv_b, 512, (uint64_t)cfg.n_heads * (cfg.qk_nope + cfg.v_head), 64, 128))
+    return cudaErrorInvalidValue;
+  CombineTcArgs a;
+  a.meta = meta; a.part_o = part_o; a.part_lse = part_lse; a.out = out; a.lse = lse; a.hdr = hdr;
+  a.H = cfg.n_heads; a.C = cfg.kv_lora; a.N = cfg.qk_nope; a.V = cfg.v_head; a.B = B;
+  a.hpg = plan.part_hpg; a.n_slots = plan.n_slots;
+  a.max_slots = plan.path == PATH_TC ? plan.ctas_per_group : plan.splits;
+  const int smem = CMB_TC_WSMEM + 1024 + CMB_TC_BCHUNK * a.max_slots * (int)sizeof(float);
+  cudaError_t e = ensure_smem((const void*)combine_tc_kernel, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(cfg.n_heads, (B + CMB_TC_BCHUNK - 1) / CMB_TC_BCHUNK);
+  combine_tc_kernel<<<grid, G_THREADS, smem, st>>>(w_map, a);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

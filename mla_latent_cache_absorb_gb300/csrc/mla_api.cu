@@ -82,6 +82,9 @@ static mla_status make_plan(const mla_config& cfg, int B, DecodePlan* p) {
     p->heads_per_cta = tc_heads_per_cta();
     p->n_groups = (cfg.n_heads + p->heads_per_cta - 1) / p->heads_per_cta;
     p->ctas_per_group = sms / p->n_groups > 0 ? sms / p->n_groups : 1;
+    // never more CTAs than the batch can have 128-row tiles
+    const int64_t max_tiles = (int64_t)B * ((p->capacity + 127) / 128);
+    if (max_tiles < p->ctas_per_group) p->ctas_per_group = (int)max_tiles;
     p->splits = p->ctas_per_group;
     p->chunk_rows = 0;
     p->part_groups = p->n_groups;
@@ -337,9 +340,12 @@ mla_status mla_decode_absorb(const mla_config* cfg, const void* q, const void* k
   if (st != MLA_OK) return st;
   if (q == nullptr || kv_b == nullptr) return MLA_ERR_INVALID_ARG;
   if (positions != nullptr && cfg->rope_inv_freq == nullptr) return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv_b, 16)) return MLA_ERR_INVALID_ARG;
   void* q_abs = static_cast<char*>(workspace) + plan.off_qabs;
-  return cuda_status(launch_absorb(*cfg, q, kv_b, positions, q_abs, B,
-                                   reinterpret_cast<cudaStream_t>(stream)));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (absorb_tc_supported(*cfg, B))
+    return cuda_status(launch_absorb_tc(*cfg, q, kv_b, positions, q_abs, B, static_cast<WsHeader*>(workspace), s));
+  return cuda_status(launch_absorb(*cfg, q, kv_b, positions, q_abs, B, s));
 }
 
 mla_status mla_decode_partial(const mla_config* cfg, const mla_cache* cache, const int32_t* seq_lens,
@@ -369,11 +375,16 @@ mla_status mla_decode_combine(const mla_config* cfg, const void* kv_b, const int
   if (st != MLA_OK) return st;
   if (kv_b == nullptr || out == nullptr) return MLA_ERR_INVALID_ARG;
   (void)seq_lens;   // the partial stage recorded each sequence's slots (and validity) in meta
+  if (!aligned(kv_b, 16)) return MLA_ERR_INVALID_ARG;
   char* ws = static_cast<char*>(workspace);
-  return cuda_status(launch_combine(*cfg, plan, kv_b, reinterpret_cast<const int32_t*>(ws + plan.off_meta),
-                                    reinterpret_cast<const float*>(ws + plan.off_po),
-                                    reinterpret_cast<const float*>(ws + plan.off_plse), out, lse, B,
-                                    reinterpret_cast<cudaStream_t>(stream)));
+  const int32_t* meta = reinterpret_cast<const int32_t*>(ws + plan.off_meta);
+  const float* po = reinterpret_cast<const float*>(ws + plan.off_po);
+  const float* pl = reinterpret_cast<const float*>(ws + plan.off_plse);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (combine_tc_supported(*cfg, B))
+    return cuda_status(launch_combine_tc(*cfg, plan, kv_b, meta, po, pl, out, lse, B,
+                                         reinterpret_cast<WsHeader*>(ws), s));
+  return cuda_status(launch_combine(*cfg, plan, kv_b, meta, po, pl, out, lse, B, s));
 }
 
 mla_status mla_decode_attn(const mla_config* cfg, const void* q, const void* kv_b, const mla_cache* cache,
@@ -385,6 +396,7 @@ mla_status mla_decode_attn(const mla_config* cfg, const void* q, const void* kv_
   if (st != MLA_OK) return st;
   if (q == nullptr || kv_b == nullptr || seq_lens == nullptr || out == nullptr) return MLA_ERR_INVALID_ARG;
   if (positions != nullptr && cfg->rope_inv_freq == nullptr) return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv_b, 16)) return MLA_ERR_INVALID_ARG;
   st = check_cache(cfg, cache, B);
   if (st != MLA_OK) return st;
   st = mla_decode_absorb(cfg, q, kv_b, positions, B, workspace, ws_bytes, stream);
