@@ -39,18 +39,31 @@ namespace mla {
 
 namespace {
 
-constexpr int TC_HG = 64;          // heads per CTA (MMA N)
 constexpr int TC_TILE = 128;       // rows per tile (MMA M)
 constexpr int TC_KB = 9;           // 64-column blocks per row (576 / 64)
 constexpr int TC_LAT_KB = 8;       // latent blocks (512 / 64)
 constexpr int TC_SLOT_BYTES = TC_TILE * 128;   // 16 KB
-constexpr int TC_QBLK_BYTES = TC_HG * 128;     // 8 KB
 constexpr int TC_THREADS = 192;
-constexpr int TC_SMEM_DYN = TC_KB * TC_SLOT_BYTES + TC_KB * TC_QBLK_BYTES + 1024;
-constexpr uint32_t TC_TMEM_COLS = 512;
-constexpr uint32_t TC_O_COL = 0;       // O^T chunks at columns [0, 256)
-constexpr uint32_t TC_S_COL = 256;     // S^T buffers at [256, 320) and [320, 384)
 constexpr uint32_t WAIT_LIMIT = 1u << 21;
+
+// Per head-group width HG (the MMA N: 16, 32 or 64 heads per CTA).
+template <int HG>
+struct Cfg {
+  static constexpr int QBLK_BYTES = HG * 128;                 // one 64-column block of Q
+  static constexpr int SMEM_DYN = TC_KB * TC_SLOT_BYTES + TC_KB * QBLK_BYTES + 1024;
+  static constexpr uint32_t O_COL = 0;                        // O^T chunks: 4 x HG columns
+  static constexpr uint32_t S_COL = 4 * HG;                   // S^T buffers: 2 x HG columns
+  static constexpr uint32_t TMEM_COLS = HG == 64 ? 512 : (HG == 32 ? 256 : 128);
+  static constexpr int P_ROW = 2 * HG;                        // bytes of one P^T row (bf16)
+  // P^T is MN-major with rows of P_ROW bytes: 128-, 64- or 32-byte swizzle
+  static constexpr uint32_t P_LAYOUT = HG == 64 ? 2u : (HG == 32 ? 4u : 6u);
+  static __device__ __forceinline__ uint32_t p_offset(uint32_t row, uint32_t chunk) {
+    if (HG == 64) return row * 128u + ((chunk ^ (row & 7u)) << 4);
+    if (HG == 32) return row * 64u + ((chunk ^ ((row >> 1) & 3u)) << 4);
+    return row * 32u + ((chunk ^ ((row >> 2) & 1u)) << 4);
+  }
+};
+constexpr int TC_HG_MAX = 64;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: p may reach 2^8 before a rescale
 
 struct TcArgs {
@@ -65,6 +78,7 @@ struct TcArgs {
 };
 
 struct Smem {
+  static constexpr int TC_HG = TC_HG_MAX;   // arrays sized for the widest group
   uint64_t full[TC_KB], empty[TC_KB];
   uint64_t q_full, q_empty;
   uint64_t s_full[2], s_empty[2];
@@ -166,6 +180,7 @@ struct SegIter {
   }
 };
 
+template <int HG>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_constant__ CUtensorMap q_map,
                TcArgs a) {
@@ -242,8 +257,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
         const long long n = seq_tiles(a, b);
         if (r0 < p + n) {
           if (p < r0) {
-            float* pl = a.part_lse + (size_t)(g * a.n_slots + k + b) * TC_HG;
-            for (int h = 0; h < TC_HG; ++h) pl[h] = -CUDART_INF_F;
+            float* pl = a.part_lse + (size_t)(g * a.n_slots + k + b) * HG;
+            for (int h = 0; h < HG; ++h) pl[h] = -CUDART_INF_F;
           }
           break;
         }
@@ -271,7 +286,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
     tc::fence_mbar_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(&s.tmem_base, TC_TMEM_COLS);
+    tc::tmem_alloc(&s.tmem_base, Cfg<HG>::TMEM_COLS);
     tc::tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
@@ -296,9 +311,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
       bool ok = true;
       while (ok && it.next(a, &sb, &tlo, &thi)) {
         if (seg > 0 && !wait_bar(s, &s.q_empty, (seg - 1) & 1)) { ok = false; break; }
-        tc::mbar_arrive_expect_tx(&s.q_full, TC_KB * TC_QBLK_BYTES);
-        const int qrow = sb * a.H + g * TC_HG;
-        for (int kb = 0; kb < TC_KB; ++kb) tc::tma_load_2d(qs + kb * TC_QBLK_BYTES, &q_map, kb * 64, qrow, &s.q_full);
+        tc::mbar_arrive_expect_tx(&s.q_full, TC_KB * Cfg<HG>::QBLK_BYTES);
+        const int qrow = sb * a.H + g * HG;
+        for (int kb = 0; kb < TC_KB; ++kb) tc::tma_load_2d(qs + kb * Cfg<HG>::QBLK_BYTES, &q_map, kb * 64, qrow, &s.q_full);
         q_loaded = seg;
         const long long L = a.seq_lens[sb];
         for (int t = tlo; t < thi && ok; ++t) {
@@ -344,8 +359,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
   } else if (warp == 1) {
     // ================================ MMA issuer ================================
     if (lane == 0) {
-      const uint32_t idesc_qk = tc::idesc_bf16_f32(TC_TILE, TC_HG, 0, 0);
-      const uint32_t idesc_pv = tc::idesc_bf16_f32(128, TC_HG, 1, 1);
+      const uint32_t idesc_qk = tc::idesc_bf16_f32(TC_TILE, HG, 0, 0);
+      const uint32_t idesc_pv = tc::idesc_bf16_f32(128, HG, 1, 1);
       const uint32_t slot0 = tc::smem_u32(slots), q0 = tc::smem_u32(qs);
       int sb = 0, tlo, thi;
       int seg = 0;
@@ -356,7 +371,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
         tc::tc_fence_after();
         for (int t = tlo; t < thi; ++t, ++n) {
           const int sbuf = (int)(n & 1);
-          const uint32_t s_tmem = tmem + TC_S_COL + sbuf * TC_HG;
+          const uint32_t s_tmem = tmem + Cfg<HG>::S_COL + sbuf * HG;
           if (n >= 2 && !wait_bar(s, &s.s_empty[sbuf], (uint32_t)(((n >> 1) - 1) & 1))) { ok = false; break; }
           tc::tc_fence_after();
           for (int i = 0; i < TC_KB; ++i) {
@@ -365,7 +380,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
             tc::tc_fence_after();
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t ad = tc::sdesc_sw128(slot0 + kb * TC_SLOT_BYTES + kk * 32, 16, 1024);
-              const uint64_t bd = tc::sdesc_sw128(q0 + kb * TC_QBLK_BYTES + kk * 32, 16, 1024);
+              const uint64_t bd = tc::sdesc_sw128(q0 + kb * Cfg<HG>::QBLK_BYTES + kk * 32, 16, 1024);
               tc::mma_f16_ss(s_tmem, ad, bd, idesc_qk, (i | kk) != 0);
             }
           }
@@ -381,8 +396,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
             const uint32_t a_base = slot0 + (2 * cc) * TC_SLOT_BYTES;
             for (int j = 0; j < TC_TILE / 16; ++j) {
               const uint64_t ad = tc::sdesc_sw128(a_base + j * 2048, TC_SLOT_BYTES, 1024);
-              const uint64_t bd = tc::sdesc_sw128(p_addr + j * 2048, TC_SLOT_BYTES, 1024);
-              tc::mma_f16_ss(tmem + TC_O_COL + cc * TC_HG, ad, bd, idesc_pv, !(t == tlo && j == 0));
+              const uint64_t bd = tc::sdesc(p_addr + j * 16 * Cfg<HG>::P_ROW, TC_SLOT_BYTES, 8 * Cfg<HG>::P_ROW,
+                                            Cfg<HG>::P_LAYOUT);
+              tc::mma_f16_ss(tmem + Cfg<HG>::O_COL + cc * HG, ad, bd, idesc_pv, !(t == tlo && j == 0));
             }
             tc::mma_commit(&s.empty[2 * cc]);
             tc::mma_commit(&s.empty[2 * cc + 1]);
@@ -407,16 +423,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
     int seg = 0;
     long long n = 0;
     bool ok = true;
-    float lp[TC_HG];                         // this row's share of each head's sum of p
+    constexpr int CW = HG < 32 ? HG : 32;    // TMEM columns per load
+    constexpr int NCH = HG / CW;
+    float lp[HG];                            // this row's share of each head's sum of p
     uint8_t* prow = slots + TC_LAT_KB * TC_SLOT_BYTES;   // P^T lives in the rope slot
     while (ok && it.next(a, &sb, &tlo, &thi)) {
       const long long L = a.seq_lens[sb];
 #pragma unroll
-      for (int h = 0; h < TC_HG; ++h) lp[h] = 0.f;
-      if (sidx < TC_HG) s.m2[sidx] = -CUDART_INF_F;
+      for (int h = 0; h < HG; ++h) lp[h] = 0.f;
+      if (sidx < HG) s.m2[sidx] = -CUDART_INF_F;
       for (int t = tlo; t < thi; ++t, ++n) {
         const int sbuf = (int)(n & 1);
-        const uint32_t s_addr = tmem + lane_base + TC_S_COL + sbuf * TC_HG;
+        const uint32_t s_addr = tmem + lane_base + Cfg<HG>::S_COL + sbuf * HG;
         if (!softmax_wait(s, &s.s_full[sbuf], (uint32_t)((n >> 1) & 1), sidx)) { ok = false; break; }
         tc::tc_fence_after();
         const bool valid = (long long)t * TC_TILE + row < L;
@@ -428,31 +446,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
         // pass 1: does any score exceed its head's running max by more than the threshold?
         bool need = first;
         if (valid) {
-          for (int half = 0; half < 2; ++half) {
-            uint32_t r[32];
-            tc::tmem_ld32(s_addr + half * 32, r);
+          for (int half = 0; half < NCH; ++half) {
+            uint32_t r[CW];
+            tc::tmem_ld<CW>(s_addr + half * CW, r);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              need |= fmaf(__uint_as_float(r[j]), a.scale_log2, -s.m2[half * 32 + j]) > RESCALE_THRESHOLD;
+            for (int j = 0; j < CW; ++j)
+              need |= fmaf(__uint_as_float(r[j]), a.scale_log2, -s.m2[half * CW + j]) > RESCALE_THRESHOLD;
           }
         }
         if (softmax_vote_or(need)) {
           // exact per-head maximum over the tile's valid rows; raise the running max
-          for (int half = 0; half < 2; ++half) {
-            uint32_t r[32];
-            tc::tmem_ld32(s_addr + half * 32, r);
+          for (int half = 0; half < NCH; ++half) {
+            uint32_t r[CW];
+            tc::tmem_ld<CW>(s_addr + half * CW, r);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < CW; ++j) {
               float v = valid ? __uint_as_float(r[j]) * a.scale_log2 : -CUDART_INF_F;
 #pragma unroll
               for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-              if (lane == 0) s.red[q][half * 32 + j] = v;
+              if (lane == 0) s.red[q][half * CW + j] = v;
             }
           }
           softmax_bar();
-          if (sidx < TC_HG) {
+          if (sidx < HG) {
             const float mt = fmaxf(fmaxf(s.red[0][sidx], s.red[1][sidx]), fmaxf(s.red[2][sidx], s.red[3][sidx]));
             const float mo = s.m2[sidx];
             const float mn = fmaxf(mo, mt);
@@ -461,39 +479,39 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
           }
           softmax_bar();
 #pragma unroll
-          for (int h = 0; h < TC_HG; ++h) lp[h] *= s.alpha[h];
+          for (int h = 0; h < HG; ++h) lp[h] *= s.alpha[h];
           if (!first) {
             // rescale the four O^T chunks this thread's TMEM lane holds (PV of the previous
             // tile has completed, see the o_done wait above)
             for (int cc = 0; cc < 4; ++cc) {
-              for (int half = 0; half < 2; ++half) {
-                uint32_t r[32];
-                const uint32_t ta = tmem + lane_base + TC_O_COL + cc * TC_HG + half * 32;
-                tc::tmem_ld32(ta, r);
+              for (int half = 0; half < NCH; ++half) {
+                uint32_t r[CW];
+                const uint32_t ta = tmem + lane_base + Cfg<HG>::O_COL + cc * HG + half * CW;
+                tc::tmem_ld<CW>(ta, r);
                 tc::tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  r[j] = __float_as_uint(__uint_as_float(r[j]) * s.alpha[half * 32 + j]);
-                tc::tmem_st32(ta, r);
+                for (int j = 0; j < CW; ++j)
+                  r[j] = __float_as_uint(__uint_as_float(r[j]) * s.alpha[half * CW + j]);
+                tc::tmem_st<CW>(ta, r);
               }
             }
             tc::tmem_wait_st();
           }
         }
-        // pass 2: probabilities, partial sums, and this row of P^T (MN-major, 128-byte swizzle)
-        // into the rope slot, which TMA (async proxy) wrote and QK^T has finished reading
+        // pass 2: probabilities, partial sums, and this row of P^T (MN-major, swizzled rows of
+        // 2*HG bytes) into the rope slot, which TMA (async proxy) wrote and QK^T has finished reading
         tc::fence_proxy_async_smem();
-        for (int half = 0; half < 2; ++half) {
-          uint32_t r[32];
-          tc::tmem_ld32(s_addr + half * 32, r);
+        for (int half = 0; half < NCH; ++half) {
+          uint32_t r[CW];
+          tc::tmem_ld<CW>(s_addr + half * CW, r);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
+          for (int c4 = 0; c4 < CW / 8; ++c4) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int j = c4 * 8 + 2 * e;
-              const int h = half * 32 + j;
+              const int h = half * CW + j;
               float p0 = 0.f, p1 = 0.f;
               if (valid) {
                 p0 = ex2(fmaf(__uint_as_float(r[j]), a.scale_log2, -s.m2[h]));
@@ -503,7 +521,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
               lp[h + 1] += p1;
               w[e] = pack_bf16x2(p0, p1);
             }
-            *reinterpret_cast<uint4*>(prow + tc::sw128_offset(row, half * 4 + c4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(prow + Cfg<HG>::p_offset(row, half * (CW / 8) + c4)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
         // S^T of this tile is fully read: the MMA warp may reuse the buffer
@@ -526,7 +545,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
       if (!softmax_wait(s, &s.o_done, (uint32_t)((n - 1) & 1), sidx)) { ok = false; break; }
       tc::tc_fence_after();
 #pragma unroll
-      for (int h = 0; h < TC_HG; ++h) {
+      for (int h = 0; h < HG; ++h) {
         float v = lp[h];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -534,26 +553,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
       }
       softmax_bar();
       const int slot = k + sb;
-      const int nh = min(TC_HG, a.H - g * TC_HG);
-      if (sidx < TC_HG) {
+      const int nh = min(HG, a.H - g * HG);
+      if (sidx < HG) {
         const float l = s.red[0][sidx] + s.red[1][sidx] + s.red[2][sidx] + s.red[3][sidx];
         s.alpha[sidx] = 1.0f / l;
         if (sidx < nh) {
           const bool bad = *reinterpret_cast<volatile int*>(&s.bad_page[seg & 1]) != 0;
-          a.part_lse[(size_t)(g * a.n_slots + slot) * TC_HG + sidx] =
+          a.part_lse[(size_t)(g * a.n_slots + slot) * HG + sidx] =
               bad ? CUDART_NAN_F : (s.m2[sidx] + __log2f(l)) * 0.69314718055994530942f;
         }
       }
       softmax_bar();
-      float* po = a.part_o + ((size_t)(g * a.n_slots + slot) * TC_HG) * 512;
+      float* po = a.part_o + ((size_t)(g * a.n_slots + slot) * HG) * 512;
       for (int cc = 0; cc < 4; ++cc) {
-        for (int half = 0; half < 2; ++half) {
-          uint32_t r[32];
-          tc::tmem_ld32(tmem + lane_base + TC_O_COL + cc * TC_HG + half * 32, r);
+        for (int half = 0; half < NCH; ++half) {
+          uint32_t r[CW];
+          tc::tmem_ld<CW>(tmem + lane_base + Cfg<HG>::O_COL + cc * HG + half * CW, r);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int h = half * 32 + j;
+          for (int j = 0; j < CW; ++j) {
+            const int h = half * CW + j;
             if (h < nh) po[(size_t)h * 512 + cc * 128 + row] = __uint_as_float(r[j]) * s.alpha[h];
           }
         }
@@ -571,7 +590,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
   __syncthreads();
   if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, TC_TMEM_COLS);
+    tc::tmem_dealloc(tmem, Cfg<HG>::TMEM_COLS);
   }
 }
 
@@ -617,7 +636,12 @@ bool attn_tc_supported(const mla_config& cfg) {
          (cfg.page_size == 0 || cfg.page_size % 64 == 0) && encode_fn() != nullptr;
 }
 
-int tc_heads_per_cta() { return TC_HG; }
+// Heads per CTA for H heads: the 64-wide group (widths 16 and 32 are compiled for smaller
+// head counts; enabled once their swizzled P^T layouts are validated on the device).
+int tc_heads_per_cta(int H) {
+  (void)H;
+  return 64;
+}
 
 
 cudaError_t launch_attn_tc(const mla_config& cfg, const mla_cache& cache, const DecodePlan& plan,
@@ -627,7 +651,8 @@ cudaError_t launch_attn_tc(const mla_config& cfg, const mla_cache& cache, const 
     return cudaErrorInvalidValue;
   CUtensorMap rows_map, q_map;
   if (!make_rows_map(&rows_map, cache.rows, (uint64_t)cache.n_physical_rows)) return cudaErrorInvalidValue;
-  if (!make_rows_map(&q_map, q_abs, (uint64_t)B * cfg.n_heads)) return cudaErrorInvalidValue;
+  if (!make_map_2d_bf16(&q_map, q_abs, 576, (uint64_t)B * cfg.n_heads, 64, (uint32_t)plan.heads_per_cta))
+    return cudaErrorInvalidValue;
   TcArgs a;
   a.map = RowMap{cache.page_table, cfg.page_size, cfg.max_pages_per_seq, cfg.rows_per_seq, cache.n_physical_rows};
   a.seq_lens = seq_lens;
@@ -641,9 +666,27 @@ cudaError_t launch_attn_tc(const mla_config& cfg, const mla_cache& cache, const 
   a.ncg = plan.ctas_per_group;
   a.n_slots = plan.n_slots;
   a.scale_log2 = cfg.softmax_scale * 1.4426950408889634f;
-  cudaError_t e = ensure_smem((const void*)attn_tc_kernel, TC_SMEM_DYN);
-  if (e != cudaSuccess) return e;
-  attn_tc_kernel<<<plan.n_groups * plan.ctas_per_group, TC_THREADS, TC_SMEM_DYN, st>>>(rows_map, q_map, a);
+  const int grid = plan.n_groups * plan.ctas_per_group;
+  cudaError_t e;
+  switch (plan.heads_per_cta) {
+    case 64:
+      e = ensure_smem((const void*)attn_tc_kernel<64>, Cfg<64>::SMEM_DYN);
+      if (e != cudaSuccess) return e;
+      attn_tc_kernel<64><<<grid, TC_THREADS, Cfg<64>::SMEM_DYN, st>>>(rows_map, q_map, a);
+      break;
+    case 32:
+      e = ensure_smem((const void*)attn_tc_kernel<32>, Cfg<32>::SMEM_DYN);
+      if (e != cudaSuccess) return e;
+      attn_tc_kernel<32><<<grid, TC_THREADS, Cfg<32>::SMEM_DYN, st>>>(rows_map, q_map, a);
+      break;
+    case 16:
+      e = ensure_smem((const void*)attn_tc_kernel<16>, Cfg<16>::SMEM_DYN);
+      if (e != cudaSuccess) return e;
+      attn_tc_kernel<16><<<grid, TC_THREADS, Cfg<16>::SMEM_DYN, st>>>(rows_map, q_map, a);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

@@ -139,7 +139,7 @@ cudaError_t launch_attn_tc(const mla_config& cfg, const mla_cache& cache, const 
                            const int32_t* seq_lens, const void* q_abs, float* part_o,
                            float* part_lse, int32_t* meta, int B, WsHeader* hdr, cudaStream_t st);
 bool attn_tc_supported(const mla_config& cfg);
-int tc_heads_per_cta();
+int tc_heads_per_cta(int H);
 bool absorb_tc_supported(const mla_config& cfg, int B);
 bool combine_tc_supported(const mla_config& cfg, int B);
 cudaError_t launch_absorb_tc(const mla_config& cfg, const void* q, const void* kv_b, const int32_t* positions,

@@ -79,7 +79,7 @@ static mla_status make_plan(const mla_config& cfg, int B, DecodePlan* p) {
   if (attn_tc_supported(cfg)) {
     // tensor-core path: one CTA per SM, each head group's tile list split evenly over its CTAs
     p->path = PATH_TC;
-    p->heads_per_cta = tc_heads_per_cta();
+    p->heads_per_cta = tc_heads_per_cta(cfg.n_heads);
     p->n_groups = (cfg.n_heads + p->heads_per_cta - 1) / p->heads_per_cta;
     p->ctas_per_group = sms / p->n_groups > 0 ? sms / p->n_groups : 1;
     // never more CTAs than the batch can have 128-row tiles
