@@ -44,7 +44,7 @@ constexpr int TC_KB = 9;           // 64-column blocks per row (576 / 64)
 constexpr int TC_LAT_KB = 8;       // latent blocks (512 / 64)
 constexpr int TC_SLOT_BYTES = TC_TILE * 128;   // 16 KB
 constexpr int TC_THREADS = 192;
-constexpr uint32_t WAIT_LIMIT = 1u << 21;
+constexpr uint64_t WAIT_NS = 200ull * 1000 * 1000;   // a wait gives up after 200 ms
 
 // Per head-group width HG (the MMA N: 16, 32 or 64 heads per CTA).
 template <int HG>
@@ -106,7 +106,7 @@ __device__ __forceinline__ bool softmax_vote_or(bool v) {
   asm volatile(
       "{\n\t.reg .pred pi, po;\n\t"
       "setp.ne.u32 pi, %1, 0;\n\t"
-      "bar.red.or.pred po, 1, 128, pi;\n\t"
+      "barrier.red.or.pred po, 1, 128, pi;\n\t"
       "selp.u32 %0, 1, 0, po;\n\t}"
       : "=r"(out)
       : "r"((uint32_t)v)
@@ -114,7 +114,10 @@ __device__ __forceinline__ bool softmax_vote_or(bool v) {
   return out != 0;
 }
 
-__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void softmax_bar() {
+  __syncwarp();
+  asm volatile("barrier.sync 1, 128;" ::: "memory");
+}
 
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -135,13 +138,16 @@ __device__ __forceinline__ void cta_range(long long T, int k, int ncg, long long
   *r1 = (T * (k + 1)) / ncg;
 }
 
-// A bounded wait that also gives up once another role has aborted.
+// A bounded wait (WAIT_NS) that also gives up once another role has aborted.
 __device__ __forceinline__ bool wait_bar(Smem& s, uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+  const uint64_t t0 = tc::global_ns();
+  for (uint32_t i = 0;; ++i) {
     if (tc::mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 63 && *reinterpret_cast<volatile int*>(&s.abort)) return false;
+    if ((i & 15) == 15) {
+      if (*reinterpret_cast<volatile int*>(&s.abort)) return false;
+      if (tc::global_ns() - t0 > WAIT_NS) return false;
+    }
   }
-  return false;
 }
 
 // Softmax-side wait: one thread polls, then all 128 softmax threads agree on the outcome, so
@@ -149,6 +155,7 @@ __device__ __forceinline__ bool wait_bar(Smem& s, uint64_t* bar, uint32_t parity
 __device__ __forceinline__ bool softmax_wait(Smem& s, uint64_t* bar, uint32_t parity, int sidx) {
   bool ok = true;
   if (sidx == 0) ok = wait_bar(s, bar, parity);
+  __syncwarp();
   return !softmax_vote_or(!ok);
 }
 
@@ -206,6 +213,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
     s.bad_page[0] = 0;
     s.bad_page[1] = 0;
   }
+  __syncwarp();
   __syncthreads();
   long long before = 0, T = 0;
   for (int i = 0; i < TC_THREADS; ++i) {   // 192 smem reads, broadcast
@@ -294,6 +302,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
     tc::tma_prefetch_desc(&q_map);
   }
   tc::tc_fence_before();
+  __syncwarp();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = s.tmem_base;
@@ -352,8 +361,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
         fail(s, a.hdr, sb);
         // wait (bounded) for every copy already issued, so none lands after the CTA exits
         for (int kb = 0; kb < TC_KB; ++kb)
-          if (last_n[kb] >= 0) tc::mbar_wait(&s.full[kb], (uint32_t)(last_n[kb] & 1), WAIT_LIMIT);
-        if (q_loaded >= 0) tc::mbar_wait(&s.q_full, (uint32_t)(q_loaded & 1), WAIT_LIMIT);
+          if (last_n[kb] >= 0) tc::mbar_wait(&s.full[kb], (uint32_t)(last_n[kb] & 1), WAIT_NS);
+        if (q_loaded >= 0) tc::mbar_wait(&s.q_full, (uint32_t)(q_loaded & 1), WAIT_NS);
       }
     }
   } else if (warp == 1) {
@@ -411,7 +420,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
       if (!ok) fail(s, a.hdr, sb);
       // every MMA issued must finish before TMEM is released
       tc::mma_commit(&s.mma_fin);
-      tc::mbar_wait(&s.mma_fin, 0, WAIT_LIMIT);
+      tc::mbar_wait(&s.mma_fin, 0, WAIT_NS);
     }
   } else {
     // ================================ softmax + epilogue ================================
@@ -455,6 +464,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
               need |= fmaf(__uint_as_float(r[j]), a.scale_log2, -s.m2[half * CW + j]) > RESCALE_THRESHOLD;
           }
         }
+        __syncwarp();
         if (softmax_vote_or(need)) {
           // exact per-head maximum over the tile's valid rows; raise the running max
           for (int half = 0; half < NCH; ++half) {
@@ -586,6 +596,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
     if (!ok) fail(s, a.hdr, sb);
   }
 
+  __syncwarp();   // lanes that skipped a role wait here for their lane 0
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 1) {

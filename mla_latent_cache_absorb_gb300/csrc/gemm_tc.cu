@@ -22,7 +22,7 @@ namespace mla {
 namespace {
 
 constexpr int G_THREADS = 128;
-constexpr uint32_t G_WAIT = 1u << 21;
+constexpr uint64_t G_WAIT = 200ull * 1000 * 1000;   // a wait gives up after 200 ms
 constexpr int ABS_TC_BCHUNK = 64;
 constexpr int CMB_TC_BCHUNK = 32;
 constexpr int ABS_TC_SMEM = 4 * 16384 + 2 * 8192 + 1024;
@@ -73,6 +73,7 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
+  __syncwarp();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = tmem_base;
@@ -89,6 +90,7 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
     *reinterpret_cast<uint4*>(qs + kb * 8192 + tc::sw128_offset(r, c8)) = v;
   }
   tc::fence_proxy_async_smem();
+  __syncwarp();
   __syncthreads();
   if (tid == 0) {
     if (!tc::mbar_wait(&bar_w, 0, G_WAIT)) {
@@ -107,7 +109,7 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
     }
     tc::mma_commit(&bar_mma);   // arrives once every MMA issued above has completed
   }
-  __syncwarp();
+  __syncwarp();   // lanes 1-31 of warp 0 wait for lane 0
   const bool ok = tc::mbar_wait(&bar_mma, 0, G_WAIT) && !*reinterpret_cast<volatile int*>(&failed);
   tc::tc_fence_after();
   if (ok) {
@@ -143,6 +145,7 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
       a.q_abs[ai + 1] = bf16_bits(y1);
     }
   }
+  __syncwarp();
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -193,6 +196,7 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
+  __syncwarp();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = tmem_base;
@@ -222,6 +226,7 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
       cnt_s[bb] = ns;
     }
   }
+  __syncwarp();
   __syncthreads();
   // vc = sum_s w_s O_s as bf16 hi + lo, 8 latent columns per item, 128-byte swizzled
   for (int i = tid; i < CMB_TC_BCHUNK * 64; i += G_THREADS) {
@@ -259,6 +264,7 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
     *reinterpret_cast<uint4*>(vl + kb * 4096 + tc::sw128_offset(bb, c8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
   }
   tc::fence_proxy_async_smem();
+  __syncwarp();
   __syncthreads();
   if (tid == 0) {
     if (!tc::mbar_wait(&bar_w, 0, G_WAIT)) {
@@ -291,6 +297,7 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
   }
   if (a.lse != nullptr)
     for (int bb = tid; bb < nb; bb += G_THREADS) a.lse[(size_t)(b0 + bb) * a.H + h] = lse_s[bb];
+  __syncwarp();
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) {

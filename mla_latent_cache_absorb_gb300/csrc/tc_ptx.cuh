@@ -42,12 +42,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Poll until the phase with `parity` completes; false after `limit` polls (each try_wait
-// itself blocks for a short, hardware-bounded time).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
-  for (uint32_t i = 0; i < limit; ++i)
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Poll until the phase with `parity` completes; false once `limit_ns` nanoseconds have passed
+// (each try_wait itself blocks only for a short, hardware-bounded time).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_ns();
+  while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-  return false;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
 }
 
 // ---- async-proxy fences ------------------------------------------------------------------------
