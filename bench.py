@@ -154,11 +154,44 @@ def summarize_clocks(samples, window):
 # events that can live inside a CUDA graph
 # ------------------------------------------------------------------------------------------------
 
+class _CudartEvent:
+    """A timing event recorded with cudaEventRecordExternal, so that it becomes an event-record
+    node when recorded during stream capture (for torch builds without external events)."""
+    _rt = None
+
+    @classmethod
+    def _lib(cls):
+        if cls._rt is None:
+            import ctypes
+            cls._rt = ctypes.CDLL("libcudart.so.13")   # the runtime torch has already loaded
+        return cls._rt
+
+    def __init__(self):
+        import ctypes
+        self._c = ctypes
+        self.ev = ctypes.c_void_p()
+        if self._lib().cudaEventCreateWithFlags(ctypes.byref(self.ev), 0) != 0:
+            raise RuntimeError("cudaEventCreateWithFlags failed")
+
+    def record(self, stream):
+        if self._lib().cudaEventRecordWithFlags(self.ev, self._c.c_void_p(stream.cuda_stream), 1) != 0:
+            raise RuntimeError("cudaEventRecordWithFlags failed")
+
+    def synchronize(self):
+        self._lib().cudaEventSynchronize(self.ev)
+
+    def elapsed_time(self, other):
+        ms = self._c.c_float()
+        if self._lib().cudaEventElapsedTime(self._c.byref(ms), self.ev, other.ev) != 0:
+            raise RuntimeError("cudaEventElapsedTime failed")
+        return ms.value
+
+
 def graph_event(torch):
     try:
         return torch.cuda.Event(enable_timing=True, external=True)
-    except TypeError as e:  # very old torch: no external events
-        raise RuntimeError("torch.cuda.Event(external=True) is required for in-graph timing") from e
+    except TypeError:  # torch without external events: record through the runtime directly
+        return _CudartEvent()
 
 
 # ------------------------------------------------------------------------------------------------
