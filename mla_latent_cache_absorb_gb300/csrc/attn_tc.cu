@@ -453,12 +453,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
         if (n > 0 && !softmax_wait(s, &s.o_done, (uint32_t)((n - 1) & 1), sidx)) { ok = false; break; }
         tc::tc_fence_after();
         // pass 1: does any score exceed its head's running max by more than the threshold?
+        // (TMEM loads are warp-collective: every lane loads, validity only gates the arithmetic)
         bool need = first;
-        if (valid) {
-          for (int half = 0; half < NCH; ++half) {
-            uint32_t r[CW];
-            tc::tmem_ld<CW>(s_addr + half * CW, r);
-            tc::tmem_wait_ld();
+        for (int half = 0; half < NCH; ++half) {
+          uint32_t r[CW];
+          tc::tmem_ld<CW>(s_addr + half * CW, r);
+          tc::tmem_wait_ld();
+          if (valid) {
 #pragma unroll
             for (int j = 0; j < CW; ++j)
               need |= fmaf(__uint_as_float(r[j]), a.scale_log2, -s.m2[half * CW + j]) > RESCALE_THRESHOLD;

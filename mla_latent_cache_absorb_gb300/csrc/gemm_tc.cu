@@ -110,7 +110,9 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
     tc::mma_commit(&bar_mma);   // arrives once every MMA issued above has completed
   }
   __syncwarp();   // lanes 1-31 of warp 0 wait for lane 0
-  const bool ok = tc::mbar_wait(&bar_mma, 0, G_WAIT) && !*reinterpret_cast<volatile int*>(&failed);
+  // warp-uniform: the TMEM loads below are warp-collective
+  const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&bar_mma, 0, G_WAIT) &&
+                                             !*reinterpret_cast<volatile int*>(&failed));
   tc::tc_fence_after();
   if (ok) {
     for (int mc = 0; mc < 2; ++mc) {
@@ -284,7 +286,9 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
     tc::mma_commit(&bar_mma);
   }
   __syncwarp();
-  const bool ok = tc::mbar_wait(&bar_mma, 0, G_WAIT) && !*reinterpret_cast<volatile int*>(&failed);
+  // warp-uniform: the TMEM loads below are warp-collective
+  const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&bar_mma, 0, G_WAIT) &&
+                                             !*reinterpret_cast<volatile int*>(&failed));
   tc::tc_fence_after();
   if (ok) {
     uint32_t r[32];
