@@ -20,7 +20,13 @@ constexpr int ABS_BCHUNK = 32;   // sequences per shared-memory pass
 template <int DT>
 __global__ void __launch_bounds__(ABS_THREADS)
 absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const void* __restrict__ kv_b,
-              const int32_t* __restrict__ positions, typename Act<DT>::T* __restrict__ q_abs, int B) {
+              const int32_t* __restrict__ positions, typename Act<DT>::T* __restrict__ q_abs,
+              typename Act<DT>::T* __restrict__ q_res, int B) {
+  // value v goes out as its storage rounding, and (bf16 only) the rounding residual to q_res
+  auto put = [&](int64_t i, float v) {
+    Act<DT>::store(q_abs, i, v);
+    if (q_res != nullptr) Act<DT>::store(q_res, i, v - Act<DT>::load(q_abs, i));
+  };
   extern __shared__ float sm[];
   const int H = cfg.n_heads, C = cfg.kv_lora, N = cfg.qk_nope, R = cfg.qk_rope, V = cfg.v_head;
   const int h = blockIdx.x;
@@ -30,11 +36,7 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
   float* q_s = sm + N * ABS_COLS;           // [ABS_BCHUNK][N]
 
   const int64_t wrow0 = (int64_t)h * (N + V);
-  for (int i = threadIdx.x; i < N * ABS_COLS; i += ABS_THREADS) {
-    const int n = i / ABS_COLS, cc = i % ABS_COLS;
-    const int c = c0 + cc;
-    w_s[i] = (c < C) ? kv_b_load(kv_b, cfg.kv_b_dtype, wrow0 + n, c, C) : 0.f;
-  }
+  stage_kv_b_rows(w_s, ABS_COLS, kv_b, cfg.kv_b_dtype, wrow0, N, c0, min(ABS_COLS, C - c0), C, ABS_THREADS);
 
   const int cc = threadIdx.x % ABS_COLS;
   const int bsub = threadIdx.x / ABS_COLS;   // 0..3
@@ -50,7 +52,7 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
       for (int bb = bsub; bb < nb; bb += ABS_THREADS / ABS_COLS) {
         float acc = 0.f;
         for (int n = 0; n < N; ++n) acc = fmaf(q_s[bb * N + n], w_s[n * ABS_COLS + cc], acc);
-        Act<DT>::store(q_abs, ((int64_t)(b0 + bb) * H + h) * arow + c0 + cc, acc);
+        put(((int64_t)(b0 + bb) * H + h) * arow + c0 + cc, acc);
       }
     }
   }
@@ -65,18 +67,18 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
       if (positions != nullptr) {
         float c, s;
         rope_cs(cfg.rope_inv_freq, p, positions[b], &c, &s);
-        Act<DT>::store(q_abs, ai, x0 * c - x1 * s);
-        Act<DT>::store(q_abs, ai + 1, x0 * s + x1 * c);
+        put(ai, x0 * c - x1 * s);
+        put(ai + 1, x0 * s + x1 * c);
       } else {
-        Act<DT>::store(q_abs, ai, x0);
-        Act<DT>::store(q_abs, ai + 1, x1);
+        put(ai, x0);
+        put(ai + 1, x1);
       }
     }
   }
 }
 
 cudaError_t launch_absorb(const mla_config& cfg, const void* q, const void* kv_b,
-                          const int32_t* positions, void* q_abs, int B, cudaStream_t st) {
+                          const int32_t* positions, void* q_abs, void* q_res, int B, cudaStream_t st) {
   dim3 grid(cfg.n_heads, (cfg.kv_lora + ABS_COLS - 1) / ABS_COLS);
   const size_t smem = sizeof(float) * ((size_t)cfg.qk_nope * ABS_COLS + (size_t)ABS_BCHUNK * cfg.qk_nope);
   if (cfg.act_dtype == MLA_BF16) {
@@ -84,13 +86,13 @@ cudaError_t launch_absorb(const mla_config& cfg, const void* q, const void* kv_b
     cudaError_t e = ensure_smem((const void*)k, (int)smem);
     if (e != cudaSuccess) return e;
     k<<<grid, ABS_THREADS, smem, st>>>(cfg, static_cast<const uint16_t*>(q), kv_b, positions,
-                                       static_cast<uint16_t*>(q_abs), B);
+                                       static_cast<uint16_t*>(q_abs), static_cast<uint16_t*>(q_res), B);
   } else {
     auto k = absorb_kernel<MLA_F32>;
     cudaError_t e = ensure_smem((const void*)k, (int)smem);
     if (e != cudaSuccess) return e;
     k<<<grid, ABS_THREADS, smem, st>>>(cfg, static_cast<const float*>(q), kv_b, positions,
-                                       static_cast<float*>(q_abs), B);
+                                       static_cast<float*>(q_abs), nullptr, B);
   }
   return cudaGetLastError();
 }

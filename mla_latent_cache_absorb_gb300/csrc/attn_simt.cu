@@ -23,6 +23,7 @@ struct SimtArgs {
   const void* rows;
   const int32_t* seq_lens;
   const void* q_abs;
+  const uint16_t* q_res;   // bf16 rounding residual of q_abs (bf16 rows) or nullptr
   float* part_o;
   float* part_lse;
   int32_t* meta;
@@ -64,8 +65,10 @@ __global__ void __launch_bounds__(SIMT_THREADS) attn_simt_kernel(SimtArgs a) {
   int* bad_s = reinterpret_cast<int*>(al_s + a.hpb);
 
   const T* qa = static_cast<const T*>(a.q_abs);
-  for (int i = threadIdx.x; i < nh * row; i += SIMT_THREADS)
-    q_s[i] = Act<DT>::load(qa, ((int64_t)b * a.H + h0) * row + i);
+  for (int i = threadIdx.x; i < nh * row; i += SIMT_THREADS) {
+    const int64_t qi = ((int64_t)b * a.H + h0) * row + i;
+    q_s[i] = Act<DT>::load(qa, qi) + (a.q_res != nullptr ? bf16_bits_to_f32(a.q_res[qi]) : 0.f);
+  }
   for (int i = threadIdx.x; i < a.hpb; i += SIMT_THREADS) {
     m_s[i] = -CUDART_INF_F;
     l_s[i] = 0.f;
@@ -156,7 +159,7 @@ size_t simt_smem_bytes(const mla_config& cfg, int hpb) {
 }
 
 cudaError_t launch_attn_simt(const mla_config& cfg, const mla_cache& cache, const DecodePlan& plan,
-                             const int32_t* seq_lens, const void* q_abs, float* part_o,
+                             const int32_t* seq_lens, const void* q_abs, const void* q_res, float* part_o,
                              float* part_lse, int32_t* meta, int B, WsHeader* hdr, cudaStream_t st) {
   SimtArgs a;
   a.map = RowMap{cache.page_table, cfg.page_size, cfg.max_pages_per_seq, cfg.rows_per_seq,
@@ -164,6 +167,7 @@ cudaError_t launch_attn_simt(const mla_config& cfg, const mla_cache& cache, cons
   a.rows = cache.rows;
   a.seq_lens = seq_lens;
   a.q_abs = q_abs;
+  a.q_res = static_cast<const uint16_t*>(q_res);
   a.part_o = part_o;
   a.part_lse = part_lse;
   a.meta = meta;

@@ -50,7 +50,10 @@ constexpr uint64_t WAIT_NS = 200ull * 1000 * 1000;   // a wait gives up after 20
 template <int HG>
 struct Cfg {
   static constexpr int QBLK_BYTES = HG * 128;                 // one 64-column block of Q
-  static constexpr int SMEM_DYN = TC_KB * TC_SLOT_BYTES + TC_KB * QBLK_BYTES + 1024;
+  // Q blocks: 9 of the bf16 fused query rows + the bf16 residual of the rope block, so the
+  // rope part of every score is exact to ~2^-16 (hi + lo)
+  static constexpr int Q_BLOCKS = TC_KB + 1;
+  static constexpr int SMEM_DYN = TC_KB * TC_SLOT_BYTES + Q_BLOCKS * QBLK_BYTES + 1024;
   static constexpr uint32_t O_COL = 0;                        // O^T chunks: 4 x HG columns
   static constexpr uint32_t S_COL = 4 * HG;                   // S^T buffers: 2 x HG columns
   static constexpr uint32_t TMEM_COLS = HG == 64 ? 512 : (HG == 32 ? 256 : 128);
@@ -91,7 +94,6 @@ struct Smem {
   float red[4][TC_HG];
   float m2[TC_HG];        // running max per head, log2 units
   float alpha[TC_HG];     // rescale factors (then 1/l in the epilogue)
-  long long scan[TC_THREADS];
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -150,11 +152,13 @@ __device__ __forceinline__ bool wait_bar(Smem& s, uint64_t* bar, uint32_t parity
   }
 }
 
-// Softmax-side wait: one thread polls, then all 128 softmax threads agree on the outcome, so
-// they always leave (or stay in) their loops together and never strand a named barrier.
+// Softmax-side wait: every softmax thread polls the barrier itself (a warp whose lane 0 alone
+// polled would run split afterwards: collective operations then serialise and the warp's
+// arrivals at the group barrier stop lining up), then all 128 agree on the outcome, so they
+// always leave (or stay in) their loops together and never strand a group barrier.
 __device__ __forceinline__ bool softmax_wait(Smem& s, uint64_t* bar, uint32_t parity, int sidx) {
-  bool ok = true;
-  if (sidx == 0) ok = wait_bar(s, bar, parity);
+  (void)sidx;
+  const bool ok = wait_bar(s, bar, parity);
   __syncwarp();
   return !softmax_vote_or(!ok);
 }
@@ -190,12 +194,14 @@ struct SegIter {
 template <int HG>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_constant__ CUtensorMap q_map,
-               TcArgs a) {
+               const __grid_constant__ CUtensorMap qres_map, TcArgs a) {
   extern __shared__ uint8_t dyn_raw[];
   __shared__ Smem s;
   uint8_t* dyn = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* slots = dyn;                                 // 9 x 16 KB
-  uint8_t* qs = dyn + TC_KB * TC_SLOT_BYTES;            // 9 x 8 KB
+  uint8_t* qs = dyn + TC_KB * TC_SLOT_BYTES;            // 10 Q blocks
+  // prologue scratch: the slots are free until the first TMA load
+  long long* scan = reinterpret_cast<long long*>(slots);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x % a.G;
   const int k = blockIdx.x / a.G;
@@ -205,7 +211,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
   const int cb0 = min(a.B, tid * chunk), cb1 = min(a.B, cb0 + chunk);
   long long mine = 0;
   for (int b = cb0; b < cb1; ++b) mine += seq_tiles(a, b);
-  s.scan[tid] = mine;
+  scan[tid] = mine;
   if (tid == 0) {
     s.abort = 0;
     s.seg_b0 = a.B;
@@ -217,7 +223,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
   __syncthreads();
   long long before = 0, T = 0;
   for (int i = 0; i < TC_THREADS; ++i) {   // 192 smem reads, broadcast
-    const long long v = s.scan[i];
+    const long long v = scan[i];
     if (i < tid) before += v;
     T += v;
   }
@@ -300,7 +306,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
   if (warp == 0 && lane == 0) {
     tc::tma_prefetch_desc(&rows_map);
     tc::tma_prefetch_desc(&q_map);
+    tc::tma_prefetch_desc(&qres_map);
   }
+  tc::fence_proxy_async_smem();   // the prologue's generic writes to the slots precede TMA writes
   tc::tc_fence_before();
   __syncwarp();
   __syncthreads();
@@ -320,9 +328,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
       bool ok = true;
       while (ok && it.next(a, &sb, &tlo, &thi)) {
         if (seg > 0 && !wait_bar(s, &s.q_empty, (seg - 1) & 1)) { ok = false; break; }
-        tc::mbar_arrive_expect_tx(&s.q_full, TC_KB * Cfg<HG>::QBLK_BYTES);
+        tc::mbar_arrive_expect_tx(&s.q_full, Cfg<HG>::Q_BLOCKS * Cfg<HG>::QBLK_BYTES);
         const int qrow = sb * a.H + g * HG;
         for (int kb = 0; kb < TC_KB; ++kb) tc::tma_load_2d(qs + kb * Cfg<HG>::QBLK_BYTES, &q_map, kb * 64, qrow, &s.q_full);
+        tc::tma_load_2d(qs + TC_KB * Cfg<HG>::QBLK_BYTES, &qres_map, TC_LAT_KB * 64, qrow, &s.q_full);
         q_loaded = seg;
         const long long L = a.seq_lens[sb];
         for (int t = tlo; t < thi && ok; ++t) {
@@ -394,6 +403,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
             }
           }
           if (!ok) break;
+          // the rope block once more against the residual of the rope queries (hi + lo)
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = tc::sdesc_sw128(slot0 + TC_LAT_KB * TC_SLOT_BYTES + kk * 32, 16, 1024);
+            const uint64_t bd = tc::sdesc_sw128(q0 + TC_KB * Cfg<HG>::QBLK_BYTES + kk * 32, 16, 1024);
+            tc::mma_f16_ss(s_tmem, ad, bd, idesc_qk, 1);
+          }
           tc::mma_commit(&s.s_full[sbuf]);
           if (t + 1 == thi) tc::mma_commit(&s.q_empty);
           // PV needs P^T (slot 8) and, on a segment's first tile, the previous O^T read out
@@ -591,6 +606,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
       tc::tc_fence_before();
       softmax_bar();   // s.red, s.alpha and s.m2 free; every thread has read bad_page
       if (sidx == 0) s.bad_page[seg & 1] = 0;
+      __syncwarp();
       tc::mbar_arrive(&s.o_empty);
       ++seg;
     }
@@ -657,13 +673,16 @@ int tc_heads_per_cta(int H) {
 
 
 cudaError_t launch_attn_tc(const mla_config& cfg, const mla_cache& cache, const DecodePlan& plan,
-                           const int32_t* seq_lens, const void* q_abs, float* part_o, float* part_lse,
-                           int32_t* meta, int B, WsHeader* hdr, cudaStream_t st) {
+                           const int32_t* seq_lens, const void* q_abs, const void* q_res, float* part_o,
+                           float* part_lse, int32_t* meta, int B, WsHeader* hdr, cudaStream_t st) {
   if (cache.n_physical_rows >= (int64_t(1) << 31) || (int64_t)B * cfg.n_heads >= (int64_t(1) << 31))
     return cudaErrorInvalidValue;
   CUtensorMap rows_map, q_map;
   if (!make_rows_map(&rows_map, cache.rows, (uint64_t)cache.n_physical_rows)) return cudaErrorInvalidValue;
-  if (!make_map_2d_bf16(&q_map, q_abs, 576, (uint64_t)B * cfg.n_heads, 64, (uint32_t)plan.heads_per_cta))
+  CUtensorMap qres_map;
+  if (q_res == nullptr) return cudaErrorInvalidValue;
+  if (!make_map_2d_bf16(&q_map, q_abs, 576, (uint64_t)B * cfg.n_heads, 64, (uint32_t)plan.heads_per_cta) ||
+      !make_map_2d_bf16(&qres_map, q_res, 576, (uint64_t)B * cfg.n_heads, 64, (uint32_t)plan.heads_per_cta))
     return cudaErrorInvalidValue;
   TcArgs a;
   a.map = RowMap{cache.page_table, cfg.page_size, cfg.max_pages_per_seq, cfg.rows_per_seq, cache.n_physical_rows};
@@ -684,17 +703,17 @@ cudaError_t launch_attn_tc(const mla_config& cfg, const mla_cache& cache, const 
     case 64:
       e = ensure_smem((const void*)attn_tc_kernel<64>, Cfg<64>::SMEM_DYN);
       if (e != cudaSuccess) return e;
-      attn_tc_kernel<64><<<grid, TC_THREADS, Cfg<64>::SMEM_DYN, st>>>(rows_map, q_map, a);
+      attn_tc_kernel<64><<<grid, TC_THREADS, Cfg<64>::SMEM_DYN, st>>>(rows_map, q_map, qres_map, a);
       break;
     case 32:
       e = ensure_smem((const void*)attn_tc_kernel<32>, Cfg<32>::SMEM_DYN);
       if (e != cudaSuccess) return e;
-      attn_tc_kernel<32><<<grid, TC_THREADS, Cfg<32>::SMEM_DYN, st>>>(rows_map, q_map, a);
+      attn_tc_kernel<32><<<grid, TC_THREADS, Cfg<32>::SMEM_DYN, st>>>(rows_map, q_map, qres_map, a);
       break;
     case 16:
       e = ensure_smem((const void*)attn_tc_kernel<16>, Cfg<16>::SMEM_DYN);
       if (e != cudaSuccess) return e;
-      attn_tc_kernel<16><<<grid, TC_THREADS, Cfg<16>::SMEM_DYN, st>>>(rows_map, q_map, a);
+      attn_tc_kernel<16><<<grid, TC_THREADS, Cfg<16>::SMEM_DYN, st>>>(rows_map, q_map, qres_map, a);
       break;
     default:
       return cudaErrorInvalidValue;

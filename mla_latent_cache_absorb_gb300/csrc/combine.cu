@@ -26,8 +26,10 @@ struct CombineArgs {
   const float* part_lse;    // [groups][n_slots][hpg]
   float* out;
   float* lse;
+  const uint16_t* q_res;    // bf16 query residual [B][H][C+R] or nullptr (no LSE correction)
+  float scale;
   int kv_b_dtype;
-  int H, C, N, V, B;
+  int H, C, N, V, R, B;
   int hpg, n_slots, max_slots;
 };
 
@@ -50,10 +52,7 @@ __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
   auto lse_at = [&](int slot) { return ((int64_t)pg * a.n_slots + slot) * a.hpg + hh; };
 
   const int64_t wrow0 = (int64_t)h * (a.N + a.V) + a.N + j0;
-  for (int i = threadIdx.x; i < CMB_VJ * a.C; i += CMB_THREADS) {
-    const int j = i / a.C, c = i % a.C;
-    w_s[j * Cp + c] = (j < nj) ? kv_b_load(a.kv_b, a.kv_b_dtype, wrow0 + j, c, a.C) : 0.f;
-  }
+  stage_kv_b_rows(w_s, Cp, a.kv_b, a.kv_b_dtype, wrow0, nj, 0, a.C, a.C, CMB_THREADS);
 
   // split weights: one warp per sequence
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -90,6 +89,18 @@ __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
     vc_s[bb * a.C + c] = v;
   }
   __syncthreads();
+  if (a.q_res != nullptr) {
+    // the scores used bf16 latent queries q_hi = q' - res: to first order the exact log-sum-exp
+    // is lse + scale * (sum_t p_t kv_lat_t) . res = lse + scale * vc . res
+    for (int bb = warp; bb < nb; bb += CMB_THREADS / 32) {
+      const uint16_t* res = a.q_res + ((int64_t)(b0 + bb) * a.H + h) * (a.C + a.R);
+      float d = 0.f;
+      for (int c = lane; c < a.C; c += 32) d = fmaf(vc_s[bb * a.C + c], bf16_bits_to_f32(res[c]), d);
+      d = warp_sum(d);
+      if (lane == 0) lse_s[bb] += a.scale * d;
+    }
+    __syncthreads();
+  }
   // out[b, h, j0 + j]: one warp per sequence, lane = j
   for (int bb = warp; bb < nb; bb += CMB_THREADS / 32) {
     if (lane < nj) {
@@ -105,12 +116,14 @@ __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
 }
 
 cudaError_t launch_combine(const mla_config& cfg, const DecodePlan& plan, const void* kv_b,
-                           const int32_t* meta, const float* part_o, const float* part_lse,
+                           const int32_t* meta, const float* part_o, const float* part_lse, const void* q_res,
                            float* out, float* lse, int B, cudaStream_t st) {
   CombineArgs a;
   a.kv_b = kv_b; a.meta = meta; a.part_o = part_o; a.part_lse = part_lse;
   a.out = out; a.lse = lse; a.kv_b_dtype = cfg.kv_b_dtype;
-  a.H = cfg.n_heads; a.C = cfg.kv_lora; a.N = cfg.qk_nope; a.V = cfg.v_head; a.B = B;
+  a.q_res = static_cast<const uint16_t*>(q_res);
+  a.scale = cfg.softmax_scale;
+  a.H = cfg.n_heads; a.C = cfg.kv_lora; a.N = cfg.qk_nope; a.V = cfg.v_head; a.R = cfg.qk_rope; a.B = B;
   a.hpg = plan.part_hpg; a.n_slots = plan.n_slots;
   // most slots one sequence can span: splits (CUDA-core path) or CTAs per group (tensor path)
   a.max_slots = plan.path == PATH_TC ? plan.ctas_per_group : plan.splits;

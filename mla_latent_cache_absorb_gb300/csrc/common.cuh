@@ -58,6 +58,48 @@ __device__ __forceinline__ float kv_b_load(const void* kv_b, int dtype, int64_t 
   }
 }
 
+// Stage kv_b rows [r0, r0 + nrows) x columns [c0, c0 + ncols) as float32 into dst (row stride
+// dst_stride floats; columns past ncols, up to a multiple of 8, are zero). Each item is 8
+// consecutive columns: one 16-byte load for bf16, two for f32, and the 8 codes plus the block
+// scale for Q8_0; every thread issues all of its loads before using them.
+__device__ __forceinline__ void stage_kv_b_rows(float* dst, int dst_stride, const void* kv_b, int dtype,
+                                                int64_t r0, int nrows, int c0, int ncols, int C, int nthreads) {
+  const int ngrp = (ncols + 7) / 8;
+  for (int i = threadIdx.x; i < nrows * ngrp; i += nthreads) {
+    const int r = i / ngrp, g = i % ngrp;
+    const int c = c0 + 8 * g;
+    float v[8];
+    if (8 * g + 8 <= ncols && (C % 8) == 0) {
+      if (dtype == MLA_BF16) {
+        const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(kv_b) + (r0 + r) * C + c);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v[2 * e] = __uint_as_float(w[e] << 16);
+          v[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+        }
+      } else if (dtype == MLA_F32) {
+        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(kv_b) + (r0 + r) * C + c);
+        const float4 a = src[0], b = src[1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+      } else {
+        const uint8_t* blk = static_cast<const uint8_t*>(kv_b) + (r0 + r) * (int64_t)(C / 32) * 34 + (c / 32) * 34;
+        const uint16_t dbits = static_cast<uint16_t>(blk[0]) | (static_cast<uint16_t>(blk[1]) << 8);
+        const float d = __half2float(__ushort_as_half(dbits));
+        const int o = 2 + (c & 31);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = d * static_cast<float>(static_cast<int8_t>(blk[o + e]));
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = (8 * g + e < ncols) ? kv_b_load(kv_b, dtype, r0 + r, c + e, C) : 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (8 * g + e < dst_stride) dst[r * dst_stride + 8 * g + e] = v[e];
+  }
+}
+
 // Logical row t of sequence b -> physical row, or -1 when the page id is out of range.
 struct RowMap {
   const int32_t* page_table;
@@ -110,7 +152,8 @@ struct DecodePlan {
   // partials: part_o[g][slot][hh][C], part_lse[g][slot][hh] for part_groups x n_slots slots of
   // part_hpg heads; meta[b] = {first slot, slot count} of sequence b (count 0: invalid length)
   int part_groups, part_hpg, n_slots;
-  size_t off_qabs, off_po, off_plse, off_meta, total;
+  // q_res: bf16 rounding residual of the fused query rows (bf16 activations only)
+  size_t off_qabs, off_qres, off_po, off_plse, off_meta, total;
 };
 enum { PATH_SIMT = 0, PATH_TC = 1 };
 
@@ -131,24 +174,26 @@ cudaError_t launch_append_finish(const mla_config& cfg, const mla_cache& cache, 
                                  const float* norm_w, const int32_t* positions,
                                  const int32_t* seq_lens, int B, WsHeader* hdr, cudaStream_t st);
 cudaError_t launch_absorb(const mla_config& cfg, const void* q, const void* kv_b,
-                          const int32_t* positions, void* q_abs, int B, cudaStream_t st);
+                          const int32_t* positions, void* q_abs, void* q_res, int B, cudaStream_t st);
 cudaError_t launch_attn_simt(const mla_config& cfg, const mla_cache& cache, const DecodePlan& plan,
-                             const int32_t* seq_lens, const void* q_abs, float* part_o,
+                             const int32_t* seq_lens, const void* q_abs, const void* q_res, float* part_o,
                              float* part_lse, int32_t* meta, int B, WsHeader* hdr, cudaStream_t st);
 cudaError_t launch_attn_tc(const mla_config& cfg, const mla_cache& cache, const DecodePlan& plan,
-                           const int32_t* seq_lens, const void* q_abs, float* part_o,
+                           const int32_t* seq_lens, const void* q_abs, const void* q_res, float* part_o,
                            float* part_lse, int32_t* meta, int B, WsHeader* hdr, cudaStream_t st);
 bool attn_tc_supported(const mla_config& cfg);
 int tc_heads_per_cta(int H);
 bool absorb_tc_supported(const mla_config& cfg, int B);
 bool combine_tc_supported(const mla_config& cfg, int B);
 cudaError_t launch_absorb_tc(const mla_config& cfg, const void* q, const void* kv_b, const int32_t* positions,
-                             void* q_abs, int B, WsHeader* hdr, cudaStream_t st);
+                             void* q_abs, void* q_res, int B, WsHeader* hdr, cudaStream_t st);
+// q_res != nullptr: the partials came from bf16 latent queries; the combine adds the first-order
+// LSE correction softmax_scale * (vc . q_res[latent]) for the residual the scores did not see.
 cudaError_t launch_combine_tc(const mla_config& cfg, const DecodePlan& plan, const void* kv_b,
-                              const int32_t* meta, const float* part_o, const float* part_lse, float* out,
-                              float* lse, int B, WsHeader* hdr, cudaStream_t st);
+                              const int32_t* meta, const float* part_o, const float* part_lse, const void* q_res,
+                              float* out, float* lse, int B, WsHeader* hdr, cudaStream_t st);
 cudaError_t launch_combine(const mla_config& cfg, const DecodePlan& plan, const void* kv_b,
-                           const int32_t* meta, const float* part_o, const float* part_lse,
+                           const int32_t* meta, const float* part_o, const float* part_lse, const void* q_res,
                            float* out, float* lse, int B, cudaStream_t st);
 
 }  // namespace mla

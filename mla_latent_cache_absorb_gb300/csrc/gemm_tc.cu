@@ -40,6 +40,7 @@ __device__ __forceinline__ uint16_t bf16_bits(float v) {
 struct AbsorbTcArgs {
   const uint16_t* q;        // [B][H][N+R] bf16
   uint16_t* q_abs;          // [B][H][C+R] bf16
+  uint16_t* q_res;          // [B][H][C+R] bf16 rounding residual of q_abs
   const int32_t* positions;
   const double* inv_freq;
   WsHeader* hdr;
@@ -124,7 +125,13 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int b = col0 + j;
-          if (b < nb) a.q_abs[((size_t)(b0 + b) * a.H + h) * arow + c] = bf16_bits(__uint_as_float(r[j]));
+          if (b < nb) {
+            const size_t ai = ((size_t)(b0 + b) * a.H + h) * arow + c;
+            const float v = __uint_as_float(r[j]);
+            const uint16_t hi = bf16_bits(v);
+            a.q_abs[ai] = hi;
+            a.q_res[ai] = bf16_bits(v - bf16_bits_to_f32(hi));
+          }
         }
       }
     }
@@ -143,8 +150,11 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
         y0 = x0 * c - x1 * s;
         y1 = x0 * s + x1 * c;
       }
-      a.q_abs[ai] = bf16_bits(y0);
-      a.q_abs[ai + 1] = bf16_bits(y1);
+      const uint16_t h0 = bf16_bits(y0), h1 = bf16_bits(y1);
+      a.q_abs[ai] = h0;
+      a.q_abs[ai + 1] = h1;
+      a.q_res[ai] = bf16_bits(y0 - bf16_bits_to_f32(h0));
+      a.q_res[ai + 1] = bf16_bits(y1 - bf16_bits_to_f32(h1));
     }
   }
   __syncwarp();
@@ -162,8 +172,10 @@ struct CombineTcArgs {
   const float* part_lse;
   float* out;
   float* lse;
+  const uint16_t* q_res;    // bf16 query residual [B][H][C+R] (LSE correction) or nullptr
+  float scale;
   WsHeader* hdr;
-  int H, C, N, V, B, hpg, n_slots, max_slots;
+  int H, C, N, V, R, B, hpg, n_slots, max_slots;
 };
 
 // grid (H, batch chunks of 32); 128 threads
@@ -179,7 +191,8 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
   uint8_t* wu = dyn;                           // 8 blocks [128 j rows x 64 c] (K-major A)
   uint8_t* vh = dyn + 8 * 16384;               // 8 blocks [32 b rows x 64 c] (K-major B), hi
   uint8_t* vl = vh + 8 * 4096;                 // same, lo
-  float* wt_s = reinterpret_cast<float*>(vl + 8 * 4096);   // [32][max_slots]
+  float* dres = reinterpret_cast<float*>(vl + 8 * 4096);   // [32][64] partial vc . res
+  float* wt_s = dres + CMB_TC_BCHUNK * 64;                  // [32][max_slots]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x, b0 = blockIdx.y * CMB_TC_BCHUNK;
   const int nb = min(CMB_TC_BCHUNK, a.B - b0);
@@ -253,6 +266,17 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
         }
       }
     }
+    if (a.q_res != nullptr) {
+      float d = 0.f;
+      if (bb < nb) {
+        const uint4 u = *reinterpret_cast<const uint4*>(a.q_res + ((size_t)(b0 + bb) * a.H + h) * (a.C + a.R) + ch * 8);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          d += acc[2 * e] * __uint_as_float(w[e] << 16) + acc[2 * e + 1] * __uint_as_float(w[e] & 0xFFFF0000u);
+      }
+      dres[bb * 64 + ch] = d;
+    }
     uint32_t hi[4], lo[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -268,6 +292,17 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
   tc::fence_proxy_async_smem();
   __syncwarp();
   __syncthreads();
+  if (a.q_res != nullptr) {
+    // first-order LSE correction for the bf16 latent queries the scores used:
+    // lse += scale * vc . res, summed in a fixed order (one warp per sequence)
+    for (int bb = warp; bb < nb; bb += G_THREADS / 32) {
+      float d = dres[bb * 64 + lane] + dres[bb * 64 + 32 + lane];
+      d = warp_sum(d);
+      if (lane == 0) lse_s[bb] += a.scale * d;
+    }
+    __syncwarp();
+    __syncthreads();
+  }
   if (tid == 0) {
     if (!tc::mbar_wait(&bar_w, 0, G_WAIT)) {
       failed = 1;
@@ -325,13 +360,14 @@ bool combine_tc_supported(const mla_config& cfg, int B) {
 }
 
 cudaError_t launch_absorb_tc(const mla_config& cfg, const void* q, const void* kv_b, const int32_t* positions,
-                             void* q_abs, int B, WsHeader* hdr, cudaStream_t st) {
+                             void* q_abs, void* q_res, int B, WsHeader* hdr, cudaStream_t st) {
   CUtensorMap w_map;
   if (!make_map_2d_bf16(&w_map, kv_b, 512, (uint64_t)cfg.n_heads * (cfg.qk_nope + cfg.v_head), 64, 128))
     return cudaErrorInvalidValue;
   AbsorbTcArgs a;
   a.q = static_cast<const uint16_t*>(q);
   a.q_abs = static_cast<uint16_t*>(q_abs);
+  a.q_res = static_cast<uint16_t*>(q_res);
   a.positions = positions;
   a.inv_freq = cfg.rope_inv_freq;
   a.hdr = hdr;
@@ -344,17 +380,19 @@ cudaError_t launch_absorb_tc(const mla_config& cfg, const void* q, const void* k
 }
 
 cudaError_t launch_combine_tc(const mla_config& cfg, const DecodePlan& plan, const void* kv_b,
-                              const int32_t* meta, const float* part_o, const float* part_lse, float* out,
-                              float* lse, int B, WsHeader* hdr, cudaStream_t st) {
+                              const int32_t* meta, const float* part_o, const float* part_lse, const void* q_res,
+                              float* out, float* lse, int B, WsHeader* hdr, cudaStream_t st) {
   CUtensorMap w_map;
   if (!make_map_2d_bf16(&w_map, kv_b, 512, (uint64_t)cfg.n_heads * (cfg.qk_nope + cfg.v_head), 64, 128))
     return cudaErrorInvalidValue;
   CombineTcArgs a;
   a.meta = meta; a.part_o = part_o; a.part_lse = part_lse; a.out = out; a.lse = lse; a.hdr = hdr;
-  a.H = cfg.n_heads; a.C = cfg.kv_lora; a.N = cfg.qk_nope; a.V = cfg.v_head; a.B = B;
+  a.q_res = static_cast<const uint16_t*>(q_res);
+  a.scale = cfg.softmax_scale;
+  a.H = cfg.n_heads; a.C = cfg.kv_lora; a.N = cfg.qk_nope; a.V = cfg.v_head; a.R = cfg.qk_rope; a.B = B;
   a.hpg = plan.part_hpg; a.n_slots = plan.n_slots;
   a.max_slots = plan.path == PATH_TC ? plan.ctas_per_group : plan.splits;
-  const int smem = CMB_TC_WSMEM + 1024 + CMB_TC_BCHUNK * a.max_slots * (int)sizeof(float);
+  const int smem = CMB_TC_WSMEM + 1024 + CMB_TC_BCHUNK * (64 + a.max_slots) * (int)sizeof(float);
   cudaError_t e = ensure_smem((const void*)combine_tc_kernel, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(cfg.n_heads, (B + CMB_TC_BCHUNK - 1) / CMB_TC_BCHUNK);

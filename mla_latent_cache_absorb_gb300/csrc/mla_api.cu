@@ -114,6 +114,8 @@ static mla_status make_plan(const mla_config& cfg, int B, DecodePlan* p) {
   size_t off = sizeof(WsHeader);
   p->off_qabs = off;
   off = align256(off + (size_t)B * cfg.n_heads * row * act_size(cfg.act_dtype));
+  p->off_qres = off;
+  if (cfg.act_dtype == MLA_BF16) off = align256(off + (size_t)B * cfg.n_heads * row * 2);
   p->off_po = off;
   off = align256(off + n_part * cfg.kv_lora * sizeof(float));
   p->off_plse = off;
@@ -342,10 +344,11 @@ mla_status mla_decode_absorb(const mla_config* cfg, const void* q, const void* k
   if (positions != nullptr && cfg->rope_inv_freq == nullptr) return MLA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(kv_b, 16)) return MLA_ERR_INVALID_ARG;
   void* q_abs = static_cast<char*>(workspace) + plan.off_qabs;
+  void* q_res = cfg->act_dtype == MLA_BF16 ? static_cast<char*>(workspace) + plan.off_qres : nullptr;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (absorb_tc_supported(*cfg, B))
-    return cuda_status(launch_absorb_tc(*cfg, q, kv_b, positions, q_abs, B, static_cast<WsHeader*>(workspace), s));
-  return cuda_status(launch_absorb(*cfg, q, kv_b, positions, q_abs, B, s));
+    return cuda_status(launch_absorb_tc(*cfg, q, kv_b, positions, q_abs, q_res, B, static_cast<WsHeader*>(workspace), s));
+  return cuda_status(launch_absorb(*cfg, q, kv_b, positions, q_abs, q_res, B, s));
 }
 
 mla_status mla_decode_partial(const mla_config* cfg, const mla_cache* cache, const int32_t* seq_lens,
@@ -362,9 +365,10 @@ mla_status mla_decode_partial(const mla_config* cfg, const mla_cache* cache, con
   float* pl = reinterpret_cast<float*>(ws + plan.off_plse);
   int32_t* meta = reinterpret_cast<int32_t*>(ws + plan.off_meta);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const void* q_res = cfg->act_dtype == MLA_BF16 ? ws + plan.off_qres : nullptr;
   if (plan.path == PATH_TC)
-    return cuda_status(launch_attn_tc(*cfg, *cache, plan, seq_lens, ws + plan.off_qabs, po, pl, meta, B, hdr, s));
-  return cuda_status(launch_attn_simt(*cfg, *cache, plan, seq_lens, ws + plan.off_qabs, po, pl, meta, B, hdr, s));
+    return cuda_status(launch_attn_tc(*cfg, *cache, plan, seq_lens, ws + plan.off_qabs, q_res, po, pl, meta, B, hdr, s));
+  return cuda_status(launch_attn_simt(*cfg, *cache, plan, seq_lens, ws + plan.off_qabs, q_res, po, pl, meta, B, hdr, s));
 }
 
 mla_status mla_decode_combine(const mla_config* cfg, const void* kv_b, const int32_t* seq_lens,
@@ -381,10 +385,12 @@ mla_status mla_decode_combine(const mla_config* cfg, const void* kv_b, const int
   const float* po = reinterpret_cast<const float*>(ws + plan.off_po);
   const float* pl = reinterpret_cast<const float*>(ws + plan.off_plse);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the tensor-core attention scores used bf16 latent queries: correct the LSE for the residual
+  const void* q_res = plan.path == PATH_TC ? ws + plan.off_qres : nullptr;
   if (combine_tc_supported(*cfg, B))
-    return cuda_status(launch_combine_tc(*cfg, plan, kv_b, meta, po, pl, out, lse, B,
+    return cuda_status(launch_combine_tc(*cfg, plan, kv_b, meta, po, pl, q_res, out, lse, B,
                                          reinterpret_cast<WsHeader*>(ws), s));
-  return cuda_status(launch_combine(*cfg, plan, kv_b, meta, po, pl, out, lse, B, s));
+  return cuda_status(launch_combine(*cfg, plan, kv_b, meta, po, pl, q_res, out, lse, B, s));
 }
 
 mla_status mla_decode_attn(const mla_config* cfg, const void* q, const void* kv_b, const mla_cache* cache,
