@@ -23,7 +23,8 @@
  *     holds C+R elements: [kv_lat (C) ; k_pe (R)].
  *   - Pointers marked "device" are CUDA device (or managed) pointers on the current device;
  *     "host" pointers are plain host memory. The caller owns every buffer; the library
- *     allocates no device memory and keeps no per-call state.
+ *     allocates no device memory and keeps no per-call state (mla_decode_attn_noalloc,
+ *     at the end, uses one fixed device array that is part of the library).
  *   - Calls marked "async" only validate on the host and enqueue kernels on `stream`;
  *     they return before the GPU work ends and never synchronise. Errors found on the
  *     host return before anything is enqueued. Conditions only the GPU can see (a bad
@@ -238,6 +239,41 @@ mla_status mla_get_device_error(const void* workspace, int32_t* seq_out, mla_str
 /* Clears the workspace's error word (async, on `stream`). A fresh workspace must be
  * cleared once (or zero-filled) before its first use. */
 mla_status mla_clear_device_error(void* workspace, mla_stream_t stream);
+
+/* ---- allocation-free decode --------------------------------------------------------------
+ * An addition of this library: the papers and write-ups the method comes from have no
+ * counterpart. It serves callers that may not allocate device memory when they decode (an
+ * engine plugin whose host owns all device memory, a server whose memory budget was fixed
+ * at start-up, a loop that cannot take the synchronisation an allocation implies).
+ *
+ * Bytes of the device array mla_decode_attn_noalloc uses as its workspace. */
+#define MLA_NOALLOC_SCRATCH_BYTES (64ull * 1024ull * 1024ull)
+
+/* mla_decode_attn (async) with the workspace taken from one array of
+ * MLA_NOALLOC_SCRATCH_BYTES bytes of device memory that is part of the library
+ * (a file-scope __device__ array, 256-byte aligned, one per device context), not from the
+ * caller. It calls no allocator: no cudaMalloc/cudaFree, no allocating library.
+ *   q, kv_b, cache, seq_lens, positions, out, lse, B, stream: as in mla_decode_attn.
+ *   device_error  device int32[2] (4-byte aligned) or NULL: receives {status, sequence} of
+ *                 the first device error of this call (MLA_OK = 0 when none), written on
+ *                 `stream` after the decode.
+ * Zero state: the array's first 256 bytes (the device error word) must be zero when the
+ * kernels start; every call clears them on `stream` before its launches, and nothing else
+ * in the array is read before it is written in the same call.
+ * First call: the first call on each device (with that device current) looks the array's
+ * address up with cudaGetSymbolAddress, which may load the library's module for that
+ * device; make that first call before any stream capture.
+ * Concurrency: every call on a device shares the one array. Calls that may overlap on the
+ * GPU (different streams without ordering between them, or several host threads) race on
+ * it and corrupt each other's results; order them on one stream or with events.
+ * Errors: MLA_ERR_WORKSPACE when mla_decode_workspace_size(cfg, B) exceeds
+ * MLA_NOALLOC_SCRATCH_BYTES (nothing enqueued); MLA_ERR_CUDA when the address lookup fails;
+ * otherwise as mla_decode_attn. On an argument error found after the size check at most the
+ * clearing of the array's error word has been enqueued. */
+mla_status mla_decode_attn_noalloc(const mla_config* cfg, const void* q, const void* kv_b,
+                                   const mla_cache* cache, const int32_t* seq_lens,
+                                   const int32_t* positions, float* out, float* lse, int32_t B,
+                                   int32_t* device_error, mla_stream_t stream);
 
 #ifdef __cplusplus
 }

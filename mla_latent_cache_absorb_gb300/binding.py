@@ -67,6 +67,8 @@ _SIGS = {
                                      c_size_t, c_void_p]),
     "mla_get_device_error": (c_int32, [c_void_p, POINTER(c_int32), c_void_p]),
     "mla_clear_device_error": (c_int32, [c_void_p, c_void_p]),
+    "mla_decode_attn_noalloc": (c_int32, [_CFG, c_void_p, c_void_p, _CACHE, c_void_p, c_void_p, c_void_p,
+                                          c_void_p, c_int32, c_void_p, c_void_p]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -193,3 +195,13 @@ def mla_get_device_error(workspace, stream=None):
 
 def mla_clear_device_error(workspace, stream=None):
     return _lib.mla_clear_device_error(_p(workspace), _s(stream))
+
+
+MLA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+
+
+def mla_decode_attn_noalloc(cfg, q, kv_b, cache, seq_lens, positions, out, lse, B, device_error=None,
+                            stream=None):
+    return _lib.mla_decode_attn_noalloc(ctypes.byref(cfg), _p(q), _p(kv_b), ctypes.byref(cache),
+                                        _p(seq_lens), _p(positions), _p(out), _p(lse), B,
+                                        _p(device_error), _s(stream))
