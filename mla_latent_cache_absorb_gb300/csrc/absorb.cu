@@ -34,18 +34,81 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
   const int qrow = N + R, arow = C + R;
   float* w_s = sm;                          // [N][ABS_COLS]
   float* q_s = sm + N * ABS_COLS;           // [ABS_BCHUNK][N]
+  const int tid = threadIdx.x;
 
+  // Loads of the first pass go out together: this thread's q_pe pair (the head's B*R/2 pairs
+  // are shared out over the CTAs of the head), its q_nope elements of the first sequence chunk,
+  // then the W_UK slice; nothing waits for a load before all of them are in flight.
+  const int n_pairs = B * (R / 2);
+  const int pair0 = blockIdx.y * ABS_THREADS + tid;
+  const int pair_stride = gridDim.y * ABS_THREADS;
+  float px0 = 0.f, px1 = 0.f;
+  int ppos = 0;
+  double pinv = 0.0;
+  if (pair0 < n_pairs) {
+    const int b = pair0 / (R / 2), p = pair0 % (R / 2);
+    const int64_t qi = ((int64_t)b * H + h) * qrow + N + 2 * p;
+    px0 = Act<DT>::load(q, qi);
+    px1 = Act<DT>::load(q, qi + 1);
+    if (positions != nullptr) {
+      ppos = positions[b];
+      pinv = cfg.rope_inv_freq[p];
+    }
+  }
+  constexpr int QPRE = 16;                  // q_nope elements prefetched per thread
+  const int nb0 = min(ABS_BCHUNK, B);
+  float qv[QPRE];
+#pragma unroll
+  for (int u = 0; u < QPRE; ++u) {
+    const int i = tid + u * ABS_THREADS;
+    qv[u] = 0.f;
+    if (i < nb0 * N) qv[u] = Act<DT>::load(q, ((int64_t)(i / N) * H + h) * qrow + i % N);
+  }
   const int64_t wrow0 = (int64_t)h * (N + V);
   stage_kv_b_rows(w_s, ABS_COLS, kv_b, cfg.kv_b_dtype, wrow0, N, c0, min(ABS_COLS, C - c0), C, ABS_THREADS);
 
-  const int cc = threadIdx.x % ABS_COLS;
-  const int bsub = threadIdx.x / ABS_COLS;   // 0..3
+  // q_pe: rotate at positions[b] (or copy when positions == NULL) into the row's tail
+  for (int i = pair0; i < n_pairs; i += pair_stride) {
+    const int b = i / (R / 2), p = i % (R / 2);
+    if (i != pair0) {
+      const int64_t qi = ((int64_t)b * H + h) * qrow + N + 2 * p;
+      px0 = Act<DT>::load(q, qi);
+      px1 = Act<DT>::load(q, qi + 1);
+      if (positions != nullptr) {
+        ppos = positions[b];
+        pinv = cfg.rope_inv_freq[p];
+      }
+    }
+    const int64_t ai = ((int64_t)b * H + h) * arow + C + 2 * p;
+    if (positions != nullptr) {
+      float c, s;
+      rope_cs_value(pinv, ppos, &c, &s);
+      put(ai, px0 * c - px1 * s);
+      put(ai + 1, px0 * s + px1 * c);
+    } else {
+      put(ai, px0);
+      put(ai + 1, px1);
+    }
+  }
+
+  const int cc = tid % ABS_COLS;
+  const int bsub = tid / ABS_COLS;   // 0..3
   for (int b0 = 0; b0 < B; b0 += ABS_BCHUNK) {
     const int nb = min(ABS_BCHUNK, B - b0);
     __syncthreads();
-    for (int i = threadIdx.x; i < nb * N; i += ABS_THREADS) {
-      const int bb = i / N, n = i % N;
-      q_s[bb * N + n] = Act<DT>::load(q, ((int64_t)(b0 + bb) * H + h) * qrow + n);
+    if (b0 == 0) {
+#pragma unroll
+      for (int u = 0; u < QPRE; ++u) {
+        const int i = tid + u * ABS_THREADS;
+        if (i < nb * N) q_s[i] = qv[u];
+      }
+      for (int i = tid + QPRE * ABS_THREADS; i < nb * N; i += ABS_THREADS)
+        q_s[i] = Act<DT>::load(q, ((int64_t)(i / N) * H + h) * qrow + i % N);
+    } else {
+      for (int i = tid; i < nb * N; i += ABS_THREADS) {
+        const int bb = i / N, n = i % N;
+        q_s[bb * N + n] = Act<DT>::load(q, ((int64_t)(b0 + bb) * H + h) * qrow + n);
+      }
     }
     __syncthreads();
     if (c0 + cc < C) {
@@ -53,25 +116,6 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
         float acc = 0.f;
         for (int n = 0; n < N; ++n) acc = fmaf(q_s[bb * N + n], w_s[n * ABS_COLS + cc], acc);
         put(((int64_t)(b0 + bb) * H + h) * arow + c0 + cc, acc);
-      }
-    }
-  }
-
-  // q_pe: rotate at positions[b] (or copy when positions == NULL) into the row's tail
-  if (blockIdx.y == 0) {
-    for (int i = threadIdx.x; i < B * (R / 2); i += ABS_THREADS) {
-      const int b = i / (R / 2), p = i % (R / 2);
-      const int64_t qi = ((int64_t)b * H + h) * qrow + N + 2 * p;
-      const int64_t ai = ((int64_t)b * H + h) * arow + C + 2 * p;
-      const float x0 = Act<DT>::load(q, qi), x1 = Act<DT>::load(q, qi + 1);
-      if (positions != nullptr) {
-        float c, s;
-        rope_cs(cfg.rope_inv_freq, p, positions[b], &c, &s);
-        put(ai, x0 * c - x1 * s);
-        put(ai + 1, x0 * s + x1 * c);
-      } else {
-        put(ai, x0);
-        put(ai + 1, x1);
       }
     }
   }

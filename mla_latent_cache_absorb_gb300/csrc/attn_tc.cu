@@ -5,12 +5,14 @@
 // same rows); moeflux 0.1.0-pre.3, src/riir/attn/mla_attn_forward.rs, mla_sdpa_folded.
 //
 // Shape: rows of 576 = 512 latent + 64 rope, bf16. One CTA per SM streams 128-row tiles of the
-// cache through shared memory with TMA and computes, for 64 heads at once,
-//     S^T = K_tile . Q^T          (M = 128 rows, N = 64 heads, K = 576)    K-major operands
-//     O^T += V_tile^T . P^T       (M = 4 x 128 latent, N = 64 heads, K = 128 rows)  MN-major
-// with both accumulators in TMEM (S^T 2 x 64 columns, O^T 4 x 64 columns). The row tile is the
-// A operand of both products, so every staged row is shared by all 64 heads and read from
-// shared memory twice. The tile's nine 64-column blocks live in nine 16 KB slots; the rope slot
+// cache through shared memory with TMA and computes, for a group of HG heads at once (HG = 64;
+// 16 or 32 when the model has that few heads),
+//     S^T = K_tile . Q^T          (M = 128 rows, N = HG heads, K = 576)    K-major operands
+//     O^T += V_tile^T . P^T       (M = 4 x 128 latent, N = HG heads, K = 128 rows)  MN-major
+// with both accumulators in TMEM (S^T 2 x HG columns, O^T 4 x HG columns). The row tile is the
+// A operand of both products, so every staged row is shared by all heads of the group and read
+// from shared memory twice. While a tile is processed the producer prefetches the next one
+// into L2. The tile's nine 64-column blocks live in nine 16 KB slots; the rope slot
 // is reused for P^T once QK^T has read it, and each pair of latent slots is handed back to the
 // TMA producer as soon as its 128-column chunk of PV has completed, so the next tile streams in
 // while this one finishes.
@@ -21,7 +23,7 @@
 // segment and on those rare tiles only. Each thread keeps per-head partial sums of p; they are
 // reduced once per segment.
 //
-// Work split: the tiles of all sequences form one list per 64-head group; CTA k of a group takes
+// Work split: the tiles of all sequences form one list per head group; CTA k of a group takes
 // the k-th equal share of it (crossing sequence boundaries), so every SM gets the same number of
 // tiles whatever the length mix. Each (CTA, sequence) piece writes a partial (O normalised, lse)
 // into slot k + b, and the combine stage merges the slots of a sequence.
@@ -211,7 +213,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
   const int cb0 = min(a.B, tid * chunk), cb1 = min(a.B, cb0 + chunk);
   long long mine = 0;
   for (int b = cb0; b < cb1; ++b) mine += seq_tiles(a, b);
-  scan[tid] = mine;
+  long long incl = mine;   // inclusive scan within the warp, then across the six warp totals
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) scan[warp] = incl;
   if (tid == 0) {
     s.abort = 0;
     s.seg_b0 = a.B;
@@ -221,10 +229,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
   }
   __syncwarp();
   __syncthreads();
-  long long before = 0, T = 0;
-  for (int i = 0; i < TC_THREADS; ++i) {   // 192 smem reads, broadcast
-    const long long v = scan[i];
-    if (i < tid) before += v;
+  long long before = incl - mine, T = 0;
+#pragma unroll
+  for (int w = 0; w < TC_THREADS / 32; ++w) {
+    const long long v = scan[w];
+    if (w < warp) before += v;
     T += v;
   }
   long long r0, r1;
@@ -351,6 +360,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
               }
               y[j] = (int)pr;
               bytes += 64 * 128;
+            }
+          }
+          // the next tile of the segment goes to L2 now, so its loads hit L2 once slots free up
+          if (t + 1 < thi) {
+            const long long nt0 = t0 + TC_TILE;
+            for (int j = 0; j < 2; ++j) {
+              const long long lt = nt0 + 64 * j;
+              if (lt < L) {
+                const int64_t pr = a.map.phys(sb, lt);
+                if (pr >= 0)
+                  for (int kb = 0; kb < TC_KB; ++kb) tc::tma_prefetch_l2_2d(&rows_map, kb * 64, (int)pr);
+              }
             }
           }
           for (int i = 0; i < TC_KB; ++i) {
@@ -664,11 +685,10 @@ bool attn_tc_supported(const mla_config& cfg) {
          (cfg.page_size == 0 || cfg.page_size % 64 == 0) && encode_fn() != nullptr;
 }
 
-// Heads per CTA for H heads: the 64-wide group (widths 16 and 32 are compiled for smaller
-// head counts; enabled once their swizzled P^T layouts are validated on the device).
+// Heads per CTA for H heads: the narrowest group width (16, 32 or 64) that holds all heads,
+// else 64-head groups. Narrow groups write proportionally smaller partials.
 int tc_heads_per_cta(int H) {
-  (void)H;
-  return 64;
+  return H <= 16 ? 16 : (H <= 32 ? 32 : 64);
 }
 
 

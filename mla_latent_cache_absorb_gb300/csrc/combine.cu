@@ -6,9 +6,11 @@
 // src/families/deepseek2/attn.rs, encode_mla_v_combine (Q8_0 W_UV). The split + COMBINE pass
 // structure follows turbospark-runtime 0.3.0, src/families/gptoss/attn.rs.
 //
-// Grid (head, 32-wide slice of V, block of sequences). Each CTA merges the splits of its
-// sequences for its head into float32 latent vectors in shared memory, stages its slice of
-// W_UV (dequantised), and forms the dot products.
+// Grid (head, 32-wide slice of V, block of 8 sequences). Each CTA stages its slice of W_UV
+// (dequantised) in shared memory, merges the splits of its sequences for its head into float32
+// latent vectors (every thread keeps several partial loads in flight; with few sequences the
+// slots are shared out over several threads and summed in a fixed order), and forms the dot
+// products one warp per output with the lanes across the latent.
 #include "common.cuh"
 
 #include <math_constants.h>
@@ -17,7 +19,8 @@ namespace mla {
 
 constexpr int CMB_THREADS = 256;
 constexpr int CMB_VJ = 32;      // V outputs per CTA
-constexpr int CMB_BC = 16;      // sequences per CTA
+constexpr int CMB_BC = 8;       // sequences per CTA
+constexpr int CMB_U = 8;        // partial loads in flight per thread
 
 struct CombineArgs {
   const void* kv_b;
@@ -40,21 +43,22 @@ __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
   const int b0 = blockIdx.z * CMB_BC;
   const int nb = min(CMB_BC, a.B - b0);
   const int nj = min(CMB_VJ, a.V - j0);
-  const int Cp = a.C + 1;                  // padded W row: conflict-free across j
-  float* w_s = sm;                         // [CMB_VJ][C+1]
-  float* vc_s = w_s + CMB_VJ * Cp;         // [CMB_BC][C]
-  float* wt_s = vc_s + CMB_BC * a.C;       // [CMB_BC][max_slots] split weights
-  float* lse_s = wt_s + CMB_BC * a.max_slots;  // [CMB_BC]
-  int* first_s = reinterpret_cast<int*>(lse_s + CMB_BC);  // [CMB_BC]
-  int* cnt_s = first_s + CMB_BC;                           // [CMB_BC]
+  const int C = a.C;
+  const int C4 = (C + 3) / 4;               // latent in groups of 4
+  float* w_s = sm;                          // [CMB_VJ][4*C4]
+  float* vc_s = w_s + CMB_VJ * 4 * C4;      // [CMB_BC][4*C4]
+  float4* red_s = reinterpret_cast<float4*>(vc_s + CMB_BC * 4 * C4);   // [CMB_THREADS]
+  float* wt_s = reinterpret_cast<float*>(red_s + CMB_THREADS);         // [CMB_BC][max_slots]
+  float* lse_s = wt_s + CMB_BC * a.max_slots;                          // [CMB_BC]
+  int* first_s = reinterpret_cast<int*>(lse_s + CMB_BC);               // [CMB_BC]
+  int* cnt_s = first_s + CMB_BC;                                        // [CMB_BC]
   const int pg = h / a.hpg, hh = h % a.hpg;
-  // partial (slot, head) -> element offsets
   auto lse_at = [&](int slot) { return ((int64_t)pg * a.n_slots + slot) * a.hpg + hh; };
 
   const int64_t wrow0 = (int64_t)h * (a.N + a.V) + a.N + j0;
-  stage_kv_b_rows(w_s, Cp, a.kv_b, a.kv_b_dtype, wrow0, nj, 0, a.C, a.C, CMB_THREADS);
+  stage_kv_b_rows(w_s, 4 * C4, a.kv_b, a.kv_b_dtype, wrow0, nj, 0, C, C, CMB_THREADS);
 
-  // split weights: one warp per sequence
+  // split weights exp(lse_s - lse): one warp per sequence
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int bb = warp; bb < nb; bb += CMB_THREADS / 32) {
     const int b = b0 + bb;
@@ -75,40 +79,98 @@ __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < nb * a.C; i += CMB_THREADS) {
-    const int bb = i / a.C, c = i % a.C;
-    float v = 0.f;
-    if (isnan(lse_s[bb])) {
-      v = CUDART_NAN_F;
-    } else {
-      for (int s = 0; s < cnt_s[bb]; ++s) {
-        const float w = wt_s[bb * a.max_slots + s];
-        if (w != 0.f) v = fmaf(w, a.part_o[lse_at(first_s[bb] + s) * a.C + c], v);   // empty slots: skip
+
+  // vc[bb][4g..4g+3] = sum_s w_s * O_s; item = (bb, g); `split` threads share an item's slots
+  const int nitems = nb * C4;
+  int split = 1;
+  while (split < 8 && 2 * split * nitems <= CMB_THREADS) split *= 2;
+  const bool vec = (C % 4) == 0;
+  for (int it = threadIdx.x; it < nitems * split; it += CMB_THREADS) {
+    const int item = it % nitems, sp = it / nitems;
+    const int bb = item / C4, g = item % C4;
+    const int ns = cnt_s[bb], first = first_s[bb];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = sp; s0 < ns; s0 += split * CMB_U) {
+      float4 x[CMB_U];
+#pragma unroll
+      for (int u = 0; u < CMB_U; ++u) {
+        const int s = s0 + u * split;
+        x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (s < ns) {
+          const float* src = a.part_o + lse_at(first + s) * C + 4 * g;
+          if (vec) {
+            x[u] = *reinterpret_cast<const float4*>(src);
+          } else {
+            x[u].x = src[0];
+            if (4 * g + 1 < C) x[u].y = src[1];
+            if (4 * g + 2 < C) x[u].z = src[2];
+            if (4 * g + 3 < C) x[u].w = src[3];
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < CMB_U; ++u) {
+        const int s = s0 + u * split;
+        const float w = (s < ns) ? wt_s[bb * a.max_slots + s] : 0.f;
+        if (w != 0.f) {   // empty slots carry weight 0 and unwritten data: skip, never 0 * x
+          acc.x = fmaf(w, x[u].x, acc.x);
+          acc.y = fmaf(w, x[u].y, acc.y);
+          acc.z = fmaf(w, x[u].z, acc.z);
+          acc.w = fmaf(w, x[u].w, acc.w);
+        }
       }
     }
-    vc_s[bb * a.C + c] = v;
+    if (split == 1) {
+      if (isnan(lse_s[bb])) acc = make_float4(CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F);
+      reinterpret_cast<float4*>(vc_s)[bb * C4 + g] = acc;
+    } else {
+      red_s[it] = acc;
+    }
+  }
+  if (split > 1) {
+    __syncthreads();
+    for (int item = threadIdx.x; item < nitems; item += CMB_THREADS) {
+      const int bb = item / C4;
+      float4 v = red_s[item];
+      for (int sp = 1; sp < split; ++sp) {   // fixed order: results do not depend on timing
+        const float4 t = red_s[sp * nitems + item];
+        v.x += t.x; v.y += t.y; v.z += t.z; v.w += t.w;
+      }
+      if (isnan(lse_s[bb])) v = make_float4(CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F);
+      reinterpret_cast<float4*>(vc_s)[item] = v;
+    }
   }
   __syncthreads();
   if (a.q_res != nullptr) {
     // the scores used bf16 latent queries q_hi = q' - res: to first order the exact log-sum-exp
     // is lse + scale * (sum_t p_t kv_lat_t) . res = lse + scale * vc . res
     for (int bb = warp; bb < nb; bb += CMB_THREADS / 32) {
-      const uint16_t* res = a.q_res + ((int64_t)(b0 + bb) * a.H + h) * (a.C + a.R);
+      const uint16_t* res = a.q_res + ((int64_t)(b0 + bb) * a.H + h) * (C + a.R);
       float d = 0.f;
-      for (int c = lane; c < a.C; c += 32) d = fmaf(vc_s[bb * a.C + c], bf16_bits_to_f32(res[c]), d);
+      for (int c = lane; c < C; c += 32) d = fmaf(vc_s[bb * 4 * C4 + c], bf16_bits_to_f32(res[c]), d);
       d = warp_sum(d);
       if (lane == 0) lse_s[bb] += a.scale * d;
     }
     __syncthreads();
   }
-  // out[b, h, j0 + j]: one warp per sequence, lane = j
-  for (int bb = warp; bb < nb; bb += CMB_THREADS / 32) {
-    if (lane < nj) {
-      float acc = 0.f;
-      const float* wr = w_s + lane * Cp;
-      const float* vr = vc_s + bb * a.C;
-      for (int c = 0; c < a.C; ++c) acc = fmaf(wr[c], vr[c], acc);
-      a.out[((int64_t)(b0 + bb) * a.H + h) * a.V + j0 + lane] = acc;
+  // out[b, h, j0 + j]: one warp per output j, lanes across the latent, all sequences at once
+  for (int j = warp; j < nj; j += CMB_THREADS / 32) {
+    float acc[CMB_BC];
+#pragma unroll
+    for (int bb = 0; bb < CMB_BC; ++bb) acc[bb] = 0.f;
+    const float* wr = w_s + j * 4 * C4;
+    for (int c = lane; c < C; c += 32) {
+      const float wv = wr[c];
+#pragma unroll
+      for (int bb = 0; bb < CMB_BC; ++bb)
+        if (bb < nb) acc[bb] = fmaf(wv, vc_s[bb * 4 * C4 + c], acc[bb]);
+    }
+#pragma unroll
+    for (int bb = 0; bb < CMB_BC; ++bb) {
+      if (bb < nb) {
+        const float v = warp_sum(acc[bb]);
+        if (lane == 0) a.out[((int64_t)(b0 + bb) * a.H + h) * a.V + j0 + j] = v;
+      }
     }
   }
   if (blockIdx.y == 0 && a.lse != nullptr)
@@ -128,7 +190,8 @@ cudaError_t launch_combine(const mla_config& cfg, const DecodePlan& plan, const 
   // most slots one sequence can span: splits (CUDA-core path) or CTAs per group (tensor path)
   a.max_slots = plan.path == PATH_TC ? plan.ctas_per_group : plan.splits;
   dim3 grid(cfg.n_heads, (cfg.v_head + CMB_VJ - 1) / CMB_VJ, (B + CMB_BC - 1) / CMB_BC);
-  const size_t smem = sizeof(float) * ((size_t)CMB_VJ * (cfg.kv_lora + 1) + (size_t)CMB_BC * cfg.kv_lora +
+  const size_t c4 = 4 * (size_t)((cfg.kv_lora + 3) / 4);
+  const size_t smem = sizeof(float) * ((size_t)CMB_VJ * c4 + (size_t)CMB_BC * c4 + 4 * (size_t)CMB_THREADS +
                                        (size_t)CMB_BC * a.max_slots + 3 * CMB_BC);
   cudaError_t e = ensure_smem((const void*)combine_kernel, (int)smem);
   if (e != cudaSuccess) return e;

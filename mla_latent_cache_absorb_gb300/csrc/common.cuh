@@ -58,45 +58,71 @@ __device__ __forceinline__ float kv_b_load(const void* kv_b, int dtype, int64_t 
   }
 }
 
+// Eight consecutive kv_b elements of row r from column c as float32 (zero past ncols_left):
+// one 16-byte load for bf16, two for f32, the 8 codes plus the block scale for Q8_0.
+__device__ __forceinline__ void kv_b_load8(float v[8], const void* kv_b, int dtype, int64_t r, int c,
+                                           int ncols_left, int C) {
+  if (ncols_left >= 8 && (C % 8) == 0) {
+    if (dtype == MLA_BF16) {
+      const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(kv_b) + r * C + c);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[2 * e] = __uint_as_float(w[e] << 16);
+        v[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+      }
+    } else if (dtype == MLA_F32) {
+      const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(kv_b) + r * C + c);
+      const float4 a = src[0], b = src[1];
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+      const uint8_t* blk = static_cast<const uint8_t*>(kv_b) + r * (int64_t)(C / 32) * 34 + (c / 32) * 34;
+      const uint16_t dbits = static_cast<uint16_t>(blk[0]) | (static_cast<uint16_t>(blk[1]) << 8);
+      const float d = __half2float(__ushort_as_half(dbits));
+      const int o = 2 + (c & 31);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = d * static_cast<float>(static_cast<int8_t>(blk[o + e]));
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = (e < ncols_left) ? kv_b_load(kv_b, dtype, r, c + e, C) : 0.f;
+  }
+}
+
 // Stage kv_b rows [r0, r0 + nrows) x columns [c0, c0 + ncols) as float32 into dst (row stride
-// dst_stride floats; columns past ncols, up to a multiple of 8, are zero). Each item is 8
-// consecutive columns: one 16-byte load for bf16, two for f32, and the 8 codes plus the block
-// scale for Q8_0; every thread issues all of its loads before using them.
+// dst_stride floats; columns past ncols, up to a multiple of 8, are zero), in items of 8
+// columns; each thread issues the loads of four items before it stores any of them.
 __device__ __forceinline__ void stage_kv_b_rows(float* dst, int dst_stride, const void* kv_b, int dtype,
                                                 int64_t r0, int nrows, int c0, int ncols, int C, int nthreads) {
+  constexpr int U = 4;   // items in flight per thread
   const int ngrp = (ncols + 7) / 8;
-  for (int i = threadIdx.x; i < nrows * ngrp; i += nthreads) {
-    const int r = i / ngrp, g = i % ngrp;
-    const int c = c0 + 8 * g;
-    float v[8];
-    if (8 * g + 8 <= ncols && (C % 8) == 0) {
-      if (dtype == MLA_BF16) {
-        const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(kv_b) + (r0 + r) * C + c);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  const int total = nrows * ngrp;
+  for (int base = threadIdx.x; base < total; base += nthreads * U) {
+    float v[U][8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          v[2 * e] = __uint_as_float(w[e] << 16);
-          v[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-        }
-      } else if (dtype == MLA_F32) {
-        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(kv_b) + (r0 + r) * C + c);
-        const float4 a = src[0], b = src[1];
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-      } else {
-        const uint8_t* blk = static_cast<const uint8_t*>(kv_b) + (r0 + r) * (int64_t)(C / 32) * 34 + (c / 32) * 34;
-        const uint16_t dbits = static_cast<uint16_t>(blk[0]) | (static_cast<uint16_t>(blk[1]) << 8);
-        const float d = __half2float(__ushort_as_half(dbits));
-        const int o = 2 + (c & 31);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = d * static_cast<float>(static_cast<int8_t>(blk[o + e]));
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * nthreads;
+      if (i < total) {
+        const int r = i / ngrp, g = i % ngrp;
+        kv_b_load8(v[u], kv_b, dtype, r0 + r, c0 + 8 * g, ncols - 8 * g, C);
       }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = (8 * g + e < ncols) ? kv_b_load(kv_b, dtype, r0 + r, c + e, C) : 0.f;
     }
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-      if (8 * g + e < dst_stride) dst[r * dst_stride + 8 * g + e] = v[e];
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * nthreads;
+      if (i < total) {
+        const int r = i / ngrp, g = i % ngrp;
+        float* d = dst + r * dst_stride + 8 * g;
+        if (8 * g + 8 <= dst_stride && (reinterpret_cast<uintptr_t>(d) & 15) == 0) {
+          reinterpret_cast<float4*>(d)[0] = make_float4(v[u][0], v[u][1], v[u][2], v[u][3]);
+          reinterpret_cast<float4*>(d)[1] = make_float4(v[u][4], v[u][5], v[u][6], v[u][7]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (8 * g + e < dst_stride) d[e] = v[u][e];
+        }
+      }
+    }
   }
 }
 
@@ -132,12 +158,16 @@ __device__ __forceinline__ float warp_max(float v) {
 // RoPE angle for pair i at position pos. The angle pos * inv_freq[i] is formed in float64 and
 // reduced to [-pi, pi] there (a - 2*pi*round(a / 2*pi)), so positions in the hundreds of
 // thousands keep full accuracy; the reduced angle then goes to the float sincos.
-__device__ __forceinline__ void rope_cs(const double* inv_freq, int i, int pos, float* c, float* s) {
+__device__ __forceinline__ void rope_cs_value(double inv_freq, int pos, float* c, float* s) {
   const double two_pi = 6.283185307179586476925286766559;
-  const double a = static_cast<double>(pos) * inv_freq[i];
+  const double a = static_cast<double>(pos) * inv_freq;
   const double turns = rint(a * (1.0 / two_pi));
   const float r = static_cast<float>(fma(-turns, two_pi, a));
   sincosf(r, s, c);
+}
+
+__device__ __forceinline__ void rope_cs(const double* inv_freq, int i, int pos, float* c, float* s) {
+  rope_cs_value(inv_freq[i], pos, c, s);
 }
 
 // ---- decode plan: how the rows of a sequence are split, and the workspace layout -------------
