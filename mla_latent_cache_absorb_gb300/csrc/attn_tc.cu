@@ -11,13 +11,13 @@
 //     O^T += V_tile^T . P^T       (M = 4 x 128 latent, N = HG heads, K = 128 rows)  MN-major
 // with both accumulators in TMEM (S^T 2 x HG columns, O^T 4 x HG columns). The row tile is the
 // A operand of both products, so every staged row is shared by all heads of the group and read
-// from shared memory twice. While a tile is processed the producer prefetches the next one
-// into L2. The tile's nine 64-column blocks live in nine 16 KB slots; the rope slot
+// from shared memory twice. The tile's nine 64-column blocks live in nine 16 KB slots; the rope slot
 // is reused for P^T once QK^T has read it, and each pair of latent slots is handed back to the
 // TMA producer as soon as its 128-column chunk of PV has completed, so the next tile streams in
 // while this one finishes.
 //
-// Softmax (four warps, one thread per tile row) runs in the log2 domain with a per-head running
+// Softmax: one thread per tile row in each of one or two warpgroups (HG = 64: two, each owning
+// 32 heads, so two warps share every SM sub-partition), log2 domain, with a per-head running
 // maximum that is only raised when a score exceeds it by more than 2^8: the exact column max
 // (a cross-thread reduction) and the rescale of O^T in TMEM happen on the first tile of a
 // segment and on those rare tiles only. Each thread keeps per-head partial sums of p; they are
@@ -28,9 +28,11 @@
 // tiles whatever the length mix. Each (CTA, sequence) piece writes a partial (O normalised, lse)
 // into slot k + b, and the combine stage merges the slots of a sequence.
 //
-// Roles: warp 0 issues TMA loads, warp 1 owns TMEM and issues the MMAs (one thread), warps 2-5
-// do the softmax and the epilogue. Every mbarrier wait is bounded; on a timeout the CTA records
-// MLA_ERR_TIMEOUT, every role stops, and TMEM is freed before exit.
+// Roles: warps 0-1 issue the TMA loads (alternate 64-column blocks of each tile; one issuing
+// thread alone streams well below what an SM can take in), warp 2 owns TMEM and issues the MMAs
+// (one thread), the remaining warps do the softmax and the epilogue. Every mbarrier wait is
+// bounded; on a timeout the CTA records MLA_ERR_TIMEOUT, every role stops, and TMEM is freed
+// before exit.
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -45,7 +47,9 @@ constexpr int TC_TILE = 128;       // rows per tile (MMA M)
 constexpr int TC_KB = 9;           // 64-column blocks per row (576 / 64)
 constexpr int TC_LAT_KB = 8;       // latent blocks (512 / 64)
 constexpr int TC_SLOT_BYTES = TC_TILE * 128;   // 16 KB
-constexpr int TC_THREADS = 192;
+constexpr int TC_PRODUCERS = 2;   // TMA producer warps (a single issuing thread tops out near 45 GB/s)
+constexpr int TC_MMA_WARP = TC_PRODUCERS;
+constexpr int TC_SM_WARP0 = TC_PRODUCERS + 1;   // first softmax warp
 constexpr uint64_t WAIT_NS = 200ull * 1000 * 1000;   // a wait gives up after 200 ms
 
 // Per head-group width HG (the MMA N: 16, 32 or 64 heads per CTA).
@@ -55,6 +59,11 @@ struct Cfg {
   // Q blocks: 9 of the bf16 fused query rows + the bf16 residual of the rope block, so the
   // rope part of every score is exact to ~2^-16 (hi + lo)
   static constexpr int Q_BLOCKS = TC_KB + 1;
+  // softmax warpgroups: each owns HW = HG / NWG heads of every tile row (four warps, one per
+  // TMEM lane quarter)
+  static constexpr int NWG = HG == 64 ? 2 : 1;
+  static constexpr int HW = HG / NWG;
+  static constexpr int THREADS = 32 * TC_SM_WARP0 + 128 * NWG;
   static constexpr int SMEM_DYN = TC_KB * TC_SLOT_BYTES + Q_BLOCKS * QBLK_BYTES + 1024;
   static constexpr uint32_t O_COL = 0;                        // O^T chunks: 4 x HG columns
   static constexpr uint32_t S_COL = 4 * HG;                   // S^T buffers: 2 x HG columns
@@ -92,7 +101,7 @@ struct Smem {
   int abort;
   int seg_b0;
   long long seg_p0;
-  int bad_page[2];        // per segment parity: the producer runs at most one segment ahead
+  int bad_page[2][2];     // [segment parity][warpgroup]: the producers run at most one segment ahead
   float red[4][TC_HG];
   float m2[TC_HG];        // running max per head, log2 units
   float alpha[TC_HG];     // rescale factors (then 1/l in the epilogue)
@@ -104,23 +113,24 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// OR of `v` over the 128 softmax threads (named barrier 1), returned to all of them.
-__device__ __forceinline__ bool softmax_vote_or(bool v) {
+// OR of `v` over the 128 threads of softmax warpgroup `wg` (named barrier 1 + wg), returned to
+// all of them.
+__device__ __forceinline__ bool softmax_vote_or(bool v, int wg) {
   uint32_t out;
   asm volatile(
       "{\n\t.reg .pred pi, po;\n\t"
       "setp.ne.u32 pi, %1, 0;\n\t"
-      "barrier.red.or.pred po, 1, 128, pi;\n\t"
+      "barrier.red.or.pred po, %2, 128, pi;\n\t"
       "selp.u32 %0, 1, 0, po;\n\t}"
       : "=r"(out)
-      : "r"((uint32_t)v)
+      : "r"((uint32_t)v), "r"(1 + wg)
       : "memory");
   return out != 0;
 }
 
-__device__ __forceinline__ void softmax_bar() {
+__device__ __forceinline__ void softmax_bar(int wg) {
   __syncwarp();
-  asm volatile("barrier.sync 1, 128;" ::: "memory");
+  asm volatile("barrier.sync %0, 128;" ::"r"(1 + wg) : "memory");
 }
 
 
@@ -156,13 +166,12 @@ __device__ __forceinline__ bool wait_bar(Smem& s, uint64_t* bar, uint32_t parity
 
 // Softmax-side wait: every softmax thread polls the barrier itself (a warp whose lane 0 alone
 // polled would run split afterwards: collective operations then serialise and the warp's
-// arrivals at the group barrier stop lining up), then all 128 agree on the outcome, so they
-// always leave (or stay in) their loops together and never strand a group barrier.
-__device__ __forceinline__ bool softmax_wait(Smem& s, uint64_t* bar, uint32_t parity, int sidx) {
-  (void)sidx;
+// arrivals at the group barrier stop lining up), then the warpgroup's 128 threads agree on the
+// outcome, so they always leave (or stay in) their loops together and never strand a barrier.
+__device__ __forceinline__ bool softmax_wait(Smem& s, uint64_t* bar, uint32_t parity, int wg) {
   const bool ok = wait_bar(s, bar, parity);
   __syncwarp();
-  return !softmax_vote_or(!ok);
+  return !softmax_vote_or(!ok, wg);
 }
 
 __device__ __forceinline__ void fail(Smem& s, WsHeader* hdr, int b) {
@@ -194,7 +203,7 @@ struct SegIter {
 };
 
 template <int HG>
-__global__ void __launch_bounds__(TC_THREADS, 1)
+__global__ void __launch_bounds__(Cfg<HG>::THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_constant__ CUtensorMap q_map,
                const __grid_constant__ CUtensorMap qres_map, TcArgs a) {
   extern __shared__ uint8_t dyn_raw[];
@@ -209,7 +218,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
   const int k = blockIdx.x / a.G;
 
   // ---- every thread: total tile count (block scan over per-thread chunks of sequences) ----------
-  const int chunk = (a.B + TC_THREADS - 1) / TC_THREADS;
+  constexpr int NT = Cfg<HG>::THREADS;
+  const int chunk = (a.B + NT - 1) / NT;
   const int cb0 = min(a.B, tid * chunk), cb1 = min(a.B, cb0 + chunk);
   long long mine = 0;
   for (int b = cb0; b < cb1; ++b) mine += seq_tiles(a, b);
@@ -224,14 +234,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
     s.abort = 0;
     s.seg_b0 = a.B;
     s.seg_p0 = 0;
-    s.bad_page[0] = 0;
-    s.bad_page[1] = 0;
+    s.bad_page[0][0] = s.bad_page[0][1] = 0;
+    s.bad_page[1][0] = s.bad_page[1][1] = 0;
   }
   __syncwarp();
   __syncthreads();
   long long before = incl - mine, T = 0;
 #pragma unroll
-  for (int w = 0; w < TC_THREADS / 32; ++w) {
+  for (int w = 0; w < NT / 32; ++w) {
     const long long v = scan[w];
     if (w < warp) before += v;
     T += v;
@@ -300,15 +310,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
     tc::mbar_init(&s.q_empty, 1);
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&s.s_full[i], 1);
-      tc::mbar_init(&s.s_empty[i], 128);
+      tc::mbar_init(&s.s_empty[i], 128 * Cfg<HG>::NWG);
     }
-    tc::mbar_init(&s.p_full, 128);
+    tc::mbar_init(&s.p_full, 128 * Cfg<HG>::NWG);
     tc::mbar_init(&s.o_done, 1);
-    tc::mbar_init(&s.o_empty, 128);
+    tc::mbar_init(&s.o_empty, 128 * Cfg<HG>::NWG);
     tc::mbar_init(&s.mma_fin, 1);
     tc::fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == TC_MMA_WARP) {
     tc::tmem_alloc(&s.tmem_base, Cfg<HG>::TMEM_COLS);
     tc::tmem_relinquish();
   }
@@ -325,9 +335,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
   const uint32_t tmem = s.tmem_base;
   SegIter it{s.seg_b0, s.seg_p0, r0, r1};
 
-  if (warp == 0) {
-    // ================================ TMA producer ================================
+  if (warp < TC_PRODUCERS) {
+    // ============================ TMA producers ============================
+    // Producer p issues the blocks kb = p, p + 2, ... of every tile (the loads of one tile are
+    // spread over two issuing threads); producer 0 also loads each segment's queries.
     if (lane == 0) {
+      const int pw = warp;
       int sb = 0, tlo, thi;
       int seg = 0;
       long long n = 0;            // global tile counter of this CTA
@@ -336,12 +349,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
       int q_loaded = -1;
       bool ok = true;
       while (ok && it.next(a, &sb, &tlo, &thi)) {
-        if (seg > 0 && !wait_bar(s, &s.q_empty, (seg - 1) & 1)) { ok = false; break; }
-        tc::mbar_arrive_expect_tx(&s.q_full, Cfg<HG>::Q_BLOCKS * Cfg<HG>::QBLK_BYTES);
-        const int qrow = sb * a.H + g * HG;
-        for (int kb = 0; kb < TC_KB; ++kb) tc::tma_load_2d(qs + kb * Cfg<HG>::QBLK_BYTES, &q_map, kb * 64, qrow, &s.q_full);
-        tc::tma_load_2d(qs + TC_KB * Cfg<HG>::QBLK_BYTES, &qres_map, TC_LAT_KB * 64, qrow, &s.q_full);
-        q_loaded = seg;
+        if (pw == 0) {
+          if (seg > 0 && !wait_bar(s, &s.q_empty, (seg - 1) & 1)) { ok = false; break; }
+          tc::mbar_arrive_expect_tx(&s.q_full, Cfg<HG>::Q_BLOCKS * Cfg<HG>::QBLK_BYTES);
+          const int qrow = sb * a.H + g * HG;
+          for (int kb = 0; kb < TC_KB; ++kb)
+            tc::tma_load_2d(qs + kb * Cfg<HG>::QBLK_BYTES, &q_map, kb * 64, qrow, &s.q_full);
+          tc::tma_load_2d(qs + TC_KB * Cfg<HG>::QBLK_BYTES, &qres_map, TC_LAT_KB * 64, qrow, &s.q_full);
+          q_loaded = seg;
+        }
         const long long L = a.seq_lens[sb];
         for (int t = tlo; t < thi && ok; ++t) {
           const long long t0 = (long long)t * TC_TILE;
@@ -354,7 +370,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
             if (lt < L) {
               int64_t pr = a.map.phys(sb, lt);
               if (pr < 0) {   // out-of-range page id: load a valid row, flag the segment
-                atomicExch(&s.bad_page[seg & 1], 1);
+                for (int w = 0; w < Cfg<HG>::NWG; ++w) atomicExch(&s.bad_page[seg & 1][w], 1);
                 set_error(a.hdr, MLA_ERR_BAD_PAGE, sb);
                 pr = 0;
               }
@@ -362,20 +378,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
               bytes += 64 * 128;
             }
           }
-          // the next tile of the segment goes to L2 now, so its loads hit L2 once slots free up
-          if (t + 1 < thi) {
-            const long long nt0 = t0 + TC_TILE;
-            for (int j = 0; j < 2; ++j) {
-              const long long lt = nt0 + 64 * j;
-              if (lt < L) {
-                const int64_t pr = a.map.phys(sb, lt);
-                if (pr >= 0)
-                  for (int kb = 0; kb < TC_KB; ++kb) tc::tma_prefetch_l2_2d(&rows_map, kb * 64, (int)pr);
-              }
-            }
-          }
-          for (int i = 0; i < TC_KB; ++i) {
-            const int kb = (i < TC_LAT_KB) ? i : TC_LAT_KB;   // latent blocks first, rope last
+          // latent blocks 0..7 in order, the rope block (8) last: the order QK^T consumes them
+          for (int kb = pw; kb < TC_KB; kb += TC_PRODUCERS) {
             if (n > 0 && !wait_bar(s, &s.empty[kb], (uint32_t)((n - 1) & 1))) { ok = false; break; }
             tc::mbar_arrive_expect_tx(&s.full[kb], bytes);
             for (int j = 0; j < 2; ++j)
@@ -390,12 +394,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
       if (!ok) {
         fail(s, a.hdr, sb);
         // wait (bounded) for every copy already issued, so none lands after the CTA exits
-        for (int kb = 0; kb < TC_KB; ++kb)
+        for (int kb = pw; kb < TC_KB; kb += TC_PRODUCERS)
           if (last_n[kb] >= 0) tc::mbar_wait(&s.full[kb], (uint32_t)(last_n[kb] & 1), WAIT_NS);
         if (q_loaded >= 0) tc::mbar_wait(&s.q_full, (uint32_t)(q_loaded & 1), WAIT_NS);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == TC_MMA_WARP) {
     // ================================ MMA issuer ================================
     if (lane == 0) {
       const uint32_t idesc_qk = tc::idesc_bf16_f32(TC_TILE, HG, 0, 0);
@@ -460,33 +464,38 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
     }
   } else {
     // ================================ softmax + epilogue ================================
+    // Warpgroup wg owns heads [h0, h0 + HW) of every row: its own running maxima, votes and
+    // rescales (TMEM columns and P^T chunks of those heads only), its own named barrier.
+    constexpr int HW = Cfg<HG>::HW;
+    const int wg = (warp - TC_SM_WARP0) >> 2;
+    const int h0 = wg * HW;
     const int q = warp & 3;                  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;           // tile row (and O^T latent row within a chunk)
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    const int sidx = tid - 64;               // 0..127
+    const int sidx = (tid - 32 * TC_SM_WARP0) & 127;   // 0..127 within the warpgroup
     int sb = 0, tlo, thi;
     int seg = 0;
     long long n = 0;
     bool ok = true;
-    constexpr int CW = HG < 32 ? HG : 32;    // TMEM columns per load
-    constexpr int NCH = HG / CW;
-    float lp[HG];                            // this row's share of each head's sum of p
+    constexpr int CW = HW < 32 ? HW : 32;    // TMEM columns per load
+    constexpr int NCH = HW / CW;
+    float lp[HW];                            // this row's share of each owned head's sum of p
     uint8_t* prow = slots + TC_LAT_KB * TC_SLOT_BYTES;   // P^T lives in the rope slot
     while (ok && it.next(a, &sb, &tlo, &thi)) {
       const long long L = a.seq_lens[sb];
 #pragma unroll
-      for (int h = 0; h < HG; ++h) lp[h] = 0.f;
-      if (sidx < HG) s.m2[sidx] = -CUDART_INF_F;
+      for (int h = 0; h < HW; ++h) lp[h] = 0.f;
+      if (sidx < HW) s.m2[h0 + sidx] = -CUDART_INF_F;
       for (int t = tlo; t < thi; ++t, ++n) {
         const int sbuf = (int)(n & 1);
-        const uint32_t s_addr = tmem + lane_base + Cfg<HG>::S_COL + sbuf * HG;
-        if (!softmax_wait(s, &s.s_full[sbuf], (uint32_t)((n >> 1) & 1), sidx)) { ok = false; break; }
+        const uint32_t s_addr = tmem + lane_base + Cfg<HG>::S_COL + sbuf * HG + h0;
+        if (!softmax_wait(s, &s.s_full[sbuf], (uint32_t)((n >> 1) & 1), wg)) { ok = false; break; }
         tc::tc_fence_after();
         const bool valid = (long long)t * TC_TILE + row < L;
         const bool first = (t == tlo);
         // PV of the previous tile has completed (its commit preceded this tile's QK commit);
         // waiting keeps the o_done phases in step for every softmax thread
-        if (n > 0 && !softmax_wait(s, &s.o_done, (uint32_t)((n - 1) & 1), sidx)) { ok = false; break; }
+        if (n > 0 && !softmax_wait(s, &s.o_done, (uint32_t)((n - 1) & 1), wg)) { ok = false; break; }
         tc::tc_fence_after();
         // pass 1: does any score exceed its head's running max by more than the threshold?
         // (TMEM loads are warp-collective: every lane loads, validity only gates the arithmetic)
@@ -498,11 +507,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
           if (valid) {
 #pragma unroll
             for (int j = 0; j < CW; ++j)
-              need |= fmaf(__uint_as_float(r[j]), a.scale_log2, -s.m2[half * CW + j]) > RESCALE_THRESHOLD;
+              need |= fmaf(__uint_as_float(r[j]), a.scale_log2, -s.m2[h0 + half * CW + j]) > RESCALE_THRESHOLD;
           }
         }
         __syncwarp();
-        if (softmax_vote_or(need)) {
+        if (softmax_vote_or(need, wg)) {
           // exact per-head maximum over the tile's valid rows; raise the running max
           for (int half = 0; half < NCH; ++half) {
             uint32_t r[CW];
@@ -513,40 +522,42 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
               float v = valid ? __uint_as_float(r[j]) * a.scale_log2 : -CUDART_INF_F;
 #pragma unroll
               for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-              if (lane == 0) s.red[q][half * CW + j] = v;
+              if (lane == 0) s.red[q][h0 + half * CW + j] = v;
             }
           }
-          softmax_bar();
-          if (sidx < HG) {
-            const float mt = fmaxf(fmaxf(s.red[0][sidx], s.red[1][sidx]), fmaxf(s.red[2][sidx], s.red[3][sidx]));
-            const float mo = s.m2[sidx];
+          softmax_bar(wg);
+          if (sidx < HW) {
+            const int h = h0 + sidx;
+            const float mt = fmaxf(fmaxf(s.red[0][h], s.red[1][h]), fmaxf(s.red[2][h], s.red[3][h]));
+            const float mo = s.m2[h];
             const float mn = fmaxf(mo, mt);
-            s.alpha[sidx] = first ? 0.f : ex2(mo - mn);
-            s.m2[sidx] = mn;
+            s.alpha[h] = first ? 0.f : ex2(mo - mn);
+            s.m2[h] = mn;
           }
-          softmax_bar();
+          softmax_bar(wg);
 #pragma unroll
-          for (int h = 0; h < HG; ++h) lp[h] *= s.alpha[h];
+          for (int h = 0; h < HW; ++h) lp[h] *= s.alpha[h0 + h];
           if (!first) {
-            // rescale the four O^T chunks this thread's TMEM lane holds (PV of the previous
-            // tile has completed, see the o_done wait above)
+            // rescale the four O^T chunks this thread's TMEM lane holds, owned heads only (PV
+            // of the previous tile has completed, see the o_done wait above)
             for (int cc = 0; cc < 4; ++cc) {
               for (int half = 0; half < NCH; ++half) {
                 uint32_t r[CW];
-                const uint32_t ta = tmem + lane_base + Cfg<HG>::O_COL + cc * HG + half * CW;
+                const uint32_t ta = tmem + lane_base + Cfg<HG>::O_COL + cc * HG + h0 + half * CW;
                 tc::tmem_ld<CW>(ta, r);
                 tc::tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < CW; ++j)
-                  r[j] = __float_as_uint(__uint_as_float(r[j]) * s.alpha[half * CW + j]);
+                  r[j] = __float_as_uint(__uint_as_float(r[j]) * s.alpha[h0 + half * CW + j]);
                 tc::tmem_st<CW>(ta, r);
               }
             }
             tc::tmem_wait_st();
           }
         }
-        // pass 2: probabilities, partial sums, and this row of P^T (MN-major, swizzled rows of
-        // 2*HG bytes) into the rope slot, which TMA (async proxy) wrote and QK^T has finished reading
+        // pass 2: probabilities, partial sums, and this row's owned chunks of P^T (MN-major,
+        // swizzled rows of 2*HG bytes) into the rope slot, which TMA (async proxy) wrote and
+        // QK^T has finished reading
         tc::fence_proxy_async_smem();
         for (int half = 0; half < NCH; ++half) {
           uint32_t r[CW];
@@ -561,14 +572,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
               const int h = half * CW + j;
               float p0 = 0.f, p1 = 0.f;
               if (valid) {
-                p0 = ex2(fmaf(__uint_as_float(r[j]), a.scale_log2, -s.m2[h]));
-                p1 = ex2(fmaf(__uint_as_float(r[j + 1]), a.scale_log2, -s.m2[h + 1]));
+                p0 = ex2(fmaf(__uint_as_float(r[j]), a.scale_log2, -s.m2[h0 + h]));
+                p1 = ex2(fmaf(__uint_as_float(r[j + 1]), a.scale_log2, -s.m2[h0 + h + 1]));
               }
               lp[h] += p0;
               lp[h + 1] += p1;
               w[e] = pack_bf16x2(p0, p1);
             }
-            *reinterpret_cast<uint4*>(prow + Cfg<HG>::p_offset(row, half * (CW / 8) + c4)) =
+            *reinterpret_cast<uint4*>(prow + Cfg<HG>::p_offset(row, (h0 + half * CW) / 8 + c4)) =
                 make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
@@ -577,8 +588,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
         tc::mbar_arrive(&s.s_empty[sbuf]);
         if (!valid) {
           // rows past the sequence: zero their latent so 0 * (stale or NaN) cannot reach O^T
+          // (the warpgroups share the eight latent slots)
           const uint4 z = make_uint4(0, 0, 0, 0);
-          for (int kb = 0; kb < TC_LAT_KB; ++kb)
+          for (int kb = wg; kb < TC_LAT_KB; kb += Cfg<HG>::NWG)
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8)
               *reinterpret_cast<uint4*>(slots + kb * TC_SLOT_BYTES + row * 128 + c8 * 16) = z;
@@ -589,44 +601,45 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
       }
       if (!ok) break;
       // ---- epilogue of the segment: wait for its last PV, normalise, write the partial ----
-      if (!softmax_wait(s, &s.o_done, (uint32_t)((n - 1) & 1), sidx)) { ok = false; break; }
+      if (!softmax_wait(s, &s.o_done, (uint32_t)((n - 1) & 1), wg)) { ok = false; break; }
       tc::tc_fence_after();
 #pragma unroll
-      for (int h = 0; h < HG; ++h) {
+      for (int h = 0; h < HW; ++h) {
         float v = lp[h];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) s.red[q][h] = v;
+        if (lane == 0) s.red[q][h0 + h] = v;
       }
-      softmax_bar();
+      softmax_bar(wg);
       const int slot = k + sb;
       const int nh = min(HG, a.H - g * HG);
-      if (sidx < HG) {
-        const float l = s.red[0][sidx] + s.red[1][sidx] + s.red[2][sidx] + s.red[3][sidx];
-        s.alpha[sidx] = 1.0f / l;
-        if (sidx < nh) {
-          const bool bad = *reinterpret_cast<volatile int*>(&s.bad_page[seg & 1]) != 0;
-          a.part_lse[(size_t)(g * a.n_slots + slot) * HG + sidx] =
-              bad ? CUDART_NAN_F : (s.m2[sidx] + __log2f(l)) * 0.69314718055994530942f;
+      if (sidx < HW) {
+        const int h = h0 + sidx;
+        const float l = s.red[0][h] + s.red[1][h] + s.red[2][h] + s.red[3][h];
+        s.alpha[h] = 1.0f / l;
+        if (h < nh) {
+          const bool bad = *reinterpret_cast<volatile int*>(&s.bad_page[seg & 1][wg]) != 0;
+          a.part_lse[(size_t)(g * a.n_slots + slot) * HG + h] =
+              bad ? CUDART_NAN_F : (s.m2[h] + __log2f(l)) * 0.69314718055994530942f;
         }
       }
-      softmax_bar();
+      softmax_bar(wg);
       float* po = a.part_o + ((size_t)(g * a.n_slots + slot) * HG) * 512;
       for (int cc = 0; cc < 4; ++cc) {
         for (int half = 0; half < NCH; ++half) {
           uint32_t r[CW];
-          tc::tmem_ld<CW>(tmem + lane_base + Cfg<HG>::O_COL + cc * HG + half * CW, r);
+          tc::tmem_ld<CW>(tmem + lane_base + Cfg<HG>::O_COL + cc * HG + h0 + half * CW, r);
           tc::tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < CW; ++j) {
-            const int h = half * CW + j;
+            const int h = h0 + half * CW + j;
             if (h < nh) po[(size_t)h * 512 + cc * 128 + row] = __uint_as_float(r[j]) * s.alpha[h];
           }
         }
       }
       tc::tc_fence_before();
-      softmax_bar();   // s.red, s.alpha and s.m2 free; every thread has read bad_page
-      if (sidx == 0) s.bad_page[seg & 1] = 0;
+      softmax_bar(wg);   // this warpgroup's s.red / s.alpha / s.m2 free; its threads have read bad_page
+      if (sidx == 0) s.bad_page[seg & 1][wg] = 0;
       __syncwarp();
       tc::mbar_arrive(&s.o_empty);
       ++seg;
@@ -637,7 +650,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
   __syncwarp();   // lanes that skipped a role wait here for their lane 0
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == TC_MMA_WARP) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, Cfg<HG>::TMEM_COLS);
   }
@@ -723,17 +736,17 @@ cudaError_t launch_attn_tc(const mla_config& cfg, const mla_cache& cache, const 
     case 64:
       e = ensure_smem((const void*)attn_tc_kernel<64>, Cfg<64>::SMEM_DYN);
       if (e != cudaSuccess) return e;
-      attn_tc_kernel<64><<<grid, TC_THREADS, Cfg<64>::SMEM_DYN, st>>>(rows_map, q_map, qres_map, a);
+      attn_tc_kernel<64><<<grid, Cfg<64>::THREADS, Cfg<64>::SMEM_DYN, st>>>(rows_map, q_map, qres_map, a);
       break;
     case 32:
       e = ensure_smem((const void*)attn_tc_kernel<32>, Cfg<32>::SMEM_DYN);
       if (e != cudaSuccess) return e;
-      attn_tc_kernel<32><<<grid, TC_THREADS, Cfg<32>::SMEM_DYN, st>>>(rows_map, q_map, qres_map, a);
+      attn_tc_kernel<32><<<grid, Cfg<32>::THREADS, Cfg<32>::SMEM_DYN, st>>>(rows_map, q_map, qres_map, a);
       break;
     case 16:
       e = ensure_smem((const void*)attn_tc_kernel<16>, Cfg<16>::SMEM_DYN);
       if (e != cudaSuccess) return e;
-      attn_tc_kernel<16><<<grid, TC_THREADS, Cfg<16>::SMEM_DYN, st>>>(rows_map, q_map, qres_map, a);
+      attn_tc_kernel<16><<<grid, Cfg<16>::THREADS, Cfg<16>::SMEM_DYN, st>>>(rows_map, q_map, qres_map, a);
       break;
     default:
       return cudaErrorInvalidValue;
