@@ -81,6 +81,24 @@ append_finish_kernel(mla_config cfg, RowMap map, typename Act<DT>::T* __restrict
                      WsHeader* hdr) {
   const int b = blockIdx.x;
   const int C = cfg.kv_lora, R = cfg.qk_rope, row = C + R;
+  // every load that does not depend on another goes out first: the row, the norm weights,
+  // this thread's RoPE pair and frequency, the position and the length
+  float v[FIN_MAX_PER_THREAD], wn[FIN_MAX_PER_THREAD];
+  const float* src = kva + (int64_t)b * row;
+#pragma unroll
+  for (int k = 0; k < FIN_MAX_PER_THREAD; ++k) {
+    const int i = threadIdx.x + k * FIN_THREADS;
+    v[k] = (i < row) ? src[i] : 0.f;
+    wn[k] = (i < C) ? norm_w[i] : 0.f;
+  }
+  const bool has_pair = threadIdx.x < R / 2;
+  float x0 = 0.f, x1 = 0.f;
+  double inv = 0.0;
+  if (has_pair) {
+    x0 = src[C + 2 * threadIdx.x];
+    x1 = src[C + 2 * threadIdx.x + 1];
+    inv = cfg.rope_inv_freq[threadIdx.x];
+  }
   const int pos = positions[b];
   if (seq_lens != nullptr && seq_lens[b] != pos) {
     if (threadIdx.x == 0) set_error(hdr, MLA_ERR_POS_MISMATCH, b);
@@ -97,13 +115,10 @@ append_finish_kernel(mla_config cfg, RowMap map, typename Act<DT>::T* __restrict
   }
 
   __shared__ float red[FIN_THREADS / 32];
-  float v[FIN_MAX_PER_THREAD];
   float ss = 0.f;
-  const float* src = kva + (int64_t)b * row;
 #pragma unroll
   for (int k = 0; k < FIN_MAX_PER_THREAD; ++k) {
     const int i = threadIdx.x + k * FIN_THREADS;
-    v[k] = (i < row) ? src[i] : 0.f;
     if (i < C) ss = fmaf(v[k], v[k], ss);
   }
   ss = warp_sum(ss);
@@ -118,15 +133,21 @@ append_finish_kernel(mla_config cfg, RowMap map, typename Act<DT>::T* __restrict
 #pragma unroll
   for (int k = 0; k < FIN_MAX_PER_THREAD; ++k) {
     const int i = threadIdx.x + k * FIN_THREADS;
-    if (i < C) Act<DT>::store(dst, i, v[k] * inv_rms * norm_w[i]);
+    if (i < C) Act<DT>::store(dst, i, v[k] * inv_rms * wn[k]);
   }
   // RoPE over the pe tail: one thread per pair (2i, 2i+1)
-  for (int i = threadIdx.x; i < R / 2; i += FIN_THREADS) {
+  if (has_pair) {
+    float c, s;
+    rope_cs_value(inv, pos, &c, &s);
+    Act<DT>::store(dst, C + 2 * threadIdx.x, x0 * c - x1 * s);
+    Act<DT>::store(dst, C + 2 * threadIdx.x + 1, x0 * s + x1 * c);
+  }
+  for (int i = threadIdx.x + FIN_THREADS; i < R / 2; i += FIN_THREADS) {   // R / 2 > 128 only
     float c, s;
     rope_cs(cfg.rope_inv_freq, i, pos, &c, &s);
-    const float x0 = src[C + 2 * i], x1 = src[C + 2 * i + 1];
-    Act<DT>::store(dst, C + 2 * i, x0 * c - x1 * s);
-    Act<DT>::store(dst, C + 2 * i + 1, x0 * s + x1 * c);
+    const float y0 = src[C + 2 * i], y1 = src[C + 2 * i + 1];
+    Act<DT>::store(dst, C + 2 * i, y0 * c - y1 * s);
+    Act<DT>::store(dst, C + 2 * i + 1, y0 * s + y1 * c);
   }
 }
 

@@ -25,6 +25,7 @@ constexpr int G_THREADS = 128;
 constexpr uint64_t G_WAIT = 200ull * 1000 * 1000;   // a wait gives up after 200 ms
 constexpr int ABS_TC_BCHUNK = 64;
 constexpr int CMB_TC_BCHUNK = 32;
+constexpr int CMB_TC_THREADS = 512;   // 4 merge items per thread, loads of 2 items x 4 slots in flight
 constexpr int ABS_TC_SMEM = 4 * 16384 + 2 * 8192 + 1024;
 constexpr int CMB_TC_WSMEM = 8 * 16384 + 2 * 8 * 4096;   // W_UV + vc hi/lo
 
@@ -83,12 +84,24 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
     for (int cb = 0; cb < 4; ++cb)
       tc::tma_load_2d(ws + cb * 16384, &w_map, 256 * lh + 64 * cb, h * (a.N + a.V), &bar_w);
   }
-  // q_nope rows of this batch chunk, 128-byte swizzled, zero rows past the batch
-  for (int i = tid; i < ABS_TC_BCHUNK * 16; i += G_THREADS) {
-    const int r = i >> 4, ch = i & 15, kb = ch >> 3, c8 = ch & 7;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < nb) v = *reinterpret_cast<const uint4*>(a.q + ((size_t)(b0 + r) * a.H + h) * qrow + kb * 64 + c8 * 8);
-    *reinterpret_cast<uint4*>(qs + kb * 8192 + tc::sw128_offset(r, c8)) = v;
+  // q_nope rows of this batch chunk, 128-byte swizzled, zero rows past the batch (all of a
+  // thread's loads are issued before its first store)
+  {
+    constexpr int QI = ABS_TC_BCHUNK * 16 / G_THREADS;
+    uint4 v[QI];
+#pragma unroll
+    for (int m = 0; m < QI; ++m) {
+      const int i = tid + m * G_THREADS;
+      const int r = i >> 4, ch = i & 15, kb = ch >> 3, c8 = ch & 7;
+      v[m] = make_uint4(0, 0, 0, 0);
+      if (r < nb) v[m] = *reinterpret_cast<const uint4*>(a.q + ((size_t)(b0 + r) * a.H + h) * qrow + kb * 64 + c8 * 8);
+    }
+#pragma unroll
+    for (int m = 0; m < QI; ++m) {
+      const int i = tid + m * G_THREADS;
+      const int r = i >> 4, ch = i & 15, kb = ch >> 3, c8 = ch & 7;
+      *reinterpret_cast<uint4*>(qs + kb * 8192 + tc::sw128_offset(r, c8)) = v[m];
+    }
   }
   tc::fence_proxy_async_smem();
   __syncwarp();
@@ -109,6 +122,67 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
         }
     }
     tc::mma_commit(&bar_mma);   // arrives once every MMA issued above has completed
+  }
+  // rotated q_pe into the row's tail (once per head and batch chunk), while the MMAs run; a
+  // thread loads all of its pairs (and their positions and frequencies) before using any
+  if (lh == 0) {
+    constexpr int RI = ABS_TC_BCHUNK * 32 / G_THREADS;   // pairs per thread for R <= 64
+    const int npairs = nb * (a.R / 2);
+    uint32_t xv[RI];
+    int pv[RI];
+    double fv[RI];
+#pragma unroll
+    for (int m = 0; m < RI; ++m) {
+      const int i = tid + m * G_THREADS;
+      xv[m] = 0; pv[m] = 0; fv[m] = 0.0;
+      if (i < npairs) {
+        const int bb = i / (a.R / 2), p = i % (a.R / 2);
+        xv[m] = *reinterpret_cast<const uint32_t*>(a.q + ((size_t)(b0 + bb) * a.H + h) * qrow + a.N + 2 * p);
+        if (a.positions != nullptr) {
+          pv[m] = a.positions[b0 + bb];
+          fv[m] = a.inv_freq[p];
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < RI; ++m) {
+      const int i = tid + m * G_THREADS;
+      if (i < npairs) {
+        const int bb = i / (a.R / 2), p = i % (a.R / 2);
+        const size_t ai = ((size_t)(b0 + bb) * a.H + h) * arow + a.C + 2 * p;
+        const float x0 = __uint_as_float(xv[m] << 16), x1 = __uint_as_float(xv[m] & 0xFFFF0000u);
+        float y0 = x0, y1 = x1;
+        if (a.positions != nullptr) {
+          float c, sn;
+          rope_cs_value(fv[m], pv[m], &c, &sn);
+          y0 = x0 * c - x1 * sn;
+          y1 = x0 * sn + x1 * c;
+        }
+        const uint16_t h0 = bf16_bits(y0), h1 = bf16_bits(y1);
+        *reinterpret_cast<uint32_t*>(a.q_abs + ai) = (uint32_t)h0 | ((uint32_t)h1 << 16);
+        *reinterpret_cast<uint32_t*>(a.q_res + ai) =
+            (uint32_t)bf16_bits(y0 - bf16_bits_to_f32(h0)) | ((uint32_t)bf16_bits(y1 - bf16_bits_to_f32(h1)) << 16);
+      }
+    }
+    // rope widths above 64 leave pairs for a plain loop
+    for (int i = tid + RI * G_THREADS; i < npairs; i += G_THREADS) {
+      const int bb = i / (a.R / 2), p = i % (a.R / 2);
+      const size_t qi = ((size_t)(b0 + bb) * a.H + h) * qrow + a.N + 2 * p;
+      const size_t ai = ((size_t)(b0 + bb) * a.H + h) * arow + a.C + 2 * p;
+      const float x0 = bf16_bits_to_f32(a.q[qi]), x1 = bf16_bits_to_f32(a.q[qi + 1]);
+      float y0 = x0, y1 = x1;
+      if (a.positions != nullptr) {
+        float c, sn;
+        rope_cs(a.inv_freq, p, a.positions[b0 + bb], &c, &sn);
+        y0 = x0 * c - x1 * sn;
+        y1 = x0 * sn + x1 * c;
+      }
+      const uint16_t h0 = bf16_bits(y0), h1 = bf16_bits(y1);
+      a.q_abs[ai] = h0;
+      a.q_abs[ai + 1] = h1;
+      a.q_res[ai] = bf16_bits(y0 - bf16_bits_to_f32(h0));
+      a.q_res[ai + 1] = bf16_bits(y1 - bf16_bits_to_f32(h1));
+    }
   }
   __syncwarp();   // lanes 1-31 of warp 0 wait for lane 0
   // warp-uniform: the TMEM loads below are warp-collective
@@ -136,27 +210,6 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
       }
     }
   }
-  // rotated q_pe into the row's tail (once per head and batch chunk)
-  if (lh == 0) {
-    for (int i = tid; i < nb * (a.R / 2); i += G_THREADS) {
-      const int bb = i / (a.R / 2), p = i % (a.R / 2);
-      const size_t qi = ((size_t)(b0 + bb) * a.H + h) * qrow + a.N + 2 * p;
-      const size_t ai = ((size_t)(b0 + bb) * a.H + h) * arow + a.C + 2 * p;
-      const float x0 = bf16_bits_to_f32(a.q[qi]), x1 = bf16_bits_to_f32(a.q[qi + 1]);
-      float y0 = x0, y1 = x1;
-      if (a.positions != nullptr) {
-        float c, s;
-        rope_cs(a.inv_freq, p, a.positions[b0 + bb], &c, &s);
-        y0 = x0 * c - x1 * s;
-        y1 = x0 * s + x1 * c;
-      }
-      const uint16_t h0 = bf16_bits(y0), h1 = bf16_bits(y1);
-      a.q_abs[ai] = h0;
-      a.q_abs[ai + 1] = h1;
-      a.q_res[ai] = bf16_bits(y0 - bf16_bits_to_f32(h0));
-      a.q_res[ai + 1] = bf16_bits(y1 - bf16_bits_to_f32(h1));
-    }
-  }
   __syncwarp();
   tc::tc_fence_before();
   __syncthreads();
@@ -178,8 +231,8 @@ struct CombineTcArgs {
   int H, C, N, V, R, B, hpg, n_slots, max_slots;
 };
 
-// grid (H, batch chunks of 32); 128 threads
-__global__ void __launch_bounds__(G_THREADS, 1)
+// grid (H, batch chunks of 32); 512 threads
+__global__ void __launch_bounds__(CMB_TC_THREADS, 1)
 combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
   extern __shared__ uint8_t dyn_raw[];
   __shared__ uint64_t bar_w, bar_mma;
@@ -221,7 +274,7 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
       tc::tma_load_2d(wu + kb * 16384, &w_map, 64 * kb, h * (a.N + a.V) + a.N, &bar_w);
   }
   // split weights, one warp per sequence
-  for (int bb = warp; bb < CMB_TC_BCHUNK; bb += G_THREADS / 32) {
+  for (int bb = warp; bb < CMB_TC_BCHUNK; bb += CMB_TC_THREADS / 32) {
     int first = 0, ns = 0;
     if (bb < nb) {
       first = a.meta[2 * (b0 + bb)];
@@ -243,51 +296,82 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
   }
   __syncwarp();
   __syncthreads();
-  // vc = sum_s w_s O_s as bf16 hi + lo, 8 latent columns per item, 128-byte swizzled
-  for (int i = tid; i < CMB_TC_BCHUNK * 64; i += G_THREADS) {
-    const int bb = i >> 6, ch = i & 63, kb = ch >> 3, c8 = ch & 7;
-    float acc[8];
+  // vc = sum_s w_s O_s as bf16 hi + lo, 8 latent columns per item, 128-byte swizzled. Item
+  // (bb, ch) = sequence bb, latent columns 8*ch..8*ch+7; a thread takes items of one column
+  // group and four sequences, two at a time, with the loads of up to four slots of both items
+  // (and their query residuals) issued before any is used.
+  constexpr int MU = 2, SU = 4;
+  const int ch = tid & 63, kb = ch >> 3, c8 = ch & 7;
+  for (int m0 = 0; m0 < CMB_TC_BCHUNK / (CMB_TC_THREADS / 64); m0 += MU) {
+    int bbv[MU], nsv[MU], fv[MU];
+    float acc[MU][8];
+    uint4 resv[MU];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    if (bb < nb) {
-      if (isnan(lse_s[bb])) {
+    for (int u = 0; u < MU; ++u) {
+      bbv[u] = (tid >> 6) + (CMB_TC_THREADS / 64) * (m0 + u);
+      const bool live = bbv[u] < nb && !isnan(lse_s[bbv[u]]);
+      nsv[u] = live ? cnt_s[bbv[u]] : 0;
+      fv[u] = first_s[bbv[u]];
+      resv[u] = make_uint4(0, 0, 0, 0);
+      if (a.q_res != nullptr && bbv[u] < nb)
+        resv[u] = *reinterpret_cast<const uint4*>(a.q_res + ((size_t)(b0 + bbv[u]) * a.H + h) * (a.C + a.R) + ch * 8);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = CUDART_NAN_F;
-      } else {
-        for (int s = 0; s < cnt_s[bb]; ++s) {
-          const float w = wt_s[bb * a.max_slots + s];
-          if (w == 0.f) continue;   // empty slot
-          const float4* src = reinterpret_cast<const float4*>(a.part_o + lse_at(first_s[bb] + s) * a.C + ch * 8);
-          const float4 u = src[0], v = src[1];
-          acc[0] = fmaf(w, u.x, acc[0]); acc[1] = fmaf(w, u.y, acc[1]);
-          acc[2] = fmaf(w, u.z, acc[2]); acc[3] = fmaf(w, u.w, acc[3]);
-          acc[4] = fmaf(w, v.x, acc[4]); acc[5] = fmaf(w, v.y, acc[5]);
-          acc[6] = fmaf(w, v.z, acc[6]); acc[7] = fmaf(w, v.w, acc[7]);
-        }
-      }
+      for (int e = 0; e < 8; ++e) acc[u][e] = 0.f;
     }
-    if (a.q_res != nullptr) {
-      float d = 0.f;
-      if (bb < nb) {
-        const uint4 u = *reinterpret_cast<const uint4*>(a.q_res + ((size_t)(b0 + bb) * a.H + h) * (a.C + a.R) + ch * 8);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    const int smax = max(nsv[0], nsv[1]);
+    for (int s0 = 0; s0 < smax; s0 += SU) {
+      float4 x[MU][SU][2];
+#pragma unroll
+      for (int u = 0; u < MU; ++u)
+#pragma unroll
+        for (int v = 0; v < SU; ++v) {
+          x[u][v][0] = x[u][v][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (s0 + v < nsv[u]) {
+            const float4* src = reinterpret_cast<const float4*>(a.part_o + lse_at(fv[u] + s0 + v) * a.C + ch * 8);
+            x[u][v][0] = src[0];
+            x[u][v][1] = src[1];
+          }
+        }
+#pragma unroll
+      for (int u = 0; u < MU; ++u)
+#pragma unroll
+        for (int v = 0; v < SU; ++v) {
+          const float w = (s0 + v < nsv[u]) ? wt_s[bbv[u] * a.max_slots + s0 + v] : 0.f;
+          if (w != 0.f) {   // empty slots carry weight 0 and unwritten data: skip, never 0 * x
+            acc[u][0] = fmaf(w, x[u][v][0].x, acc[u][0]); acc[u][1] = fmaf(w, x[u][v][0].y, acc[u][1]);
+            acc[u][2] = fmaf(w, x[u][v][0].z, acc[u][2]); acc[u][3] = fmaf(w, x[u][v][0].w, acc[u][3]);
+            acc[u][4] = fmaf(w, x[u][v][1].x, acc[u][4]); acc[u][5] = fmaf(w, x[u][v][1].y, acc[u][5]);
+            acc[u][6] = fmaf(w, x[u][v][1].z, acc[u][6]); acc[u][7] = fmaf(w, x[u][v][1].w, acc[u][7]);
+          }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < MU; ++u) {
+      const int bb = bbv[u];
+      if (bb < nb && isnan(lse_s[bb])) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[u][e] = CUDART_NAN_F;
+      }
+      if (a.q_res != nullptr) {
+        const uint32_t w[4] = {resv[u].x, resv[u].y, resv[u].z, resv[u].w};
+        float d = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          d += acc[2 * e] * __uint_as_float(w[e] << 16) + acc[2 * e + 1] * __uint_as_float(w[e] & 0xFFFF0000u);
+          d += acc[u][2 * e] * __uint_as_float(w[e] << 16) + acc[u][2 * e + 1] * __uint_as_float(w[e] & 0xFFFF0000u);
+        dres[bb * 64 + ch] = (bb < nb) ? d : 0.f;
       }
-      dres[bb * 64 + ch] = d;
-    }
-    uint32_t hi[4], lo[4];
+      uint32_t hi[4], lo[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint16_t h0 = bf16_bits(acc[2 * e]), h1 = bf16_bits(acc[2 * e + 1]);
-      const uint16_t l0 = bf16_bits(acc[2 * e] - bf16_bits_to_f32(h0));
-      const uint16_t l1 = bf16_bits(acc[2 * e + 1] - bf16_bits_to_f32(h1));
-      hi[e] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-      lo[e] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+      for (int e = 0; e < 4; ++e) {
+        const uint16_t h0 = bf16_bits(acc[u][2 * e]), h1 = bf16_bits(acc[u][2 * e + 1]);
+        const uint16_t l0 = bf16_bits(acc[u][2 * e] - bf16_bits_to_f32(h0));
+        const uint16_t l1 = bf16_bits(acc[u][2 * e + 1] - bf16_bits_to_f32(h1));
+        hi[e] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+        lo[e] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+      }
+      *reinterpret_cast<uint4*>(vh + kb * 4096 + tc::sw128_offset(bb, c8)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(vl + kb * 4096 + tc::sw128_offset(bb, c8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
-    *reinterpret_cast<uint4*>(vh + kb * 4096 + tc::sw128_offset(bb, c8)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    *reinterpret_cast<uint4*>(vl + kb * 4096 + tc::sw128_offset(bb, c8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
   }
   tc::fence_proxy_async_smem();
   __syncwarp();
@@ -295,7 +379,7 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
   if (a.q_res != nullptr) {
     // first-order LSE correction for the bf16 latent queries the scores used:
     // lse += scale * vc . res, summed in a fixed order (one warp per sequence)
-    for (int bb = warp; bb < nb; bb += G_THREADS / 32) {
+    for (int bb = warp; bb < nb; bb += CMB_TC_THREADS / 32) {
       float d = dres[bb * 64 + lane] + dres[bb * 64 + 32 + lane];
       d = warp_sum(d);
       if (lane == 0) lse_s[bb] += a.scale * d;
@@ -321,9 +405,9 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
     tc::mma_commit(&bar_mma);
   }
   __syncwarp();
-  // warp-uniform: the TMEM loads below are warp-collective
-  const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&bar_mma, 0, G_WAIT) &&
-                                             !*reinterpret_cast<volatile int*>(&failed));
+  // warp-uniform: the TMEM loads below are warp-collective; warps 0-3 read the 128 TMEM lanes
+  const bool ok = warp < 4 && __all_sync(0xffffffffu, tc::mbar_wait(&bar_mma, 0, G_WAIT) &&
+                                                           !*reinterpret_cast<volatile int*>(&failed));
   tc::tc_fence_after();
   if (ok) {
     uint32_t r[32];
@@ -335,7 +419,7 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
       if (b < nb) a.out[((size_t)(b0 + b) * a.H + h) * a.V + j] = __uint_as_float(r[b]);
   }
   if (a.lse != nullptr)
-    for (int bb = tid; bb < nb; bb += G_THREADS) a.lse[(size_t)(b0 + bb) * a.H + h] = lse_s[bb];
+    for (int bb = tid; bb < nb; bb += CMB_TC_THREADS) a.lse[(size_t)(b0 + bb) * a.H + h] = lse_s[bb];
   __syncwarp();
   tc::tc_fence_before();
   __syncthreads();
@@ -396,7 +480,7 @@ cudaError_t launch_combine_tc(const mla_config& cfg, const DecodePlan& plan, con
   cudaError_t e = ensure_smem((const void*)combine_tc_kernel, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(cfg.n_heads, (B + CMB_TC_BCHUNK - 1) / CMB_TC_BCHUNK);
-  combine_tc_kernel<<<grid, G_THREADS, smem, st>>>(w_map, a);
+  combine_tc_kernel<<<grid, CMB_TC_THREADS, smem, st>>>(w_map, a);
   return cudaGetLastError();
 }
 
