@@ -10,8 +10,9 @@ up-projection). The default workload is the DeepSeek-V2-Lite-shaped single-seque
 
 Timing: inputs resident in HBM; each step uses the next of R rotating input copies whose total
 exceeds 2x L2, so no step reads another's data from L2; the timed K steps are replayed as CUDA
-graphs with CUDA events on the launching stream; the attention kernel is bracketed by events
-inside the graphs (every step). N > 1 (torchrun) runs independent replicas per GPU (the
+graphs with CUDA events on the launching stream; the attention kernel of the first step of
+every graph is bracketed by events inside the graph (an event between two kernels makes their
+overlapped launch a plain one, so the other steps run without). N > 1 (torchrun) runs independent replicas per GPU (the
 sequences are independent: no data-path collective) and reports the max over ranks.
 """
 from __future__ import annotations
@@ -270,19 +271,22 @@ def run_ours(args, rank, world, device):
             ev[1].record(s)
         L.check(ds.combine(s), "mla_decode_combine")
 
-    # graphs of G steps (one pass over the R copies), two of them to double-buffer the
-    # in-graph attention events, plus a tail graph for K mod G steps
+    # graphs of G steps (whole passes over the R copies, at least 16 steps), two of them to
+    # double-buffer the in-graph attention events, plus a tail graph for K mod G steps. Only
+    # the first step of each graph has its attention launch bracketed by events: an event
+    # between two kernels turns their programmatic (overlapped) launch into a plain one.
     K, W = args.steps, args.warmup
-    G = R if R > 1 else max(1, min(64, K))
+    G = R * max(1, math.ceil(16 / R)) if R > 1 else max(1, min(64, K))
+    G = max(1, min(G, max(R, 64)))
     torch.cuda.synchronize(device)
 
     def capture(n, with_events):
         g = torch.cuda.CUDAGraph()
-        evs = [(graph_event(torch), graph_event(torch)) for _ in range(n)] if with_events else None
+        evs = [(graph_event(torch), graph_event(torch))] if with_events else None
         with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
             s = torch.cuda.current_stream(device)
             for i in range(n):
-                one_step(steps[i % R], s, evs[i] if evs else None)
+                one_step(steps[i % R], s, evs[0] if (evs and i == 0) else None)
         return g, evs
 
     with torch.cuda.stream(stream):
@@ -370,7 +374,8 @@ def run_ours(args, rank, world, device):
             "v_head": wl.V, "rows_per_step": work["rows"], "kv_b": wl.kv_b,
             "paged": bool(wl.page_size), "append": wl.append,
             "l2": f"rotating {R} input copies ({R * per_copy / 2 ** 20:.0f} MB, L2 {l2 / 2 ** 20:.0f} MB)",
-            "timing": f"CUDA graphs of {G} steps, events on the launching stream",
+            "timing": f"CUDA graphs of {G} steps, events on the launching stream; the attention "
+                      f"launch of each graph's first step bracketed by in-graph events",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "attention_kernel": "tcgen05" if plan.kernel == 1 else "cuda-core",
             "splits": plan.splits, "rows_per_split": plan.rows_per_split,

@@ -28,12 +28,14 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
     if (q_res != nullptr) Act<DT>::store(q_res, i, v - Act<DT>::load(q_abs, i));
   };
   extern __shared__ float sm[];
+  pdl_trigger();
   const int H = cfg.n_heads, C = cfg.kv_lora, N = cfg.qk_nope, R = cfg.qk_rope, V = cfg.v_head;
   const int h = blockIdx.x;
   const int c0 = blockIdx.y * ABS_COLS;
   const int qrow = N + R, arow = C + R;
   float* w_s = sm;                          // [N][ABS_COLS]
   float* q_s = sm + N * ABS_COLS;           // [ABS_BCHUNK][N]
+  float* red_s = q_s + ABS_BCHUNK * N;      // [4][ABS_BCHUNK][ABS_COLS] partial sums over nope quarters
   const int tid = threadIdx.x;
 
   // Loads of the first pass go out together: this thread's q_pe pair (the head's B*R/2 pairs
@@ -66,6 +68,7 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
   }
   const int64_t wrow0 = (int64_t)h * (N + V);
   stage_kv_b_rows(w_s, ABS_COLS, kv_b, cfg.kv_b_dtype, wrow0, N, c0, min(ABS_COLS, C - c0), C, ABS_THREADS);
+  pdl_wait();   // the fused query rows may still be read by the previous step's attention
 
   // q_pe: rotate at positions[b] (or copy when positions == NULL) into the row's tail
   for (int i = pair0; i < n_pairs; i += pair_stride) {
@@ -91,8 +94,11 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
     }
   }
 
+  // thread (cc, part): latent column c0 + cc, nope quarter `part`, every sequence of the chunk;
+  // the four quarter sums are added in a fixed order afterwards
   const int cc = tid % ABS_COLS;
-  const int bsub = tid / ABS_COLS;   // 0..3
+  const int part = tid / ABS_COLS;   // 0..3
+  const int n_lo = part * N / 4, n_hi = (part + 1) * N / 4;
   for (int b0 = 0; b0 < B; b0 += ABS_BCHUNK) {
     const int nb = min(ABS_BCHUNK, B - b0);
     __syncthreads();
@@ -111,11 +117,18 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
       }
     }
     __syncthreads();
-    if (c0 + cc < C) {
-      for (int bb = bsub; bb < nb; bb += ABS_THREADS / ABS_COLS) {
-        float acc = 0.f;
-        for (int n = 0; n < N; ++n) acc = fmaf(q_s[bb * N + n], w_s[n * ABS_COLS + cc], acc);
-        put(((int64_t)(b0 + bb) * H + h) * arow + c0 + cc, acc);
+    for (int bb = 0; bb < nb; ++bb) {
+      float acc = 0.f;
+      for (int n = n_lo; n < n_hi; ++n) acc = fmaf(q_s[bb * N + n], w_s[n * ABS_COLS + cc], acc);
+      red_s[(part * ABS_BCHUNK + bb) * ABS_COLS + cc] = acc;
+    }
+    __syncthreads();
+    for (int i = tid; i < nb * ABS_COLS; i += ABS_THREADS) {
+      const int bb = i / ABS_COLS, c = i % ABS_COLS;
+      if (c0 + c < C) {
+        const float* r = red_s + bb * ABS_COLS + c;
+        const float v = ((r[0] + r[ABS_BCHUNK * ABS_COLS]) + r[2 * ABS_BCHUNK * ABS_COLS]) + r[3 * ABS_BCHUNK * ABS_COLS];
+        put(((int64_t)(b0 + bb) * H + h) * arow + c0 + c, v);
       }
     }
   }
@@ -124,21 +137,21 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
 cudaError_t launch_absorb(const mla_config& cfg, const void* q, const void* kv_b,
                           const int32_t* positions, void* q_abs, void* q_res, int B, cudaStream_t st) {
   dim3 grid(cfg.n_heads, (cfg.kv_lora + ABS_COLS - 1) / ABS_COLS);
-  const size_t smem = sizeof(float) * ((size_t)cfg.qk_nope * ABS_COLS + (size_t)ABS_BCHUNK * cfg.qk_nope);
+  const size_t smem = sizeof(float) * ((size_t)cfg.qk_nope * ABS_COLS + (size_t)ABS_BCHUNK * cfg.qk_nope +
+                                       4 * (size_t)ABS_BCHUNK * ABS_COLS);
   if (cfg.act_dtype == MLA_BF16) {
     auto k = absorb_kernel<MLA_BF16>;
     cudaError_t e = ensure_smem((const void*)k, (int)smem);
     if (e != cudaSuccess) return e;
-    k<<<grid, ABS_THREADS, smem, st>>>(cfg, static_cast<const uint16_t*>(q), kv_b, positions,
-                                       static_cast<uint16_t*>(q_abs), static_cast<uint16_t*>(q_res), B);
+    return launch_pdl(k, grid, dim3(ABS_THREADS), smem, st, cfg, static_cast<const uint16_t*>(q), kv_b, positions,
+                      static_cast<uint16_t*>(q_abs), static_cast<uint16_t*>(q_res), B);
   } else {
     auto k = absorb_kernel<MLA_F32>;
     cudaError_t e = ensure_smem((const void*)k, (int)smem);
     if (e != cudaSuccess) return e;
-    k<<<grid, ABS_THREADS, smem, st>>>(cfg, static_cast<const float*>(q), kv_b, positions,
-                                       static_cast<float*>(q_abs), nullptr, B);
+    return launch_pdl(k, grid, dim3(ABS_THREADS), smem, st, cfg, static_cast<const float*>(q), kv_b, positions,
+                      static_cast<float*>(q_abs), static_cast<float*>(nullptr), B);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace mla

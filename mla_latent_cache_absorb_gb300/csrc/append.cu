@@ -24,6 +24,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32)
 append_gemv_kernel(const typename Act<DT>::T* __restrict__ x, const typename Act<DT>::T* __restrict__ w,
                    int hidden, int rows, int B, float* __restrict__ kva) {
   using T = typename Act<DT>::T;
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * GEMV_WARPS + warp;
   if (r >= rows) return;
@@ -48,6 +49,7 @@ append_gemv_kernel(const typename Act<DT>::T* __restrict__ x, const typename Act
         }
       }
     }
+    pdl_wait();   // the previous step's finish kernel may still read kva
 #pragma unroll
     for (int j = 0; j < GEMV_BMAX; ++j) {
       float v = warp_sum(acc[j]);
@@ -61,12 +63,10 @@ cudaError_t launch_append_gemv(const mla_config& cfg, const void* x, const void*
   const int rows = cfg.kv_lora + cfg.qk_rope;
   dim3 grid((rows + GEMV_WARPS - 1) / GEMV_WARPS);
   if (cfg.act_dtype == MLA_BF16)
-    append_gemv_kernel<MLA_BF16><<<grid, GEMV_WARPS * 32, 0, st>>>(
-        static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(w), hidden, rows, B, kva_out);
-  else
-    append_gemv_kernel<MLA_F32><<<grid, GEMV_WARPS * 32, 0, st>>>(
-        static_cast<const float*>(x), static_cast<const float*>(w), hidden, rows, B, kva_out);
-  return cudaGetLastError();
+    return launch_pdl(append_gemv_kernel<MLA_BF16>, grid, dim3(GEMV_WARPS * 32), 0, st,
+                      static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(w), hidden, rows, B, kva_out);
+  return launch_pdl(append_gemv_kernel<MLA_F32>, grid, dim3(GEMV_WARPS * 32), 0, st,
+                    static_cast<const float*>(x), static_cast<const float*>(w), hidden, rows, B, kva_out);
 }
 
 // ---- finish: norm + rope + store, one CTA per sequence ---------------------------------------
@@ -78,29 +78,41 @@ __global__ void __launch_bounds__(FIN_THREADS)
 append_finish_kernel(mla_config cfg, RowMap map, typename Act<DT>::T* __restrict__ rows_out,
                      const float* __restrict__ kva, const float* __restrict__ norm_w,
                      const int32_t* __restrict__ positions, const int32_t* __restrict__ seq_lens,
-                     WsHeader* hdr) {
+                     WsHeader* hdr, int kva_dep) {
+  pdl_trigger();
   const int b = blockIdx.x;
   const int C = cfg.kv_lora, R = cfg.qk_rope, row = C + R;
-  // every load that does not depend on another goes out first: the row, the norm weights,
-  // this thread's RoPE pair and frequency, the position and the length
+  // every load that does not depend on another goes out first: the row (unless the projection
+  // kernel just before produces it), the norm weights, this thread's RoPE pair and frequency,
+  // the position and the length
   float v[FIN_MAX_PER_THREAD], wn[FIN_MAX_PER_THREAD];
   const float* src = kva + (int64_t)b * row;
-#pragma unroll
-  for (int k = 0; k < FIN_MAX_PER_THREAD; ++k) {
-    const int i = threadIdx.x + k * FIN_THREADS;
-    v[k] = (i < row) ? src[i] : 0.f;
-    wn[k] = (i < C) ? norm_w[i] : 0.f;
-  }
   const bool has_pair = threadIdx.x < R / 2;
   float x0 = 0.f, x1 = 0.f;
   double inv = 0.0;
-  if (has_pair) {
-    x0 = src[C + 2 * threadIdx.x];
-    x1 = src[C + 2 * threadIdx.x + 1];
-    inv = cfg.rope_inv_freq[threadIdx.x];
+  auto load_row = [&]() {
+#pragma unroll
+    for (int k = 0; k < FIN_MAX_PER_THREAD; ++k) {
+      const int i = threadIdx.x + k * FIN_THREADS;
+      v[k] = (i < row) ? src[i] : 0.f;
+    }
+    if (has_pair) {
+      x0 = src[C + 2 * threadIdx.x];
+      x1 = src[C + 2 * threadIdx.x + 1];
+    }
+  };
+  if (!kva_dep) load_row();
+#pragma unroll
+  for (int k = 0; k < FIN_MAX_PER_THREAD; ++k) {
+    const int i = threadIdx.x + k * FIN_THREADS;
+    wn[k] = (i < C) ? norm_w[i] : 0.f;
   }
+  if (has_pair) inv = cfg.rope_inv_freq[threadIdx.x];
   const int pos = positions[b];
-  if (seq_lens != nullptr && seq_lens[b] != pos) {
+  const int len = seq_lens != nullptr ? seq_lens[b] : pos;
+  pdl_wait();   // the cache row may still be read by the previous step's attention
+  if (kva_dep) load_row();
+  if (len != pos) {
     if (threadIdx.x == 0) set_error(hdr, MLA_ERR_POS_MISMATCH, b);
     return;
   }
@@ -153,16 +165,14 @@ append_finish_kernel(mla_config cfg, RowMap map, typename Act<DT>::T* __restrict
 
 cudaError_t launch_append_finish(const mla_config& cfg, const mla_cache& cache, const float* kva,
                                  const float* norm_w, const int32_t* positions,
-                                 const int32_t* seq_lens, int B, WsHeader* hdr, cudaStream_t st) {
+                                 const int32_t* seq_lens, int B, WsHeader* hdr, bool kva_dep, cudaStream_t st) {
   RowMap map{cache.page_table, cfg.page_size, cfg.max_pages_per_seq, cfg.rows_per_seq,
              cache.n_physical_rows};
   if (cfg.act_dtype == MLA_BF16)
-    append_finish_kernel<MLA_BF16><<<B, FIN_THREADS, 0, st>>>(
-        cfg, map, static_cast<uint16_t*>(cache.rows), kva, norm_w, positions, seq_lens, hdr);
-  else
-    append_finish_kernel<MLA_F32><<<B, FIN_THREADS, 0, st>>>(
-        cfg, map, static_cast<float*>(cache.rows), kva, norm_w, positions, seq_lens, hdr);
-  return cudaGetLastError();
+    return launch_pdl(append_finish_kernel<MLA_BF16>, dim3(B), dim3(FIN_THREADS), 0, st, cfg, map,
+                      static_cast<uint16_t*>(cache.rows), kva, norm_w, positions, seq_lens, hdr, (int)kva_dep);
+  return launch_pdl(append_finish_kernel<MLA_F32>, dim3(B), dim3(FIN_THREADS), 0, st, cfg, map,
+                    static_cast<float*>(cache.rows), kva, norm_w, positions, seq_lens, hdr, (int)kva_dep);
 }
 
 }  // namespace mla

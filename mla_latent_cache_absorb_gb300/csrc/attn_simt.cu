@@ -37,6 +37,8 @@ template <int DT>
 __global__ void __launch_bounds__(SIMT_THREADS) attn_simt_kernel(SimtArgs a) {
   using T = typename Act<DT>::T;
   extern __shared__ float sm[];
+  pdl_trigger();
+  pdl_wait();   // fused query rows from the absorb, the appended row, partials the combine reads
   const int s = blockIdx.x, b = blockIdx.y, g = blockIdx.z;
   const int row = a.C + a.R;
   const int h0 = g * a.hpb;
@@ -183,13 +185,12 @@ cudaError_t launch_attn_simt(const mla_config& cfg, const mla_cache& cache, cons
   if (cfg.act_dtype == MLA_BF16) {
     e = ensure_smem((const void*)attn_simt_kernel<MLA_BF16>, (int)smem);
     if (e != cudaSuccess) return e;
-    attn_simt_kernel<MLA_BF16><<<grid, SIMT_THREADS, smem, st>>>(a);
+    return launch_pdl(attn_simt_kernel<MLA_BF16>, grid, dim3(SIMT_THREADS), smem, st, a);
   } else {
     e = ensure_smem((const void*)attn_simt_kernel<MLA_F32>, (int)smem);
     if (e != cudaSuccess) return e;
-    attn_simt_kernel<MLA_F32><<<grid, SIMT_THREADS, smem, st>>>(a);
+    return launch_pdl(attn_simt_kernel<MLA_F32>, grid, dim3(SIMT_THREADS), smem, st, a);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace mla

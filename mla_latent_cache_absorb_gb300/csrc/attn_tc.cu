@@ -208,6 +208,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
                const __grid_constant__ CUtensorMap qres_map, TcArgs a) {
   extern __shared__ uint8_t dyn_raw[];
   __shared__ Smem s;
+  pdl_trigger();
   uint8_t* dyn = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* slots = dyn;                                 // 9 x 16 KB
   uint8_t* qs = dyn + TC_KB * TC_SLOT_BYTES;            // 10 Q blocks
@@ -248,6 +249,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
   }
   long long r0, r1;
   cta_range(T, k, a.ncg, &r0, &r1);
+  // everything below reads what the absorb / append kernels wrote (query rows, the new cache
+  // row) or writes what the previous step's combine may still read (meta, partials)
+  pdl_wait();
   // the thread whose chunk holds tile r0 finds the first sequence of this CTA's share
   if (r0 < r1 && before <= r0 && r0 < before + mine) {
     long long p = before;
@@ -736,22 +740,25 @@ cudaError_t launch_attn_tc(const mla_config& cfg, const mla_cache& cache, const 
     case 64:
       e = ensure_smem((const void*)attn_tc_kernel<64>, Cfg<64>::SMEM_DYN);
       if (e != cudaSuccess) return e;
-      attn_tc_kernel<64><<<grid, Cfg<64>::THREADS, Cfg<64>::SMEM_DYN, st>>>(rows_map, q_map, qres_map, a);
+      e = launch_pdl(attn_tc_kernel<64>, dim3(grid), dim3(Cfg<64>::THREADS), Cfg<64>::SMEM_DYN, st, rows_map, q_map,
+                     qres_map, a);
       break;
     case 32:
       e = ensure_smem((const void*)attn_tc_kernel<32>, Cfg<32>::SMEM_DYN);
       if (e != cudaSuccess) return e;
-      attn_tc_kernel<32><<<grid, Cfg<32>::THREADS, Cfg<32>::SMEM_DYN, st>>>(rows_map, q_map, qres_map, a);
+      e = launch_pdl(attn_tc_kernel<32>, dim3(grid), dim3(Cfg<32>::THREADS), Cfg<32>::SMEM_DYN, st, rows_map, q_map,
+                     qres_map, a);
       break;
     case 16:
       e = ensure_smem((const void*)attn_tc_kernel<16>, Cfg<16>::SMEM_DYN);
       if (e != cudaSuccess) return e;
-      attn_tc_kernel<16><<<grid, Cfg<16>::THREADS, Cfg<16>::SMEM_DYN, st>>>(rows_map, q_map, qres_map, a);
+      e = launch_pdl(attn_tc_kernel<16>, dim3(grid), dim3(Cfg<16>::THREADS), Cfg<16>::SMEM_DYN, st, rows_map, q_map,
+                     qres_map, a);
       break;
     default:
       return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace mla

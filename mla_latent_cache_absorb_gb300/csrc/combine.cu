@@ -38,6 +38,7 @@ struct CombineArgs {
 
 __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
   extern __shared__ float sm[];
+  pdl_trigger();
   const int h = blockIdx.x;
   const int j0 = blockIdx.y * CMB_VJ;
   const int b0 = blockIdx.z * CMB_BC;
@@ -57,6 +58,7 @@ __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
 
   const int64_t wrow0 = (int64_t)h * (a.N + a.V) + a.N + j0;
   stage_kv_b_rows(w_s, 4 * C4, a.kv_b, a.kv_b_dtype, wrow0, nj, 0, C, C, CMB_THREADS);
+  pdl_wait();   // the partials and meta come from the attention kernel
 
   // split weights exp(lse_s - lse): one warp per sequence
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -195,8 +197,7 @@ cudaError_t launch_combine(const mla_config& cfg, const DecodePlan& plan, const 
                                        (size_t)CMB_BC * a.max_slots + 3 * CMB_BC);
   cudaError_t e = ensure_smem((const void*)combine_kernel, (int)smem);
   if (e != cudaSuccess) return e;
-  combine_kernel<<<grid, CMB_THREADS, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, grid, dim3(CMB_THREADS), smem, st, a);
 }
 
 }  // namespace mla

@@ -19,6 +19,32 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
+// ---- programmatic dependent launch -------------------------------------------------------------
+// Every kernel of a step is launched so that it may start while the kernel before it on the
+// stream is still running: it lets its own successor start at once (pdl_trigger) and, before
+// touching anything an earlier kernel of the library writes or still reads, waits until its
+// predecessor has completed (pdl_wait). Because every kernel waits before it completes, the
+// predecessor's completion implies that of all earlier kernels. Launched without the attribute,
+// both are no-ops.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kernel, static_cast<KArgs>(args)...);
+}
+
 __device__ __forceinline__ void set_error(WsHeader* hdr, int code, int seq) {
   if (atomicCAS(&hdr->code, 0, code) == 0) atomicExch(&hdr->seq, seq);
 }
@@ -202,7 +228,7 @@ cudaError_t launch_append_gemv(const mla_config& cfg, const void* x, const void*
                                float* kva_out, int B, cudaStream_t st);
 cudaError_t launch_append_finish(const mla_config& cfg, const mla_cache& cache, const float* kva,
                                  const float* norm_w, const int32_t* positions,
-                                 const int32_t* seq_lens, int B, WsHeader* hdr, cudaStream_t st);
+                                 const int32_t* seq_lens, int B, WsHeader* hdr, bool kva_dep, cudaStream_t st);
 cudaError_t launch_absorb(const mla_config& cfg, const void* q, const void* kv_b,
                           const int32_t* positions, void* q_abs, void* q_res, int B, cudaStream_t st);
 cudaError_t launch_attn_simt(const mla_config& cfg, const mla_cache& cache, const DecodePlan& plan,

@@ -58,6 +58,7 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
   uint8_t* dyn = align1024(dyn_raw);
   uint8_t* ws = dyn;                 // 4 blocks [128 n rows x 64 latent] (MN-major A)
   uint8_t* qs = dyn + 4 * 16384;     // 2 blocks [64 b rows x 64 n] (K-major B)
+  pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x, lh = blockIdx.y, b0 = blockIdx.z * ABS_TC_BCHUNK;
   const int nb = min(ABS_TC_BCHUNK, a.B - b0);
@@ -123,6 +124,7 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
     }
     tc::mma_commit(&bar_mma);   // arrives once every MMA issued above has completed
   }
+  pdl_wait();   // the fused query rows may still be read by the previous step's attention
   // rotated q_pe into the row's tail (once per head and batch chunk), while the MMAs run; a
   // thread loads all of its pairs (and their positions and frequencies) before using any
   if (lh == 0) {
@@ -246,6 +248,7 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
   uint8_t* vl = vh + 8 * 4096;                 // same, lo
   float* dres = reinterpret_cast<float*>(vl + 8 * 4096);   // [32][64] partial vc . res
   float* wt_s = dres + CMB_TC_BCHUNK * 64;                  // [32][max_slots]
+  pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x, b0 = blockIdx.y * CMB_TC_BCHUNK;
   const int nb = min(CMB_TC_BCHUNK, a.B - b0);
@@ -273,6 +276,7 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
     for (int kb = 0; kb < 8; ++kb)
       tc::tma_load_2d(wu + kb * 16384, &w_map, 64 * kb, h * (a.N + a.V) + a.N, &bar_w);
   }
+  pdl_wait();   // the partials and meta come from the attention kernel
   // split weights, one warp per sequence
   for (int bb = warp; bb < CMB_TC_BCHUNK; bb += CMB_TC_THREADS / 32) {
     int first = 0, ns = 0;
@@ -459,8 +463,7 @@ cudaError_t launch_absorb_tc(const mla_config& cfg, const void* q, const void* k
   cudaError_t e = ensure_smem((const void*)absorb_tc_kernel, ABS_TC_SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(cfg.n_heads, 2, (B + ABS_TC_BCHUNK - 1) / ABS_TC_BCHUNK);
-  absorb_tc_kernel<<<grid, G_THREADS, ABS_TC_SMEM, st>>>(w_map, a);
-  return cudaGetLastError();
+  return launch_pdl(absorb_tc_kernel, grid, dim3(G_THREADS), ABS_TC_SMEM, st, w_map, a);
 }
 
 cudaError_t launch_combine_tc(const mla_config& cfg, const DecodePlan& plan, const void* kv_b,
@@ -480,8 +483,7 @@ cudaError_t launch_combine_tc(const mla_config& cfg, const DecodePlan& plan, con
   cudaError_t e = ensure_smem((const void*)combine_tc_kernel, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(cfg.n_heads, (B + CMB_TC_BCHUNK - 1) / CMB_TC_BCHUNK);
-  combine_tc_kernel<<<grid, CMB_TC_THREADS, smem, st>>>(w_map, a);
-  return cudaGetLastError();
+  return launch_pdl(combine_tc_kernel, grid, dim3(CMB_TC_THREADS), (size_t)smem, st, w_map, a);
 }
 
 }  // namespace mla

@@ -321,7 +321,8 @@ mla_status mla_cache_append(const mla_config* cfg, const mla_cache* cache, const
     if (st != MLA_OK) return st;
     kva = kva_ws;
   }
-  return cuda_status(launch_append_finish(*cfg, *cache, kva, norm_w, positions, seq_lens, B, hdr, s));
+  return cuda_status(launch_append_finish(*cfg, *cache, kva, norm_w, positions, seq_lens, B, hdr,
+                                          w_kva != nullptr, s));
 }
 
 static mla_status decode_prologue(const mla_config* cfg, int32_t B, void* workspace, size_t ws_bytes,
