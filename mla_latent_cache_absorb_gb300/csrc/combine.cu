@@ -36,6 +36,32 @@ struct CombineArgs {
   int hpg, n_slots, max_slots;
 };
 
+// out[b0 + bb, h, j0 + j] = W_UV row j . vc[bb] for bb < nb <= NBT: one warp per output, lanes
+// across the latent, NBT accumulators per lane.
+template <int NBT>
+__device__ __forceinline__ void combine_outputs(const CombineArgs& a, const float* w_s, const float* vc_s, int stride,
+                                                int nb, int nj, int b0, int h, int j0, int warp, int lane) {
+  for (int j = warp; j < nj; j += CMB_THREADS / 32) {
+    float acc[NBT];
+#pragma unroll
+    for (int bb = 0; bb < NBT; ++bb) acc[bb] = 0.f;
+    const float* wr = w_s + j * stride;
+    for (int c = lane; c < a.C; c += 32) {
+      const float wv = wr[c];
+#pragma unroll
+      for (int bb = 0; bb < NBT; ++bb)
+        if (bb < nb) acc[bb] = fmaf(wv, vc_s[bb * stride + c], acc[bb]);
+    }
+#pragma unroll
+    for (int bb = 0; bb < NBT; ++bb) {
+      if (bb < nb) {
+        const float v = warp_sum(acc[bb]);
+        if (lane == 0) a.out[((int64_t)(b0 + bb) * a.H + h) * a.V + j0 + j] = v;
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
   extern __shared__ float sm[];
   pdl_trigger();
@@ -156,24 +182,14 @@ __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
     __syncthreads();
   }
   // out[b, h, j0 + j]: one warp per output j, lanes across the latent, all sequences at once
-  for (int j = warp; j < nj; j += CMB_THREADS / 32) {
-    float acc[CMB_BC];
-#pragma unroll
-    for (int bb = 0; bb < CMB_BC; ++bb) acc[bb] = 0.f;
-    const float* wr = w_s + j * 4 * C4;
-    for (int c = lane; c < C; c += 32) {
-      const float wv = wr[c];
-#pragma unroll
-      for (int bb = 0; bb < CMB_BC; ++bb)
-        if (bb < nb) acc[bb] = fmaf(wv, vc_s[bb * 4 * C4 + c], acc[bb]);
-    }
-#pragma unroll
-    for (int bb = 0; bb < CMB_BC; ++bb) {
-      if (bb < nb) {
-        const float v = warp_sum(acc[bb]);
-        if (lane == 0) a.out[((int64_t)(b0 + bb) * a.H + h) * a.V + j0 + j] = v;
-      }
-    }
+  if (nb == 1) {
+    combine_outputs<1>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0, warp, lane);
+  } else if (nb == 2) {
+    combine_outputs<2>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0, warp, lane);
+  } else if (nb <= 4) {
+    combine_outputs<4>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0, warp, lane);
+  } else {
+    combine_outputs<CMB_BC>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0, warp, lane);
   }
   if (blockIdx.y == 0 && a.lse != nullptr)
     for (int bb = threadIdx.x; bb < nb; bb += CMB_THREADS) a.lse[(int64_t)(b0 + bb) * a.H + h] = lse_s[bb];
