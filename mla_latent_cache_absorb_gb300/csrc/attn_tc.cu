@@ -249,6 +249,35 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
   }
   long long r0, r1;
   cta_range(T, k, a.ncg, &r0, &r1);
+  // on-chip set-up (barriers, TMEM, tensor-map prefetch) overlaps the previous kernel
+  if (r0 < r1) {
+    if (tid == 0) {
+      for (int i = 0; i < TC_KB; ++i) {
+        tc::mbar_init(&s.full[i], 1);
+        tc::mbar_init(&s.empty[i], 1);
+      }
+      tc::mbar_init(&s.q_full, 1);
+      tc::mbar_init(&s.q_empty, 1);
+      for (int i = 0; i < 2; ++i) {
+        tc::mbar_init(&s.s_full[i], 1);
+        tc::mbar_init(&s.s_empty[i], 128 * Cfg<HG>::NWG);
+      }
+      tc::mbar_init(&s.p_full, 128 * Cfg<HG>::NWG);
+      tc::mbar_init(&s.o_done, 1);
+      tc::mbar_init(&s.o_empty, 128 * Cfg<HG>::NWG);
+      tc::mbar_init(&s.mma_fin, 1);
+      tc::fence_mbar_init();
+    }
+    if (warp == TC_MMA_WARP) {
+      tc::tmem_alloc(&s.tmem_base, Cfg<HG>::TMEM_COLS);
+      tc::tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+      tc::tma_prefetch_desc(&rows_map);
+      tc::tma_prefetch_desc(&q_map);
+      tc::tma_prefetch_desc(&qres_map);
+    }
+  }
   // everything below reads what the absorb / append kernels wrote (query rows, the new cache
   // row) or writes what the previous step's combine may still read (meta, partials)
   pdl_wait();
@@ -305,32 +334,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
     return;   // uniform: every thread computed the same range
   }
 
-  if (tid == 0) {
-    for (int i = 0; i < TC_KB; ++i) {
-      tc::mbar_init(&s.full[i], 1);
-      tc::mbar_init(&s.empty[i], 1);
-    }
-    tc::mbar_init(&s.q_full, 1);
-    tc::mbar_init(&s.q_empty, 1);
-    for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&s.s_full[i], 1);
-      tc::mbar_init(&s.s_empty[i], 128 * Cfg<HG>::NWG);
-    }
-    tc::mbar_init(&s.p_full, 128 * Cfg<HG>::NWG);
-    tc::mbar_init(&s.o_done, 1);
-    tc::mbar_init(&s.o_empty, 128 * Cfg<HG>::NWG);
-    tc::mbar_init(&s.mma_fin, 1);
-    tc::fence_mbar_init();
-  }
-  if (warp == TC_MMA_WARP) {
-    tc::tmem_alloc(&s.tmem_base, Cfg<HG>::TMEM_COLS);
-    tc::tmem_relinquish();
-  }
-  if (warp == 0 && lane == 0) {
-    tc::tma_prefetch_desc(&rows_map);
-    tc::tma_prefetch_desc(&q_map);
-    tc::tma_prefetch_desc(&qres_map);
-  }
   tc::fence_proxy_async_smem();   // the prologue's generic writes to the slots precede TMA writes
   tc::tc_fence_before();
   __syncwarp();

@@ -17,7 +17,7 @@
 
 namespace mla {
 
-constexpr int CMB_THREADS = 256;
+constexpr int CMB_THREADS = 512;
 constexpr int CMB_VJ = 32;      // V outputs per CTA
 constexpr int CMB_BC = 8;       // sequences per CTA
 constexpr int CMB_U = 8;        // partial loads in flight per thread
