@@ -14,10 +14,11 @@
 namespace mla {
 
 // ---- kv_a projection: kva[b, r] = sum_k x[b, k] * W[r, k] ------------------------------------
-// One warp per output row r, all B sequences at once (W is read once, 16-byte vectors);
-// x is small and stays in L1/L2.
-constexpr int GEMV_WARPS = 8;
+// One warp per output row r, all B sequences at once (W is read once, 16-byte vectors, four
+// of them in flight per lane); x is small and stays in L1/L2.
+constexpr int GEMV_WARPS = 4;
 constexpr int GEMV_BMAX = 8;   // sequences per register pass
+constexpr int GEMV_UNROLL = 4;
 
 template <int DT>
 __global__ void __launch_bounds__(GEMV_WARPS * 32)
@@ -35,17 +36,27 @@ append_gemv_kernel(const typename Act<DT>::T* __restrict__ x, const typename Act
     float acc[GEMV_BMAX];
 #pragma unroll
     for (int j = 0; j < GEMV_BMAX; ++j) acc[j] = 0.f;
-    for (int k = lane * VEC; k < hidden; k += 32 * VEC) {
-      uint4 wv = *reinterpret_cast<const uint4*>(wr + k);
-      const T* we = reinterpret_cast<const T*>(&wv);
+    for (int k0 = lane * VEC; k0 < hidden; k0 += 32 * VEC * GEMV_UNROLL) {
+      uint4 wv[GEMV_UNROLL];
 #pragma unroll
-      for (int j = 0; j < GEMV_BMAX; ++j) {
-        if (j < nb) {
-          uint4 xv = *reinterpret_cast<const uint4*>(x + (int64_t)(b0 + j) * hidden + k);
-          const T* xe = reinterpret_cast<const T*>(&xv);
+      for (int u = 0; u < GEMV_UNROLL; ++u) {
+        const int k = k0 + u * 32 * VEC;
+        wv[u] = k < hidden ? *reinterpret_cast<const uint4*>(wr + k) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-          for (int e = 0; e < VEC; ++e)
-            acc[j] = fmaf(Act<DT>::load(we, e), Act<DT>::load(xe, e), acc[j]);
+      for (int u = 0; u < GEMV_UNROLL; ++u) {
+        const int k = k0 + u * 32 * VEC;
+        if (k >= hidden) break;
+        const T* we = reinterpret_cast<const T*>(&wv[u]);
+#pragma unroll
+        for (int j = 0; j < GEMV_BMAX; ++j) {
+          if (j < nb) {
+            uint4 xv = *reinterpret_cast<const uint4*>(x + (int64_t)(b0 + j) * hidden + k);
+            const T* xe = reinterpret_cast<const T*>(&xv);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+              acc[j] = fmaf(Act<DT>::load(we, e), Act<DT>::load(xe, e), acc[j]);
+          }
         }
       }
     }

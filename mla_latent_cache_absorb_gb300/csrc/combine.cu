@@ -6,11 +6,12 @@
 // src/families/deepseek2/attn.rs, encode_mla_v_combine (Q8_0 W_UV). The split + COMBINE pass
 // structure follows turbospark-runtime 0.3.0, src/families/gptoss/attn.rs.
 //
-// Grid (head, 32-wide slice of V, block of 8 sequences). Each CTA stages its slice of W_UV
-// (dequantised) in shared memory, merges the splits of its sequences for its head into float32
-// latent vectors (every thread keeps several partial loads in flight; with few sequences the
-// slots are shared out over several threads and summed in a fixed order), and forms the dot
-// products one warp per output with the lanes across the latent.
+// Grid (head, slice of V, block of 8 sequences); the V-slices per head are as few as still give
+// about one CTA per SM, since every slice merges the partials again. Each CTA merges the splits
+// of its sequences for its head into float32 latent vectors (every thread keeps several partial
+// loads in flight; with few sequences the slots are shared out over several threads and summed
+// in a fixed order), then, 32 outputs at a time, stages those rows of W_UV (dequantised) in
+// shared memory and forms the dot products one warp per output with the lanes across the latent.
 #include "common.cuh"
 
 #include <math_constants.h>
@@ -34,6 +35,7 @@ struct CombineArgs {
   int kv_b_dtype;
   int H, C, N, V, R, B;
   int hpg, n_slots, max_slots;
+  int vper;                 // outputs per CTA (a multiple of CMB_VJ): the merge is done once per CTA
 };
 
 // out[b0 + bb, h, j0 + j] = W_UV row j . vc[bb] for bb < nb <= NBT: one warp per output, lanes
@@ -66,10 +68,10 @@ __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
   extern __shared__ float sm[];
   pdl_trigger();
   const int h = blockIdx.x;
-  const int j0 = blockIdx.y * CMB_VJ;
+  const int jbeg = blockIdx.y * a.vper;
+  const int jend = min(a.V, jbeg + a.vper);
   const int b0 = blockIdx.z * CMB_BC;
   const int nb = min(CMB_BC, a.B - b0);
-  const int nj = min(CMB_VJ, a.V - j0);
   const int C = a.C;
   const int C4 = (C + 3) / 4;               // latent in groups of 4
   float* w_s = sm;                          // [CMB_VJ][4*C4]
@@ -82,8 +84,9 @@ __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
   const int pg = h / a.hpg, hh = h % a.hpg;
   auto lse_at = [&](int slot) { return ((int64_t)pg * a.n_slots + slot) * a.hpg + hh; };
 
-  const int64_t wrow0 = (int64_t)h * (a.N + a.V) + a.N + j0;
-  stage_kv_b_rows(w_s, 4 * C4, a.kv_b, a.kv_b_dtype, wrow0, nj, 0, C, C, CMB_THREADS);
+  // W_UV rows of the first 32-output chunk (the rest follow after the merge)
+  const int64_t wrow0 = (int64_t)h * (a.N + a.V) + a.N;
+  stage_kv_b_rows(w_s, 4 * C4, a.kv_b, a.kv_b_dtype, wrow0 + jbeg, min(CMB_VJ, jend - jbeg), 0, C, C, CMB_THREADS);
   pdl_wait();   // the partials and meta come from the attention kernel
 
   // split weights exp(lse_s - lse): one warp per sequence
@@ -181,15 +184,24 @@ __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
     }
     __syncthreads();
   }
-  // out[b, h, j0 + j]: one warp per output j, lanes across the latent, all sequences at once
-  if (nb == 1) {
-    combine_outputs<1>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0, warp, lane);
-  } else if (nb == 2) {
-    combine_outputs<2>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0, warp, lane);
-  } else if (nb <= 4) {
-    combine_outputs<4>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0, warp, lane);
-  } else {
-    combine_outputs<CMB_BC>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0, warp, lane);
+  // out[b, h, j0 + j]: one warp per output j, lanes across the latent, all sequences at once;
+  // the CTA's outputs in chunks of 32 W_UV rows
+  for (int j0 = jbeg; j0 < jend; j0 += CMB_VJ) {
+    const int nj = min(CMB_VJ, jend - j0);
+    if (j0 != jbeg) {
+      __syncthreads();   // the previous chunk's dot products are done with w_s
+      stage_kv_b_rows(w_s, 4 * C4, a.kv_b, a.kv_b_dtype, wrow0 + j0, nj, 0, C, C, CMB_THREADS);
+      __syncthreads();
+    }
+    if (nb == 1) {
+      combine_outputs<1>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0, warp, lane);
+    } else if (nb == 2) {
+      combine_outputs<2>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0, warp, lane);
+    } else if (nb <= 4) {
+      combine_outputs<4>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0, warp, lane);
+    } else {
+      combine_outputs<CMB_BC>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0, warp, lane);
+    }
   }
   if (blockIdx.y == 0 && a.lse != nullptr)
     for (int bb = threadIdx.x; bb < nb; bb += CMB_THREADS) a.lse[(int64_t)(b0 + bb) * a.H + h] = lse_s[bb];
@@ -207,7 +219,16 @@ cudaError_t launch_combine(const mla_config& cfg, const DecodePlan& plan, const 
   a.hpg = plan.part_hpg; a.n_slots = plan.n_slots;
   // most slots one sequence can span: splits (CUDA-core path) or CTAs per group (tensor path)
   a.max_slots = plan.path == PATH_TC ? plan.ctas_per_group : plan.splits;
-  dim3 grid(cfg.n_heads, (cfg.v_head + CMB_VJ - 1) / CMB_VJ, (B + CMB_BC - 1) / CMB_BC);
+  // V-slices per head: enough CTAs to cover the SMs, but every slice merges the partials again
+  const int chunks = (cfg.v_head + CMB_VJ - 1) / CMB_VJ;
+  const int64_t base_ctas = (int64_t)cfg.n_heads * ((B + CMB_BC - 1) / CMB_BC);
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 152;
+  int vsplit = (int)((sms + base_ctas - 1) / base_ctas);
+  vsplit = vsplit < 1 ? 1 : (vsplit > chunks ? chunks : vsplit);
+  a.vper = ((chunks + vsplit - 1) / vsplit) * CMB_VJ;
+  dim3 grid(cfg.n_heads, (cfg.v_head + a.vper - 1) / a.vper, (B + CMB_BC - 1) / CMB_BC);
   const size_t c4 = 4 * (size_t)((cfg.kv_lora + 3) / 4);
   const size_t smem = sizeof(float) * ((size_t)CMB_VJ * c4 + (size_t)CMB_BC * c4 + 4 * (size_t)CMB_THREADS +
                                        (size_t)CMB_BC * a.max_slots + 3 * CMB_BC);

@@ -102,12 +102,18 @@ __device__ __forceinline__ void kv_b_load8(float v[8], const void* kv_b, int dty
       const float4 a = src[0], b = src[1];
       v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
     } else {
-      const uint8_t* blk = static_cast<const uint8_t*>(kv_b) + r * (int64_t)(C / 32) * 34 + (c / 32) * 34;
-      const uint16_t dbits = static_cast<uint16_t>(blk[0]) | (static_cast<uint16_t>(blk[1]) << 8);
-      const float d = __half2float(__ushort_as_half(dbits));
-      const int o = 2 + (c & 31);
+      // a block starts at an even byte offset (34 bytes each), so the scale and the codes are
+      // read as 16-bit words (little endian: the lower byte is the lower element)
+      const uint16_t* blk = reinterpret_cast<const uint16_t*>(static_cast<const uint8_t*>(kv_b) +
+                                                              r * (int64_t)(C / 32) * 34 + (c / 32) * 34);
+      const float d = __half2float(__ushort_as_half(blk[0]));
+      const int o = 1 + (c & 31) / 2;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = d * static_cast<float>(static_cast<int8_t>(blk[o + e]));
+      for (int e = 0; e < 4; ++e) {
+        const uint16_t w = blk[o + e];
+        v[2 * e] = d * static_cast<float>(static_cast<int8_t>(w & 0xFF));
+        v[2 * e + 1] = d * static_cast<float>(static_cast<int8_t>(w >> 8));
+      }
     }
   } else {
 #pragma unroll
