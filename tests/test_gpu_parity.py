@@ -23,6 +23,8 @@ SMALL = [
     ("ragged_contig_small", W["ragged_paged_b64"].with_(B=5, page_size=0, context=("uniform", 1, 700))),
     ("q8_gemv_small", W["long_q8_b4_t131072"].with_(B=2, context=("fixed", 1500))),
     ("q8_gemv_h16", W["long_q8_b4_t131072"].with_(B=3, H=16, context=("fixed", 129), hidden=1024)),
+    # nine sequences: the kv_a projection's second register pass and a second combine block
+    ("q8_gemv_b9", W["long_q8_b4_t131072"].with_(B=9, H=16, context=("fixed", 200), hidden=1024)),
     ("bf16_odd_heads", W["v3_b32_t4096"].with_(B=2, H=24, context=("fixed", 200))),
 ]
 
