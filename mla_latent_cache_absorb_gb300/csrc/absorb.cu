@@ -25,7 +25,7 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
   // value v goes out as its storage rounding, and (bf16 only) the rounding residual to q_res
   auto put = [&](int64_t i, float v) {
     Act<DT>::store(q_abs, i, v);
-    if (q_res != nullptr) Act<DT>::store(q_res, i, v - Act<DT>::load(q_abs, i));
+    if (q_res != nullptr) Act<DT>::store(q_res, i, v - Act<DT>::rounded(v));
   };
   extern __shared__ float sm[];
   pdl_trigger();

@@ -21,6 +21,7 @@ namespace mla {
 constexpr int CMB_THREADS = 512;
 constexpr int CMB_VJ = 32;      // V outputs per CTA
 constexpr int CMB_BC = 8;       // sequences per CTA
+constexpr int CMB_RES_MAX = 512; // latent widths whose query residual is staged in shared memory
 constexpr int CMB_U = 8;        // partial loads in flight per thread
 
 struct CombineArgs {
@@ -81,6 +82,7 @@ __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
   float* lse_s = wt_s + CMB_BC * a.max_slots;                          // [CMB_BC]
   int* first_s = reinterpret_cast<int*>(lse_s + CMB_BC);               // [CMB_BC]
   int* cnt_s = first_s + CMB_BC;                                        // [CMB_BC]
+  uint16_t* res_s = reinterpret_cast<uint16_t*>(cnt_s + CMB_BC);        // [CMB_BC][C] when C <= 512
   const int pg = h / a.hpg, hh = h % a.hpg;
   auto lse_at = [&](int slot) { return ((int64_t)pg * a.n_slots + slot) * a.hpg + hh; };
 
@@ -88,6 +90,12 @@ __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
   const int64_t wrow0 = (int64_t)h * (a.N + a.V) + a.N;
   stage_kv_b_rows(w_s, 4 * C4, a.kv_b, a.kv_b_dtype, wrow0 + jbeg, min(CMB_VJ, jend - jbeg), 0, C, C, CMB_THREADS);
   pdl_wait();   // the partials and meta come from the attention kernel
+  // the query residual (first-order LSE correction below) goes to shared memory together with
+  // the split metadata: one memory round trip less on the way to the output
+  const bool res_pre = a.q_res != nullptr && C <= CMB_RES_MAX;
+  if (res_pre)
+    for (int i = threadIdx.x; i < nb * C; i += CMB_THREADS)
+      res_s[i] = a.q_res[((int64_t)(b0 + i / C) * a.H + h) * (C + a.R) + i % C];
 
   // split weights exp(lse_s - lse): one warp per sequence
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -176,7 +184,7 @@ __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
     // the scores used bf16 latent queries q_hi = q' - res: to first order the exact log-sum-exp
     // is lse + scale * (sum_t p_t kv_lat_t) . res = lse + scale * vc . res
     for (int bb = warp; bb < nb; bb += CMB_THREADS / 32) {
-      const uint16_t* res = a.q_res + ((int64_t)(b0 + bb) * a.H + h) * (C + a.R);
+      const uint16_t* res = res_pre ? res_s + bb * C : a.q_res + ((int64_t)(b0 + bb) * a.H + h) * (C + a.R);
       float d = 0.f;
       for (int c = lane; c < C; c += 32) d = fmaf(vc_s[bb * 4 * C4 + c], bf16_bits_to_f32(res[c]), d);
       d = warp_sum(d);
@@ -231,7 +239,8 @@ cudaError_t launch_combine(const mla_config& cfg, const DecodePlan& plan, const 
   dim3 grid(cfg.n_heads, (cfg.v_head + a.vper - 1) / a.vper, (B + CMB_BC - 1) / CMB_BC);
   const size_t c4 = 4 * (size_t)((cfg.kv_lora + 3) / 4);
   const size_t smem = sizeof(float) * ((size_t)CMB_VJ * c4 + (size_t)CMB_BC * c4 + 4 * (size_t)CMB_THREADS +
-                                       (size_t)CMB_BC * a.max_slots + 3 * CMB_BC);
+                                       (size_t)CMB_BC * a.max_slots + 3 * CMB_BC) +
+                      sizeof(uint16_t) * (size_t)CMB_BC * CMB_RES_MAX;
   cudaError_t e = ensure_smem((const void*)combine_kernel, (int)smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(combine_kernel, grid, dim3(CMB_THREADS), smem, st, a);

@@ -59,6 +59,7 @@ template <> struct Act<MLA_F32> {
   using T = float;
   static __device__ __forceinline__ float load(const T* p, int64_t i) { return p[i]; }
   static __device__ __forceinline__ void store(T* p, int64_t i, float v) { p[i] = v; }
+  static __device__ __forceinline__ float rounded(float v) { return v; }   // the stored value
 };
 template <> struct Act<MLA_BF16> {
   using T = uint16_t;
@@ -67,6 +68,7 @@ template <> struct Act<MLA_BF16> {
     __nv_bfloat16 h = __float2bfloat16_rn(v);
     p[i] = *reinterpret_cast<uint16_t*>(&h);
   }
+  static __device__ __forceinline__ float rounded(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 };
 
 // One kv_b element (row r, column c) in any weight dtype. Q8_0: fp16 scale then 32 codes
