@@ -33,7 +33,9 @@ def test_bad_seq_len_sets_error_and_nan_only_for_that_sequence(bad_len):
     assert st == L.STATUS_CODE["MLA_ERR_BAD_SEQ_LEN"] and seq == 1
     out = ds.out.cpu().numpy()
     assert np.all(np.isnan(out[1])) and np.all(np.isnan(ds.lse[1].cpu().numpy()))
-    assert np.array_equal(out[0], good[0].cpu().numpy()) and np.array_equal(out[2], good[2].cpu().numpy())
+    # the other sequences are unaffected; an invalid length can move the split boundaries (one
+    # sequence fewer in the tile list), which changes only float32 summation order
+    assert max_rel(out[0], good[0].cpu().numpy()) <= 1e-5 and max_rel(out[2], good[2].cpu().numpy()) <= 1e-5
     # the error is sticky until cleared
     ds.seq_lens[1] = 201
     L.check(ds.decode(), "decode")

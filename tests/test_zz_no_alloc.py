@@ -85,7 +85,9 @@ def test_noalloc_reports_each_calls_own_device_error():
     assert err.tolist() == [L.STATUS_CODE["MLA_ERR_BAD_SEQ_LEN"], 2]
     assert torch.isnan(out[2]).all() and torch.isnan(lse[2]).all()
     keep = [0, 1, 3]
-    assert torch.equal(out[keep], ref_out[keep])
+    # unaffected up to float32 summation order (the invalid length can move split boundaries)
+    ref = ref_out[keep]
+    assert float((out[keep] - ref).abs().max()) <= 1e-5 * float(ref.abs().max())
     # the next call starts from a cleared error word
     L.check(_noalloc(ds, out, lse, err), "mla_decode_attn_noalloc")
     torch.cuda.synchronize()
