@@ -26,7 +26,12 @@
  *     allocates no device memory and keeps no per-call state (mla_decode_attn_noalloc,
  *     at the end, uses one fixed device array that is part of the library).
  *   - Calls marked "async" only validate on the host and enqueue kernels on `stream`;
- *     they return before the GPU work ends and never synchronise. Errors found on the
+ *     they return before the GPU work ends and never synchronise. The kernels are launched
+ *     with programmatic stream serialization: each lets the next kernel on the stream launch
+ *     early and waits for its predecessor before touching data another kernel produces. A
+ *     caller's own kernel launched right after with that same launch attribute must execute
+ *     griddepcontrol.wait before it reads a call's outputs; ordinary launches, copies and events
+ *     wait for completion as usual. Errors found on the
  *     host return before anything is enqueued. Conditions only the GPU can see (a bad
  *     length, a position that does not match the cache length, a page id out of range)
  *     set a sticky error word in the call's workspace; the affected sequence's outputs
