@@ -26,6 +26,10 @@ SMALL = [
     # nine sequences: the kv_a projection's second register pass and a second combine block
     ("q8_gemv_b9", W["long_q8_b4_t131072"].with_(B=9, H=16, context=("fixed", 200), hidden=1024)),
     ("bf16_odd_heads", W["v3_b32_t4096"].with_(B=2, H=24, context=("fixed", 200))),
+    # one 64-head group (two softmax warpgroups); 96 heads: a second group half filled, so its
+    # second warpgroup owns no real head
+    ("h64_one_group", W["v3_b32_t4096"].with_(B=3, H=64, context=("fixed", 500))),
+    ("h96_partial_group", W["v3_b32_t4096"].with_(B=2, H=96, context=("uniform", 100, 600))),
 ]
 
 
