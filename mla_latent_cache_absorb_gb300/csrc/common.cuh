@@ -204,6 +204,26 @@ __device__ __forceinline__ void rope_cs(const double* inv_freq, int i, int pos, 
   rope_cs_value(inv_freq[i], pos, c, s);
 }
 
+// The same angle in float arithmetic only (double throughput is very low on this GPU), for a
+// frequency given as two floats inv_hi + inv_lo with 0 < inv_hi <= 1 and 0 <= pos < ROPE_F32_MAX_POS:
+// the product pos * inv as an unevaluated sum a_hi + a_lo (the FMA yields the rounding error of
+// pos * inv_hi exactly), then a three-term Cody-Waite reduction by 2 pi = P1 + P2 + P3 with
+// P1 = 201/32 (8 significant bits, so k * P1 is exact for quotients k < 2^16 and a_hi - k * P1
+// is exact), P2 and P3 the float roundings of the successive remainders: about 5e-7 rad of
+// absolute error. The reduced angle lies in [-pi, pi] (to rounding), where the hardware sine and
+// cosine approximations are accurate to about 2^-21 absolute.
+constexpr int ROPE_F32_MAX_POS = 1 << 18;
+__device__ __forceinline__ void rope_cs_f32(float inv_hi, float inv_lo, int pos, float* c, float* s) {
+  const float x = static_cast<float>(pos);                 // exact: pos < 2^24
+  const float a_hi = x * inv_hi;
+  const float a_lo = fmaf(x, inv_hi, -a_hi) + x * inv_lo;
+  const float k = rintf(a_hi * 0.15915494f);               // whole turns
+  float r = fmaf(-k, 6.28125f, a_hi);
+  r = fmaf(-k, 1.9353071693331003e-3f, r);
+  r = fmaf(-k, 1.0253131677018246e-11f, r);
+  __sincosf(r + a_lo, s, c);
+}
+
 // ---- decode plan: how the rows of a sequence are split, and the workspace layout -------------
 struct DecodePlan {
   int path;              // PATH_SIMT or PATH_TC

@@ -58,6 +58,7 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
   uint8_t* dyn = align1024(dyn_raw);
   uint8_t* ws = dyn;                 // 4 blocks [128 n rows x 64 latent] (MN-major A)
   uint8_t* qs = dyn + 4 * 16384;     // 2 blocks [64 b rows x 64 n] (K-major B)
+  __shared__ float rope_hi[32], rope_lo[32];   // the RoPE frequencies as float pairs (rope <= 64)
   pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x, lh = blockIdx.y, b0 = blockIdx.z * ABS_TC_BCHUNK;
@@ -74,6 +75,13 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
   if (warp == 0) {
     tc::tmem_alloc(&tmem_base, 128);
     tc::tmem_relinquish();
+  }
+  const bool rope_f32 = a.positions != nullptr && a.R <= 64;
+  if (rope_f32 && tid < a.R / 2) {
+    const double inv = a.inv_freq[tid];
+    const float hi = __double2float_rn(inv);
+    rope_hi[tid] = hi;
+    rope_lo[tid] = __double2float_rn(inv - static_cast<double>(hi));
   }
   tc::tc_fence_before();
   __syncwarp();
@@ -125,65 +133,56 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
     tc::mma_commit(&bar_mma);   // arrives once every MMA issued above has completed
   }
   pdl_wait();   // the fused query rows may still be read by the previous step's attention
-  // rotated q_pe into the row's tail (once per head and batch chunk), while the MMAs run; a
-  // thread loads all of its pairs (and their positions and frequencies) before using any
-  if (lh == 0) {
-    constexpr int RI = ABS_TC_BCHUNK * 32 / G_THREADS;   // pairs per thread for R <= 64
-    const int npairs = nb * (a.R / 2);
+  // rotated q_pe into the row's tail, while the MMAs run: the batch chunk's pairs are shared
+  // by the CTAs of the two latent halves; a thread loads all of its pairs (and positions)
+  // before using any
+  {
+    const int hr = a.R / 2;
+    const int npairs = nb * hr;
+    const int pb = lh == 0 ? 0 : npairs / 2, pe = lh == 0 ? npairs / 2 : npairs;
+    constexpr int RI = (ABS_TC_BCHUNK * 32 / 2 + G_THREADS - 1) / G_THREADS;   // rope <= 64
     uint32_t xv[RI];
     int pv[RI];
-    double fv[RI];
 #pragma unroll
     for (int m = 0; m < RI; ++m) {
-      const int i = tid + m * G_THREADS;
-      xv[m] = 0; pv[m] = 0; fv[m] = 0.0;
-      if (i < npairs) {
-        const int bb = i / (a.R / 2), p = i % (a.R / 2);
+      const int i = pb + tid + m * G_THREADS;
+      xv[m] = 0;
+      pv[m] = 0;
+      if (i < pe) {
+        const int bb = i / hr, p = i - bb * hr;
         xv[m] = *reinterpret_cast<const uint32_t*>(a.q + ((size_t)(b0 + bb) * a.H + h) * qrow + a.N + 2 * p);
-        if (a.positions != nullptr) {
-          pv[m] = a.positions[b0 + bb];
-          fv[m] = a.inv_freq[p];
-        }
+        if (a.positions != nullptr) pv[m] = a.positions[b0 + bb];
       }
     }
-#pragma unroll
-    for (int m = 0; m < RI; ++m) {
-      const int i = tid + m * G_THREADS;
-      if (i < npairs) {
-        const int bb = i / (a.R / 2), p = i % (a.R / 2);
-        const size_t ai = ((size_t)(b0 + bb) * a.H + h) * arow + a.C + 2 * p;
-        const float x0 = __uint_as_float(xv[m] << 16), x1 = __uint_as_float(xv[m] & 0xFFFF0000u);
-        float y0 = x0, y1 = x1;
-        if (a.positions != nullptr) {
-          float c, sn;
-          rope_cs_value(fv[m], pv[m], &c, &sn);
-          y0 = x0 * c - x1 * sn;
-          y1 = x0 * sn + x1 * c;
-        }
-        const uint16_t h0 = bf16_bits(y0), h1 = bf16_bits(y1);
-        *reinterpret_cast<uint32_t*>(a.q_abs + ai) = (uint32_t)h0 | ((uint32_t)h1 << 16);
-        *reinterpret_cast<uint32_t*>(a.q_res + ai) =
-            (uint32_t)bf16_bits(y0 - bf16_bits_to_f32(h0)) | ((uint32_t)bf16_bits(y1 - bf16_bits_to_f32(h1)) << 16);
-      }
-    }
-    // rope widths above 64 leave pairs for a plain loop
-    for (int i = tid + RI * G_THREADS; i < npairs; i += G_THREADS) {
-      const int bb = i / (a.R / 2), p = i % (a.R / 2);
-      const size_t qi = ((size_t)(b0 + bb) * a.H + h) * qrow + a.N + 2 * p;
+    auto rotate = [&](int i, uint32_t x, int pos) {
+      const int bb = i / hr, p = i - bb * hr;
       const size_t ai = ((size_t)(b0 + bb) * a.H + h) * arow + a.C + 2 * p;
-      const float x0 = bf16_bits_to_f32(a.q[qi]), x1 = bf16_bits_to_f32(a.q[qi + 1]);
+      const float x0 = __uint_as_float(x << 16), x1 = __uint_as_float(x & 0xFFFF0000u);
       float y0 = x0, y1 = x1;
       if (a.positions != nullptr) {
         float c, sn;
-        rope_cs(a.inv_freq, p, a.positions[b0 + bb], &c, &sn);
+        if (rope_f32 && pos >= 0 && pos < ROPE_F32_MAX_POS && rope_hi[p] > 0.f && rope_hi[p] <= 1.f)
+          rope_cs_f32(rope_hi[p], rope_lo[p], pos, &c, &sn);
+        else
+          rope_cs(a.inv_freq, p, pos, &c, &sn);
         y0 = x0 * c - x1 * sn;
         y1 = x0 * sn + x1 * c;
       }
       const uint16_t h0 = bf16_bits(y0), h1 = bf16_bits(y1);
-      a.q_abs[ai] = h0;
-      a.q_abs[ai + 1] = h1;
-      a.q_res[ai] = bf16_bits(y0 - bf16_bits_to_f32(h0));
-      a.q_res[ai + 1] = bf16_bits(y1 - bf16_bits_to_f32(h1));
+      *reinterpret_cast<uint32_t*>(a.q_abs + ai) = (uint32_t)h0 | ((uint32_t)h1 << 16);
+      *reinterpret_cast<uint32_t*>(a.q_res + ai) =
+          (uint32_t)bf16_bits(y0 - bf16_bits_to_f32(h0)) | ((uint32_t)bf16_bits(y1 - bf16_bits_to_f32(h1)) << 16);
+    };
+#pragma unroll
+    for (int m = 0; m < RI; ++m) {
+      const int i = pb + tid + m * G_THREADS;
+      if (i < pe) rotate(i, xv[m], pv[m]);
+    }
+    // rope widths above 64 leave pairs for a plain loop
+    for (int i = pb + tid + RI * G_THREADS; i < pe; i += G_THREADS) {
+      const int bb = i / hr, p = i - bb * hr;
+      rotate(i, *reinterpret_cast<const uint32_t*>(a.q + ((size_t)(b0 + bb) * a.H + h) * qrow + a.N + 2 * p),
+             a.positions != nullptr ? a.positions[b0 + bb] : 0);
     }
   }
   __syncwarp();   // lanes 1-31 of warp 0 wait for lane 0
@@ -192,23 +191,36 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
                                              !*reinterpret_cast<volatile int*>(&failed));
   tc::tc_fence_after();
   if (ok) {
+    // Lane = latent column, TMEM column = sequence: each warp transposes its 32 x 32 block
+    // through shared memory (the B operand's space, free once the MMAs are done) so that every
+    // lane then writes 16-byte pieces of 8 consecutive latent columns of one sequence.
+    uint16_t* hi_s = reinterpret_cast<uint16_t*>(qs + warp * 4096);   // [32 sequences][32 columns]
+    uint16_t* lo_s = hi_s + 32 * 32;
     for (int mc = 0; mc < 2; ++mc) {
-      const int c = 256 * lh + 128 * mc + 32 * warp + lane;
+      const int cw = 256 * lh + 128 * mc + 32 * warp;   // this warp's first latent column
       for (int col0 = 0; col0 < NB; col0 += 32) {
         uint32_t r[32];
         tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + mc * 64 + col0, r);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const int b = col0 + j;
+          const float v = __uint_as_float(r[j]);
+          const uint16_t hi = bf16_bits(v);
+          hi_s[j * 32 + lane] = hi;
+          lo_s[j * 32 + lane] = bf16_bits(v - bf16_bits_to_f32(hi));
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int chunk = lane + 32 * i, bj = chunk >> 2, g = chunk & 3;
+          const int b = col0 + bj;
           if (b < nb) {
-            const size_t ai = ((size_t)(b0 + b) * a.H + h) * arow + c;
-            const float v = __uint_as_float(r[j]);
-            const uint16_t hi = bf16_bits(v);
-            a.q_abs[ai] = hi;
-            a.q_res[ai] = bf16_bits(v - bf16_bits_to_f32(hi));
+            const size_t ai = ((size_t)(b0 + b) * a.H + h) * arow + cw + 8 * g;
+            *reinterpret_cast<uint4*>(a.q_abs + ai) = *reinterpret_cast<const uint4*>(hi_s + bj * 32 + 8 * g);
+            *reinterpret_cast<uint4*>(a.q_res + ai) = *reinterpret_cast<const uint4*>(lo_s + bj * 32 + 8 * g);
           }
         }
+        __syncwarp();
       }
     }
   }

@@ -72,6 +72,36 @@ def test_prerotated_q_pe_matches_positions_path():
         assert np.max(np.abs(lse[b] - lb)) <= LSE_TOL
 
 
+@gpu
+def test_large_query_positions_on_the_tensor_core_absorb():
+    """The batched (tcgen05) absorb rotates q_pe with float-only angle arithmetic below 2^18 and
+    the double path above it: query positions from 0 past that limit, against the oracle."""
+    torch = need_gpu()
+    from oracle import mla_oracle as O
+    from oracle import step as OS
+    from mla_latent_cache_absorb_gb300 import binding as L
+    from mla_latent_cache_absorb_gb300.runner import DeviceStep
+    wl = W["v3_b32_t4096"].with_(B=8, context=("fixed", 160))
+    prob = synth.make_problem(wl)
+    qpos = np.array([0, 1, 4095, 65535, 131072, 200003, 262143, 262144 + 12345], dtype=np.int32)
+    ds = DeviceStep(prob)
+    st, plan = L.mla_decode_plan(ds.cfg, wl.B)
+    L.check(st, "plan")
+    L.check(ds.append(), "append")                 # the new rows at their own positions
+    ds.positions = torch.from_numpy(qpos).to(ds.device)
+    L.check(ds.decode(), "decode")
+    torch.cuda.synchronize()
+    out, lse = ds.out.cpu().numpy(), ds.lse.cpu().numpy()
+    inv, scale = OS.tables(wl)
+    W_UK, W_UV = O.split_kv_b(OS.kv_b_f64(prob), wl.H, wl.N, wl.V)
+    new = OS.store(OS.appended_rows(prob), wl.act)
+    q = OS.decode_act(prob.q, wl.act)
+    for b in range(wl.B):
+        ob, lb = O.decode_one(q[b], W_UK, W_UV, OS.sequence_rows(prob, b, new[b]), int(qpos[b]), inv, scale, wl.C)
+        assert max_rel(out[b], ob) <= OUT_TOL, b
+        assert np.max(np.abs(lse[b] - lb)) <= LSE_TOL, b
+
+
 # ---- full-size workloads ------------------------------------------------------------------------
 
 @gpu
