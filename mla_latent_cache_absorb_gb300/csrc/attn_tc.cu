@@ -355,6 +355,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
       for (int kb = 0; kb < TC_KB; ++kb) last_n[kb] = -1;
       int q_loaded = -1;
       bool ok = true;
+      // cache rows are read once per head group, by CTAs that run side by side: mark them first
+      // to leave L2, so that the split partials this kernel writes stay there for the combine
+      const uint64_t kv_policy = tc::l2_policy_evict_first();
       while (ok && it.next(a, &sb, &tlo, &thi)) {
         if (pw == 0) {
           if (seg > 0 && !wait_bar(s, &s.q_empty, (seg - 1) & 1)) { ok = false; break; }
@@ -391,7 +394,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
             tc::mbar_arrive_expect_tx(&s.full[kb], bytes);
             for (int j = 0; j < 2; ++j)
               if (y[j] >= 0)
-                tc::tma_load_2d(slots + kb * TC_SLOT_BYTES + j * 64 * 128, &rows_map, kb * 64, y[j], &s.full[kb]);
+                tc::tma_load_2d_hint(slots + kb * TC_SLOT_BYTES + j * 64 * 128, &rows_map, kb * 64, y[j],
+                                     &s.full[kb], kv_policy);
             last_n[kb] = n;
           }
           if (ok) ++n;

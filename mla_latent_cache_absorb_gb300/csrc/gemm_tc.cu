@@ -27,7 +27,7 @@ constexpr int ABS_TC_BCHUNK = 64;
 constexpr int CMB_TC_BCHUNK = 32;
 constexpr int CMB_TC_THREADS = 512;   // 4 merge items per thread, loads of 2 items x 4 slots in flight
 constexpr int ABS_TC_SMEM = 4 * 16384 + 2 * 8192 + 1024;
-constexpr int CMB_TC_WSMEM = 8 * 16384 + 2 * 8 * 4096;   // W_UV + vc hi/lo
+constexpr int CMB_TC_WSMEM = 8 * 16384 + 8 * 8192;   // W_UV + vc hi/lo
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -256,15 +256,15 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
   __shared__ int first_s[CMB_TC_BCHUNK], cnt_s[CMB_TC_BCHUNK];
   uint8_t* dyn = align1024(dyn_raw);
   uint8_t* wu = dyn;                           // 8 blocks [128 j rows x 64 c] (K-major A)
-  uint8_t* vh = dyn + 8 * 16384;               // 8 blocks [32 b rows x 64 c] (K-major B), hi
-  uint8_t* vl = vh + 8 * 4096;                 // same, lo
-  float* dres = reinterpret_cast<float*>(vl + 8 * 4096);   // [32][64] partial vc . res
+  // 8 blocks [64 rows x 64 c] (K-major B): rows 0-31 the bf16 high parts of vc for the 32
+  // sequences, rows 32-63 their low parts, so one N=64 MMA per k-step takes both
+  uint8_t* vb = dyn + 8 * 16384;
+  float* dres = reinterpret_cast<float*>(vb + 8 * 8192);   // [32][64] partial vc . res
   float* wt_s = dres + CMB_TC_BCHUNK * 64;                  // [32][max_slots]
   pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x, b0 = blockIdx.y * CMB_TC_BCHUNK;
   const int nb = min(CMB_TC_BCHUNK, a.B - b0);
-  const int NB = (nb + 15) & ~15;
   const int pg = h / a.hpg, hh = h % a.hpg;
   auto lse_at = [&](int slot) { return ((int64_t)pg * a.n_slots + slot) * a.hpg + hh; };
 
@@ -275,7 +275,7 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
     tc::fence_mbar_init();
   }
   if (warp == 0) {
-    tc::tmem_alloc(&tmem_base, 32);
+    tc::tmem_alloc(&tmem_base, 64);
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
@@ -289,22 +289,42 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
       tc::tma_load_2d(wu + kb * 16384, &w_map, 64 * kb, h * (a.N + a.V) + a.N, &bar_w);
   }
   pdl_wait();   // the partials and meta come from the attention kernel
-  // split weights, one warp per sequence
-  for (int bb = warp; bb < CMB_TC_BCHUNK; bb += CMB_TC_THREADS / 32) {
+  // split weights: 16 lanes per sequence, every sequence of the chunk at once, the first
+  // slots' LSEs kept in registers so the partials' LSEs are read from memory once
+  static_assert(CMB_TC_THREADS / 16 == CMB_TC_BCHUNK, "one 16-lane group per sequence");
+  {
+    constexpr int KEEP = 4;
+    const int bb = tid >> 4, l16 = tid & 15;
     int first = 0, ns = 0;
     if (bb < nb) {
       first = a.meta[2 * (b0 + bb)];
       ns = min(a.meta[2 * (b0 + bb) + 1], a.max_slots);
     }
+    float v[KEEP];
     float mx = -CUDART_INF_F;
-    for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, a.part_lse[lse_at(first + s)]);
-    mx = warp_max(mx);
+#pragma unroll
+    for (int k = 0; k < KEEP; ++k) {
+      const int s = l16 + 16 * k;
+      v[k] = (s < ns) ? a.part_lse[lse_at(first + s)] : -CUDART_INF_F;
+      mx = fmaxf(mx, v[k]);
+    }
+    for (int s = l16 + 16 * KEEP; s < ns; s += 16) mx = fmaxf(mx, a.part_lse[lse_at(first + s)]);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     float tot = 0.f;
-    for (int s = lane; s < ns; s += 32) tot += expf(a.part_lse[lse_at(first + s)] - mx);
-    tot = warp_sum(tot);
+#pragma unroll
+    for (int k = 0; k < KEEP; ++k)
+      if (l16 + 16 * k < ns) tot += expf(v[k] - mx);
+    for (int s = l16 + 16 * KEEP; s < ns; s += 16) tot += expf(a.part_lse[lse_at(first + s)] - mx);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
     const float l = (ns > 0) ? mx + logf(tot) : CUDART_NAN_F;
-    for (int s = lane; s < ns; s += 32) wt_s[bb * a.max_slots + s] = expf(a.part_lse[lse_at(first + s)] - l);
-    if (lane == 0) {
+#pragma unroll
+    for (int k = 0; k < KEEP; ++k)
+      if (l16 + 16 * k < ns) wt_s[bb * a.max_slots + l16 + 16 * k] = expf(v[k] - l);
+    for (int s = l16 + 16 * KEEP; s < ns; s += 16)
+      wt_s[bb * a.max_slots + s] = expf(a.part_lse[lse_at(first + s)] - l);
+    if (l16 == 0) {
       lse_s[bb] = l;
       first_s[bb] = first;
       cnt_s[bb] = ns;
@@ -385,8 +405,8 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
         hi[e] = (uint32_t)h0 | ((uint32_t)h1 << 16);
         lo[e] = (uint32_t)l0 | ((uint32_t)l1 << 16);
       }
-      *reinterpret_cast<uint4*>(vh + kb * 4096 + tc::sw128_offset(bb, c8)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(vl + kb * 4096 + tc::sw128_offset(bb, c8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      *reinterpret_cast<uint4*>(vb + kb * 8192 + tc::sw128_offset(bb, c8)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(vb + kb * 8192 + tc::sw128_offset(bb + 32, c8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
   }
   tc::fence_proxy_async_smem();
@@ -409,14 +429,13 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
       set_error(a.hdr, MLA_ERR_TIMEOUT, b0);
     } else {
       tc::tc_fence_after();
-      const uint32_t idesc = tc::idesc_bf16_f32(128, NB, 0, 0);
-      const uint32_t w0 = tc::smem_u32(wu), h0 = tc::smem_u32(vh), l0 = tc::smem_u32(vl);
+      // D[j, 0..31] = W . vc_hi, D[j, 32..63] = W . vc_lo; the epilogue adds the halves
+      const uint32_t idesc = tc::idesc_bf16_f32(128, 64, 0, 0);
+      const uint32_t w0 = tc::smem_u32(wu), v0 = tc::smem_u32(vb);
       for (int kb = 0; kb < 8; ++kb)
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ad = tc::sdesc_sw128(w0 + kb * 16384 + kk * 32, 16, 1024);
-          tc::mma_f16_ss(tmem, ad, tc::sdesc_sw128(h0 + kb * 4096 + kk * 32, 16, 1024), idesc, (kb | kk) != 0);
-          tc::mma_f16_ss(tmem, ad, tc::sdesc_sw128(l0 + kb * 4096 + kk * 32, 16, 1024), idesc, 1);
-        }
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_f16_ss(tmem, tc::sdesc_sw128(w0 + kb * 16384 + kk * 32, 16, 1024),
+                         tc::sdesc_sw128(v0 + kb * 8192 + kk * 32, 16, 1024), idesc, (kb | kk) != 0);
     }
     tc::mma_commit(&bar_mma);
   }
@@ -426,13 +445,14 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
                                                            !*reinterpret_cast<volatile int*>(&failed));
   tc::tc_fence_after();
   if (ok) {
-    uint32_t r[32];
+    uint32_t r[32], rl[32];
     tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16), r);
+    tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 32, rl);
     tc::tmem_wait_ld();
     const int j = 32 * warp + lane;
 #pragma unroll
     for (int b = 0; b < 32; ++b)
-      if (b < nb) a.out[((size_t)(b0 + b) * a.H + h) * a.V + j] = __uint_as_float(r[b]);
+      if (b < nb) a.out[((size_t)(b0 + b) * a.H + h) * a.V + j] = __uint_as_float(r[b]) + __uint_as_float(rl[b]);
   }
   if (a.lse != nullptr)
     for (int bb = tid; bb < nb; bb += CMB_TC_THREADS) a.lse[(size_t)(b0 + bb) * a.H + h] = lse_s[bb];
@@ -441,7 +461,7 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
   __syncthreads();
   if (warp == 0) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, 32);
+    tc::tmem_dealloc(tmem, 64);
   }
 }
 
