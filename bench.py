@@ -262,13 +262,16 @@ def run_ours(args, rank, world, device):
     launches_per_step = (2 if wl.append == "gemv" else 1) + 3
 
     def one_step(ds, s, ev=None):
+        # the user's calls: mla_cache_append, then mla_decode_attn; a step whose attention is
+        # bracketed by events enqueues the same kernels through the three step calls instead
         L.check(ds.append(s), "mla_cache_append")
+        if ev is None:
+            L.check(ds.decode(s), "mla_decode_attn")
+            return
         L.check(ds.absorb(s), "mla_decode_absorb")
-        if ev is not None:
-            ev[0].record(s)
+        ev[0].record(s)
         L.check(ds.partial(s), "mla_decode_partial")
-        if ev is not None:
-            ev[1].record(s)
+        ev[1].record(s)
         L.check(ds.combine(s), "mla_decode_combine")
 
     # graphs of G steps (whole passes over the R copies, at least 16 steps), two of them to

@@ -27,8 +27,9 @@
  *     at the end, uses one fixed device array that is part of the library).
  *   - Calls marked "async" only validate on the host and enqueue kernels on `stream`;
  *     they return before the GPU work ends and never synchronise. The kernels are launched
- *     with programmatic stream serialization: each lets the next kernel on the stream launch
- *     early and waits for its predecessor before touching data another kernel produces. A
+ *     with programmatic stream serialization (mla_decode_attn's first kernel at times
+ *     excepted, see there): each lets the next kernel on the stream launch early and waits
+ *     for its predecessor before touching data another kernel produces. A
  *     caller's own kernel launched right after with that same launch attribute must execute
  *     griddepcontrol.wait before it reads a call's outputs; ordinary launches, copies and events
  *     wait for completion as usual. Errors found on the
@@ -205,6 +206,13 @@ mla_status mla_cache_append(const mla_config* cfg, const mla_cache* cache,
  *   out        device [B, H, V] float32: out[b,h] = W_UV,h * sum_t p_t kv_lat_t.
  *   lse        device [B, H] float32 natural-log sum-exp of the scaled scores, or NULL.
  * Scores are s_t = softmax_scale * ([q' ; q_pe] . row_t) with q' = W_UK,h^T q_nope.
+ * Launch order: when the cache capacity gives each attention CTA at least four 128-row tiles
+ * (B * ceil(capacity / 128) >= 4 * the plan's ctas_per_group, tensor-core path), the first
+ * kernel (the absorb) is launched in plain stream order: it starts only after all earlier
+ * work on the stream, a cache append above all, has completed, and the attention kernel
+ * after it streams cache rows while the absorb still runs, waiting only for the fused
+ * queries. Otherwise every kernel is launched as described at the top. The three step calls
+ * below always keep every kernel's wait in place; the results are bit-identical either way.
  * Device errors: BAD_SEQ_LEN, BAD_PAGE (that sequence's out/lse become NaN). */
 mla_status mla_decode_attn(const mla_config* cfg, const void* q, const void* kv_b,
                            const mla_cache* cache, const int32_t* seq_lens,

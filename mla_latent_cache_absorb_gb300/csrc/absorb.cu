@@ -135,7 +135,7 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
 }
 
 cudaError_t launch_absorb(const mla_config& cfg, const void* q, const void* kv_b,
-                          const int32_t* positions, void* q_abs, void* q_res, int B, cudaStream_t st) {
+                          const int32_t* positions, void* q_abs, void* q_res, int B, bool pdl, cudaStream_t st) {
   dim3 grid(cfg.n_heads, (cfg.kv_lora + ABS_COLS - 1) / ABS_COLS);
   const size_t smem = sizeof(float) * ((size_t)cfg.qk_nope * ABS_COLS + (size_t)ABS_BCHUNK * cfg.qk_nope +
                                        4 * (size_t)ABS_BCHUNK * ABS_COLS);
@@ -143,13 +143,13 @@ cudaError_t launch_absorb(const mla_config& cfg, const void* q, const void* kv_b
     auto k = absorb_kernel<MLA_BF16>;
     cudaError_t e = ensure_smem((const void*)k, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(k, grid, dim3(ABS_THREADS), smem, st, cfg, static_cast<const uint16_t*>(q), kv_b, positions,
+    return launch_kernel(pdl, k, grid, dim3(ABS_THREADS), smem, st, cfg, static_cast<const uint16_t*>(q), kv_b, positions,
                       static_cast<uint16_t*>(q_abs), static_cast<uint16_t*>(q_res), B);
   } else {
     auto k = absorb_kernel<MLA_F32>;
     cudaError_t e = ensure_smem((const void*)k, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(k, grid, dim3(ABS_THREADS), smem, st, cfg, static_cast<const float*>(q), kv_b, positions,
+    return launch_kernel(pdl, k, grid, dim3(ABS_THREADS), smem, st, cfg, static_cast<const float*>(q), kv_b, positions,
                       static_cast<float*>(q_abs), static_cast<float*>(nullptr), B);
   }
 }

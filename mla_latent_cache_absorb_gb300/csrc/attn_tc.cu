@@ -89,6 +89,10 @@ struct TcArgs {
   WsHeader* hdr;
   int B, H, G, ncg, n_slots;
   float scale_log2;
+  // 1: the kernel launched just before this one started only after all earlier work on the
+  // stream had completed, and writes no cache row; cache rows may then be read before the
+  // dependency wait (only the queries wait for it)
+  int kv_early;
 };
 
 struct Smem {
@@ -278,10 +282,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
       tc::tma_prefetch_desc(&qres_map);
     }
   }
-  // everything below reads what the absorb / append kernels wrote (query rows, the new cache
-  // row) or writes what the previous step's combine may still read (meta, partials)
-  pdl_wait();
-  // the thread whose chunk holds tile r0 finds the first sequence of this CTA's share
+  // the thread whose chunk holds tile r0 finds the first sequence of this CTA's share (the
+  // lengths are the caller's input: no kernel of the step writes them)
   if (r0 < r1 && before <= r0 && r0 < before + mine) {
     long long p = before;
     for (int b = cb0; b < cb1; ++b) {
@@ -294,6 +296,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
       p += n;
     }
   }
+  // Everything below reads what the absorb / append kernels wrote (query rows, the new cache
+  // row) or writes what the previous step's combine may still read (meta, partials). In the
+  // early mode the only kernel that can still be running is the absorb, which began after all
+  // earlier work (append, previous combine) had completed: then only the query loads wait.
+  if (!a.kv_early) pdl_wait();
   // CTA 0 of group 0 publishes, per sequence, which partial slots the combine must merge
   if (blockIdx.x == 0) {
     long long p = before;
@@ -315,6 +322,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
     }
   }
   if (r0 >= r1) {
+    // Wait even in the early mode: a grid completes only after its predecessor has, also when
+    // no CTA has a share.
+    pdl_wait();
     // No share. If the empty range sits strictly inside a sequence, this CTA's slot lies in
     // that sequence's slot interval: mark it empty (lse = -inf, weight 0 in the combine).
     if (before <= r0 && r0 < before + mine) {
@@ -358,16 +368,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
       // cache rows are read once per head group, by CTAs that run side by side: mark them first
       // to leave L2, so that the split partials this kernel writes stay there for the combine
       const uint64_t kv_policy = tc::l2_policy_evict_first();
+      auto load_q = [&]() -> bool {
+        if (seg > 0 && !wait_bar(s, &s.q_empty, (seg - 1) & 1)) return false;
+        tc::mbar_arrive_expect_tx(&s.q_full, Cfg<HG>::Q_BLOCKS * Cfg<HG>::QBLK_BYTES);
+        const int qrow = sb * a.H + g * HG;
+        for (int kb = 0; kb < TC_KB; ++kb)
+          tc::tma_load_2d(qs + kb * Cfg<HG>::QBLK_BYTES, &q_map, kb * 64, qrow, &s.q_full);
+        tc::tma_load_2d(qs + TC_KB * Cfg<HG>::QBLK_BYTES, &qres_map, TC_LAT_KB * 64, qrow, &s.q_full);
+        q_loaded = seg;
+        return true;
+      };
       while (ok && it.next(a, &sb, &tlo, &thi)) {
-        if (pw == 0) {
-          if (seg > 0 && !wait_bar(s, &s.q_empty, (seg - 1) & 1)) { ok = false; break; }
-          tc::mbar_arrive_expect_tx(&s.q_full, Cfg<HG>::Q_BLOCKS * Cfg<HG>::QBLK_BYTES);
-          const int qrow = sb * a.H + g * HG;
-          for (int kb = 0; kb < TC_KB; ++kb)
-            tc::tma_load_2d(qs + kb * Cfg<HG>::QBLK_BYTES, &q_map, kb * 64, qrow, &s.q_full);
-          tc::tma_load_2d(qs + TC_KB * Cfg<HG>::QBLK_BYTES, &qres_map, TC_LAT_KB * 64, qrow, &s.q_full);
-          q_loaded = seg;
-        }
+        // early mode: the first tile's rows go out before the wait for the absorb's queries
+        const bool defer_q = a.kv_early && seg == 0;
+        if (pw == 0 && !defer_q && !load_q()) { ok = false; break; }
         const long long L = a.seq_lens[sb];
         for (int t = tlo; t < thi && ok; ++t) {
           const long long t0 = (long long)t * TC_TILE;
@@ -398,6 +412,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
                                      &s.full[kb], kv_policy);
             last_n[kb] = n;
           }
+          if (ok && pw == 0 && defer_q && t == tlo) {
+            pdl_wait();
+            if (!load_q()) ok = false;
+          }
           if (ok) ++n;
         }
         if (ok) ++seg;
@@ -412,6 +430,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
     }
   } else if (warp == TC_MMA_WARP) {
     // ================================ MMA issuer ================================
+    if (a.kv_early) pdl_wait();   // only the producers run ahead of the absorb
     if (lane == 0) {
       const uint32_t idesc_qk = tc::idesc_bf16_f32(TC_TILE, HG, 0, 0);
       const uint32_t idesc_pv = tc::idesc_bf16_f32(128, HG, 1, 1);
@@ -483,6 +502,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
     const int q = warp & 3;                  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;           // tile row (and O^T latent row within a chunk)
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    if (a.kv_early) pdl_wait();   // only the producers run ahead of the absorb
     const int sidx = (tid - 32 * TC_SM_WARP0) & 127;   // 0..127 within the warpgroup
     int sb = 0, tlo, thi;
     int seg = 0;
@@ -742,7 +762,7 @@ int tc_heads_per_cta(int H) {
 
 cudaError_t launch_attn_tc(const mla_config& cfg, const mla_cache& cache, const DecodePlan& plan,
                            const int32_t* seq_lens, const void* q_abs, const void* q_res, float* part_o,
-                           float* part_lse, int32_t* meta, int B, WsHeader* hdr, cudaStream_t st) {
+                           float* part_lse, int32_t* meta, int B, WsHeader* hdr, bool kv_early, cudaStream_t st) {
   if (cache.n_physical_rows >= (int64_t(1) << 31) || (int64_t)B * cfg.n_heads >= (int64_t(1) << 31))
     return cudaErrorInvalidValue;
   CUtensorMap rows_map, q_map;
@@ -765,6 +785,7 @@ cudaError_t launch_attn_tc(const mla_config& cfg, const mla_cache& cache, const 
   a.ncg = plan.ctas_per_group;
   a.n_slots = plan.n_slots;
   a.scale_log2 = cfg.softmax_scale * 1.4426950408889634f;
+  a.kv_early = kv_early ? 1 : 0;
   const int grid = plan.n_groups * plan.ctas_per_group;
   cudaError_t e;
   switch (plan.heads_per_cta) {

@@ -90,31 +90,49 @@ __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
   const int64_t wrow0 = (int64_t)h * (a.N + a.V) + a.N;
   stage_kv_b_rows(w_s, 4 * C4, a.kv_b, a.kv_b_dtype, wrow0 + jbeg, min(CMB_VJ, jend - jbeg), 0, C, C, CMB_THREADS);
   pdl_wait();   // the partials and meta come from the attention kernel
-  // the query residual (first-order LSE correction below) goes to shared memory together with
-  // the split metadata: one memory round trip less on the way to the output
-  const bool res_pre = a.q_res != nullptr && C <= CMB_RES_MAX;
-  if (res_pre)
-    for (int i = threadIdx.x; i < nb * C; i += CMB_THREADS)
-      res_s[i] = a.q_res[((int64_t)(b0 + i / C) * a.H + h) * (C + a.R) + i % C];
-
-  // split weights exp(lse_s - lse): one warp per sequence
+  // Loads that do not depend on one another go out together: each warp's sequence metadata
+  // and the query residual (for the first-order LSE correction below); the partial LSEs follow
+  // one memory round trip later.
+  static_assert(CMB_BC <= CMB_THREADS / 32, "one warp per sequence of the block");
+  constexpr int RES_PER = CMB_BC * CMB_RES_MAX / CMB_THREADS;   // residual elements per thread
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int bb = warp; bb < nb; bb += CMB_THREADS / 32) {
-    const int b = b0 + bb;
-    const int first = a.meta[2 * b];
-    const int ns = min(a.meta[2 * b + 1], a.max_slots);
-    float mx = -CUDART_INF_F;
-    for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, a.part_lse[lse_at(first + s)]);
+  int first = 0, ns = 0;
+  if (warp < nb) {
+    first = a.meta[2 * (b0 + warp)];
+    ns = min(a.meta[2 * (b0 + warp) + 1], a.max_slots);
+  }
+  const bool res_pre = a.q_res != nullptr && C <= CMB_RES_MAX;
+  uint16_t rv[RES_PER];
+  if (res_pre) {
+#pragma unroll
+    for (int u = 0; u < RES_PER; ++u) {
+      const int i = threadIdx.x + u * CMB_THREADS;
+      rv[u] = (i < nb * C) ? a.q_res[((int64_t)(b0 + i / C) * a.H + h) * (C + a.R) + i % C] : 0;
+    }
+  }
+  // split weights exp(lse_s - lse): one warp per sequence, each lane's first slot kept in a register
+  if (warp < nb) {
+    const float v0 = (lane < ns) ? a.part_lse[lse_at(first + lane)] : -CUDART_INF_F;
+    float mx = v0;
+    for (int s = lane + 32; s < ns; s += 32) mx = fmaxf(mx, a.part_lse[lse_at(first + s)]);
     mx = warp_max(mx);
-    float tot = 0.f;
-    for (int s = lane; s < ns; s += 32) tot += expf(a.part_lse[lse_at(first + s)] - mx);
+    float tot = (lane < ns) ? expf(v0 - mx) : 0.f;
+    for (int s = lane + 32; s < ns; s += 32) tot += expf(a.part_lse[lse_at(first + s)] - mx);
     tot = warp_sum(tot);
     const float l = (ns > 0) ? mx + logf(tot) : CUDART_NAN_F;
-    for (int s = lane; s < ns; s += 32) wt_s[bb * a.max_slots + s] = expf(a.part_lse[lse_at(first + s)] - l);
+    if (lane < ns) wt_s[warp * a.max_slots + lane] = expf(v0 - l);
+    for (int s = lane + 32; s < ns; s += 32) wt_s[warp * a.max_slots + s] = expf(a.part_lse[lse_at(first + s)] - l);
     if (lane == 0) {
-      lse_s[bb] = l;
-      first_s[bb] = first;
-      cnt_s[bb] = ns;
+      lse_s[warp] = l;
+      first_s[warp] = first;
+      cnt_s[warp] = ns;
+    }
+  }
+  if (res_pre) {
+#pragma unroll
+    for (int u = 0; u < RES_PER; ++u) {
+      const int i = threadIdx.x + u * CMB_THREADS;
+      if (i < nb * C) res_s[i] = rv[u];
     }
   }
   __syncthreads();

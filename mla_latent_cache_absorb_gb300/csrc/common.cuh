@@ -24,14 +24,15 @@ static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 // stream is still running: it lets its own successor start at once (pdl_trigger) and, before
 // touching anything an earlier kernel of the library writes or still reads, waits until its
 // predecessor has completed (pdl_wait). Because every kernel waits before it completes, the
-// predecessor's completion implies that of all earlier kernels. Launched without the attribute,
-// both are no-ops.
+// predecessor's completion implies that of all earlier kernels. Launched without the attribute
+// (launch_kernel with pdl = false), a kernel starts only after all earlier work on the stream has
+// completed and its pdl_wait is a no-op.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                              Args&&... args) {
+inline cudaError_t launch_kernel(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t st, Args&&... args) {
   cudaLaunchConfig_t lc = {};
   lc.gridDim = grid;
   lc.blockDim = block;
@@ -41,8 +42,14 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = at;
-  lc.numAttrs = 1;
+  lc.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&lc, kernel, static_cast<KArgs>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  return launch_kernel(true, kernel, grid, block, smem, st, static_cast<Args&&>(args)...);
 }
 
 __device__ __forceinline__ void set_error(WsHeader* hdr, int code, int seq) {
@@ -257,20 +264,23 @@ cudaError_t launch_append_gemv(const mla_config& cfg, const void* x, const void*
 cudaError_t launch_append_finish(const mla_config& cfg, const mla_cache& cache, const float* kva,
                                  const float* norm_w, const int32_t* positions,
                                  const int32_t* seq_lens, int B, WsHeader* hdr, bool kva_dep, cudaStream_t st);
+// pdl = false: the absorb starts only after all earlier work on the stream has completed
 cudaError_t launch_absorb(const mla_config& cfg, const void* q, const void* kv_b,
-                          const int32_t* positions, void* q_abs, void* q_res, int B, cudaStream_t st);
+                          const int32_t* positions, void* q_abs, void* q_res, int B, bool pdl, cudaStream_t st);
 cudaError_t launch_attn_simt(const mla_config& cfg, const mla_cache& cache, const DecodePlan& plan,
                              const int32_t* seq_lens, const void* q_abs, const void* q_res, float* part_o,
                              float* part_lse, int32_t* meta, int B, WsHeader* hdr, cudaStream_t st);
+// kv_early: the kernel launched just before is an absorb launched with pdl = false, so cache rows
+// may be read before the dependency wait (only the queries wait for the absorb)
 cudaError_t launch_attn_tc(const mla_config& cfg, const mla_cache& cache, const DecodePlan& plan,
                            const int32_t* seq_lens, const void* q_abs, const void* q_res, float* part_o,
-                           float* part_lse, int32_t* meta, int B, WsHeader* hdr, cudaStream_t st);
+                           float* part_lse, int32_t* meta, int B, WsHeader* hdr, bool kv_early, cudaStream_t st);
 bool attn_tc_supported(const mla_config& cfg);
 int tc_heads_per_cta(int H);
 bool absorb_tc_supported(const mla_config& cfg, int B);
 bool combine_tc_supported(const mla_config& cfg, int B);
 cudaError_t launch_absorb_tc(const mla_config& cfg, const void* q, const void* kv_b, const int32_t* positions,
-                             void* q_abs, void* q_res, int B, WsHeader* hdr, cudaStream_t st);
+                             void* q_abs, void* q_res, int B, WsHeader* hdr, bool pdl, cudaStream_t st);
 // q_res != nullptr: the partials came from bf16 latent queries; the combine adds the first-order
 // LSE correction softmax_scale * (vc . q_res[latent]) for the residual the scores did not see.
 cudaError_t launch_combine_tc(const mla_config& cfg, const DecodePlan& plan, const void* kv_b,

@@ -480,7 +480,7 @@ bool combine_tc_supported(const mla_config& cfg, int B) {
 }
 
 cudaError_t launch_absorb_tc(const mla_config& cfg, const void* q, const void* kv_b, const int32_t* positions,
-                             void* q_abs, void* q_res, int B, WsHeader* hdr, cudaStream_t st) {
+                             void* q_abs, void* q_res, int B, WsHeader* hdr, bool pdl, cudaStream_t st) {
   CUtensorMap w_map;
   if (!make_map_2d_bf16(&w_map, kv_b, 512, (uint64_t)cfg.n_heads * (cfg.qk_nope + cfg.v_head), 64, 128))
     return cudaErrorInvalidValue;
@@ -495,7 +495,7 @@ cudaError_t launch_absorb_tc(const mla_config& cfg, const void* q, const void* k
   cudaError_t e = ensure_smem((const void*)absorb_tc_kernel, ABS_TC_SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(cfg.n_heads, 2, (B + ABS_TC_BCHUNK - 1) / ABS_TC_BCHUNK);
-  return launch_pdl(absorb_tc_kernel, grid, dim3(G_THREADS), ABS_TC_SMEM, st, w_map, a);
+  return launch_kernel(pdl, absorb_tc_kernel, grid, dim3(G_THREADS), ABS_TC_SMEM, st, w_map, a);
 }
 
 cudaError_t launch_combine_tc(const mla_config& cfg, const DecodePlan& plan, const void* kv_b,

@@ -335,9 +335,14 @@ static mla_status decode_prologue(const mla_config* cfg, int32_t B, void* worksp
   return check_ws(workspace, ws_bytes, plan->total);
 }
 
-mla_status mla_decode_absorb(const mla_config* cfg, const void* q, const void* kv_b,
-                             const int32_t* positions, int32_t B, void* workspace, size_t ws_bytes,
-                             mla_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// ordered: launch the absorb without programmatic serialization, so that it starts only after
+// all earlier work on the stream has completed
+mla_status decode_absorb(const mla_config* cfg, const void* q, const void* kv_b, const int32_t* positions,
+                         int32_t B, void* workspace, size_t ws_bytes, bool ordered, mla_stream_t stream) {
   DecodePlan plan;
   mla_status st = decode_prologue(cfg, B, workspace, ws_bytes, &plan);
   if (st != MLA_OK) return st;
@@ -348,12 +353,14 @@ mla_status mla_decode_absorb(const mla_config* cfg, const void* q, const void* k
   void* q_res = cfg->act_dtype == MLA_BF16 ? static_cast<char*>(workspace) + plan.off_qres : nullptr;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (absorb_tc_supported(*cfg, B))
-    return cuda_status(launch_absorb_tc(*cfg, q, kv_b, positions, q_abs, q_res, B, static_cast<WsHeader*>(workspace), s));
-  return cuda_status(launch_absorb(*cfg, q, kv_b, positions, q_abs, q_res, B, s));
+    return cuda_status(launch_absorb_tc(*cfg, q, kv_b, positions, q_abs, q_res, B, static_cast<WsHeader*>(workspace),
+                                        !ordered, s));
+  return cuda_status(launch_absorb(*cfg, q, kv_b, positions, q_abs, q_res, B, !ordered, s));
 }
 
-mla_status mla_decode_partial(const mla_config* cfg, const mla_cache* cache, const int32_t* seq_lens,
-                              int32_t B, void* workspace, size_t ws_bytes, mla_stream_t stream) {
+// kv_early: the kernel just before is an ordered absorb (decode_absorb with ordered = true)
+mla_status decode_partial(const mla_config* cfg, const mla_cache* cache, const int32_t* seq_lens, int32_t B,
+                          void* workspace, size_t ws_bytes, bool kv_early, mla_stream_t stream) {
   DecodePlan plan;
   mla_status st = decode_prologue(cfg, B, workspace, ws_bytes, &plan);
   if (st != MLA_OK) return st;
@@ -368,8 +375,24 @@ mla_status mla_decode_partial(const mla_config* cfg, const mla_cache* cache, con
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const void* q_res = cfg->act_dtype == MLA_BF16 ? ws + plan.off_qres : nullptr;
   if (plan.path == PATH_TC)
-    return cuda_status(launch_attn_tc(*cfg, *cache, plan, seq_lens, ws + plan.off_qabs, q_res, po, pl, meta, B, hdr, s));
+    return cuda_status(
+        launch_attn_tc(*cfg, *cache, plan, seq_lens, ws + plan.off_qabs, q_res, po, pl, meta, B, hdr, kv_early, s));
   return cuda_status(launch_attn_simt(*cfg, *cache, plan, seq_lens, ws + plan.off_qabs, q_res, po, pl, meta, B, hdr, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status mla_decode_absorb(const mla_config* cfg, const void* q, const void* kv_b,
+                             const int32_t* positions, int32_t B, void* workspace, size_t ws_bytes,
+                             mla_stream_t stream) {
+  return decode_absorb(cfg, q, kv_b, positions, B, workspace, ws_bytes, false, stream);
+}
+
+mla_status mla_decode_partial(const mla_config* cfg, const mla_cache* cache, const int32_t* seq_lens,
+                              int32_t B, void* workspace, size_t ws_bytes, mla_stream_t stream) {
+  return decode_partial(cfg, cache, seq_lens, B, workspace, ws_bytes, false, stream);
 }
 
 mla_status mla_decode_combine(const mla_config* cfg, const void* kv_b, const int32_t* seq_lens,
@@ -406,9 +429,15 @@ mla_status mla_decode_attn(const mla_config* cfg, const void* q, const void* kv_
   if (!aligned(q, 16) || !aligned(kv_b, 16)) return MLA_ERR_INVALID_ARG;
   st = check_cache(cfg, cache, B);
   if (st != MLA_OK) return st;
-  st = mla_decode_absorb(cfg, q, kv_b, positions, B, workspace, ws_bytes, stream);
+  // Long attentions (at the cache's capacity, at least four 128-row tiles per CTA): the absorb
+  // starts once everything before it on the stream, the cache append above all, has completed,
+  // and the attention then streams cache rows while the absorb still runs. Short ones keep the
+  // absorb's own overlap with the kernels before it, which is worth more to them.
+  const int64_t max_tiles = (int64_t)B * ((plan.capacity + 127) / 128);
+  const bool early = plan.path == PATH_TC && max_tiles >= 4 * (int64_t)plan.ctas_per_group;
+  st = decode_absorb(cfg, q, kv_b, positions, B, workspace, ws_bytes, early, stream);
   if (st != MLA_OK) return st;
-  st = mla_decode_partial(cfg, cache, seq_lens, B, workspace, ws_bytes, stream);
+  st = decode_partial(cfg, cache, seq_lens, B, workspace, ws_bytes, early, stream);
   if (st != MLA_OK) return st;
   return mla_decode_combine(cfg, kv_b, seq_lens, out, lse, B, workspace, ws_bytes, stream);
 }

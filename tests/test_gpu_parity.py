@@ -199,3 +199,43 @@ def test_batched_slice_equals_single_sequence():
     for b in range(3):
         assert max_rel(o3[b], o1[0]) <= 1e-5 and np.max(np.abs(l3[b] - l1[0])) <= 1e-5
     assert np.array_equal(o3[0], o3[1]) and np.array_equal(o3[1], o3[2])
+
+
+STEP_CASES = [
+    # short attentions: every kernel launched with programmatic serialization
+    ("v2lite_b1", W["v2lite_b1_t4096"].with_(context=("fixed", 1500))),              # SIMT absorb + combine
+    ("v3_b9_h128", W["v3_b32_t4096"].with_(B=9, context=("uniform", 100, 1200))),    # tensor-core absorb + combine
+    ("ragged_paged_b6", W["ragged_paged_b64"].with_(B=6, context=("uniform", 1, 900))),
+    ("tiny_f32", W["tiny_f32"]),                                                      # CUDA-core attention
+    # long attentions (>= 4 tiles per CTA at capacity): absorb in plain order, early cache reads
+    ("v3_b16_long", W["v3_b32_t4096"].with_(B=16, context=("uniform", 1500, 2500))),
+    ("q8_b2_long", W["long_q8_b4_t131072"].with_(B=2, context=("fixed", 20000))),    # SIMT absorb + combine
+    ("ragged_paged_b24_long", W["ragged_paged_b64"].with_(B=24, context=("uniform", 200, 3000))),
+]
+
+
+@gpu
+@pytest.mark.parametrize("name,wl", STEP_CASES, ids=[c[0] for c in STEP_CASES])
+def test_fused_call_equals_the_three_step_calls(name, wl):
+    # for long attentions mla_decode_attn launches its absorb in plain stream order and lets
+    # the attention read cache rows before waiting for it; the three step calls keep every wait
+    # in place. Same kernels, same split plan: the results agree bit for bit.
+    torch = need_gpu()
+    from mla_latent_cache_absorb_gb300 import binding as L
+    from mla_latent_cache_absorb_gb300.runner import DeviceStep
+    ds = DeviceStep(synth.make_problem(wl))
+    L.check(ds.append(), "mla_cache_append")
+    L.check(ds.absorb(), "mla_decode_absorb")
+    L.check(ds.partial(), "mla_decode_partial")
+    L.check(ds.combine(), "mla_decode_combine")
+    torch.cuda.synchronize()
+    o_steps, l_steps = ds.out.clone(), ds.lse.clone()
+    assert torch.isfinite(o_steps).all()
+    ds.out.fill_(float("nan"))
+    ds.lse.fill_(float("nan"))
+    for _ in range(2):   # twice: the second call follows the first call's combine, not an append
+        L.check(ds.decode(), "mla_decode_attn")
+        torch.cuda.synchronize()
+        assert torch.equal(ds.out, o_steps) and torch.equal(ds.lse, l_steps)
+    e, seq = L.mla_get_device_error(ds.ws_decode, ds.stream)
+    assert e == 0, (e, seq)
