@@ -39,33 +39,43 @@ struct CombineArgs {
   int vper;                 // outputs per CTA (a multiple of CMB_VJ): the merge is done once per CTA
 };
 
-// out[b0 + bb, h, j0 + j] = W_UV row j . vc[bb] for bb < nb <= NBT: one warp per output, lanes
-// across the latent, NBT accumulators per lane.
+// out[b0 + bb, h, j0 + j] = W_UV row j . vc[bb] for bb < nb <= NBT: 16 threads per output
+// (CMB_VJ outputs per pass), thread `part` of an output taking the latent float4s part,
+// part + 16, ... (rows of w_s and vc_s are zero past C up to `stride`), then a fixed-order
+// reduction over the 16 threads; NBT accumulators per thread.
+static_assert(CMB_THREADS / 16 == CMB_VJ, "16 threads per output of a chunk");
 template <int NBT>
 __device__ __forceinline__ void combine_outputs(const CombineArgs& a, const float* w_s, const float* vc_s, int stride,
-                                                int nb, int nj, int b0, int h, int j0, int warp, int lane) {
-  for (int j = warp; j < nj; j += CMB_THREADS / 32) {
-    float acc[NBT];
+                                                int nb, int nj, int b0, int h, int j0) {
+  const int j = threadIdx.x >> 4, part = threadIdx.x & 15;
+  float acc[NBT];
 #pragma unroll
-    for (int bb = 0; bb < NBT; ++bb) acc[bb] = 0.f;
-    const float* wr = w_s + j * stride;
-    for (int c = lane; c < a.C; c += 32) {
-      const float wv = wr[c];
+  for (int bb = 0; bb < NBT; ++bb) acc[bb] = 0.f;
+  if (j < nj) {
+    const float4* wr = reinterpret_cast<const float4*>(w_s + j * stride);
+    const float4* vc4 = reinterpret_cast<const float4*>(vc_s);
+    const int s4 = stride / 4;
+#pragma unroll 1
+    for (int c4 = part; c4 < s4; c4 += 16) {
+      const float4 w = wr[c4];
 #pragma unroll
-      for (int bb = 0; bb < NBT; ++bb)
-        if (bb < nb) acc[bb] = fmaf(wv, vc_s[bb * stride + c], acc[bb]);
-    }
-#pragma unroll
-    for (int bb = 0; bb < NBT; ++bb) {
-      if (bb < nb) {
-        const float v = warp_sum(acc[bb]);
-        if (lane == 0) a.out[((int64_t)(b0 + bb) * a.H + h) * a.V + j0 + j] = v;
+      for (int bb = 0; bb < NBT; ++bb) {
+        if (bb < nb) {
+          const float4 v = vc4[bb * s4 + c4];
+          acc[bb] = fmaf(w.x, v.x, fmaf(w.y, v.y, fmaf(w.z, v.z, fmaf(w.w, v.w, acc[bb]))));
+        }
       }
     }
   }
+#pragma unroll
+  for (int bb = 0; bb < NBT; ++bb) {
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) acc[bb] += __shfl_xor_sync(0xffffffffu, acc[bb], o);
+    if (part == 0 && j < nj && bb < nb) a.out[((int64_t)(b0 + bb) * a.H + h) * a.V + j0 + j] = acc[bb];
+  }
 }
 
-__global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
+__global__ void __launch_bounds__(CMB_THREADS, 2) combine_kernel(CombineArgs a) {
   extern __shared__ float sm[];
   pdl_trigger();
   const int h = blockIdx.x;
@@ -198,20 +208,24 @@ __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
     }
   }
   __syncthreads();
-  if (a.q_res != nullptr) {
-    // the scores used bf16 latent queries q_hi = q' - res: to first order the exact log-sum-exp
-    // is lse + scale * (sum_t p_t kv_lat_t) . res = lse + scale * vc . res
+  // lse, written by the first V-slice's CTA, one warp per sequence (no barrier: nothing else
+  // reads lse_s from here on). When the scores used bf16 latent queries q_hi = q' - res, to
+  // first order the exact log-sum-exp is lse + scale * (sum_t p_t kv_lat_t) . res
+  // = lse + scale * vc . res.
+  if (blockIdx.y == 0 && a.lse != nullptr) {
     for (int bb = warp; bb < nb; bb += CMB_THREADS / 32) {
-      const uint16_t* res = res_pre ? res_s + bb * C : a.q_res + ((int64_t)(b0 + bb) * a.H + h) * (C + a.R);
-      float d = 0.f;
-      for (int c = lane; c < C; c += 32) d = fmaf(vc_s[bb * 4 * C4 + c], bf16_bits_to_f32(res[c]), d);
-      d = warp_sum(d);
-      if (lane == 0) lse_s[bb] += a.scale * d;
+      float l = lse_s[bb];
+      if (a.q_res != nullptr) {
+        const uint16_t* res = res_pre ? res_s + bb * C : a.q_res + ((int64_t)(b0 + bb) * a.H + h) * (C + a.R);
+        float d = 0.f;
+        for (int c = lane; c < C; c += 32) d = fmaf(vc_s[bb * 4 * C4 + c], bf16_bits_to_f32(res[c]), d);
+        d = warp_sum(d);
+        l += a.scale * d;
+      }
+      if (lane == 0) a.lse[(int64_t)(b0 + bb) * a.H + h] = l;
     }
-    __syncthreads();
   }
-  // out[b, h, j0 + j]: one warp per output j, lanes across the latent, all sequences at once;
-  // the CTA's outputs in chunks of 32 W_UV rows
+  // out[b, h, j0 + j] for all sequences of the block, the CTA's outputs in chunks of 32 W_UV rows
   for (int j0 = jbeg; j0 < jend; j0 += CMB_VJ) {
     const int nj = min(CMB_VJ, jend - j0);
     if (j0 != jbeg) {
@@ -220,17 +234,19 @@ __global__ void __launch_bounds__(CMB_THREADS) combine_kernel(CombineArgs a) {
       __syncthreads();
     }
     if (nb == 1) {
-      combine_outputs<1>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0, warp, lane);
+      combine_outputs<1>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0);
     } else if (nb == 2) {
-      combine_outputs<2>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0, warp, lane);
+      combine_outputs<2>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0);
     } else if (nb <= 4) {
-      combine_outputs<4>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0, warp, lane);
+      combine_outputs<4>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0);
     } else {
-      combine_outputs<CMB_BC>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0, warp, lane);
+      // more than four sequences: two passes over the W_UV rows, four sequences each (eight
+      // accumulators a thread would not fit the register budget of two CTAs per SM)
+      static_assert(CMB_BC <= 8, "at most two passes of four sequences");
+      combine_outputs<4>(a, w_s, vc_s, 4 * C4, 4, nj, b0, h, j0);
+      combine_outputs<4>(a, w_s, vc_s + 4 * (4 * C4), 4 * C4, nb - 4, nj, b0 + 4, h, j0);
     }
   }
-  if (blockIdx.y == 0 && a.lse != nullptr)
-    for (int bb = threadIdx.x; bb < nb; bb += CMB_THREADS) a.lse[(int64_t)(b0 + bb) * a.H + h] = lse_s[bb];
 }
 
 cudaError_t launch_combine(const mla_config& cfg, const DecodePlan& plan, const void* kv_b,
