@@ -689,19 +689,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
 
 }  // namespace
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 namespace {
 
 // 2D bf16 map over `rows` rows of 576 elements, boxes of 64 columns x 64 rows, 128-byte swizzle.
@@ -711,46 +698,9 @@ bool make_rows_map(CUtensorMap* m, const void* base, uint64_t rows) {
 
 }  // namespace
 
-bool make_map_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
-                      uint32_t box_rows) {
-  // The encoding depends only on these arguments, so recent ones are kept per host thread: a
-  // decode step encodes up to five maps, mostly the same ones call after call.
-  struct Entry {
-    const void* base;
-    uint64_t inner, rows;
-    uint32_t box_inner, box_rows;
-    CUtensorMap map;
-  };
-  constexpr int kEntries = 16;
-  thread_local Entry cache[kEntries];
-  thread_local int n_used = 0, next = 0;
-  for (int i = 0; i < n_used; ++i) {
-    const Entry& en = cache[i];
-    if (en.base == base && en.inner == inner && en.rows == rows && en.box_inner == box_inner &&
-        en.box_rows == box_rows) {
-      *m = en.map;
-      return true;
-    }
-  }
-  auto enc = encode_fn();
-  if (enc == nullptr) return false;
-  cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {box_inner, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  if (enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return false;
-  cache[next] = Entry{base, inner, rows, box_inner, box_rows, *m};
-  next = (next + 1) % kEntries;
-  if (n_used < kEntries) ++n_used;
-  return true;
-}
-
 bool attn_tc_supported(const mla_config& cfg) {
   return cfg.act_dtype == MLA_BF16 && cfg.kv_lora == 512 && cfg.qk_rope == 64 &&
-         (cfg.page_size == 0 || cfg.page_size % 64 == 0) && encode_fn() != nullptr;
+         (cfg.page_size == 0 || cfg.page_size % 64 == 0) && tma_encoder_available();
 }
 
 // Heads per CTA for H heads: the narrowest group width (16, 32 or 64) that holds all heads,

@@ -264,9 +264,8 @@ cudaError_t launch_combine(const mla_config& cfg, const DecodePlan& plan, const 
   // V-slices per head: enough CTAs to cover the SMs, but every slice merges the partials again
   const int chunks = (cfg.v_head + CMB_VJ - 1) / CMB_VJ;
   const int64_t base_ctas = (int64_t)cfg.n_heads * ((B + CMB_BC - 1) / CMB_BC);
-  int sms = 0, dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    sms = 152;
+  int sms = device_sms();
+  if (sms <= 0) sms = 152;
   int vsplit = (int)((sms + base_ctas - 1) / base_ctas);
   vsplit = vsplit < 1 ? 1 : (vsplit > chunks ? chunks : vsplit);
   a.vper = ((chunks + vsplit - 1) / vsplit) * CMB_VJ;

@@ -251,12 +251,16 @@ enum { PATH_SIMT = 0, PATH_TC = 1 };
 // 2D bf16 TMA map over a row-major [rows, inner] tensor (inner elements contiguous) with
 // boxes of box_inner x box_rows and the 128-byte swizzle. False when the driver entry point
 // is unavailable or the encoding is rejected.
+// True when the driver's tensor-map encoder could be found (looked up once per process).
+bool tma_encoder_available();
 bool make_map_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
                       uint32_t box_rows);
 
 // Raise a kernel's dynamic shared memory limit once per (kernel, device), so that repeated
 // launches (and launches under stream capture) make no attribute calls.
 cudaError_t ensure_smem(const void* func, int bytes);
+// Multiprocessor count of the current device (cached per device), or -1 on a CUDA error.
+int device_sms();
 
 // host launchers (defined in the kernel files)
 cudaError_t launch_append_gemv(const mla_config& cfg, const void* x, const void* w, int hidden,

@@ -2,6 +2,7 @@
 // Every entry point validates on the host before enqueueing anything; kernels report what
 // only the GPU can see through the workspace's error word.
 #include <cmath>
+#include <atomic>
 #include <cstring>
 #include <limits>
 
@@ -57,13 +58,16 @@ static mla_status check_cache(const mla_config* cfg, const mla_cache* cache, int
   return MLA_OK;
 }
 
-static int device_sms() {
-  static int cached[64] = {0};
+int device_sms() {
+  static std::atomic<int> cached[64] = {};
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  if (dev >= 0 && dev < 64) {
+    n = cached[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+  }
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-  if (dev >= 0 && dev < 64) cached[dev] = n;
+  if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -127,9 +131,10 @@ static mla_status make_plan(const mla_config& cfg, int B, DecodePlan* p) {
 }
 
 cudaError_t ensure_smem(const void* func, int bytes) {
+  // per host thread: no locking, and setting the attribute again from another thread is harmless
   struct Entry { const void* f; int dev; int bytes; };
-  static Entry table[128];
-  static int n = 0;
+  thread_local Entry table[128];
+  thread_local int n = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
