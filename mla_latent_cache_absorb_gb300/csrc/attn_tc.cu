@@ -291,6 +291,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
       if (r0 < p + n) {
         s.seg_b0 = b;
         s.seg_p0 = p;
+        if constexpr (HG < 64) {   // narrow groups: few heads, short latency-bound attentions
+          // Warm L2 and the address translation for this CTA's first tile while the kernel
+          // before runs. A prefetch delivers nothing to this SM, and L2 stays coherent with any
+          // write to those rows (the appended one) made before the loads that follow the wait.
+          if (!a.kv_early) {
+            const long long L = a.seq_lens[b], t0 = (r0 - p) * TC_TILE;
+            for (int j = 0; j < 2; ++j) {
+              const long long lt = t0 + 64 * j;
+              const int64_t pr = lt < L ? a.map.phys(b, lt) : -1;
+              if (pr >= 0)
+                for (int kb = 0; kb < TC_KB; ++kb) tc::tma_prefetch_l2_2d(&rows_map, kb * 64, (int32_t)pr);
+            }
+          }
+        }
         break;
       }
       p += n;
