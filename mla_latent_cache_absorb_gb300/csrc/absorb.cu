@@ -33,9 +33,12 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
   const int h = blockIdx.x;
   const int c0 = blockIdx.y * ABS_COLS;
   const int qrow = N + R, arow = C + R;
+  // sequences per shared-memory pass: no more than the batch has, so that small batches leave
+  // room for more CTAs per SM
+  const int bchunk = min(ABS_BCHUNK, B);
   float* w_s = sm;                          // [N][ABS_COLS]
-  float* q_s = sm + N * ABS_COLS;           // [ABS_BCHUNK][N]
-  float* red_s = q_s + ABS_BCHUNK * N;      // [4][ABS_BCHUNK][ABS_COLS] partial sums over nope quarters
+  float* q_s = sm + N * ABS_COLS;           // [bchunk][N]
+  float* red_s = q_s + bchunk * N;          // [4][bchunk][ABS_COLS] partial sums over nope quarters
   const int tid = threadIdx.x;
 
   // Loads of the first pass go out together: this thread's q_pe pair (the head's B*R/2 pairs
@@ -99,8 +102,8 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
   const int cc = tid % ABS_COLS;
   const int part = tid / ABS_COLS;   // 0..3
   const int n_lo = part * N / 4, n_hi = (part + 1) * N / 4;
-  for (int b0 = 0; b0 < B; b0 += ABS_BCHUNK) {
-    const int nb = min(ABS_BCHUNK, B - b0);
+  for (int b0 = 0; b0 < B; b0 += bchunk) {
+    const int nb = min(bchunk, B - b0);
     __syncthreads();
     if (b0 == 0) {
 #pragma unroll
@@ -120,14 +123,14 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
     for (int bb = 0; bb < nb; ++bb) {
       float acc = 0.f;
       for (int n = n_lo; n < n_hi; ++n) acc = fmaf(q_s[bb * N + n], w_s[n * ABS_COLS + cc], acc);
-      red_s[(part * ABS_BCHUNK + bb) * ABS_COLS + cc] = acc;
+      red_s[(part * bchunk + bb) * ABS_COLS + cc] = acc;
     }
     __syncthreads();
     for (int i = tid; i < nb * ABS_COLS; i += ABS_THREADS) {
       const int bb = i / ABS_COLS, c = i % ABS_COLS;
       if (c0 + c < C) {
         const float* r = red_s + bb * ABS_COLS + c;
-        const float v = ((r[0] + r[ABS_BCHUNK * ABS_COLS]) + r[2 * ABS_BCHUNK * ABS_COLS]) + r[3 * ABS_BCHUNK * ABS_COLS];
+        const float v = ((r[0] + r[bchunk * ABS_COLS]) + r[2 * bchunk * ABS_COLS]) + r[3 * bchunk * ABS_COLS];
         put(((int64_t)(b0 + bb) * H + h) * arow + c0 + c, v);
       }
     }
@@ -137,8 +140,8 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
 cudaError_t launch_absorb(const mla_config& cfg, const void* q, const void* kv_b,
                           const int32_t* positions, void* q_abs, void* q_res, int B, bool pdl, cudaStream_t st) {
   dim3 grid(cfg.n_heads, (cfg.kv_lora + ABS_COLS - 1) / ABS_COLS);
-  const size_t smem = sizeof(float) * ((size_t)cfg.qk_nope * ABS_COLS + (size_t)ABS_BCHUNK * cfg.qk_nope +
-                                       4 * (size_t)ABS_BCHUNK * ABS_COLS);
+  const size_t bchunk = (size_t)(B < ABS_BCHUNK ? B : ABS_BCHUNK);
+  const size_t smem = sizeof(float) * ((size_t)cfg.qk_nope * ABS_COLS + bchunk * cfg.qk_nope + 4 * bchunk * ABS_COLS);
   if (cfg.act_dtype == MLA_BF16) {
     auto k = absorb_kernel<MLA_BF16>;
     cudaError_t e = ensure_smem((const void*)k, (int)smem);
