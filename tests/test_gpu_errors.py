@@ -61,6 +61,29 @@ def test_bad_page_id_sets_error(bad_page):
 
 
 @gpu
+def test_bad_page_id_in_a_long_attention():
+    # 128 heads, 24 sequences of up to 3000 rows: long enough (>= 4 tiles per CTA at capacity)
+    # that mla_decode_attn reads cache rows before its dependency wait, where the producers
+    # meet the bad page id. The split plan does not depend on page ids, so every other
+    # sequence matches a clean run bit for bit.
+    from mla_latent_cache_absorb_gb300 import binding as L
+    torch, prob, ds = _setup(W["ragged_paged_b64"].with_(B=24, context=("uniform", 200, 3000)))
+    L.check(ds.append(), "append")
+    L.check(ds.decode(), "decode")
+    torch.cuda.synchronize()
+    assert L.mla_get_device_error(ds.ws_decode, ds.stream)[0] == 0
+    clean_out, clean_lse = ds.out.clone(), ds.lse.clone()
+    assert int(ds.seq_lens[5]) > 2 * 64          # the page below is one the sequence reads
+    ds.page_table[5, 1] = -1
+    L.check(ds.decode(), "decode")
+    st, seq = L.mla_get_device_error(ds.ws_decode, ds.stream)
+    assert st == L.STATUS_CODE["MLA_ERR_BAD_PAGE"] and seq == 5
+    assert torch.isnan(ds.out[5]).all() and torch.isnan(ds.lse[5]).all()
+    keep = [b for b in range(24) if b != 5]
+    assert torch.equal(ds.out[keep], clean_out[keep]) and torch.equal(ds.lse[keep], clean_lse[keep])
+
+
+@gpu
 def test_append_position_mismatch_and_cache_full():
     from mla_latent_cache_absorb_gb300 import binding as L
     torch, prob, ds = _setup(W["v2lite_b1_t4096"].with_(B=2, context=("fixed", 100)))
