@@ -17,8 +17,10 @@ constexpr int ABS_THREADS = 256;
 constexpr int ABS_COLS = 64;     // latent columns per CTA
 constexpr int ABS_BCHUNK = 32;   // sequences per shared-memory pass
 
+// at most 64 registers: four CTAs share an SM (the grid is heads x 8 column blocks, often more
+// than one wave)
 template <int DT>
-__global__ void __launch_bounds__(ABS_THREADS)
+__global__ void __launch_bounds__(ABS_THREADS, 4)
 absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const void* __restrict__ kv_b,
               const int32_t* __restrict__ positions, typename Act<DT>::T* __restrict__ q_abs,
               typename Act<DT>::T* __restrict__ q_res, int B) {
