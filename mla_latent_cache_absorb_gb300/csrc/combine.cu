@@ -39,39 +39,46 @@ struct CombineArgs {
   int vper;                 // outputs per CTA (a multiple of CMB_VJ): the merge is done once per CTA
 };
 
-// out[b0 + bb, h, j0 + j] = W_UV row j . vc[bb] for bb < nb <= NBT: 16 threads per output
-// (CMB_VJ outputs per pass), thread `part` of an output taking the latent float4s part,
-// part + 16, ... (rows of w_s and vc_s are zero past C up to `stride`), then a fixed-order
-// reduction over the 16 threads; NBT accumulators per thread.
-static_assert(CMB_THREADS / 16 == CMB_VJ, "16 threads per output of a chunk");
+// out[b0 + bb, h, j0 + j] = W_UV row j . vc[bb] for bb < nb <= NBT: one warp per pair of outputs
+// (CMB_VJ outputs per pass), lane `lane` taking the latent float4s lane, lane + 32, ... of both
+// rows (rows of w_s and vc_s are zero past C up to `stride`), so each vc element read from
+// shared memory serves two outputs; fixed-order warp reductions; 2 x NBT accumulators per lane.
+static_assert(CMB_THREADS / 32 * 2 == CMB_VJ, "one warp per pair of outputs of a chunk");
 template <int NBT>
 __device__ __forceinline__ void combine_outputs(const CombineArgs& a, const float* w_s, const float* vc_s, int stride,
                                                 int nb, int nj, int b0, int h, int j0) {
-  const int j = threadIdx.x >> 4, part = threadIdx.x & 15;
-  float acc[NBT];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ja = 2 * warp, jb = ja + 1;
+  float acc[2][NBT];
 #pragma unroll
-  for (int bb = 0; bb < NBT; ++bb) acc[bb] = 0.f;
-  if (j < nj) {
-    const float4* wr = reinterpret_cast<const float4*>(w_s + j * stride);
+  for (int bb = 0; bb < NBT; ++bb) acc[0][bb] = acc[1][bb] = 0.f;
+  if (ja < nj) {
+    const float4* wa = reinterpret_cast<const float4*>(w_s + ja * stride);
+    // a row past nj (odd nj) holds stale data: its sums are computed and dropped
+    const float4* wb = reinterpret_cast<const float4*>(w_s + jb * stride);
     const float4* vc4 = reinterpret_cast<const float4*>(vc_s);
     const int s4 = stride / 4;
 #pragma unroll 1
-    for (int c4 = part; c4 < s4; c4 += 16) {
-      const float4 w = wr[c4];
+    for (int c4 = lane; c4 < s4; c4 += 32) {
+      const float4 x = wa[c4], y = wb[c4];
 #pragma unroll
       for (int bb = 0; bb < NBT; ++bb) {
         if (bb < nb) {
           const float4 v = vc4[bb * s4 + c4];
-          acc[bb] = fmaf(w.x, v.x, fmaf(w.y, v.y, fmaf(w.z, v.z, fmaf(w.w, v.w, acc[bb]))));
+          acc[0][bb] = fmaf(x.x, v.x, fmaf(x.y, v.y, fmaf(x.z, v.z, fmaf(x.w, v.w, acc[0][bb]))));
+          acc[1][bb] = fmaf(y.x, v.x, fmaf(y.y, v.y, fmaf(y.z, v.z, fmaf(y.w, v.w, acc[1][bb]))));
         }
       }
     }
   }
 #pragma unroll
   for (int bb = 0; bb < NBT; ++bb) {
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) acc[bb] += __shfl_xor_sync(0xffffffffu, acc[bb], o);
-    if (part == 0 && j < nj && bb < nb) a.out[((int64_t)(b0 + bb) * a.H + h) * a.V + j0 + j] = acc[bb];
+    const float va = warp_sum(acc[0][bb]), vb = warp_sum(acc[1][bb]);
+    if (lane == 0 && bb < nb) {
+      const int64_t o = ((int64_t)(b0 + bb) * a.H + h) * a.V + j0;
+      if (ja < nj) a.out[o + ja] = va;
+      if (jb < nj) a.out[o + jb] = vb;
+    }
   }
 }
 
@@ -237,14 +244,11 @@ __global__ void __launch_bounds__(CMB_THREADS, 2) combine_kernel(CombineArgs a) 
       combine_outputs<1>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0);
     } else if (nb == 2) {
       combine_outputs<2>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0);
-    } else if (nb <= 4) {
-      combine_outputs<4>(a, w_s, vc_s, 4 * C4, nb, nj, b0, h, j0);
     } else {
-      // more than four sequences: two passes over the W_UV rows, four sequences each (eight
-      // accumulators a thread would not fit the register budget of two CTAs per SM)
-      static_assert(CMB_BC <= 8, "at most two passes of four sequences");
-      combine_outputs<4>(a, w_s, vc_s, 4 * C4, 4, nj, b0, h, j0);
-      combine_outputs<4>(a, w_s, vc_s + 4 * (4 * C4), 4 * C4, nb - 4, nj, b0 + 4, h, j0);
+      // more than two sequences: passes of two over the W_UV rows (more accumulators a lane
+      // would not fit the register budget of two CTAs per SM)
+      for (int p0 = 0; p0 < nb; p0 += 2)
+        combine_outputs<2>(a, w_s, vc_s + p0 * (4 * C4), 4 * C4, min(2, nb - p0), nj, b0 + p0, h, j0);
     }
   }
 }
