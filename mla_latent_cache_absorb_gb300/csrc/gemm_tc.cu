@@ -354,7 +354,9 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[u][e] = 0.f;
     }
-    const int smax = max(nsv[0], nsv[1]);
+    int smax = 0;
+#pragma unroll
+    for (int u = 0; u < MU; ++u) smax = max(smax, nsv[u]);
     for (int s0 = 0; s0 < smax; s0 += SU) {
       float4 x[MU][SU][2];
 #pragma unroll
