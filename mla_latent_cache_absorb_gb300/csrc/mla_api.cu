@@ -344,45 +344,54 @@ static mla_status decode_prologue(const mla_config* cfg, int32_t B, void* worksp
 
 namespace {
 
+// The three stages, enqueued with a plan already made and arguments already checked.
+
 // ordered: launch the absorb without programmatic serialization, so that it starts only after
 // all earlier work on the stream has completed
-mla_status decode_absorb(const mla_config* cfg, const void* q, const void* kv_b, const int32_t* positions,
-                         int32_t B, void* workspace, size_t ws_bytes, bool ordered, mla_stream_t stream) {
-  DecodePlan plan;
-  mla_status st = decode_prologue(cfg, B, workspace, ws_bytes, &plan);
-  if (st != MLA_OK) return st;
-  if (q == nullptr || kv_b == nullptr) return MLA_ERR_INVALID_ARG;
-  if (positions != nullptr && cfg->rope_inv_freq == nullptr) return MLA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(kv_b, 16)) return MLA_ERR_INVALID_ARG;
+mla_status enqueue_absorb(const mla_config* cfg, const DecodePlan& plan, const void* q, const void* kv_b,
+                          const int32_t* positions, int32_t B, void* workspace, bool ordered, cudaStream_t s) {
   void* q_abs = static_cast<char*>(workspace) + plan.off_qabs;
   void* q_res = cfg->act_dtype == MLA_BF16 ? static_cast<char*>(workspace) + plan.off_qres : nullptr;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (absorb_tc_supported(*cfg, B))
     return cuda_status(launch_absorb_tc(*cfg, q, kv_b, positions, q_abs, q_res, B, static_cast<WsHeader*>(workspace),
                                         !ordered, s));
   return cuda_status(launch_absorb(*cfg, q, kv_b, positions, q_abs, q_res, B, !ordered, s));
 }
 
-// kv_early: the kernel just before is an ordered absorb (decode_absorb with ordered = true)
-mla_status decode_partial(const mla_config* cfg, const mla_cache* cache, const int32_t* seq_lens, int32_t B,
-                          void* workspace, size_t ws_bytes, bool kv_early, mla_stream_t stream) {
-  DecodePlan plan;
-  mla_status st = decode_prologue(cfg, B, workspace, ws_bytes, &plan);
-  if (st != MLA_OK) return st;
-  if (seq_lens == nullptr) return MLA_ERR_INVALID_ARG;
-  st = check_cache(cfg, cache, B);
-  if (st != MLA_OK) return st;
+// kv_early: the kernel just before is an ordered absorb (enqueue_absorb with ordered = true)
+mla_status enqueue_partial(const mla_config* cfg, const DecodePlan& plan, const mla_cache* cache,
+                           const int32_t* seq_lens, int32_t B, void* workspace, bool kv_early, cudaStream_t s) {
   char* ws = static_cast<char*>(workspace);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   float* po = reinterpret_cast<float*>(ws + plan.off_po);
   float* pl = reinterpret_cast<float*>(ws + plan.off_plse);
   int32_t* meta = reinterpret_cast<int32_t*>(ws + plan.off_meta);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const void* q_res = cfg->act_dtype == MLA_BF16 ? ws + plan.off_qres : nullptr;
   if (plan.path == PATH_TC)
     return cuda_status(
         launch_attn_tc(*cfg, *cache, plan, seq_lens, ws + plan.off_qabs, q_res, po, pl, meta, B, hdr, kv_early, s));
   return cuda_status(launch_attn_simt(*cfg, *cache, plan, seq_lens, ws + plan.off_qabs, q_res, po, pl, meta, B, hdr, s));
+}
+
+mla_status enqueue_combine(const mla_config* cfg, const DecodePlan& plan, const void* kv_b, float* out, float* lse,
+                           int32_t B, void* workspace, cudaStream_t s) {
+  char* ws = static_cast<char*>(workspace);
+  const int32_t* meta = reinterpret_cast<const int32_t*>(ws + plan.off_meta);
+  const float* po = reinterpret_cast<const float*>(ws + plan.off_po);
+  const float* pl = reinterpret_cast<const float*>(ws + plan.off_plse);
+  // the tensor-core attention scores used bf16 latent queries: correct the LSE for the residual
+  const void* q_res = plan.path == PATH_TC ? ws + plan.off_qres : nullptr;
+  if (combine_tc_supported(*cfg, B))
+    return cuda_status(launch_combine_tc(*cfg, plan, kv_b, meta, po, pl, q_res, out, lse, B,
+                                         reinterpret_cast<WsHeader*>(ws), s));
+  return cuda_status(launch_combine(*cfg, plan, kv_b, meta, po, pl, q_res, out, lse, B, s));
+}
+
+mla_status check_absorb_args(const mla_config* cfg, const void* q, const void* kv_b, const int32_t* positions) {
+  if (q == nullptr || kv_b == nullptr) return MLA_ERR_INVALID_ARG;
+  if (positions != nullptr && cfg->rope_inv_freq == nullptr) return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv_b, 16)) return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
 }
 
 }  // namespace
@@ -392,12 +401,23 @@ extern "C" {
 mla_status mla_decode_absorb(const mla_config* cfg, const void* q, const void* kv_b,
                              const int32_t* positions, int32_t B, void* workspace, size_t ws_bytes,
                              mla_stream_t stream) {
-  return decode_absorb(cfg, q, kv_b, positions, B, workspace, ws_bytes, false, stream);
+  DecodePlan plan;
+  mla_status st = decode_prologue(cfg, B, workspace, ws_bytes, &plan);
+  if (st != MLA_OK) return st;
+  st = check_absorb_args(cfg, q, kv_b, positions);
+  if (st != MLA_OK) return st;
+  return enqueue_absorb(cfg, plan, q, kv_b, positions, B, workspace, false, reinterpret_cast<cudaStream_t>(stream));
 }
 
 mla_status mla_decode_partial(const mla_config* cfg, const mla_cache* cache, const int32_t* seq_lens,
                               int32_t B, void* workspace, size_t ws_bytes, mla_stream_t stream) {
-  return decode_partial(cfg, cache, seq_lens, B, workspace, ws_bytes, false, stream);
+  DecodePlan plan;
+  mla_status st = decode_prologue(cfg, B, workspace, ws_bytes, &plan);
+  if (st != MLA_OK) return st;
+  if (seq_lens == nullptr) return MLA_ERR_INVALID_ARG;
+  st = check_cache(cfg, cache, B);
+  if (st != MLA_OK) return st;
+  return enqueue_partial(cfg, plan, cache, seq_lens, B, workspace, false, reinterpret_cast<cudaStream_t>(stream));
 }
 
 mla_status mla_decode_combine(const mla_config* cfg, const void* kv_b, const int32_t* seq_lens,
@@ -409,42 +429,34 @@ mla_status mla_decode_combine(const mla_config* cfg, const void* kv_b, const int
   if (kv_b == nullptr || out == nullptr) return MLA_ERR_INVALID_ARG;
   (void)seq_lens;   // the partial stage recorded each sequence's slots (and validity) in meta
   if (!aligned(kv_b, 16)) return MLA_ERR_INVALID_ARG;
-  char* ws = static_cast<char*>(workspace);
-  const int32_t* meta = reinterpret_cast<const int32_t*>(ws + plan.off_meta);
-  const float* po = reinterpret_cast<const float*>(ws + plan.off_po);
-  const float* pl = reinterpret_cast<const float*>(ws + plan.off_plse);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // the tensor-core attention scores used bf16 latent queries: correct the LSE for the residual
-  const void* q_res = plan.path == PATH_TC ? ws + plan.off_qres : nullptr;
-  if (combine_tc_supported(*cfg, B))
-    return cuda_status(launch_combine_tc(*cfg, plan, kv_b, meta, po, pl, q_res, out, lse, B,
-                                         reinterpret_cast<WsHeader*>(ws), s));
-  return cuda_status(launch_combine(*cfg, plan, kv_b, meta, po, pl, q_res, out, lse, B, s));
+  return enqueue_combine(cfg, plan, kv_b, out, lse, B, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 mla_status mla_decode_attn(const mla_config* cfg, const void* q, const void* kv_b, const mla_cache* cache,
                            const int32_t* seq_lens, const int32_t* positions, float* out, float* lse,
                            int32_t B, void* workspace, size_t ws_bytes, mla_stream_t stream) {
-  // validate everything before the first launch, so a bad argument enqueues nothing
+  // validate everything before the first launch, so a bad argument enqueues nothing; the plan
+  // is made once for the three stages
   DecodePlan plan;
   mla_status st = decode_prologue(cfg, B, workspace, ws_bytes, &plan);
   if (st != MLA_OK) return st;
-  if (q == nullptr || kv_b == nullptr || seq_lens == nullptr || out == nullptr) return MLA_ERR_INVALID_ARG;
-  if (positions != nullptr && cfg->rope_inv_freq == nullptr) return MLA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(kv_b, 16)) return MLA_ERR_INVALID_ARG;
+  st = check_absorb_args(cfg, q, kv_b, positions);
+  if (st != MLA_OK) return st;
+  if (seq_lens == nullptr || out == nullptr) return MLA_ERR_INVALID_ARG;
   st = check_cache(cfg, cache, B);
   if (st != MLA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // Long attentions (at the cache's capacity, at least four 128-row tiles per CTA): the absorb
   // starts once everything before it on the stream, the cache append above all, has completed,
   // and the attention then streams cache rows while the absorb still runs. Short ones keep the
   // absorb's own overlap with the kernels before it, which is worth more to them.
   const int64_t max_tiles = (int64_t)B * ((plan.capacity + 127) / 128);
   const bool early = plan.path == PATH_TC && max_tiles >= 4 * (int64_t)plan.ctas_per_group;
-  st = decode_absorb(cfg, q, kv_b, positions, B, workspace, ws_bytes, early, stream);
+  st = enqueue_absorb(cfg, plan, q, kv_b, positions, B, workspace, early, s);
   if (st != MLA_OK) return st;
-  st = decode_partial(cfg, cache, seq_lens, B, workspace, ws_bytes, early, stream);
+  st = enqueue_partial(cfg, plan, cache, seq_lens, B, workspace, early, s);
   if (st != MLA_OK) return st;
-  return mla_decode_combine(cfg, kv_b, seq_lens, out, lse, B, workspace, ws_bytes, stream);
+  return enqueue_combine(cfg, plan, kv_b, out, lse, B, workspace, s);
 }
 
 mla_status mla_get_device_error(const void* workspace, int32_t* seq_out, mla_stream_t stream) {
