@@ -248,11 +248,11 @@ struct DecodePlan {
 };
 enum { PATH_SIMT = 0, PATH_TC = 1 };
 
-// 2D bf16 TMA map over a row-major [rows, inner] tensor (inner elements contiguous) with
-// boxes of box_inner x box_rows and the 128-byte swizzle. False when the driver entry point
-// is unavailable or the encoding is rejected.
-// True when the driver's tensor-map encoder could be found (looked up once per process).
+// True when the CUDA driver's tensor-map encoder could be found (looked up once per process).
 bool tma_encoder_available();
+// 2D bf16 TMA map over a row-major [rows, inner] tensor (inner elements contiguous) with
+// boxes of box_inner x box_rows and the 128-byte swizzle. False when the CUDA driver entry point
+// is unavailable or the encoding is rejected.
 bool make_map_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
                       uint32_t box_rows);
 

@@ -1,4 +1,4 @@
-// Host side of the TMA loads: the driver's tensor-map encoder, looked up once, and the
+// Host side of the TMA loads: the CUDA driver's tensor-map encoder, looked up once, and the
 // encoding of 2D bf16 maps with a small per-thread cache of recent encodings. Kept apart from
 // the kernels so that host-only changes leave the kernel sources untouched.
 #include "common.cuh"
