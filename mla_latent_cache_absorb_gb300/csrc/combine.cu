@@ -11,7 +11,8 @@
 // of its sequences for its head into float32 latent vectors (every thread keeps several partial
 // loads in flight; with few sequences the slots are shared out over several threads and summed
 // in a fixed order), then, 32 outputs at a time, stages those rows of W_UV (dequantised) in
-// shared memory and forms the dot products one warp per output with the lanes across the latent.
+// shared memory and forms the dot products one warp per pair of outputs with the lanes across
+// the latent.
 #include "common.cuh"
 
 #include <math_constants.h>
