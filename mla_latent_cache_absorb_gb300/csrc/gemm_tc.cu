@@ -8,10 +8,12 @@
 //   absorb:  q'^T[c, b]  = W_UK,h^T[c, n] . q_nope^T[n, b]   (M = 2 x 128 latent, N = batch, K = 128)
 //   combine: out^T[j, b] = W_UV,h[j, c]   . vc^T[c, b]       (M = 128, N = batch, K = 512)
 // The weight slice arrives by TMA in the 128-byte swizzle layout and is the A operand (MN-major
-// for W_UK^T, K-major for W_UV); the batch is the N dimension (padded to 16), so one CTA per head
-// (and batch chunk) issues a handful of tcgen05 MMAs with the fp32 accumulator in TMEM.
-// The combine first merges the split partials into vc (float32) and feeds it as two bf16 terms
-// (hi + lo), so the up-projection keeps close to float32 accuracy on the bf16 tensor path.
+// for W_UK^T, K-major for W_UV); the batch is the N dimension, so one CTA per head (and batch
+// chunk) issues a handful of tcgen05 MMAs with the fp32 accumulator in TMEM.
+// The combine first merges the split partials into vc (float32) and feeds it as two bf16 terms,
+// hi and lo, stacked into one N = 64 operand for its 32 sequences (the two accumulator halves
+// are added in the epilogue), so the up-projection keeps close to float32 accuracy on the bf16
+// tensor path. The absorb pads its batch chunk to a multiple of 16.
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
