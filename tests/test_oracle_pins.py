@@ -335,3 +335,52 @@ def test_kv_a_projection_is_matvec():
     w = RNG.standard_normal((5, 12))
     np.testing.assert_allclose(O.kv_a_rows(x, w)[1], [sum(w[r, i] * x[1, i] for i in range(12)) for r in range(5)],
                                rtol=1e-13)
+
+
+# ----------------------------------------------------------------------------------------
+# bf16 decoding: hand-written bit patterns, the IEEE field formula, and torch's own cast
+# ----------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bits,value", [
+    (0x3F80, 1.0), (0xBF80, -1.0), (0x4000, 2.0), (0xC000, -2.0), (0x4049, 3.140625),
+    (0x3F00, 0.5), (0x0000, 0.0), (0x0080, 2.0 ** -126), (0x0001, 2.0 ** -133),
+    (0x7F7F, (2.0 - 2.0 ** -7) * 2.0 ** 127), (0x7F80, math.inf), (0xFF80, -math.inf),
+])
+def test_bf16_to_f64_hand_patterns(bits, value):
+    got = O.bf16_to_f64(np.array([bits], dtype=np.uint16))[0]
+    assert got == value and math.copysign(1.0, got) == math.copysign(1.0, value)
+
+
+def test_bf16_to_f64_signed_zero_and_nan():
+    z = O.bf16_to_f64(np.array([0x8000], dtype=np.uint16))[0]
+    assert z == 0.0 and math.copysign(1.0, z) == -1.0
+    assert np.isnan(O.bf16_to_f64(np.array([0x7FC0, 0xFFC1, 0x7F81], dtype=np.uint16))).all()
+
+
+def _bf16_fields(bits: int) -> float:
+    """bf16 value from its fields: sign 1 bit, exponent 8 bits (bias 127), fraction 7 bits."""
+    s, e, m = bits >> 15, (bits >> 7) & 0xFF, bits & 0x7F
+    if e == 0xFF:
+        return math.nan if m else (-math.inf if s else math.inf)
+    mag = math.ldexp(m, -126 - 7) if e == 0 else math.ldexp(128 + m, e - 127 - 7)
+    return -mag if s else mag
+
+
+def test_bf16_to_f64_matches_field_formula_on_every_pattern():
+    allbits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    got = O.bf16_to_f64(allbits)
+    want = np.array([_bf16_fields(int(b)) for b in allbits])
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+def test_bf16_to_f64_matches_torch_cast():
+    torch = pytest.importorskip("torch")
+    bits = np.random.default_rng(7).integers(0, 1 << 16, size=10000).astype(np.uint16)
+    t = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    got = O.bf16_to_f64(bits)
+    nan = np.isnan(t)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], t[~nan])
