@@ -3,8 +3,11 @@
 
 A step is one pass of the whole path over one batch: mla_cache_append (new row per sequence)
 then mla_decode_attn (absorb, split attention over every cached row, combine + W_UV
-up-projection). The default workload is the DeepSeek-V2-Lite-shaped single-sequence decode
-(B=1, H=16, kv_lora 512, rope 64, 4096 rows, bf16). Prints ONE JSON line.
+up-projection). The default workload is the largest single-GPU one: ragged paged decode
+(B=64 sequences of U{128..32768} rows, H=128, kv_lora 512, rope 64, bf16, 64-row pages with a
+shuffled page table). The same line carries, under "also", the attention kernel's roofline
+fraction on the single-sequence (B=1, H=16, 4096 rows) and batched (B=32, H=128, 4096 rows)
+workloads, measured in the same run. Prints ONE JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -36,7 +39,9 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 
 METRIC = "MLA decode: KV-cache rows/s, achieved TFLOP/s & HBM GB/s vs roofline"
-DEFAULT_WORKLOAD = "v2lite_b1_t4096"
+DEFAULT_WORKLOAD = "ragged_paged_b64"
+# attention-only sub-records measured in the same run: workload -> timed steps
+ALSO_WORKLOADS = {"v2lite_b1_t4096": 4000, "v3_b32_t4096": 400}
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -239,14 +244,23 @@ def aggregate_over_ranks(total_ms, world, rows_per_step, steps, device):
     return tmax, world * rows_per_step * steps / (tmax / 1e3)
 
 
-def run_ours(args, rank, world, device):
+def workload_config(wl, prob, work):
+    """The workload's own description (the same dict in both arms)."""
+    return {
+        "workload": wl.name, "B": wl.B, "H": wl.H, "kv_lora": wl.C, "qk_nope": wl.N, "qk_rope": wl.R,
+        "v_head": wl.V, "rows_per_step": work["rows"], "kv_b": wl.kv_b, "act": wl.act,
+        "paged": bool(wl.page_size), "append": wl.append, "parallelism": "replicas (independent sequences)",
+    }
+
+
+def run_ours(args, rank, world, device, workload, K, W, with_e2e=True, with_clocks=True):
     import torch
 
     from mla_latent_cache_absorb_gb300 import binding as L
     from mla_latent_cache_absorb_gb300 import synth
     from mla_latent_cache_absorb_gb300.runner import DeviceStep
 
-    wl = synth.WORKLOADS[args.workload]
+    wl = synth.WORKLOADS[workload]
     prob = synth.make_problem(wl)
     work = step_work(prob)
     props = torch.cuda.get_device_properties(device)
@@ -278,7 +292,6 @@ def run_ours(args, rank, world, device):
     # double-buffer the in-graph attention events, plus a tail graph for K mod G steps. Only
     # the first step of each graph has its attention launch bracketed by events: an event
     # between two kernels turns their programmatic (overlapped) launch into a plain one.
-    K, W = args.steps, args.warmup
     G = R * max(1, math.ceil(16 / R)) if R > 1 else max(1, min(64, K))
     G = max(1, min(G, max(R, 64)))
     torch.cuda.synchronize(device)
@@ -306,12 +319,20 @@ def run_ours(args, rank, world, device):
         tail = K % G
         gT, evT = capture(tail, True) if tail else (None, None)
         n_full = K // G
+        # one untimed replay of every graph: uploads them and warms their first launch, so the
+        # timed region holds steady-state replays only
+        for g in (gA, gB, gT):
+            if g is not None:
+                g.replay()
+        torch.cuda.synchronize(device)
 
-        sampler = ClockSampler(str(props.uuid) if hasattr(props, "uuid") else "")
-        if not str(sampler.uuid).startswith("GPU-") and sampler.uuid:
-            sampler.uuid = "GPU-" + sampler.uuid
-        sampler.start()
-        time.sleep(0.3)
+        sampler = None
+        if with_clocks:
+            sampler = ClockSampler(str(props.uuid) if hasattr(props, "uuid") else "")
+            if not str(sampler.uuid).startswith("GPU-") and sampler.uuid:
+                sampler.uuid = "GPU-" + sampler.uuid
+            sampler.start()
+            time.sleep(0.3)
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize(device)
@@ -342,24 +363,26 @@ def run_ours(args, rank, world, device):
         if world > 1:
             torch.distributed.barrier()
         total_ms = t_start.elapsed_time(t_end)
-        clk = sampler.samples(wall0, wall1)
-        window = "timed"
-        if len(clk) < 3 and args.clock_window_s > 0:
-            # the timed region was shorter than the sampler's period: sample the same graphs
-            # for about a second right after it (untimed) and say so
-            wa = time.time()
-            while time.time() - wa < args.clock_window_s:
-                gA.replay()
-                gB.replay()
-                torch.cuda.synchronize(device)
-            clk = sampler.samples(wa, time.time())
-            window = "adjacent"
-        sampler.stop()
-        clocks = summarize_clocks(clk, window)
+        clocks = None
+        if sampler is not None:
+            clk = sampler.samples(wall0, wall1)
+            window = "timed"
+            if len(clk) < 3 and args.clock_window_s > 0:
+                # the timed region was shorter than the sampler's period: sample the same graphs
+                # for about a second right after it (untimed) and say so
+                wa = time.time()
+                while time.time() - wa < args.clock_window_s:
+                    gA.replay()
+                    gB.replay()
+                    torch.cuda.synchronize(device)
+                clk = sampler.samples(wa, time.time())
+                window = "adjacent"
+            sampler.stop()
+            clocks = summarize_clocks(clk, window)
 
         # end to end through the public calls: pinned host inputs in, results out, every step
         e2e = None
-        if not args.no_e2e:
+        if with_e2e:
             e2e = run_e2e(torch, L, steps, prob, stream, device, K, W, work)
 
     tmax, value = aggregate_over_ranks(total_ms, world, work["rows"], K, device)
@@ -372,16 +395,16 @@ def run_ours(args, rank, world, device):
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.act, "data": "synthetic (seeded generator; random-init kv_b)",
-        "config": {
-            "workload": wl.name, "B": wl.B, "H": wl.H, "kv_lora": wl.C, "qk_nope": wl.N, "qk_rope": wl.R,
-            "v_head": wl.V, "rows_per_step": work["rows"], "kv_b": wl.kv_b,
-            "paged": bool(wl.page_size), "append": wl.append,
+        "config": workload_config(wl, prob, work),
+        "run": {
             "l2": f"rotating {R} input copies ({R * per_copy / 2 ** 20:.0f} MB, L2 {l2 / 2 ** 20:.0f} MB)",
-            "timing": f"CUDA graphs of {G} steps, events on the launching stream; the attention "
-                      f"launch of each graph's first step bracketed by in-graph events",
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "timing": f"CUDA graphs of {G} steps (each replayed once untimed first), events on the "
+                      f"launching stream; the attention launch of each graph's first step bracketed "
+                      f"by in-graph events",
+            "gpus": f"replicas x{world}" if world > 1 else "single GPU",
             "attention_kernel": "tcgen05" if plan.kernel == 1 else "cuda-core",
-            "splits": plan.splits, "rows_per_split": plan.rows_per_split,
+            "heads_per_cta": plan.heads_per_cta, "splits": plan.splits,
+            "rows_per_split": plan.rows_per_split,
         },
         "tflops": work["flops"] / step_s / 1e12,
         "hbm_gbs": work["bytes"] / step_s / 1e9,
@@ -398,6 +421,9 @@ def run_ours(args, rank, world, device):
         "clocks": clocks,
         "e2e": e2e,
     }
+    del steps
+    torch.cuda.synchronize(device)
+    torch.cuda.empty_cache()
     return line
 
 
@@ -476,53 +502,140 @@ def host_cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(prob, seconds):
+# The oracle runs in spawned worker processes, one sequence-step per task, each worker with one
+# BLAS thread, so `cores` is the number of processes that actually ran it. A task carries only
+# its sequence's rows (in logical order), so the workers never hold the whole cache.
+_OW = {}
+
+
+def _oracle_worker_init(wl, shared):
+    _OW["wl"] = wl
+    _OW["shared"] = shared
+
+
+def _oracle_task(task):
+    """One sequence's whole step (append + decode over `heads` heads) on the oracle, as a
+    one-sequence contiguous problem holding that sequence's rows. Returns rows credited."""
+    from mla_latent_cache_absorb_gb300 import synth
     from oracle import step as OS
-    rps, n, rows, dt = OS.rows_per_second_sample(prob, seconds=seconds)
-    return {"value": rps, "unit": "rows/s", "cores": host_cores(), "kind": "oracle",
-            "sample": f"{n} oracle sequence-steps (append + decode of one sequence, all {prob.wl.H} heads), "
-                      f"{rows:.0f} rows in {dt:.1f} s, fp64 numpy on the host"}
+    rows, q, kva, x, pos, L, nheads = task
+    wl = _OW["wl"].with_(B=1, page_size=0)
+    sh = _OW["shared"]
+    prob = synth.Problem(wl=wl, q=q, pool=rows, page_table=None, rows_per_seq=rows.shape[0], max_pages=0,
+                         positions=np.array([pos], np.int32), seq_lens=np.array([L], np.int32),
+                         norm_w=sh["norm_w"], kv_b=sh["kv_b"], kva_rows=kva, x=x, w_kva=sh["w_kva"])
+    OS.run_step(prob, seqs=[0], heads=np.arange(nheads))
+    return float(L) * nheads / _OW["wl"].H
+
+
+class OracleSampler:
+    """A pool of spawned processes that time the oracle over bounded samples of a workload."""
+
+    def __init__(self, prob, workers=None):
+        import multiprocessing as mp
+        self.prob = prob
+        self.workers = workers or host_cores()
+        shared = {"norm_w": prob.norm_w, "kv_b": prob.kv_b, "w_kva": prob.w_kva}
+        keep = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+        for k in keep:
+            os.environ[k] = "1"   # inherited by the spawned workers only
+        try:
+            self.pool = mp.get_context("spawn").Pool(self.workers, _oracle_worker_init, (prob.wl, shared))
+        finally:
+            for k, v in keep.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+
+    def task(self, b, nheads):
+        from oracle import mla_oracle as O
+        p, wl = self.prob, self.prob.wl
+        L = int(p.seq_lens[b])
+        phys = O.physical_row(b, np.arange(L), p.page_table, wl.page_size, p.rows_per_seq)
+        kva = None if p.kva_rows is None else p.kva_rows[b:b + 1]
+        x = None if p.x is None else p.x[b:b + 1]
+        return (p.pool[phys], p.q[b:b + 1], kva, x, int(p.positions[b]), L, nheads)
+
+    def run(self, seqs, nheads):
+        """Wall time of computing the given sequence-steps in parallel; rows credited."""
+        tasks = [self.task(b, nheads) for b in seqs]
+        t0 = time.perf_counter()
+        rows = sum(self.pool.map(_oracle_task, tasks, chunksize=1))
+        return rows, time.perf_counter() - t0
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def cpu_baseline(prob, seconds):
+    """The oracle on all host cores over a bounded sample: one round of one sequence-step per
+    worker to size the sample, then enough rounds to take about `seconds`."""
+    wl = prob.wl
+    smp = OracleSampler(prob)
+    try:
+        nxt = 0
+
+        def seqs(n):
+            nonlocal nxt
+            out = [(nxt + i) % wl.B for i in range(n)]
+            nxt += n
+            return out
+
+        r0, t0 = smp.run(seqs(smp.workers), wl.H)
+        rounds = max(1, int(seconds / max(t0, 1e-3)))
+        rows, dt = smp.run(seqs(rounds * smp.workers), wl.H)
+    finally:
+        smp.close()
+    return {"value": rows / dt, "unit": "rows/s", "cores": smp.workers, "kind": "oracle",
+            "sample": f"{rounds * smp.workers} oracle sequence-steps (append + decode of one sequence, all "
+                      f"{wl.H} heads; sequences taken in order, wrapping), {rows:.0f} rows in {dt:.1f} s, fp64 "
+                      f"numpy in {smp.workers} processes with one BLAS thread each, after one sizing round"}
 
 
 def run_reference(args, budget_s=150.0):
     """The oracle as it stands, timed on the host cores. Each step is a bounded sample of the
-    workload: one sequence's whole step (append + decode) with all heads when that fits the
-    time budget (budget_s over all warm-up and timed steps), else with its first heads only;
-    rows are credited in proportion to the heads computed."""
+    workload: one sequence-step per worker process (the next sequences in order), all heads when
+    that fits the time budget (budget_s over all warm-up and timed steps), else the first heads
+    only; rows are credited in proportion to the heads computed."""
     from mla_latent_cache_absorb_gb300 import synth
-    from oracle import step as OS
     wl = synth.WORKLOADS[args.workload]
     prob = synth.make_problem(wl)
-    t0 = time.perf_counter()
-    OS.run_step(prob, seqs=[0])
-    t_one = time.perf_counter() - t0
-    per_step = budget_s / (args.steps + args.warmup)
-    hs = wl.H if t_one <= per_step else max(1, int(wl.H * per_step / t_one))
-    heads = np.arange(hs)
+    work = step_work(prob)
+    smp = OracleSampler(prob)
+    try:
+        nw = smp.workers
+        _, t_one = smp.run(list(range(min(nw, wl.B))), wl.H)
+        per_step = budget_s / (args.steps + args.warmup)
+        hs = wl.H if t_one <= per_step else max(1, int(wl.H * per_step / t_one))
+        k = [0]
 
-    def sample(k):
-        b = k % wl.B
-        OS.run_step(prob, seqs=[b], heads=heads)
-        return float(prob.seq_lens[b]) * hs / wl.H
+        def step():
+            seqs = [(k[0] * nw + i) % wl.B for i in range(nw)]
+            k[0] += 1
+            return smp.run(seqs, hs)
 
-    for k in range(args.warmup):
-        sample(k)
-    rows = 0.0
-    t0 = time.perf_counter()
-    for k in range(args.steps):
-        rows += sample(k)
-    dt = time.perf_counter() - t0
+        for _ in range(args.warmup):
+            step()
+        rows, dt = 0.0, 0.0
+        for _ in range(args.steps):
+            r, t = step()
+            rows += r
+            dt += t
+    finally:
+        smp.close()
     value = rows / dt
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded generator)",
-        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "kv_lora": wl.C,
-                   "rows_per_step": int(np.sum(prob.seq_lens))},
-        "cpu_baseline": {"value": value, "unit": "rows/s", "kind": "oracle", "cores": host_cores(),
-                         "sample": f"{args.steps} oracle sequence-steps ({hs} of {wl.H} heads, append + decode) "
-                                   f"after {args.warmup} warm-up, {rows:.0f} rows credited in {dt:.1f} s"},
+        "config": workload_config(wl, prob, work),
+        "cpu_baseline": {"value": value, "unit": "rows/s", "kind": "oracle", "cores": nw,
+                         "sample": f"{args.steps} steps of {nw} oracle sequence-steps each ({hs} of {wl.H} "
+                                   f"heads, append + decode, one per worker process with one BLAS thread) "
+                                   f"after {args.warmup} warm-up steps, {rows:.0f} rows credited in {dt:.1f} s"},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -539,6 +652,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-also", action="store_true", help="skip the attention sub-records")
     ap.add_argument("--clock-window-s", type=float, default=1.2,
                     help="seconds of untimed replays to sample clocks when the timed region is too short")
     args = ap.parse_args()
@@ -558,12 +672,26 @@ def main():
 
     import torch
     if args.steps is None:
-        args.steps = 20000 if args.workload == DEFAULT_WORKLOAD else 200
+        args.steps = 20000 if args.workload == "v2lite_b1_t4096" else 200
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=device)
-    line = run_ours(args, rank, world, device)
+    line = run_ours(args, rank, world, device, args.workload, args.steps, args.warmup,
+                    with_e2e=not args.no_e2e, with_clocks=True)
+    if not args.no_also:
+        also = {}
+        for wname, k in ALSO_WORKLOADS.items():
+            if wname == args.workload:
+                continue
+            sub = run_ours(args, rank, world, device, wname, k, args.warmup, with_e2e=False, with_clocks=False)
+            also[wname] = {"roofline_frac": sub["roofline"]["frac"], "avg_launch_us": sub["roofline"]["avg_launch_us"],
+                           "attn_gbs": sub["roofline"]["achieved"], "ms_per_step": sub["ms_per_step"],
+                           "rows_per_s": sub["value"], "steps": k, "heads_per_cta": sub["run"]["heads_per_cta"]}
+            line["gpu_launches"] += sub["gpu_launches"]
+        line["also"] = {"what": "attention kernel of other workloads, same run, same timing method "
+                                "(not part of value or ms_per_step; their launches are counted in gpu_launches)",
+                        **also}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from mla_latent_cache_absorb_gb300 import synth
         line["cpu_baseline"] = cpu_baseline(synth.make_problem(synth.WORKLOADS[args.workload]), args.cpu_seconds)

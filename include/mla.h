@@ -169,6 +169,18 @@ typedef struct mla_plan_info {
 /* Fills *info with the plan for (cfg, B). Host-only query; needs a CUDA device. */
 mla_status mla_decode_plan(const mla_config* cfg, int32_t B, mla_plan_info* info);
 
+/* ---- failure detection --------------------------------------------------------------------
+ * Every wait inside the tensor-core kernels (on a TMA copy, an MMA, another role of the same
+ * CTA) is bounded: when it runs out, the kernel records MLA_ERR_TIMEOUT in the workspace,
+ * every role of the CTA stops, copies and MMAs already issued are drained, tensor memory is
+ * freed, and the outputs the CTA owns are written as NaN (their sequences' out and lse become
+ * NaN). The limit of the main-loop waits is a process-wide setting, read when a call enqueues
+ * its kernels (a captured graph keeps the value of its capture); the drains always keep
+ * 200 ms. Sets the limit in nanoseconds (0 restores the default, 200 ms) and returns the
+ * previous one. A limit far below a kernel's natural waits makes it time out on purpose: that
+ * is how the timeout path is tested. Thread-safe; host-only. */
+uint64_t mla_set_wait_limit_ns(uint64_t ns);
+
 /* ---- the method ----------------------------------------------------------------------- */
 
 /* Append one new row per sequence, in place (async).
@@ -273,9 +285,10 @@ mla_status mla_clear_device_error(void* workspace, mla_stream_t stream);
  * Zero state: the array's first 256 bytes (the device error word) must be zero when the
  * kernels start; every call clears them on `stream` before its launches, and nothing else
  * in the array is read before it is written in the same call.
- * First call: the first call on each device (with that device current) looks the array's
- * address up with cudaGetSymbolAddress, which may load the library's module for that
- * device; make that first call before any stream capture.
+ * Address: every call looks the array's address up in the current device's context with
+ * cudaGetSymbolAddress (no allocation), so a context torn down and recreated (e.g. after
+ * cudaDeviceReset) is picked up. The first call on each device may load the library's
+ * module for that device; make that first call before any stream capture.
  * Concurrency: every call on a device shares the one array. Calls that may overlap on the
  * GPU (different streams without ordering between them, or several host threads) race on
  * it and corrupt each other's results; order them on one stream or with events.

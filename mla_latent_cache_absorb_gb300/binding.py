@@ -57,6 +57,7 @@ _SIGS = {
     "mla_append_workspace_size": (c_int32, [_CFG, c_int32, POINTER(c_size_t)]),
     "mla_decode_workspace_size": (c_int32, [_CFG, c_int32, POINTER(c_size_t)]),
     "mla_decode_plan": (c_int32, [_CFG, c_int32, POINTER(MlaPlanInfo)]),
+    "mla_set_wait_limit_ns": (c_uint64, [c_uint64]),
     "mla_cache_append": (c_int32, [_CFG, _CACHE, c_void_p, c_void_p, c_int32, c_void_p, c_void_p,
                                    c_void_p, c_int32, c_void_p, c_size_t, c_void_p]),
     "mla_decode_attn": (c_int32, [_CFG, c_void_p, c_void_p, _CACHE, c_void_p, c_void_p, c_void_p,
@@ -157,6 +158,10 @@ def mla_decode_plan(cfg, B):
     info = MlaPlanInfo()
     st = _lib.mla_decode_plan(ctypes.byref(cfg), B, ctypes.byref(info))
     return st, info
+
+
+def mla_set_wait_limit_ns(ns):
+    return _lib.mla_set_wait_limit_ns(int(ns))
 
 
 def mla_cache_append(cfg, cache, kv_in, w_kva, hidden, norm_w, positions, seq_lens, B, workspace,

@@ -50,7 +50,9 @@ constexpr int TC_SLOT_BYTES = TC_TILE * 128;   // 16 KB
 constexpr int TC_PRODUCERS = 2;   // TMA producer warps (a single issuing thread tops out near 45 GB/s)
 constexpr int TC_MMA_WARP = TC_PRODUCERS;
 constexpr int TC_SM_WARP0 = TC_PRODUCERS + 1;   // first softmax warp
-constexpr uint64_t WAIT_NS = 200ull * 1000 * 1000;   // a wait gives up after 200 ms
+// Drain waits (copies and MMAs already issued, before the CTA exits) always get the full
+// limit; the main-loop waits get the launch's wait_ns (normally the same 200 ms).
+constexpr uint64_t WAIT_NS = kWaitDrainNs;
 
 // Per head-group width HG (the MMA N: 16, 32 or 64 heads per CTA).
 template <int HG>
@@ -89,6 +91,7 @@ struct TcArgs {
   WsHeader* hdr;
   int B, H, G, ncg, n_slots;
   float scale_log2;
+  uint64_t wait_ns;       // limit of the main-loop waits
   // 1: the kernel launched just before this one started only after all earlier work on the
   // stream had completed, and writes no cache row; cache rows may then be read before the
   // dependency wait (only the queries wait for it)
@@ -156,14 +159,14 @@ __device__ __forceinline__ void cta_range(long long T, int k, int ncg, long long
   *r1 = (T * (k + 1)) / ncg;
 }
 
-// A bounded wait (WAIT_NS) that also gives up once another role has aborted.
-__device__ __forceinline__ bool wait_bar(Smem& s, uint64_t* bar, uint32_t parity) {
+// A bounded wait (limit_ns) that also gives up once another role has aborted.
+__device__ __forceinline__ bool wait_bar(Smem& s, uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = tc::global_ns();
   for (uint32_t i = 0;; ++i) {
     if (tc::mbar_try_wait(bar, parity)) return true;
     if ((i & 15) == 15) {
       if (*reinterpret_cast<volatile int*>(&s.abort)) return false;
-      if (tc::global_ns() - t0 > WAIT_NS) return false;
+      if (tc::global_ns() - t0 > limit_ns) return false;
     }
   }
 }
@@ -172,8 +175,8 @@ __device__ __forceinline__ bool wait_bar(Smem& s, uint64_t* bar, uint32_t parity
 // polled would run split afterwards: collective operations then serialise and the warp's
 // arrivals at the group barrier stop lining up), then the warpgroup's 128 threads agree on the
 // outcome, so they always leave (or stay in) their loops together and never strand a barrier.
-__device__ __forceinline__ bool softmax_wait(Smem& s, uint64_t* bar, uint32_t parity, int wg) {
-  const bool ok = wait_bar(s, bar, parity);
+__device__ __forceinline__ bool softmax_wait(Smem& s, uint64_t* bar, uint32_t parity, int wg, uint64_t limit_ns) {
+  const bool ok = wait_bar(s, bar, parity, limit_ns);
   __syncwarp();
   return !softmax_vote_or(!ok, wg);
 }
@@ -383,7 +386,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
       // to leave L2, so that the split partials this kernel writes stay there for the combine
       const uint64_t kv_policy = tc::l2_policy_evict_first();
       auto load_q = [&]() -> bool {
-        if (seg > 0 && !wait_bar(s, &s.q_empty, (seg - 1) & 1)) return false;
+        if (seg > 0 && !wait_bar(s, &s.q_empty, (seg - 1) & 1, a.wait_ns)) return false;
         tc::mbar_arrive_expect_tx(&s.q_full, Cfg<HG>::Q_BLOCKS * Cfg<HG>::QBLK_BYTES);
         const int qrow = sb * a.H + g * HG;
         for (int kb = 0; kb < TC_KB; ++kb)
@@ -418,7 +421,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
           }
           // latent blocks 0..7 in order, the rope block (8) last: the order QK^T consumes them
           for (int kb = pw; kb < TC_KB; kb += TC_PRODUCERS) {
-            if (n > 0 && !wait_bar(s, &s.empty[kb], (uint32_t)((n - 1) & 1))) { ok = false; break; }
+            if (n > 0 && !wait_bar(s, &s.empty[kb], (uint32_t)((n - 1) & 1), a.wait_ns)) { ok = false; break; }
             tc::mbar_arrive_expect_tx(&s.full[kb], bytes);
             for (int j = 0; j < 2; ++j)
               if (y[j] >= 0)
@@ -434,13 +437,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
         }
         if (ok) ++seg;
       }
-      if (!ok) {
-        fail(s, a.hdr, sb);
-        // wait (bounded) for every copy already issued, so none lands after the CTA exits
-        for (int kb = pw; kb < TC_KB; kb += TC_PRODUCERS)
-          if (last_n[kb] >= 0) tc::mbar_wait(&s.full[kb], (uint32_t)(last_n[kb] & 1), WAIT_NS);
-        if (q_loaded >= 0) tc::mbar_wait(&s.q_full, (uint32_t)(q_loaded & 1), WAIT_NS);
-      }
+      if (!ok) fail(s, a.hdr, sb);
+      // Wait (bounded) for every copy this thread issued, so none lands after the CTA exits:
+      // after an abort of any role the last tiles may never have been consumed. In a clean run
+      // they have all landed already and these waits return at once.
+      for (int kb = pw; kb < TC_KB; kb += TC_PRODUCERS)
+        if (last_n[kb] >= 0) tc::mbar_wait(&s.full[kb], (uint32_t)(last_n[kb] & 1), WAIT_NS);
+      if (q_loaded >= 0) tc::mbar_wait(&s.q_full, (uint32_t)(q_loaded & 1), WAIT_NS);
     }
   } else if (warp == TC_MMA_WARP) {
     // ================================ MMA issuer ================================
@@ -454,16 +457,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
       long long n = 0;
       bool ok = true;
       while (ok && it.next(a, &sb, &tlo, &thi)) {
-        if (!wait_bar(s, &s.q_full, seg & 1)) { ok = false; break; }
+        if (!wait_bar(s, &s.q_full, seg & 1, a.wait_ns)) { ok = false; break; }
         tc::tc_fence_after();
         for (int t = tlo; t < thi; ++t, ++n) {
           const int sbuf = (int)(n & 1);
           const uint32_t s_tmem = tmem + Cfg<HG>::S_COL + sbuf * HG;
-          if (n >= 2 && !wait_bar(s, &s.s_empty[sbuf], (uint32_t)(((n >> 1) - 1) & 1))) { ok = false; break; }
+          if (n >= 2 && !wait_bar(s, &s.s_empty[sbuf], (uint32_t)(((n >> 1) - 1) & 1), a.wait_ns)) { ok = false; break; }
           tc::tc_fence_after();
           for (int i = 0; i < TC_KB; ++i) {
             const int kb = (i < TC_LAT_KB) ? i : TC_LAT_KB;
-            if (!wait_bar(s, &s.full[kb], (uint32_t)(n & 1))) { ok = false; break; }
+            if (!wait_bar(s, &s.full[kb], (uint32_t)(n & 1), a.wait_ns)) { ok = false; break; }
             tc::tc_fence_after();
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t ad = tc::sdesc_sw128(slot0 + kb * TC_SLOT_BYTES + kk * 32, 16, 1024);
@@ -481,8 +484,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
           tc::mma_commit(&s.s_full[sbuf]);
           if (t + 1 == thi) tc::mma_commit(&s.q_empty);
           // PV needs P^T (slot 8) and, on a segment's first tile, the previous O^T read out
-          if (!wait_bar(s, &s.p_full, (uint32_t)(n & 1))) { ok = false; break; }
-          if (t == tlo && seg > 0 && !wait_bar(s, &s.o_empty, (uint32_t)((seg - 1) & 1))) { ok = false; break; }
+          if (!wait_bar(s, &s.p_full, (uint32_t)(n & 1), a.wait_ns)) { ok = false; break; }
+          if (t == tlo && seg > 0 && !wait_bar(s, &s.o_empty, (uint32_t)((seg - 1) & 1), a.wait_ns)) { ok = false; break; }
           tc::tc_fence_after();
           const uint32_t p_addr = slot0 + TC_LAT_KB * TC_SLOT_BYTES;
           for (int cc = 0; cc < 4; ++cc) {
@@ -534,13 +537,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
       for (int t = tlo; t < thi; ++t, ++n) {
         const int sbuf = (int)(n & 1);
         const uint32_t s_addr = tmem + lane_base + Cfg<HG>::S_COL + sbuf * HG + h0;
-        if (!softmax_wait(s, &s.s_full[sbuf], (uint32_t)((n >> 1) & 1), wg)) { ok = false; break; }
+        if (!softmax_wait(s, &s.s_full[sbuf], (uint32_t)((n >> 1) & 1), wg, a.wait_ns)) { ok = false; break; }
         tc::tc_fence_after();
         const bool valid = (long long)t * TC_TILE + row < L;
         const bool first = (t == tlo);
         // PV of the previous tile has completed (its commit preceded this tile's QK commit);
         // waiting keeps the o_done phases in step for every softmax thread
-        if (n > 0 && !softmax_wait(s, &s.o_done, (uint32_t)((n - 1) & 1), wg)) { ok = false; break; }
+        if (n > 0 && !softmax_wait(s, &s.o_done, (uint32_t)((n - 1) & 1), wg, a.wait_ns)) { ok = false; break; }
         tc::tc_fence_after();
         // pass 1: does any score exceed its head's running max by more than the threshold?
         // (TMEM loads are warp-collective: every lane loads, validity only gates the arithmetic)
@@ -646,7 +649,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
       }
       if (!ok) break;
       // ---- epilogue of the segment: wait for its last PV, normalise, write the partial ----
-      if (!softmax_wait(s, &s.o_done, (uint32_t)((n - 1) & 1), wg)) { ok = false; break; }
+      if (!softmax_wait(s, &s.o_done, (uint32_t)((n - 1) & 1), wg, a.wait_ns)) { ok = false; break; }
       tc::tc_fence_after();
 #pragma unroll
       for (int h = 0; h < HW; ++h) {
@@ -699,6 +702,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, Cfg<HG>::TMEM_COLS);
   }
+  // After an abort some of this CTA's partials are missing or stale: mark every partial slot
+  // of its share invalid (lse = NaN), so the affected sequences' outputs come out NaN. The
+  // slots are this CTA's alone; every role has stopped (the barrier above).
+  if (*reinterpret_cast<volatile int*>(&s.abort)) {
+    SegIter jt{s.seg_b0, s.seg_p0, r0, r1};
+    int sb = 0, tlo, thi;
+    while (jt.next(a, &sb, &tlo, &thi))
+      for (int h = tid; h < HG; h += Cfg<HG>::THREADS)
+        a.part_lse[(size_t)(g * a.n_slots + k + sb) * HG + h] = CUDART_NAN_F;
+  }
 }
 
 }  // namespace
@@ -750,6 +763,7 @@ cudaError_t launch_attn_tc(const mla_config& cfg, const mla_cache& cache, const 
   a.n_slots = plan.n_slots;
   a.scale_log2 = cfg.softmax_scale * 1.4426950408889634f;
   a.kv_early = kv_early ? 1 : 0;
+  a.wait_ns = wait_limit_ns();
   const int grid = plan.n_groups * plan.ctas_per_group;
   cudaError_t e;
   switch (plan.heads_per_cta) {

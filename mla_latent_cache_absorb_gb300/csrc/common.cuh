@@ -52,6 +52,12 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return launch_kernel(true, kernel, grid, block, smem, st, static_cast<Args&&>(args)...);
 }
 
+// Bounded waits inside the kernels. A wait for copies or MMAs already issued (a drain before a
+// CTA exits) always gets kWaitDrainNs; a main-loop wait gets the limit current when the kernel
+// was enqueued, wait_limit_ns() (kWaitDrainNs unless mla_set_wait_limit_ns changed it).
+constexpr uint64_t kWaitDrainNs = 200ull * 1000 * 1000;
+uint64_t wait_limit_ns();
+
 __device__ __forceinline__ void set_error(WsHeader* hdr, int code, int seq) {
   if (atomicCAS(&hdr->code, 0, code) == 0) atomicExch(&hdr->seq, seq);
 }
@@ -167,7 +173,9 @@ __device__ __forceinline__ void stage_kv_b_rows(float* dst, int dst_stride, cons
   }
 }
 
-// Logical row t of sequence b -> physical row, or -1 when the page id is out of range.
+// Logical row t of sequence b -> physical row, or -1 when it would lie outside the pool: a
+// negative page id, a page that does not fit in n_phys rows (the product is formed in 64 bits,
+// so no page id can wrap it back into range), or a contiguous row at or past n_phys.
 struct RowMap {
   const int32_t* page_table;
   int32_t page_size;
@@ -175,10 +183,13 @@ struct RowMap {
   int64_t rows_per_seq;
   int64_t n_phys;
   __device__ __forceinline__ int64_t phys(int b, int64_t t) const {
-    if (page_size == 0) return (int64_t)b * rows_per_seq + t;
-    int32_t pg = page_table[(int64_t)b * max_pages + t / page_size];
-    if (pg < 0 || (int64_t)(pg + 1) * page_size > n_phys) return -1;
-    return (int64_t)pg * page_size + t % page_size;
+    if (page_size == 0) {
+      const int64_t r = (int64_t)b * rows_per_seq + t;
+      return (t >= 0 && r < n_phys) ? r : -1;
+    }
+    const int64_t pg = page_table[(int64_t)b * max_pages + t / page_size];
+    if (pg < 0 || (pg + 1) * (int64_t)page_size > n_phys) return -1;
+    return pg * page_size + t % page_size;
   }
   __host__ __device__ __forceinline__ int64_t capacity() const {
     return page_size == 0 ? rows_per_seq : (int64_t)max_pages * page_size;

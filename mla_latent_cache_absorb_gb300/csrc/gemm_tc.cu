@@ -24,7 +24,9 @@ namespace mla {
 namespace {
 
 constexpr int G_THREADS = 128;
-constexpr uint64_t G_WAIT = 200ull * 1000 * 1000;   // a wait gives up after 200 ms
+// Main-loop waits use the launch's wait_ns; drains of a copy or MMAs already issued always get
+// the full kWaitDrainNs, so nothing is in flight when a CTA leaves or frees tensor memory.
+constexpr uint64_t G_DRAIN = kWaitDrainNs;
 constexpr int ABS_TC_BCHUNK = 64;
 constexpr int CMB_TC_BCHUNK = 32;
 constexpr int CMB_TC_THREADS = 512;   // 4 merge items per thread, loads of 2 items x 4 slots in flight
@@ -47,6 +49,7 @@ struct AbsorbTcArgs {
   const int32_t* positions;
   const double* inv_freq;
   WsHeader* hdr;
+  uint64_t wait_ns;
   int B, H, N, R, V, C;
 };
 
@@ -118,9 +121,10 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
   __syncwarp();
   __syncthreads();
   if (tid == 0) {
-    if (!tc::mbar_wait(&bar_w, 0, G_WAIT)) {
+    if (!tc::mbar_wait(&bar_w, 0, a.wait_ns)) {
       failed = 1;
       set_error(a.hdr, MLA_ERR_TIMEOUT, b0);
+      tc::mbar_wait(&bar_w, 0, G_DRAIN);   // the weight copy must land before the CTA leaves
     } else {
       tc::tc_fence_after();
       const uint32_t idesc = tc::idesc_bf16_f32(128, NB, 1, 0);
@@ -189,10 +193,26 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
   }
   __syncwarp();   // lanes 1-31 of warp 0 wait for lane 0
   // warp-uniform: the TMEM loads below are warp-collective
-  const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&bar_mma, 0, G_WAIT) &&
-                                             !*reinterpret_cast<volatile int*>(&failed));
+  bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&bar_mma, 0, a.wait_ns) &&
+                                       !*reinterpret_cast<volatile int*>(&failed));
+  if (!ok) {
+    if (lane == 0 && atomicExch(&failed, 1) == 0) set_error(a.hdr, MLA_ERR_TIMEOUT, b0);
+    // whatever happened, every MMA issued has to complete before tensor memory is freed
+    tc::mbar_wait(&bar_mma, 0, G_DRAIN);
+  }
   tc::tc_fence_after();
-  if (ok) {
+  __syncwarp();
+  __syncthreads();
+  ok = !*reinterpret_cast<volatile int*>(&failed);
+  if (!ok) {
+    // this CTA's fused query entries (its sequences, head h, latent half lh) become NaN, so
+    // their scores, and the sequences' outputs, do too
+    for (int i = tid; i < nb * 256; i += G_THREADS) {
+      const size_t ai = ((size_t)(b0 + i / 256) * a.H + h) * arow + 256 * lh + (i % 256);
+      a.q_abs[ai] = 0x7FC0;
+      a.q_res[ai] = 0;
+    }
+  } else {
     // Lane = latent column, TMEM column = sequence: each warp transposes its 32 x 32 block
     // through shared memory (the B operand's space, free once the MMAs are done) so that every
     // lane then writes 16-byte pieces of 8 consecutive latent columns of one sequence.
@@ -244,6 +264,7 @@ struct CombineTcArgs {
   const uint16_t* q_res;    // bf16 query residual [B][H][C+R] (LSE correction) or nullptr
   float scale;
   WsHeader* hdr;
+  uint64_t wait_ns;
   int H, C, N, V, R, B, hpg, n_slots, max_slots;
 };
 
@@ -428,9 +449,10 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
     __syncthreads();
   }
   if (tid == 0) {
-    if (!tc::mbar_wait(&bar_w, 0, G_WAIT)) {
+    if (!tc::mbar_wait(&bar_w, 0, a.wait_ns)) {
       failed = 1;
       set_error(a.hdr, MLA_ERR_TIMEOUT, b0);
+      tc::mbar_wait(&bar_w, 0, G_DRAIN);   // the weight copy must land before the CTA leaves
     } else {
       tc::tc_fence_after();
       // D[j, 0..31] = W . vc_hi, D[j, 32..63] = W . vc_lo; the epilogue adds the halves
@@ -445,10 +467,23 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
   }
   __syncwarp();
   // warp-uniform: the TMEM loads below are warp-collective; warps 0-3 read the 128 TMEM lanes
-  const bool ok = warp < 4 && __all_sync(0xffffffffu, tc::mbar_wait(&bar_mma, 0, G_WAIT) &&
-                                                           !*reinterpret_cast<volatile int*>(&failed));
+  if (warp < 4 && !__all_sync(0xffffffffu, tc::mbar_wait(&bar_mma, 0, a.wait_ns) &&
+                                               !*reinterpret_cast<volatile int*>(&failed))) {
+    if (lane == 0 && atomicExch(&failed, 1) == 0) set_error(a.hdr, MLA_ERR_TIMEOUT, b0);
+    // every MMA issued has to complete before tensor memory is freed
+    tc::mbar_wait(&bar_mma, 0, G_DRAIN);
+  }
   tc::tc_fence_after();
-  if (ok) {
+  __syncwarp();
+  __syncthreads();
+  const bool ok = !*reinterpret_cast<volatile int*>(&failed);
+  if (!ok) {
+    // the chunk's outputs for head h become NaN
+    for (int i = tid; i < nb * a.V; i += CMB_TC_THREADS)
+      a.out[((size_t)(b0 + i / a.V) * a.H + h) * a.V + (i % a.V)] = CUDART_NAN_F;
+    __syncthreads();
+    if (tid < nb) lse_s[tid] = CUDART_NAN_F;
+  } else if (warp < 4) {
     uint32_t r[32], rl[32];
     tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16), r);
     tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 32, rl);
@@ -495,6 +530,7 @@ cudaError_t launch_absorb_tc(const mla_config& cfg, const void* q, const void* k
   a.positions = positions;
   a.inv_freq = cfg.rope_inv_freq;
   a.hdr = hdr;
+  a.wait_ns = wait_limit_ns();
   a.B = B; a.H = cfg.n_heads; a.N = cfg.qk_nope; a.R = cfg.qk_rope; a.V = cfg.v_head; a.C = cfg.kv_lora;
   cudaError_t e = ensure_smem((const void*)absorb_tc_kernel, ABS_TC_SMEM);
   if (e != cudaSuccess) return e;
@@ -512,6 +548,7 @@ cudaError_t launch_combine_tc(const mla_config& cfg, const DecodePlan& plan, con
   a.meta = meta; a.part_o = part_o; a.part_lse = part_lse; a.out = out; a.lse = lse; a.hdr = hdr;
   a.q_res = static_cast<const uint16_t*>(q_res);
   a.scale = cfg.softmax_scale;
+  a.wait_ns = wait_limit_ns();
   a.H = cfg.n_heads; a.C = cfg.kv_lora; a.N = cfg.qk_nope; a.V = cfg.v_head; a.R = cfg.qk_rope; a.B = B;
   a.hpg = plan.part_hpg; a.n_slots = plan.n_slots;
   a.max_slots = plan.path == PATH_TC ? plan.ctas_per_group : plan.splits;

@@ -58,6 +58,10 @@ static mla_status check_cache(const mla_config* cfg, const mla_cache* cache, int
   return MLA_OK;
 }
 
+static std::atomic<uint64_t> g_wait_ns{kWaitDrainNs};
+
+uint64_t wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+
 int device_sms() {
   static std::atomic<int> cached[64] = {};
   int dev = 0, n = 0;
@@ -180,6 +184,10 @@ const char* mla_status_string(mla_status s) {
 }
 
 int32_t mla_abi_version(void) { return 1; }
+
+uint64_t mla_set_wait_limit_ns(uint64_t ns) {
+  return g_wait_ns.exchange(ns == 0 ? kWaitDrainNs : ns, std::memory_order_relaxed);
+}
 
 mla_status mla_yarn_inv_freq(int32_t rope_dim, double theta, double factor, int32_t orig_max_pos,
                              double beta_fast, double beta_slow, double* out_host) {

@@ -12,7 +12,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <mutex>
 
 #include "mla.h"
 
@@ -23,26 +22,18 @@ namespace {
 // 152-SM device; mla_decode_workspace_size says what a given (cfg, B) needs.
 __device__ __align__(256) unsigned char g_scratch[MLA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_lock;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of g_scratch in the current device's context, looked up once per device.
+// Device address of g_scratch in the current device's context. Looked up on every call, not
+// cached: cudaGetSymbolAddress allocates nothing and is cheap once the module is loaded, and
+// a cached address would go stale if the context were torn down and recreated (after a
+// cudaDeviceReset the module can load at another address).
 mla_status scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> guard(g_lock);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      (void)cudaGetLastError();   // leave no error behind for the caller's next CUDA call
-      return MLA_ERR_CUDA;
-    }
-    g_scratch_addr[dev] = p;
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
+  if (e != cudaSuccess || p == nullptr) {
+    (void)cudaGetLastError();   // leave no error behind for the caller's next CUDA call
+    return MLA_ERR_CUDA;
   }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return MLA_OK;
 }
 

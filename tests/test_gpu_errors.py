@@ -47,7 +47,8 @@ def test_bad_seq_len_sets_error_and_nan_only_for_that_sequence(bad_len):
 
 
 @gpu
-@pytest.mark.parametrize("bad_page", [-1, 10 ** 7])
+# 2**31 - 1: the largest int32 page id, whose end row overflows 32-bit arithmetic
+@pytest.mark.parametrize("bad_page", [-1, 10 ** 7, 2 ** 31 - 1])
 def test_bad_page_id_sets_error(bad_page):
     from mla_latent_cache_absorb_gb300 import binding as L
     torch, prob, ds = _setup(W["ragged_paged_b64"].with_(B=3, H=16, context=("uniform", 200, 400)))

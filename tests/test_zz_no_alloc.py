@@ -112,3 +112,27 @@ def test_noalloc_refuses_a_batch_the_array_cannot_hold():
     assert st == L.STATUS_CODE["MLA_ERR_WORKSPACE"]
     torch.cuda.synchronize()
     assert sentinel.tolist() == [123, 123]          # nothing was enqueued
+
+
+@pytest.mark.gpu
+def test_noalloc_allocates_no_device_memory():
+    """The call's promise itself: after a first call (which may load the library's module on
+    this device), further calls change neither the caching allocator's bytes in use nor the
+    device's free memory."""
+    import torch
+    from mla_latent_cache_absorb_gb300 import binding as L
+    ds = _problem("v3_b32_t4096", B=5, context=("uniform", 200, 1500))
+    L.check(ds.append(), "mla_cache_append")
+    out, lse = torch.empty_like(ds.out), torch.empty_like(ds.lse)
+    err = torch.zeros(2, dtype=torch.int32, device=ds.device)
+    L.check(_noalloc(ds, out, lse, err), "mla_decode_attn_noalloc")
+    torch.cuda.synchronize()
+    used0 = torch.cuda.memory_allocated(ds.device)
+    free0, _ = torch.cuda.mem_get_info(ds.device)
+    for _ in range(3):
+        L.check(_noalloc(ds, out, lse, err), "mla_decode_attn_noalloc")
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info(ds.device)
+    assert torch.cuda.memory_allocated(ds.device) == used0
+    assert free1 == free0, f"device free memory changed by {free0 - free1} bytes"
+    assert err.tolist() == [0, 0]
