@@ -213,8 +213,12 @@ def peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
+# attention kernel of a plan (mla_plan_info.kernel) -> its source file and kernel name
+KERNEL_FILE = {0: "attn_simt", 1: "attn_tc", 2: "attn_pair"}
+
+
 def kernel_source_sha(kernel: int) -> str:
-    f = os.path.join(ROOT, "mla_latent_cache_absorb_gb300", "csrc", "attn_tc.cu" if kernel == 1 else "attn_simt.cu")
+    f = os.path.join(ROOT, "mla_latent_cache_absorb_gb300", "csrc", KERNEL_FILE[kernel] + ".cu")
     return hashlib.sha256(open(f, "rb").read()).hexdigest()[:16]
 
 
@@ -225,7 +229,7 @@ def ncu_traffic(kernel: int, workload: str):
         d = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
     except (OSError, ValueError):
         return None
-    ent = d.get(f"{'attn_tc' if kernel == 1 else 'attn_simt'}:{workload}")
+    ent = d.get(f"{KERNEL_FILE[kernel]}:{workload}")
     if not ent or ent.get("source_sha") != kernel_source_sha(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
@@ -402,7 +406,8 @@ def run_ours(args, rank, world, device, workload, K, W, with_e2e=True, with_cloc
                       f"launching stream; the attention launch of each graph's first step bracketed "
                       f"by in-graph events",
             "gpus": f"replicas x{world}" if world > 1 else "single GPU",
-            "attention_kernel": "tcgen05" if plan.kernel == 1 else "cuda-core",
+            "attention_kernel": {0: "cuda-core", 1: "tcgen05, one CTA per head group",
+                                 2: "tcgen05, SM pairs (clusters of two CTAs)"}[plan.kernel],
             "heads_per_cta": plan.heads_per_cta, "splits": plan.splits,
             "rows_per_split": plan.rows_per_split,
         },
@@ -410,7 +415,7 @@ def run_ours(args, rank, world, device, workload, K, W, with_e2e=True, with_cloc
         "hbm_gbs": work["bytes"] / step_s / 1e9,
         "step_roofline_frac": max(work["flops"] / (tf_burst * 1e12), work["bytes"] / (hbm * 1e9)) / step_s,
         "roofline": {
-            "kernel": "attn_tc (split attention)" if plan.kernel == 1 else "attn_simt (split attention)",
+            "kernel": f"{KERNEL_FILE[plan.kernel]} (split attention)",
             "bound": "hbm", "achieved": attn_gbs, "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm,
             "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback",
             "bytes_per_launch": work["attn_bytes"], "avg_launch_us": attn_avg_ms * 1e3,

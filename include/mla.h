@@ -158,8 +158,12 @@ mla_status mla_decode_workspace_size(const mla_config* cfg, int32_t B, size_t* b
 /* The split plan mla_decode_attn uses for (cfg, B) on the current device. */
 typedef struct mla_plan_info {
   int32_t kernel;          /* attention kernel: 0 = CUDA-core (any dims, f32 or bf16),
-                              1 = tcgen05 tensor-core (bf16 rows of 576 = 512 + 64) */
-  int32_t heads_per_cta;   /* heads that share each staged row tile */
+                              1 = tcgen05 tensor-core (bf16 rows of 576 = 512 + 64), one CTA
+                              per SM and head group, 128-row tiles,
+                              2 = tcgen05 on SM pairs (bf16 rows of 576, exactly 128 heads):
+                              a cluster of two CTAs shares each 64-row tile, one latent half
+                              each; `splits` then counts CTA pairs */
+  int32_t heads_per_cta;   /* heads that share each staged row tile (kernel 2: per CTA pair) */
   int32_t head_groups;     /* ceil(H / heads_per_cta) */
   int32_t splits;          /* row splits per sequence (partials kept in the workspace) */
   int64_t rows_per_split;  /* rows each split covers (a multiple of the row tile) */
@@ -219,7 +223,8 @@ mla_status mla_cache_append(const mla_config* cfg, const mla_cache* cache,
  *   lse        device [B, H] float32 natural-log sum-exp of the scaled scores, or NULL.
  * Scores are s_t = softmax_scale * ([q' ; q_pe] . row_t) with q' = W_UK,h^T q_nope.
  * Launch order: when the cache capacity gives each attention CTA at least four 128-row tiles
- * (B * ceil(capacity / 128) >= 4 * the plan's ctas_per_group, tensor-core path), the first
+ * (B * ceil(capacity / 128) >= 4 * the plan's splits, kernel 1) or each CTA pair at least eight
+ * 64-row tiles (B * ceil(capacity / 64) >= 8 * splits, kernel 2), the first
  * kernel (the absorb) is launched in plain stream order: it starts only after all earlier
  * work on the stream, a cache append above all, has completed, and the attention kernel
  * after it streams cache rows while the absorb still runs, waiting only for the fused

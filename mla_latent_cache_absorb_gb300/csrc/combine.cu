@@ -265,7 +265,7 @@ cudaError_t launch_combine(const mla_config& cfg, const DecodePlan& plan, const 
   a.H = cfg.n_heads; a.C = cfg.kv_lora; a.N = cfg.qk_nope; a.V = cfg.v_head; a.R = cfg.qk_rope; a.B = B;
   a.hpg = plan.part_hpg; a.n_slots = plan.n_slots;
   // most slots one sequence can span: splits (CUDA-core path) or CTAs per group (tensor path)
-  a.max_slots = plan.path == PATH_TC ? plan.ctas_per_group : plan.splits;
+  a.max_slots = plan.path != PATH_SIMT ? plan.ctas_per_group : plan.splits;
   // V-slices per head: enough CTAs to cover the SMs, but every slice merges the partials again
   const int chunks = (cfg.v_head + CMB_VJ - 1) / CMB_VJ;
   const int64_t base_ctas = (int64_t)cfg.n_heads * ((B + CMB_BC - 1) / CMB_BC);

@@ -250,22 +250,23 @@ struct DecodePlan {
   int splits;            // CUDA-core path: row splits per sequence
   int64_t chunk_rows;    // CUDA-core path: rows per split (a multiple of its row tile)
   int64_t capacity;      // maximum rows a sequence can attend
-  int ctas_per_group;    // tensor-core path: CTAs sharing one head group's tile list
+  int ctas_per_group;    // tensor-core paths: CTAs (pair path: CTA pairs) sharing one tile list
   // partials: part_o[g][slot][hh][C], part_lse[g][slot][hh] for part_groups x n_slots slots of
   // part_hpg heads; meta[b] = {first slot, slot count} of sequence b (count 0: invalid length)
   int part_groups, part_hpg, n_slots;
   // q_res: bf16 rounding residual of the fused query rows (bf16 activations only)
   size_t off_qabs, off_qres, off_po, off_plse, off_meta, total;
 };
-enum { PATH_SIMT = 0, PATH_TC = 1 };
+enum { PATH_SIMT = 0, PATH_TC = 1, PATH_PAIR = 2 };
 
 // True when the CUDA driver's tensor-map encoder could be found (looked up once per process).
 bool tma_encoder_available();
 // 2D bf16 TMA map over a row-major [rows, inner] tensor (inner elements contiguous) with
-// boxes of box_inner x box_rows and the 128-byte swizzle. False when the CUDA driver entry point
-// is unavailable or the encoding is rejected.
+// boxes of box_inner x box_rows and the 128-byte swizzle (64-byte with swizzle_bytes = 64, for
+// boxes 32 elements wide). False when the CUDA driver entry point is unavailable or the encoding
+// is rejected.
 bool make_map_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
-                      uint32_t box_rows);
+                      uint32_t box_rows, int swizzle_bytes = 128);
 
 // Raise a kernel's dynamic shared memory limit once per (kernel, device), so that repeated
 // launches (and launches under stream capture) make no attribute calls.
@@ -291,6 +292,13 @@ cudaError_t launch_attn_tc(const mla_config& cfg, const mla_cache& cache, const 
                            const int32_t* seq_lens, const void* q_abs, const void* q_res, float* part_o,
                            float* part_lse, int32_t* meta, int B, WsHeader* hdr, bool kv_early, cudaStream_t st);
 bool attn_tc_supported(const mla_config& cfg);
+// 128 heads on a pair of SMs (a cluster of two CTAs, 64-row tiles)
+bool attn_pair_supported(const mla_config& cfg);
+// cluster pairs of the pair kernel that fit on the current device at once, or -1
+int attn_pair_max_pairs();
+cudaError_t launch_attn_pair(const mla_config& cfg, const mla_cache& cache, const DecodePlan& plan,
+                             const int32_t* seq_lens, const void* q_abs, const void* q_res, float* part_o,
+                             float* part_lse, int32_t* meta, int B, WsHeader* hdr, bool kv_early, cudaStream_t st);
 int tc_heads_per_cta(int H);
 bool absorb_tc_supported(const mla_config& cfg, int B);
 bool combine_tc_supported(const mla_config& cfg, int B);

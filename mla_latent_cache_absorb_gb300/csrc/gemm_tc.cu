@@ -551,7 +551,7 @@ cudaError_t launch_combine_tc(const mla_config& cfg, const DecodePlan& plan, con
   a.wait_ns = wait_limit_ns();
   a.H = cfg.n_heads; a.C = cfg.kv_lora; a.N = cfg.qk_nope; a.V = cfg.v_head; a.R = cfg.qk_rope; a.B = B;
   a.hpg = plan.part_hpg; a.n_slots = plan.n_slots;
-  a.max_slots = plan.path == PATH_TC ? plan.ctas_per_group : plan.splits;
+  a.max_slots = plan.path != PATH_SIMT ? plan.ctas_per_group : plan.splits;
   const int smem = CMB_TC_WSMEM + 1024 + CMB_TC_BCHUNK * (64 + a.max_slots) * (int)sizeof(float);
   cudaError_t e = ensure_smem((const void*)combine_tc_kernel, smem);
   if (e != cudaSuccess) return e;

@@ -84,7 +84,23 @@ static mla_status make_plan(const mla_config& cfg, int B, DecodePlan* p) {
   if (sms <= 0) return MLA_ERR_CUDA;
   std::memset(p, 0, sizeof(*p));
   p->capacity = cfg.page_size == 0 ? cfg.rows_per_seq : (int64_t)cfg.max_pages_per_seq * cfg.page_size;
-  if (attn_tc_supported(cfg)) {
+  const int max_pairs = attn_pair_supported(cfg) ? attn_pair_max_pairs() : -1;
+  if (max_pairs > 0) {
+    // 128 heads: one cluster of two CTAs per SM pair, the 64-row tile list split evenly over
+    // the pairs that fit on the device at once
+    p->path = PATH_PAIR;
+    p->heads_per_cta = cfg.n_heads;
+    p->n_groups = 1;
+    p->ctas_per_group = max_pairs < sms / 2 ? max_pairs : sms / 2;
+    if (p->ctas_per_group < 1) p->ctas_per_group = 1;
+    const int64_t max_tiles = (int64_t)B * ((p->capacity + 63) / 64);
+    if (max_tiles < p->ctas_per_group) p->ctas_per_group = (int)max_tiles;
+    p->splits = p->ctas_per_group;
+    p->chunk_rows = 0;
+    p->part_groups = 1;
+    p->part_hpg = cfg.n_heads;
+    p->n_slots = p->ctas_per_group + B - 1;
+  } else if (attn_tc_supported(cfg)) {
     // tensor-core path: one CTA per SM, each head group's tile list split evenly over its CTAs
     p->path = PATH_TC;
     p->heads_per_cta = tc_heads_per_cta(cfg.n_heads);
@@ -375,6 +391,9 @@ mla_status enqueue_partial(const mla_config* cfg, const DecodePlan& plan, const 
   float* pl = reinterpret_cast<float*>(ws + plan.off_plse);
   int32_t* meta = reinterpret_cast<int32_t*>(ws + plan.off_meta);
   const void* q_res = cfg->act_dtype == MLA_BF16 ? ws + plan.off_qres : nullptr;
+  if (plan.path == PATH_PAIR)
+    return cuda_status(
+        launch_attn_pair(*cfg, *cache, plan, seq_lens, ws + plan.off_qabs, q_res, po, pl, meta, B, hdr, kv_early, s));
   if (plan.path == PATH_TC)
     return cuda_status(
         launch_attn_tc(*cfg, *cache, plan, seq_lens, ws + plan.off_qabs, q_res, po, pl, meta, B, hdr, kv_early, s));
@@ -388,7 +407,7 @@ mla_status enqueue_combine(const mla_config* cfg, const DecodePlan& plan, const 
   const float* po = reinterpret_cast<const float*>(ws + plan.off_po);
   const float* pl = reinterpret_cast<const float*>(ws + plan.off_plse);
   // the tensor-core attention scores used bf16 latent queries: correct the LSE for the residual
-  const void* q_res = plan.path == PATH_TC ? ws + plan.off_qres : nullptr;
+  const void* q_res = plan.path != PATH_SIMT ? ws + plan.off_qres : nullptr;
   if (combine_tc_supported(*cfg, B))
     return cuda_status(launch_combine_tc(*cfg, plan, kv_b, meta, po, pl, q_res, out, lse, B,
                                          reinterpret_cast<WsHeader*>(ws), s));
@@ -454,12 +473,15 @@ mla_status mla_decode_attn(const mla_config* cfg, const void* q, const void* kv_
   st = check_cache(cfg, cache, B);
   if (st != MLA_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // Long attentions (at the cache's capacity, at least four 128-row tiles per CTA): the absorb
-  // starts once everything before it on the stream, the cache append above all, has completed,
-  // and the attention then streams cache rows while the absorb still runs. Short ones keep the
-  // absorb's own overlap with the kernels before it, which is worth more to them.
-  const int64_t max_tiles = (int64_t)B * ((plan.capacity + 127) / 128);
-  const bool early = plan.path == PATH_TC && max_tiles >= 4 * (int64_t)plan.ctas_per_group;
+  // Long attentions (at the cache's capacity, at least four 128-row tiles per CTA, or eight
+  // 64-row tiles per CTA pair): the absorb starts once everything before it on the stream, the
+  // cache append above all, has completed, and the attention then streams cache rows while the
+  // absorb still runs. Short ones keep the absorb's own overlap with the kernels before it,
+  // which is worth more to them.
+  const int64_t tiles128 = (int64_t)B * ((plan.capacity + 127) / 128);
+  const int64_t tiles64 = (int64_t)B * ((plan.capacity + 63) / 64);
+  const bool early = (plan.path == PATH_TC && tiles128 >= 4 * (int64_t)plan.ctas_per_group) ||
+                     (plan.path == PATH_PAIR && tiles64 >= 8 * (int64_t)plan.ctas_per_group);
   st = enqueue_absorb(cfg, plan, q, kv_b, positions, B, workspace, early, s);
   if (st != MLA_OK) return st;
   st = enqueue_partial(cfg, plan, cache, seq_lens, B, workspace, early, s);

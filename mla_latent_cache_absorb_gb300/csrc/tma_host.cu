@@ -22,13 +22,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool make_map_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
-                      uint32_t box_rows) {
+                      uint32_t box_rows, int swizzle_bytes) {
   // The encoding depends only on these arguments, so recent ones are kept per host thread: a
   // decode step encodes up to five maps, mostly the same ones call after call.
   struct Entry {
     const void* base;
     uint64_t inner, rows;
     uint32_t box_inner, box_rows;
+    int swizzle;
     CUtensorMap map;
   };
   constexpr int kEntries = 16;
@@ -37,11 +38,12 @@ bool make_map_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t
   for (int i = 0; i < n_used; ++i) {
     const Entry& en = cache[i];
     if (en.base == base && en.inner == inner && en.rows == rows && en.box_inner == box_inner &&
-        en.box_rows == box_rows) {
+        en.box_rows == box_rows && en.swizzle == swizzle_bytes) {
       *m = en.map;
       return true;
     }
   }
+  if (swizzle_bytes != 128 && swizzle_bytes != 64) return false;
   auto enc = encode_fn();
   if (enc == nullptr) return false;
   cuuint64_t dims[2] = {inner, rows};
@@ -49,10 +51,11 @@ bool make_map_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t es[2] = {1, 1};
   if (enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return false;
-  cache[next] = Entry{base, inner, rows, box_inner, box_rows, *m};
+  cache[next] = Entry{base, inner, rows, box_inner, box_rows, swizzle_bytes, *m};
   next = (next + 1) % kEntries;
   if (n_used < kEntries) ++n_used;
   return true;
