@@ -40,7 +40,8 @@
 // epilogue. The own-head warps and the score senders also load each segment's latent queries
 // into tensor memory. Of warps 8-11, one issues the TMA loads and one owns tensor memory and
 // issues the MMAs (one thread), polling and issuing whichever of the next QK^T and the next PV is
-// ready; both sit on the sub-partitions of the peer-head warps. Every wait is bounded; on a timeout the CTA records MLA_ERR_TIMEOUT and tells
+// ready; both sit on the sub-partitions of the peer-head warps. A third forwards the score grants
+// to the peer, so that no softmax thread waits on a remote arrival. Every wait is bounded; on a timeout the CTA records MLA_ERR_TIMEOUT and tells
 // its peer, every role stops, transfers in flight in both directions are drained, and tensor
 // memory is freed.
 #include "common.cuh"
@@ -73,6 +74,9 @@ constexpr int AP_THREADS = 384;
 // competes with this CTA's softmax warps (which sit on the sub-partitions of their lane quarters)
 __device__ __forceinline__ int ap_tma_warp(uint32_t c) { return c == 0 ? 10 : 8; }
 __device__ __forceinline__ int ap_mma_warp(uint32_t c) { return c == 0 ? 11 : 9; }
+// one of the two remaining warps forwards the score grants: a remote arrival with release
+// semantics takes the issuing thread about half a microsecond, which must not hold up the softmax
+__device__ __forceinline__ int ap_fwd_warp(uint32_t c) { return c == 0 ? 8 : 10; }
 constexpr uint32_t AP_S_COL = 0;     // S: two buffers of 64 columns
 constexpr uint32_t AP_Q_COL = 128;   // latent queries: 128 columns of bf16 pairs (256 latent)
 constexpr uint32_t AP_O_COL = 256;   // O: 256 columns
@@ -104,6 +108,7 @@ struct __align__(16) PairSmem {
   uint64_t s_full[2], s_free[2];
   uint64_t srecv_full[2];   // the peer's partial scores of tile n landed in buffer n & 1
   uint64_t srecv_grant[2];  // the peer has read buffer n & 1 of our partial scores
+  uint64_t srecv_read[2];   // this CTA's softmax has read the peer's scores of tile n (buffer n & 1)
   uint64_t pfree[2];        // PV of tile n in both CTAs done: P buffer n & 1 free (two arrivals)
   uint64_t px_full[2];      // the peer's rows of P and its factors for tile n landed (buffer n & 1)
   uint64_t l_full[2];       // the peer's 1/l of segment j landed in l_recv[j & 1]
@@ -317,6 +322,8 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
         tc::mbar_arrive_expect_tx(&s.px_full[i], AP_PX_BYTES);
         tc::mbar_arrive_expect_tx(&s.l_full[i], 64 * 4);
       }
+      tc::mbar_init(&s.srecv_read[0], 1);
+      tc::mbar_init(&s.srecv_read[1], 1);
       tc::mbar_init(&s.o_full, 1);
       tc::mbar_init(&s.o_empty, AP_N_OWN + AP_N_RECV);
       tc::mbar_init(&s.mma_fin, 1);
@@ -550,6 +557,29 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
       tc::mma_commit(&s.mma_fin);
       tc::mbar_wait(&s.mma_fin, 0, AP_DRAIN);
     }
+  } else if (warp == ap_fwd_warp(c)) {
+    // ================================ score-grant forwarder ================================
+    // once this CTA's softmax has read the peer's partial scores of tile n out of buffer n & 1,
+    // arm that buffer for tile n + 2 and tell the peer it may send into it
+    if (lane == 0) {
+      const uint32_t pr_srecv_grant = tc::mapa(tc::smem_u32(&s.srecv_grant[0]), peer);
+      int sb = 0, tlo, thi;
+      long long n = 0;
+      bool ok = true;
+      while (ok && it.next(a, &sb, &tlo, &thi)) {
+        fail_b = sb;
+        for (int t = tlo; t < thi; ++t, ++n) {
+          const int b = (int)(n & 1);
+          if (!wait_bar(s, &s.srecv_read[b], (uint32_t)((n >> 1) & 1), a.wait_ns)) {
+            ok = false;
+            break;
+          }
+          tc::mbar_arrive_expect_tx(&s.srecv_full[b], AP_SBUF);
+          tc::mbar_arrive_remote(pr_srecv_grant + 8 * b);
+        }
+      }
+      if (!ok) pair_fail(s, a.hdr, fail_b, peer);
+    }
   } else if (warp < 8) {
     // ======================= tensor-memory lane quarters: softmax and exchange =======================
     if (a.kv_early) pdl_wait();
@@ -612,7 +642,6 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
       const uint32_t pr_px_full = tc::mapa(tc::smem_u32(&s.px_full[0]), peer);
       const uint32_t pr_l = tc::mapa(tc::smem_u32(&s.l_recv[0][0]), peer);
       const uint32_t pr_l_full0 = tc::mapa(tc::smem_u32(&s.l_full[0]), peer);
-      const uint32_t pr_srecv_grant = tc::mapa(tc::smem_u32(&s.srecv_grant[0]), peer);
       const bool leader = hl == 0 && k == 0;
       int n_sent = 0, n_got = 0, l_sent = 0;
       float m = -CUDART_INF_F, l = 0.f;                  // running max (log2 units), this half's sum
@@ -680,10 +709,7 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
           }
           s.xch[k][hl] = mt;
           group_bar(AP_BAR_OWN, AP_N_OWN);   // the received scores are read; both halves' maxima are in
-          if (leader) {
-            tc::mbar_arrive_expect_tx(&s.srecv_full[b], AP_SBUF);
-            tc::mbar_arrive_remote(pr_srecv_grant + 8 * b);
-          }
+          if (leader) tc::mbar_arrive(&s.srecv_read[b]);   // the forwarder re-arms and grants
           mt = fmaxf(s.xch[0][hl], s.xch[1][hl]);   // the same in both halves: same decisions
           float alpha = 1.f;
           if (first || mt > m + AP_RESCALE) {
