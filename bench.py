@@ -63,6 +63,8 @@ def step_work(prob):
     rows = int(np.sum(prob.seq_lens))
     if wl.kv_b == "q8_0":
         kvb = H * (N + V) * (C // 32) * 34
+    elif wl.kv_b == "q4_affine":
+        kvb = H * (N + V) * (C // 2 + (C // 64) * 4)
     else:
         kvb = H * (N + V) * C * (2 if wl.kv_b == "bf16" else 4)
     attn_flops = rows * H * (2 * (C + R) + 2 * C)

@@ -71,7 +71,14 @@ typedef enum mla_dtype {
   MLA_BF16 = 1,
   /* Q8_0: 34-byte blocks of 32 elements along a row: an fp16 scale d (little endian)
    * then 32 int8 codes q; element value d*q. Weights only (kv_b). */
-  MLA_Q8_0 = 2
+  MLA_Q8_0 = 2,
+  /* 4-bit affine, groups of 64 (moeflux mla_attn_forward.rs: a 4-bit projection is
+   * weight + scales + biases, group size 64; gpu_matvec.rs MatvecSpec: packed weight,
+   * bf16 scales, bf16 biases). One buffer holding, for an [rows, cols] matrix: the codes
+   * as rows*cols/8 little-endian uint32 words (row-major; code j of a word, bits 4j..4j+3,
+   * is column 8w+j), then scales [rows, cols/64] bf16, then biases [rows, cols/64] bf16.
+   * Element value scale*q + bias, q in 0..15. Weights only (kv_b); cols % 64 == 0. */
+  MLA_Q4_AFFINE = 3
 } mla_dtype;
 
 typedef struct mla_config {
@@ -81,7 +88,7 @@ typedef struct mla_config {
   int32_t qk_rope;            /* R >= 2, even */
   int32_t v_head;             /* V >= 1 */
   int32_t act_dtype;          /* mla_dtype, F32 or BF16: q and the cache rows */
-  int32_t kv_b_dtype;         /* mla_dtype, F32, BF16 or Q8_0 */
+  int32_t kv_b_dtype;         /* mla_dtype, F32, BF16, Q8_0 or Q4_AFFINE */
   float softmax_scale;        /* mscale^2 / sqrt(N+R); see mla_softmax_scale */
   float rms_eps;              /* RMSNorm epsilon of the latent norm (append only) */
   int32_t page_size;          /* 0: contiguous rows per sequence; else rows per page (>= 1) */
@@ -132,9 +139,10 @@ double mla_yarn_mscale(double factor, double coeff);
 float mla_softmax_scale(int32_t qk_nope, int32_t qk_rope, double mscale);
 
 /* The kv_b contract (turbospark deepseek2 attn.rs, validate_q8_0_matrix, generalised to
- * all three weight dtypes): shape must be (heads*(nope+v_dim), kv_lora); for Q8_0
- * kv_lora must be a non-zero multiple of 32; size_bytes must equal the packed size,
- * computed with overflow-checked multiplies. Returns OK, BAD_KV_B or INVALID_ARG. */
+ * all four weight dtypes): shape must be (heads*(nope+v_dim), kv_lora); for Q8_0
+ * kv_lora must be a non-zero multiple of 32, for Q4_AFFINE of 64; size_bytes must equal
+ * the packed size, computed with overflow-checked multiplies. Returns OK, BAD_KV_B or
+ * INVALID_ARG. */
 mla_status mla_validate_kv_b(int32_t dtype, int64_t rows, int64_t cols, uint64_t size_bytes,
                              int32_t heads, int32_t nope, int32_t kv_lora, int32_t v_dim);
 

@@ -13,7 +13,7 @@ from ctypes import POINTER, c_char_p, c_double, c_float, c_int32, c_int64, c_siz
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmla.so")
 
-MLA_F32, MLA_BF16, MLA_Q8_0 = 0, 1, 2
+MLA_F32, MLA_BF16, MLA_Q8_0, MLA_Q4_AFFINE = 0, 1, 2, 3
 STATUS = {
     0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "MLA_ERR_POS_MISMATCH",
     4: "MLA_ERR_CACHE_FULL", 5: "MLA_ERR_WORKSPACE", 6: "MLA_ERR_TIMEOUT", 7: "MLA_ERR_CUDA",

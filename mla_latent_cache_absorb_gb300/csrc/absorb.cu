@@ -72,7 +72,8 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
     if (i < nb0 * N) qv[u] = Act<DT>::load(q, ((int64_t)(i / N) * H + h) * qrow + i % N);
   }
   const int64_t wrow0 = (int64_t)h * (N + V);
-  stage_kv_b_rows(w_s, ABS_COLS, kv_b, cfg.kv_b_dtype, wrow0, N, c0, min(ABS_COLS, C - c0), C, ABS_THREADS);
+  stage_kv_b_rows(w_s, ABS_COLS, kv_b, cfg.kv_b_dtype, wrow0, N, c0, min(ABS_COLS, C - c0), C, ABS_THREADS,
+                  (int64_t)cfg.n_heads * (cfg.qk_nope + cfg.v_head));
   pdl_wait();   // the fused query rows may still be read by the previous step's attention
 
   // q_pe: rotate at positions[b] (or copy when positions == NULL) into the row's tail

@@ -106,7 +106,9 @@ __global__ void __launch_bounds__(CMB_THREADS, 2) combine_kernel(CombineArgs a) 
 
   // W_UV rows of the first 32-output chunk (the rest follow after the merge)
   const int64_t wrow0 = (int64_t)h * (a.N + a.V) + a.N;
-  stage_kv_b_rows(w_s, 4 * C4, a.kv_b, a.kv_b_dtype, wrow0 + jbeg, min(CMB_VJ, jend - jbeg), 0, C, C, CMB_THREADS);
+  const int64_t kv_rows = (int64_t)a.H * (a.N + a.V);
+  stage_kv_b_rows(w_s, 4 * C4, a.kv_b, a.kv_b_dtype, wrow0 + jbeg, min(CMB_VJ, jend - jbeg), 0, C, C, CMB_THREADS,
+                  kv_rows);
   pdl_wait();   // the partials and meta come from the attention kernel
   // Loads that do not depend on one another go out together: each warp's sequence metadata
   // and the query residual (for the first-order LSE correction below); the partial LSEs follow
@@ -238,7 +240,7 @@ __global__ void __launch_bounds__(CMB_THREADS, 2) combine_kernel(CombineArgs a) 
     const int nj = min(CMB_VJ, jend - j0);
     if (j0 != jbeg) {
       __syncthreads();   // the previous chunk's dot products are done with w_s
-      stage_kv_b_rows(w_s, 4 * C4, a.kv_b, a.kv_b_dtype, wrow0 + j0, nj, 0, C, C, CMB_THREADS);
+      stage_kv_b_rows(w_s, 4 * C4, a.kv_b, a.kv_b_dtype, wrow0 + j0, nj, 0, C, C, CMB_THREADS, kv_rows);
       __syncthreads();
     }
     if (nb == 1) {

@@ -84,25 +84,35 @@ template <> struct Act<MLA_BF16> {
   static __device__ __forceinline__ float rounded(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 };
 
-// One kv_b element (row r, column c) in any weight dtype. Q8_0: fp16 scale then 32 codes
-// per 34-byte block; value = scale * code (exact in float32).
-__device__ __forceinline__ float kv_b_load(const void* kv_b, int dtype, int64_t r, int c, int C) {
+// One kv_b element (row r, column c) in any weight dtype; `rows` is the matrix's row count (the
+// 4-bit format keeps its scales and biases after all the codes). Q8_0: fp16 scale then 32
+// codes per 34-byte block, value = scale * code (exact in float32). Q4_AFFINE: 8 codes per
+// little-endian 32-bit word (code j in bits 4j..4j+3), a bf16 scale and bias per 64 columns,
+// value = scale * code + bias.
+__device__ __forceinline__ float kv_b_load(const void* kv_b, int dtype, int64_t r, int c, int C, int64_t rows) {
   if (dtype == MLA_BF16) {
     return bf16_bits_to_f32(static_cast<const uint16_t*>(kv_b)[r * C + c]);
   } else if (dtype == MLA_F32) {
     return static_cast<const float*>(kv_b)[r * C + c];
-  } else {
+  } else if (dtype == MLA_Q8_0) {
     const uint8_t* blk = static_cast<const uint8_t*>(kv_b) + r * (int64_t)(C / 32) * 34 + (c / 32) * 34;
     uint16_t dbits = static_cast<uint16_t>(blk[0]) | (static_cast<uint16_t>(blk[1]) << 8);
     float d = __half2float(__ushort_as_half(dbits));
     return d * static_cast<float>(static_cast<int8_t>(blk[2 + (c & 31)]));
+  } else {
+    const uint32_t w = static_cast<const uint32_t*>(kv_b)[(r * C + c) / 8];
+    const uint16_t* sb = reinterpret_cast<const uint16_t*>(static_cast<const uint8_t*>(kv_b) + rows * (int64_t)(C / 2));
+    const int64_t g = r * (C / 64) + c / 64;
+    return fmaf(bf16_bits_to_f32(sb[g]), static_cast<float>((w >> (4 * (c & 7))) & 15u),
+                bf16_bits_to_f32(sb[rows * (C / 64) + g]));
   }
 }
 
 // Eight consecutive kv_b elements of row r from column c as float32 (zero past ncols_left):
-// one 16-byte load for bf16, two for f32, the 8 codes plus the block scale for Q8_0.
+// one 16-byte load for bf16, two for f32, the 8 codes plus the block scale for Q8_0, one word
+// plus its group's scale and bias for Q4_AFFINE.
 __device__ __forceinline__ void kv_b_load8(float v[8], const void* kv_b, int dtype, int64_t r, int c,
-                                           int ncols_left, int C) {
+                                           int ncols_left, int C, int64_t rows) {
   if (ncols_left >= 8 && (C % 8) == 0) {
     if (dtype == MLA_BF16) {
       const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(kv_b) + r * C + c);
@@ -116,7 +126,7 @@ __device__ __forceinline__ void kv_b_load8(float v[8], const void* kv_b, int dty
       const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(kv_b) + r * C + c);
       const float4 a = src[0], b = src[1];
       v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    } else {
+    } else if (dtype == MLA_Q8_0) {
       // a block starts at an even byte offset (34 bytes each), so the scale and the codes are
       // read as 16-bit words (little endian: the lower byte is the lower element)
       const uint16_t* blk = reinterpret_cast<const uint16_t*>(static_cast<const uint8_t*>(kv_b) +
@@ -129,18 +139,28 @@ __device__ __forceinline__ void kv_b_load8(float v[8], const void* kv_b, int dty
         v[2 * e] = d * static_cast<float>(static_cast<int8_t>(w & 0xFF));
         v[2 * e + 1] = d * static_cast<float>(static_cast<int8_t>(w >> 8));
       }
+    } else {
+      const uint32_t w = static_cast<const uint32_t*>(kv_b)[(r * C + c) / 8];
+      const uint16_t* sb =
+          reinterpret_cast<const uint16_t*>(static_cast<const uint8_t*>(kv_b) + rows * (int64_t)(C / 2));
+      const int64_t g = r * (C / 64) + c / 64;
+      const float sc = bf16_bits_to_f32(sb[g]), bi = bf16_bits_to_f32(sb[rows * (C / 64) + g]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = fmaf(sc, static_cast<float>((w >> (4 * e)) & 15u), bi);
     }
   } else {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = (e < ncols_left) ? kv_b_load(kv_b, dtype, r, c + e, C) : 0.f;
+    for (int e = 0; e < 8; ++e) v[e] = (e < ncols_left) ? kv_b_load(kv_b, dtype, r, c + e, C, rows) : 0.f;
   }
 }
 
 // Stage kv_b rows [r0, r0 + nrows) x columns [c0, c0 + ncols) as float32 into dst (row stride
 // dst_stride floats; columns past ncols, up to a multiple of 8, are zero), in items of 8
-// columns; each thread issues the loads of four items before it stores any of them.
+// columns; each thread issues the loads of four items before it stores any of them. `rows` is
+// the whole matrix's row count.
 __device__ __forceinline__ void stage_kv_b_rows(float* dst, int dst_stride, const void* kv_b, int dtype,
-                                                int64_t r0, int nrows, int c0, int ncols, int C, int nthreads) {
+                                                int64_t r0, int nrows, int c0, int ncols, int C, int nthreads,
+                                                int64_t rows) {
   constexpr int U = 4;   // items in flight per thread
   const int ngrp = (ncols + 7) / 8;
   const int total = nrows * ngrp;
@@ -151,7 +171,7 @@ __device__ __forceinline__ void stage_kv_b_rows(float* dst, int dst_stride, cons
       const int i = base + u * nthreads;
       if (i < total) {
         const int r = i / ngrp, g = i % ngrp;
-        kv_b_load8(v[u], kv_b, dtype, r0 + r, c0 + 8 * g, ncols - 8 * g, C);
+        kv_b_load8(v[u], kv_b, dtype, r0 + r, c0 + 8 * g, ncols - 8 * g, C, rows);
       }
     }
 #pragma unroll

@@ -29,9 +29,11 @@ static mla_status check_cfg(const mla_config* cfg) {
       (cfg->qk_rope & 1) || cfg->v_head < 1)
     return MLA_ERR_INVALID_ARG;
   if (cfg->act_dtype != MLA_F32 && cfg->act_dtype != MLA_BF16) return MLA_ERR_INVALID_ARG;
-  if (cfg->kv_b_dtype != MLA_F32 && cfg->kv_b_dtype != MLA_BF16 && cfg->kv_b_dtype != MLA_Q8_0)
+  if (cfg->kv_b_dtype != MLA_F32 && cfg->kv_b_dtype != MLA_BF16 && cfg->kv_b_dtype != MLA_Q8_0 &&
+      cfg->kv_b_dtype != MLA_Q4_AFFINE)
     return MLA_ERR_INVALID_ARG;
   if (cfg->kv_b_dtype == MLA_Q8_0 && (cfg->kv_lora % 32) != 0) return MLA_ERR_BAD_KV_B;
+  if (cfg->kv_b_dtype == MLA_Q4_AFFINE && (cfg->kv_lora % 64) != 0) return MLA_ERR_BAD_KV_B;
   if (cfg->page_size < 0) return MLA_ERR_INVALID_ARG;
   if (cfg->page_size == 0 && cfg->rows_per_seq < 1) return MLA_ERR_INVALID_ARG;
   if (cfg->page_size > 0 && cfg->max_pages_per_seq < 1) return MLA_ERR_INVALID_ARG;
@@ -252,7 +254,7 @@ float mla_softmax_scale(int32_t qk_nope, int32_t qk_rope, double mscale) {
 mla_status mla_validate_kv_b(int32_t dtype, int64_t rows, int64_t cols, uint64_t size_bytes,
                              int32_t heads, int32_t nope, int32_t kv_lora, int32_t v_dim) {
   if (heads < 1 || nope < 1 || kv_lora < 1 || v_dim < 1) return MLA_ERR_INVALID_ARG;
-  if (dtype != MLA_F32 && dtype != MLA_BF16 && dtype != MLA_Q8_0) return MLA_ERR_BAD_KV_B;
+  if (dtype != MLA_F32 && dtype != MLA_BF16 && dtype != MLA_Q8_0 && dtype != MLA_Q4_AFFINE) return MLA_ERR_BAD_KV_B;
   uint64_t exp_rows;
   if (!checked_mul((uint64_t)heads, (uint64_t)nope + (uint64_t)v_dim, &exp_rows)) return MLA_ERR_BAD_KV_B;
   if (rows < 0 || cols < 0 || (uint64_t)rows != exp_rows || cols != kv_lora) return MLA_ERR_BAD_KV_B;
@@ -260,6 +262,10 @@ mla_status mla_validate_kv_b(int32_t dtype, int64_t rows, int64_t cols, uint64_t
   if (dtype == MLA_Q8_0) {
     if (kv_lora % 32 != 0) return MLA_ERR_BAD_KV_B;
     if (!checked_mul((uint64_t)(kv_lora / 32), 34u, &row_bytes)) return MLA_ERR_BAD_KV_B;
+  } else if (dtype == MLA_Q4_AFFINE) {
+    if (kv_lora % 64 != 0) return MLA_ERR_BAD_KV_B;
+    // codes (cols / 2 bytes) plus a bf16 scale and bias per 64 columns
+    row_bytes = (uint64_t)kv_lora / 2 + (uint64_t)(kv_lora / 64) * 4u;
   } else {
     if (!checked_mul((uint64_t)kv_lora, dtype == MLA_BF16 ? 2u : 4u, &row_bytes)) return MLA_ERR_BAD_KV_B;
   }
@@ -275,6 +281,9 @@ uint64_t mla_kv_b_bytes(const mla_config* cfg) {
   if (cfg->kv_b_dtype == MLA_Q8_0) {
     if (cfg->kv_lora % 32) return 0;
     row_bytes = (uint64_t)(cfg->kv_lora / 32) * 34u;
+  } else if (cfg->kv_b_dtype == MLA_Q4_AFFINE) {
+    if (cfg->kv_lora % 64) return 0;
+    row_bytes = (uint64_t)cfg->kv_lora / 2 + (uint64_t)(cfg->kv_lora / 64) * 4u;
   } else if (cfg->kv_b_dtype == MLA_BF16) {
     row_bytes = (uint64_t)cfg->kv_lora * 2u;
   } else if (cfg->kv_b_dtype == MLA_F32) {

@@ -12,7 +12,7 @@ import torch
 
 from . import binding as L
 
-_DT = {"f32": L.MLA_F32, "bf16": L.MLA_BF16, "q8_0": L.MLA_Q8_0}
+_DT = {"f32": L.MLA_F32, "bf16": L.MLA_BF16, "q8_0": L.MLA_Q8_0, "q4_affine": L.MLA_Q4_AFFINE}
 
 
 def _dev(a: np.ndarray, device) -> torch.Tensor:

@@ -159,8 +159,33 @@ def _q8_0_pack(codes: np.ndarray, scales_f16: np.ndarray) -> np.ndarray:
     return out.reshape(rows, nb * Q8_0_BLOCK_BYTES)
 
 
+def q4_affine_pack(codes: np.ndarray, scales_bits: np.ndarray, biases_bits: np.ndarray) -> np.ndarray:
+    """Storage of a 4-bit affine matrix as one byte buffer: codes [rows, cols] (0..15) as
+    little-endian 32-bit words of 8 (code j of a word in bits 4j..4j+3), then the bf16 scale
+    and bias bit patterns [rows, cols/64], row-major."""
+    rows, cols = codes.shape
+    c = codes.astype(np.uint32).reshape(rows, cols // 8, 8)
+    words = np.zeros((rows, cols // 8), dtype=np.uint32)
+    for j in range(8):
+        words |= c[:, :, j] << np.uint32(4 * j)
+    return np.concatenate([words.astype("<u4").view(np.uint8).reshape(-1),
+                           np.ascontiguousarray(scales_bits, dtype="<u2").view(np.uint8).reshape(-1),
+                           np.ascontiguousarray(biases_bits, dtype="<u2").view(np.uint8).reshape(-1)])
+
+
 def make_kv_b(wl: Workload) -> np.ndarray:
     rows = wl.H * (wl.N + wl.V)
+    if wl.kv_b == "q4_affine":
+        # codes U{0..15}; per 64-column group a scale near 1/(4.6 sqrt(C)) (so values have about
+        # the spread of the bf16 draw's N(0, 1/C)) and a bias near -7.5 * scale (centred codes)
+        if wl.C % 64:
+            raise ValueError("4-bit affine kv_b needs kv_lora % 64 == 0")
+        g = wl.C // 64
+        codes = _rng(wl.seed, "kv_b").integers(0, 16, size=(rows, wl.C), dtype=np.int16)
+        s = _rng(wl.seed, "kv_b_d").uniform(0.5, 1.5, size=(rows, g)) / (4.6 * math.sqrt(wl.C))
+        bias = -7.5 * s * _rng(wl.seed, "kv_b_d", 1).uniform(0.9, 1.1, size=(rows, g))
+        return q4_affine_pack(codes, f32_to_bf16_bits(s.astype(np.float32)),
+                              f32_to_bf16_bits(bias.astype(np.float32)))
     if wl.kv_b == "q8_0":
         if wl.C % Q8_0_BLOCK_ELEMS:
             raise ValueError("Q8_0 kv_b needs kv_lora % 32 == 0")

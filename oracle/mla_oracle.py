@@ -23,8 +23,8 @@ the scaled scores; Q8_0 blocks are an fp16 scale followed by 32 int8 codes.
 
 Pins: tests/test_oracle_pins.py checks every function here against closed forms,
 identities and the pages' own fixture (absorbed == unabsorbed MHA, T=1, softmax sums,
-RoPE identities and pairing, YaRN limits, RMSNorm invariants, Q8_0 golden blocks,
-the kv_b validation fixture, split/merge associativity, page addressing).
+RoPE identities and pairing, YaRN limits, RMSNorm invariants, Q8_0 and 4-bit golden
+blocks, the kv_b validation fixture, split/merge associativity, page addressing).
 """
 from __future__ import annotations
 
@@ -36,6 +36,8 @@ import numpy as np
 Q8_0_BLOCK_ELEMS = 32
 Q8_0_BLOCK_BYTES = 34
 DTYPE_Q8_0 = "q8_0"
+Q4_GROUP = 64
+DTYPE_Q4_AFFINE = "q4_affine"
 
 
 # ---------------------------------------------------------------------------------------
@@ -86,6 +88,34 @@ def q8_0_validate(dtype: str, shape: tuple, size_bytes: int, heads: int, nope: i
     if size_bytes != expected:
         return f"size {size_bytes} != {expected}"
     return None
+
+
+def q4_affine_bytes(rows: int, cols: int) -> int:
+    """Bytes of a 4-bit affine matrix: the packed codes (cols/2 bytes a row), then one bf16
+    scale and one bf16 bias per 64-column group of every row."""
+    return rows * (cols // 2) + 2 * rows * (cols // Q4_GROUP) * 2
+
+
+def q4_affine_to_f64(blob: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    """Dequantise a 4-bit affine matrix [rows, cols]: w = scale * q + bias, with q an unsigned
+    4-bit code and (scale, bias) shared by 64 consecutive columns of a row (exact in float64).
+
+    [moeflux-fwd] `resolve_proj` (a 4-bit projection is three tensors: weight, scales, biases)
+    and `encode_mla_q_prime_4bit` / `encode_mla_out_per_head_4bit` (group size 64);
+    [moeflux-mv] `MatvecSpec` (packed weight, bf16 scales, bf16 biases). The byte layout is not
+    on the pages; read as: the three tensors back to back in one buffer, codes first as
+    little-endian 32-bit words of 8 codes each (code j of a word in bits 4j..4j+3, the lower
+    column first), then scales [rows, cols/64] and biases [rows, cols/64], bf16, row-major.
+    """
+    blob = np.asarray(blob, dtype=np.uint8).reshape(-1)
+    ng = cols // Q4_GROUP
+    nc = rows * (cols // 2)
+    words = blob[:nc].copy().view("<u4").reshape(rows, cols // 8)
+    shifts = (4 * np.arange(8, dtype=np.uint32))[None, None, :]
+    q = ((words[:, :, None] >> shifts) & np.uint32(15)).reshape(rows, cols).astype(np.float64)
+    scales = bf16_to_f64(blob[nc:nc + 2 * rows * ng].copy().view("<u2").reshape(rows, ng))
+    biases = bf16_to_f64(blob[nc + 2 * rows * ng:nc + 4 * rows * ng].copy().view("<u2").reshape(rows, ng))
+    return q * np.repeat(scales, Q4_GROUP, axis=1) + np.repeat(biases, Q4_GROUP, axis=1)
 
 
 # ---------------------------------------------------------------------------------------

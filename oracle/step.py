@@ -37,6 +37,8 @@ def kv_b_f64(prob) -> np.ndarray:
     wl = prob.wl
     if wl.kv_b == "q8_0":
         return O.q8_0_to_f64(prob.kv_b, wl.C)
+    if wl.kv_b == "q4_affine":
+        return O.q4_affine_to_f64(prob.kv_b, wl.H * (wl.N + wl.V), wl.C)
     return decode_act(prob.kv_b, wl.kv_b)
 
 

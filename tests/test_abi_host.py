@@ -147,3 +147,20 @@ def test_append_workspace_size_and_null_args(L):
     # gemv append: hidden must keep 16-byte vectors
     assert L.mla_cache_append(_cfg(L), cache, *dict(args, w_kva=0x6000, hidden=7167).values()) == \
         L.STATUS_CODE["MLA_ERR_INVALID_ARG"]
+
+
+def test_q4_affine_kv_b_contract(L):
+    heads, nope, kv_lora, v = 4, 2, 128, 3
+    rows = heads * (nope + v)
+    size = rows * (kv_lora // 2) + rows * (kv_lora // 64) * 4
+    assert size == O.q4_affine_bytes(rows, kv_lora)
+    assert L.mla_validate_kv_b(L.MLA_Q4_AFFINE, rows, kv_lora, size, heads, nope, kv_lora, v) == 0
+    bad = L.STATUS_CODE["MLA_ERR_BAD_KV_B"]
+    assert L.mla_validate_kv_b(L.MLA_Q4_AFFINE, rows, kv_lora, size - 1, heads, nope, kv_lora, v) == bad
+    assert L.mla_validate_kv_b(L.MLA_Q4_AFFINE, rows, 96, rows * 48 + rows * 4, heads, nope, 96, v) == bad
+    cfg = L.MlaConfig()
+    cfg.n_heads, cfg.kv_lora, cfg.qk_nope, cfg.qk_rope, cfg.v_head = heads, kv_lora, nope, 2, v
+    cfg.act_dtype, cfg.kv_b_dtype = L.MLA_BF16, L.MLA_Q4_AFFINE
+    assert L.mla_kv_b_bytes(cfg) == size
+    cfg.kv_lora = 96
+    assert L.mla_kv_b_bytes(cfg) == 0

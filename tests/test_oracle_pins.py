@@ -384,3 +384,34 @@ def test_bf16_to_f64_matches_torch_cast():
     nan = np.isnan(t)
     assert np.array_equal(np.isnan(got), nan)
     assert np.array_equal(got[~nan], t[~nan])
+
+
+# ----------------------------------------------------------------------------------------
+# 4-bit affine kv_b: hand-worked blocks (code order within a word, group boundaries)
+# ----------------------------------------------------------------------------------------
+
+def _q4_blob(case):
+    words = np.array([int(w, 16) for w in case["words_row_major"]], dtype="<u4")
+    sc = np.array([int(v, 16) for v in case["scales_bf16"]], dtype="<u2")
+    bi = np.array([int(v, 16) for v in case["biases_bf16"]], dtype="<u2")
+    return np.concatenate([words.view(np.uint8), sc.view(np.uint8), bi.view(np.uint8)])
+
+
+def test_q4_affine_golden_blocks(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "q4_affine_blocks.json")))
+    for case in g["cases"]:
+        blob = _q4_blob(case)
+        assert blob.size == O.q4_affine_bytes(case["rows"], case["cols"])
+        w = O.q4_affine_to_f64(blob, case["rows"], case["cols"])
+        for r, c, v in case["expect"]:
+            assert w[r, c] == v, (r, c, w[r, c], v)
+
+
+def test_q4_affine_code_order_within_a_word():
+    # one word 0x87654321 in a 1 x 64 matrix with scale 1, bias 0: columns 0..7 hold 1..8
+    words = np.zeros(8, dtype="<u4")
+    words[0] = 0x87654321
+    blob = np.concatenate([words.view(np.uint8), np.array([0x3F80], "<u2").view(np.uint8),
+                           np.array([0x0000], "<u2").view(np.uint8)])
+    w = O.q4_affine_to_f64(blob, 1, 64)
+    assert list(w[0, :8]) == [1, 2, 3, 4, 5, 6, 7, 8] and not w[0, 8:].any()
