@@ -18,6 +18,11 @@ definitions' own):
     N(0, 1/7168), both bf16.
   * ragged lengths L_b ~ U{lo..hi}; 64-row pages; a seeded permutation of all physical
     pages handed out to the sequences in order; unused page-table entries are -1.
+  * the layer's projections (front end and o_proj): x [B, hidden] ~ N(0, 1); every weight
+    [out, in] ~ N(0, 1/in) (as Q8_0: codes ~ U{-127..127}, scales ~ U(0.5, 1.5)/(73.3 sqrt(in));
+    4-bit: codes ~ U{0..15}, scales ~ U(0.5, 1.5)/(4.6 sqrt(in)), biases ~ -7.5 scale U(0.9, 1.1),
+    so every format has about the same spread); the q_a_layernorm weight ~ U(0.5, 1.5); the
+    attention output fed to o_proj [B, H, V] ~ N(0, 1) in fp32.
   * every cache row a step must not read (the append slot before the append, spare
     capacity, the unused tail of a last page) holds a NaN sentinel, so that a kernel
     that reads past a sequence's length shows up in the output.
@@ -42,6 +47,7 @@ BF16_NAN_BITS = 0x7FC0
 _TAG = {
     "q": 1, "lat": 2, "pe": 3, "norm_w": 4, "kv_b": 5, "kv_b_d": 6, "kva": 7,
     "x": 8, "w_kva": 9, "pages": 10, "lengths": 11,
+    "w_q_a": 12, "q_norm_w": 13, "w_q": 14, "w_o": 15, "attn": 16, "w_d": 17,
 }
 
 
@@ -195,6 +201,97 @@ def make_kv_b(wl: Workload) -> np.ndarray:
     w = _rng(wl.seed, "kv_b").standard_normal((rows, wl.C), dtype=np.float32)
     w *= np.float32(1.0 / math.sqrt(wl.C))
     return _encode_act(w, wl.kv_b)
+
+
+def make_weight(seed: int, tag: str, rows: int, cols: int, fmt: str) -> np.ndarray:
+    """A projection weight [rows, cols] (out, in) in storage format `fmt`, drawn so that each
+    element has about the spread of N(0, 1/cols) whatever the format."""
+    sub = rows * 7919 + cols
+    rng, rng_d = _rng(seed, tag, sub), _rng(seed, "w_d", sub)
+    if fmt == "q8_0":
+        if cols % Q8_0_BLOCK_ELEMS:
+            raise ValueError("Q8_0 weights need in_dim % 32 == 0")
+        codes = rng.integers(-127, 128, size=(rows, cols), dtype=np.int16)
+        d = rng_d.uniform(0.5, 1.5, size=(rows, cols // Q8_0_BLOCK_ELEMS)) / (73.3 * math.sqrt(cols))
+        return _q8_0_pack(codes, d.astype(np.float16))
+    if fmt == "q4_affine":
+        if cols % 64:
+            raise ValueError("4-bit weights need in_dim % 64 == 0")
+        codes = rng.integers(0, 16, size=(rows, cols), dtype=np.int16)
+        sc = rng_d.uniform(0.5, 1.5, size=(rows, cols // 64)) / (4.6 * math.sqrt(cols))
+        bias = -7.5 * sc * rng_d.uniform(0.9, 1.1, size=(rows, cols // 64))
+        return q4_affine_pack(codes, f32_to_bf16_bits(sc.astype(np.float32)),
+                              f32_to_bf16_bits(bias.astype(np.float32)))
+    w = rng.standard_normal((rows, cols), dtype=np.float32)
+    w *= np.float32(1.0 / math.sqrt(cols))
+    return _encode_act(w, fmt)
+
+
+@dataclass(frozen=True)
+class ProjWorkload:
+    """The layer's projections around one decode step: the front end (the Q chain or a direct
+    q projection, plus kv_a) and o_proj, for B sequences."""
+    name: str
+    B: int
+    H: int
+    C: int
+    N: int
+    R: int
+    V: int
+    hidden: int
+    q_lora: int       # 0: one direct q projection [H(N+R), hidden]
+    act: str          # "f32" | "bf16": x and q storage
+    w: str            # weight format of every projection: "f32" | "bf16" | "q8_0" | "q4_affine"
+    eps: float = 1e-6
+    seed: int = 0
+
+    def with_(self, **kw) -> "ProjWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+# V2-Lite-shaped (no q rank, hidden 2048, 16 heads) and V3-shaped (q rank 1536, hidden 7168,
+# 128 heads) layers, plus a tiny fp32 one.
+PROJ_WORKLOADS = {
+    "tiny_proj_f32": ProjWorkload(name="tiny_proj_f32", B=3, H=4, C=64, N=32, R=16, V=32, hidden=256,
+                                  q_lora=128, act="f32", w="f32"),
+    "v2lite_proj_b1": ProjWorkload(name="v2lite_proj_b1", B=1, H=16, C=512, N=128, R=64, V=128, hidden=2048,
+                                   q_lora=0, act="bf16", w="bf16"),
+    "v3_proj_b4": ProjWorkload(name="v3_proj_b4", B=4, H=128, C=512, N=128, R=64, V=128, hidden=7168,
+                               q_lora=1536, act="bf16", w="bf16"),
+    "v3_proj_b64": ProjWorkload(name="v3_proj_b64", B=64, H=128, C=512, N=128, R=64, V=128, hidden=7168,
+                                q_lora=1536, act="bf16", w="bf16"),
+}
+
+
+@dataclass
+class ProjProblem:
+    """Host-side inputs of the projections, in the library's storage formats."""
+    wl: ProjWorkload
+    x: np.ndarray                   # [B, hidden] act storage
+    w_q_a: Optional[np.ndarray]     # [q_lora, hidden] (q_lora > 0)
+    q_a_norm_w: Optional[np.ndarray]  # [q_lora] float32
+    w_q: np.ndarray                 # [H(N+R), q_lora or hidden]
+    w_kva: np.ndarray               # [C+R, hidden]
+    w_o: np.ndarray                 # [hidden, H*V]
+    attn: np.ndarray                # [B, H, V] float32: o_proj's input
+
+
+def make_proj_problem(wl: ProjWorkload) -> ProjProblem:
+    """Draw every input of the projections for workload `wl`."""
+    x = _encode_act(_rng(wl.seed, "x").standard_normal((wl.B, wl.hidden), dtype=np.float32), wl.act)
+    q_rows = wl.H * (wl.N + wl.R)
+    if wl.q_lora > 0:
+        w_q_a = make_weight(wl.seed, "w_q_a", wl.q_lora, wl.hidden, wl.w)
+        q_a_norm_w = _rng(wl.seed, "q_norm_w").uniform(0.5, 1.5, size=wl.q_lora).astype(np.float32)
+        w_q = make_weight(wl.seed, "w_q", q_rows, wl.q_lora, wl.w)
+    else:
+        w_q_a, q_a_norm_w = None, None
+        w_q = make_weight(wl.seed, "w_q", q_rows, wl.hidden, wl.w)
+    w_kva = make_weight(wl.seed, "w_kva", wl.C + wl.R, wl.hidden, wl.w)
+    w_o = make_weight(wl.seed, "w_o", wl.hidden, wl.H * wl.V, wl.w)
+    attn = _rng(wl.seed, "attn").standard_normal((wl.B, wl.H, wl.V), dtype=np.float32)
+    return ProjProblem(wl=wl, x=x, w_q_a=w_q_a, q_a_norm_w=q_a_norm_w, w_q=w_q, w_kva=w_kva, w_o=w_o,
+                       attn=attn)
 
 
 def make_problem(wl: Workload, nan_fill: bool = True) -> Problem:

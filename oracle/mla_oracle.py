@@ -24,7 +24,9 @@ the scaled scores; Q8_0 blocks are an fp16 scale followed by 32 int8 codes.
 Pins: tests/test_oracle_pins.py checks every function here against closed forms,
 identities and the pages' own fixture (absorbed == unabsorbed MHA, T=1, softmax sums,
 RoPE identities and pairing, YaRN limits, RMSNorm invariants, Q8_0 and 4-bit golden
-blocks, the kv_b validation fixture, split/merge associativity, page addressing).
+blocks, the kv_b validation fixture, split/merge associativity, page addressing, and for
+the projections rank-one closed forms, one-hot layout probes and the Q chain's scale
+invariance).
 """
 from __future__ import annotations
 
@@ -257,6 +259,62 @@ def append_rows(kva: np.ndarray, norm_w: np.ndarray, positions: Sequence[int],
         out[b, :kv_lora] = rms_norm(kva[b, :kv_lora], norm_w, eps)
         out[b, kv_lora:] = rope_pairs(kva[b, kv_lora:], int(positions[b]), inv_freq)
     return out
+
+
+# ---------------------------------------------------------------------------------------
+# The projections around the step: the Q chain, a direct q projection, o_proj
+# ---------------------------------------------------------------------------------------
+
+def matvec(W: np.ndarray, x: np.ndarray) -> np.ndarray:
+    """y = W x for every input vector: W [out_dim, in_dim], x [..., in_dim] -> [..., out_dim].
+
+    [moeflux-fwd] `encode_matvec` with `MatvecSpec { out_dim, in_dim }` (every projection
+    of the layer is one); [ts-ds2] `encode_gemv_any(tensor, out, in)`.
+    """
+    return np.asarray(x, dtype=np.float64) @ np.asarray(W, dtype=np.float64).T
+
+
+def heads_view(q_full: np.ndarray, heads: int, qk_head: int) -> np.ndarray:
+    """[..., heads*qk_head] -> [..., heads, qk_head]: head h is the run of qk_head values
+    starting at h*qk_head, its q_nope part first and its q_pe part last.
+
+    [moeflux-fwd] `q_full: [num_heads, qk_head_dim]`, split per head into (q_nope, q_pe).
+    """
+    q_full = np.asarray(q_full, dtype=np.float64)
+    return q_full.reshape(q_full.shape[:-1] + (heads, qk_head))
+
+
+def q_chain(x: np.ndarray, W_qa: np.ndarray, q_norm_w: np.ndarray, eps: float,
+            W_qb: np.ndarray, heads: int, qk_head: int) -> np.ndarray:
+    """q [B, H, N+R] from the layer's normed input x [B, D] by the low-rank Q chain.
+
+    [moeflux-fwd] Q chain: q_lat = matvec(x, q_a) with out_dim q_lora_rank and in_dim
+    hidden_dim; the RMSNorm of q_lat over its q_lora_rank values with the q_a_layernorm
+    weight and RMS_NORM_EPS; q_full = matvec(q_lat, q_b) with out_dim
+    num_heads*qk_head_dim and in_dim q_lora_rank; then the per-head split.
+    """
+    q_lat = matvec(W_qa, x)
+    return heads_view(matvec(W_qb, rms_norm(q_lat, q_norm_w, eps)), heads, qk_head)
+
+
+def q_direct(x: np.ndarray, W_q: np.ndarray, heads: int, qk_head: int) -> np.ndarray:
+    """q [B, H, N+R] = W_q x, the single q projection of a model without a q rank.
+
+    [ts-ds2] `encode_mla_attention_block`: `Q_PROJ` GEMV of the normed hidden state into
+    `[heads * head_dim]`, whose pe windows are then rotated before the absorb.
+    """
+    return heads_view(matvec(W_q, x), heads, qk_head)
+
+
+def o_proj(out: np.ndarray, W_o: np.ndarray) -> np.ndarray:
+    """y [B, D] = W_o . out[b] with out [B, H, V] read head after head (H*V values, head h
+    at h*V), W_o [D, H*V].
+
+    [moeflux-fwd] `o_proj` final matvec: input out_per_head, out_dim hidden_dim,
+    in_dim num_heads*v_head_dim; [ts-ds2] `O_PROJ` GEMV from heads*v_dim to hidden.
+    """
+    out = np.asarray(out, dtype=np.float64)
+    return matvec(W_o, out.reshape(out.shape[0], -1))
 
 
 # ---------------------------------------------------------------------------------------

@@ -115,3 +115,39 @@ def rows_per_second_sample(prob, seconds: float = 10.0, heads=None):
             break
     dt = time.perf_counter() - t0
     return rows / dt, n, rows, dt
+
+
+# ---------------------------------------------------------------------------------------
+# The layer's projections on a synthetic ProjProblem (x, w_q_a, q_a_norm_w, w_q, w_kva, w_o,
+# attn and its workload's dims and formats)
+# ---------------------------------------------------------------------------------------
+
+def weight_f64(blob: np.ndarray, rows: int, cols: int, fmt: str) -> np.ndarray:
+    """A stored [rows, cols] weight decoded exactly to float64."""
+    if fmt == "q8_0":
+        return O.q8_0_to_f64(blob, cols)
+    if fmt == "q4_affine":
+        return O.q4_affine_to_f64(blob, rows, cols)
+    return decode_act(blob, fmt).reshape(rows, cols)
+
+
+def front_end(pp):
+    """(q [B, H, N+R], kva [B, C+R]) in float64: the Q chain (or the direct q projection) and
+    the kv_a projection of the problem's x."""
+    wl = pp.wl
+    x = decode_act(pp.x, wl.act)
+    qk = wl.N + wl.R
+    if wl.q_lora > 0:
+        q = O.q_chain(x, weight_f64(pp.w_q_a, wl.q_lora, wl.hidden, wl.w), pp.q_a_norm_w, wl.eps,
+                      weight_f64(pp.w_q, wl.H * qk, wl.q_lora, wl.w), wl.H, qk)
+    else:
+        q = O.q_direct(x, weight_f64(pp.w_q, wl.H * qk, wl.hidden, wl.w), wl.H, qk)
+    kva = O.kv_a_rows(x, weight_f64(pp.w_kva, wl.C + wl.R, wl.hidden, wl.w))
+    return q, kva
+
+
+def o_proj(pp, attn=None) -> np.ndarray:
+    """y [B, hidden] in float64 = o_proj of `attn` (default: the problem's own input)."""
+    wl = pp.wl
+    a = O.f32_to_f64(pp.attn) if attn is None else np.asarray(attn, dtype=np.float64)
+    return O.o_proj(a, weight_f64(pp.w_o, wl.hidden, wl.H * wl.V, wl.w))

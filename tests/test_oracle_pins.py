@@ -415,3 +415,111 @@ def test_q4_affine_code_order_within_a_word():
                            np.array([0x0000], "<u2").view(np.uint8)])
     w = O.q4_affine_to_f64(blob, 1, 64)
     assert list(w[0, :8]) == [1, 2, 3, 4, 5, 6, 7, 8] and not w[0, 8:].any()
+
+
+# ----------------------------------------------------------------------------------------
+# The layer's projections: matvec, the Q chain, the direct q projection, o_proj
+# ----------------------------------------------------------------------------------------
+
+def test_matvec_rank_one_closed_form():
+    # W = u v^T maps x to u (v . x); a transposed W (or x on the wrong side) would give
+    # v (u . x), a vector of another length
+    u, v = RNG.standard_normal(7), RNG.standard_normal(11)
+    x = RNG.standard_normal((3, 11))
+    got = O.matvec(np.outer(u, v), x)
+    assert got.shape == (3, 7)
+    for b in range(3):
+        np.testing.assert_allclose(got[b], u * float(np.dot(v, x[b])), rtol=1e-13, atol=1e-14)
+
+
+def test_matvec_one_hot_input_picks_a_column():
+    W = RNG.standard_normal((6, 9))
+    for k in (0, 4, 8):
+        e = np.zeros((1, 9))
+        e[0, k] = 1.0
+        np.testing.assert_array_equal(O.matvec(W, e)[0], W[:, k])
+
+
+def test_heads_view_puts_each_head_in_one_run_nope_first():
+    H, N, R = 3, 4, 2
+    q = O.heads_view(np.arange(H * (N + R), dtype=np.float64)[None], H, N + R)[0]
+    for h in range(H):
+        np.testing.assert_array_equal(q[h, :N], np.arange(h * (N + R), h * (N + R) + N))
+        np.testing.assert_array_equal(q[h, N:], np.arange(h * (N + R) + N, (h + 1) * (N + R)))
+
+
+def test_q_direct_with_a_permutation_moves_input_values():
+    # W_q = a permutation matrix P (row i has its 1 in column p[i]): q_full[i] = x[p[i]]
+    H, qk, D = 2, 5, 10
+    p = RNG.permutation(D)
+    W = np.zeros((H * qk, D))
+    W[np.arange(H * qk), p] = 1.0
+    x = RNG.standard_normal((1, D))
+    q = O.q_direct(x, W, H, qk)
+    for h in range(H):
+        for j in range(qk):
+            assert q[0, h, j] == x[0, p[h * qk + j]]
+
+
+def test_q_chain_normalises_between_the_two_projections():
+    # identity q_a and rank-one q_b = u v^T: q_full = u * sum_k v_k w_k x_k / rms(x), which a
+    # norm after q_b, a missing norm weight or a norm before q_a would all change
+    D, H, qk = 16, 2, 3
+    u, v = RNG.standard_normal(H * qk), RNG.standard_normal(D)
+    w = RNG.uniform(0.5, 1.5, D)
+    x = RNG.standard_normal((2, D)) * 3
+    eps = 1e-6
+    q = O.q_chain(x, np.eye(D), w, eps, np.outer(u, v), H, qk)
+    for b in range(2):
+        rms = math.sqrt(sum(t * t for t in x[b]) / D + eps)
+        s = sum(v[k] * w[k] * x[b, k] for k in range(D)) / rms
+        np.testing.assert_allclose(q[b].reshape(-1), u * s, rtol=1e-12)
+
+
+def test_q_chain_is_invariant_to_input_scale():
+    # the RMSNorm in the middle removes any positive scale of x (eps = 0), but not the sign
+    D, L, H, qk = 24, 8, 2, 5
+    Wa, Wb = RNG.standard_normal((L, D)), RNG.standard_normal((H * qk, L))
+    w = RNG.uniform(0.5, 1.5, L)
+    x = RNG.standard_normal((3, D))
+    base = O.q_chain(x, Wa, w, 0.0, Wb, H, qk)
+    np.testing.assert_allclose(O.q_chain(37.0 * x, Wa, w, 0.0, Wb, H, qk), base, rtol=1e-12)
+    np.testing.assert_allclose(O.q_chain(-x, Wa, w, 0.0, Wb, H, qk), -base, rtol=1e-12)
+    # and each sequence's q_lat has unit rms before the norm weight: with w = 1 and q_b = I
+    q = O.q_chain(x, Wa, np.ones(L), 0.0, np.eye(L), 1, L)
+    np.testing.assert_allclose(np.sqrt(np.mean(q[:, 0, :] ** 2, axis=1)), 1.0, rtol=1e-13)
+
+
+def test_o_proj_reads_heads_in_order():
+    # a one-hot input at (head h, value j) picks column h*V + j of W_o
+    H, V, D = 3, 4, 5
+    W = RNG.standard_normal((D, H * V))
+    for h, j in ((0, 0), (1, 3), (2, 1)):
+        a = np.zeros((1, H, V))
+        a[0, h, j] = 1.0
+        np.testing.assert_array_equal(O.o_proj(a, W)[0], W[:, h * V + j])
+
+
+def test_o_proj_is_the_sum_of_per_head_blocks():
+    H, V, D = 4, 3, 6
+    W = RNG.standard_normal((D, H * V))
+    a = RNG.standard_normal((2, H, V))
+    want = sum(np.einsum("dv,bv->bd", W[:, h * V:(h + 1) * V], a[:, h, :]) for h in range(H))
+    np.testing.assert_allclose(O.o_proj(a, W), want, rtol=1e-12, atol=1e-13)
+
+
+def test_absorbed_layer_equals_mha_on_projected_inputs():
+    # the whole layer on tiny shapes: x -> q (direct) -> absorbed decode over rows appended from
+    # kv_a projections -> o_proj, against plain MHA built from the same projections
+    H, C, N, R, V, D, L = 2, 8, 4, 4, 3, 16, 5
+    Wq, Wkva = RNG.standard_normal((H * (N + R), D)), RNG.standard_normal((C + R, D))
+    kv_b, Wo = RNG.standard_normal((H * (N + V), C)), RNG.standard_normal((D, H * V))
+    xs = RNG.standard_normal((L, D))
+    nw = RNG.uniform(0.5, 1.5, C)
+    inv = O.yarn_inv_freq(R, 10000.0, 1.0, 4096, 32.0, 1.0)
+    rows = O.append_rows(O.kv_a_rows(xs, Wkva), nw, list(range(L)), inv, C, 1e-6)
+    q = O.q_direct(xs[-1:], Wq, H, N + R)
+    W_UK, W_UV = O.split_kv_b(kv_b, H, N, V)
+    out, _ = O.decode_one(q[0], W_UK, W_UV, rows, L - 1, inv, 0.3, C)
+    ref, _ = O.decode_unabsorbed_one(q[0], W_UK, W_UV, rows, L - 1, inv, 0.3, C)
+    np.testing.assert_allclose(O.o_proj(out[None], Wo), O.o_proj(ref[None], Wo), rtol=1e-11, atol=1e-12)
