@@ -7,7 +7,9 @@ up-projection). The default workload is the largest single-GPU one: ragged paged
 (B=64 sequences of U{128..32768} rows, H=128, kv_lora 512, rope 64, bf16, 64-row pages with a
 shuffled page table). The same line carries, under "also", the attention kernel's roofline
 fraction on the single-sequence (B=1, H=16, 4096 rows) and batched (B=32, H=128, 4096 rows)
-workloads, measured in the same run. Prints ONE JSON line.
+workloads, measured in the same run, and under "layer_projections" the layer's front end
+(mla_front_end: Q chain or q projection + kv_a) and o_proj (mla_o_proj) per call on V2-Lite- and
+V3-shaped layers. Prints ONE JSON line (--proj-only: one line per projection record).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -434,6 +436,92 @@ def run_ours(args, rank, world, device, workload, K, W, with_e2e=True, with_cloc
     return line
 
 
+# layer-projection sub-records measured in the same run: (workload, weight format) -> timed steps
+PROJ_BENCH = {("v3_proj_b4", "bf16"): 100, ("v3_proj_b64", "bf16"): 60, ("v3_proj_b4", "q4_affine"): 100,
+              ("v3_proj_b4", "q8_0"): 100, ("v2lite_proj_b1", "bf16"): 400}
+
+
+def weight_bytes(a):
+    return 0 if a is None else int(a.nbytes)
+
+
+def proj_work(pp):
+    """Algorithmic bytes and FLOPs of mla_front_end and of mla_o_proj: every weight byte once,
+    the inputs and outputs once (the Q chain's q_lat rows written, normalised in place and read
+    back), 2 FLOPs per weight element and sequence."""
+    wl = pp.wl
+    B, act = wl.B, (2 if wl.act == "bf16" else 4)
+    qk = wl.N + wl.R
+    fe_w = weight_bytes(pp.w_q_a) + weight_bytes(pp.w_q) + weight_bytes(pp.w_kva)
+    fe_b = fe_w + B * wl.hidden * act + B * wl.H * qk * act + B * (wl.C + wl.R) * 4
+    fe_f = 2 * B * ((wl.q_lora * wl.hidden + wl.H * qk * wl.q_lora) if wl.q_lora else wl.H * qk * wl.hidden)
+    fe_f += 2 * B * (wl.C + wl.R) * wl.hidden
+    if wl.q_lora:
+        fe_b += weight_bytes(pp.q_a_norm_w) + 4 * B * wl.q_lora * 4
+    o_b = weight_bytes(pp.w_o) + B * wl.H * wl.V * 4 + B * wl.hidden * 4
+    o_f = 2 * B * wl.hidden * wl.H * wl.V
+    return {"front_end": (fe_b, fe_f), "o_proj": (o_b, o_f)}
+
+
+def run_proj(device, name, fmt, K, W):
+    """Time mla_front_end and mla_o_proj on one projection workload: R device copies of the
+    weights (more than 2.2x L2 in all), CUDA graphs of whole passes over the copies, each call
+    bracketed by in-graph events on the launching stream."""
+    import torch
+
+    from mla_latent_cache_absorb_gb300 import binding as L
+    from mla_latent_cache_absorb_gb300 import synth
+    from mla_latent_cache_absorb_gb300.runner import DeviceProj
+
+    wl = synth.PROJ_WORKLOADS[name].with_(w=fmt)
+    pp = synth.make_proj_problem(wl)
+    work = proj_work(pp)
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 129 * 2 ** 20)
+    per_copy = work["front_end"][0] + work["o_proj"][0]
+    R = max(1, min(32, math.ceil(2.2 * l2 / per_copy)))
+    stream = torch.cuda.Stream(device=device)
+    copies = [DeviceProj(pp, device=device, stream=stream) for _ in range(R)]
+    G = R * max(1, math.ceil(8 / R))
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            L.check(copies[i % R].front_end(), "mla_front_end")
+            L.check(copies[i % R].o_proj(), "mla_o_proj")
+        torch.cuda.synchronize(device)
+        g = torch.cuda.CUDAGraph()
+        evs = [(graph_event(torch), graph_event(torch), graph_event(torch)) for _ in range(G)]
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            s = torch.cuda.current_stream(device)
+            for i in range(G):
+                dp = copies[i % R]
+                evs[i][0].record(s)
+                L.check(L.mla_front_end(dp.cfg, dp.pj, dp.x, dp.q, dp.kva, wl.B, dp.ws, dp.ws.numel(), s),
+                        "mla_front_end")
+                evs[i][1].record(s)
+                L.check(L.mla_o_proj(dp.cfg, dp.pj, dp.attn, dp.y, wl.B, s), "mla_o_proj")
+                evs[i][2].record(s)
+        g.replay()
+        torch.cuda.synchronize(device)
+        fe_ms, o_ms = [], []
+        for _ in range(max(1, K // G)):
+            g.replay()
+            evs[-1][2].synchronize()
+            fe_ms.extend(e[0].elapsed_time(e[1]) for e in evs)
+            o_ms.extend(e[1].elapsed_time(e[2]) for e in evs)
+    hbm = peaks()[0]
+    out = {"workload": wl.name, "weights": fmt, "B": wl.B, "hidden": wl.hidden, "q_lora": wl.q_lora,
+           "launches_per_step": (1 if wl.q_lora == 0 else 3) + 1, "steps": len(fe_ms)}
+    for key, ms in (("front_end", fe_ms), ("o_proj", o_ms)):
+        t = statistics.median(ms) / 1e3
+        b, f = work[key]
+        out[key] = {"median_us": t * 1e6, "bytes": b, "gbs": b / t / 1e9, "hbm_frac": b / t / 1e9 / hbm,
+                    "tflops": f / t / 1e12}
+    del copies
+    torch.cuda.synchronize(device)
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_e2e(torch, L, steps, prob, stream, device, K, W, work):
     """Same metric through the public calls with host buffers: every step copies its inputs
     (query, kv_a rows, positions, lengths) from one pinned host buffer into the step's device
@@ -660,6 +748,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-also", action="store_true", help="skip the attention sub-records")
+    ap.add_argument("--no-proj", action="store_true", help="skip the layer-projection sub-records")
+    ap.add_argument("--proj-only", action="store_true", help="print only the layer-projection records")
+    ap.add_argument("--proj-filter", default=None,
+                    help="with --proj-only: one 'workload:format' record (e.g. v3_proj_b4:bf16)")
     ap.add_argument("--clock-window-s", type=float, default=1.2,
                     help="seconds of untimed replays to sample clocks when the timed region is too short")
     args = ap.parse_args()
@@ -682,6 +774,12 @@ def main():
         args.steps = 20000 if args.workload == "v2lite_b1_t4096" else 200
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    if args.proj_only:
+        for (name, fmt), k in PROJ_BENCH.items():
+            if args.proj_filter and args.proj_filter != f"{name}:{fmt}":
+                continue
+            print(json.dumps(run_proj(device, name, fmt, k, args.warmup)), flush=True)
+        return
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=device)
     line = run_ours(args, rank, world, device, args.workload, args.steps, args.warmup,
@@ -699,6 +797,14 @@ def main():
         line["also"] = {"what": "attention kernel of other workloads, same run, same timing method "
                                 "(not part of value or ms_per_step; their launches are counted in gpu_launches)",
                         **also}
+    if not args.no_proj:
+        recs = [run_proj(device, name, fmt, k, args.warmup) for (name, fmt), k in PROJ_BENCH.items()]
+        for r in recs:
+            line["gpu_launches"] += r["launches_per_step"] * r["steps"]
+        line["layer_projections"] = {
+            "what": "mla_front_end (q chain or q projection + kv_a) and mla_o_proj per call, median of "
+                    "in-graph events, weights rotating over copies > 2.2x L2 (not part of value)",
+            "records": recs}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from mla_latent_cache_absorb_gb300 import synth
         line["cpu_baseline"] = cpu_baseline(synth.make_problem(synth.WORKLOADS[args.workload]), args.cpu_seconds)

@@ -2,7 +2,8 @@
  * mla.h -- C ABI for one decode step of Multi-head Latent Attention (MLA) over a
  * compressed latent KV cache, on an NVIDIA GB300 (sm_103a).
  *
- * Two calls carry the method:
+ * Two calls carry the method (mla_front_end and mla_o_proj, further down, add the layer's
+ * projections before and after them):
  *   mla_cache_append  writes each sequence's new compressed row [kv_lat ; k_pe] into the
  *                     cache: optional kv_a projection, RMSNorm over the latent part,
  *                     consecutive-pair YaRN RoPE over the k_pe tail.
@@ -266,6 +267,55 @@ mla_status mla_decode_partial(const mla_config* cfg, const mla_cache* cache,
 mla_status mla_decode_combine(const mla_config* cfg, const void* kv_b,
                               const int32_t* seq_lens, float* out, float* lse, int32_t B,
                               void* workspace, size_t ws_bytes, mla_stream_t stream);
+
+/* ---- the projections around the step -------------------------------------------------------
+ * moeflux mla_attn_forward.rs, mla_attn_layer_forward_gpu: Q chain (q_a_proj matvec ->
+ * q_a_layernorm -> q_b_proj matvec), KV-A chain (kv_a_proj_with_mqa matvec), o_proj final
+ * matvec; turbospark deepseek2 attn.rs, encode_mla_attention_block: Q_PROJ GEMV of the normed
+ * hidden state (a model without a q rank), O_PROJ GEMV of the combined heads.
+ * Every projection is y = W x per sequence, W row-major [out_dim, in_dim] in w_dtype (the
+ * kv_b formats: F32, BF16, Q8_0 with blocks along in_dim, Q4_AFFINE with the codes, scales and
+ * biases of the whole matrix in one buffer), accumulated in float32 in a fixed order
+ * (run-to-run identical results). in_dim must be a multiple of 8 (32 for Q8_0, 64 for
+ * Q4_AFFINE); every pointer 16-byte aligned. */
+typedef struct mla_proj {
+  int32_t hidden;          /* D: the layer's model width (in_dim of q_a / q, kv_a; out_dim of o) */
+  int32_t q_lora;          /* 0: one q projection; else the Q chain's rank (in_dim of q_b) */
+  int32_t w_dtype;         /* mla_dtype of all the weights below */
+  float q_norm_eps;        /* RMSNorm epsilon of q_a_layernorm */
+  const void* w_q_a;       /* device [q_lora, D] (q_lora > 0), else ignored */
+  const float* q_a_norm_w; /* device [q_lora] float32 q_a_layernorm weight (q_lora > 0) */
+  const void* w_q;         /* device q_b [H*(N+R), q_lora] when q_lora > 0, else q [H*(N+R), D] */
+  const void* w_kva;       /* device [C+R, D], or NULL when no kv_a output is asked for */
+  const void* w_o;         /* device [D, H*V], or NULL when mla_o_proj is not used */
+} mla_proj;
+
+/* Bytes of device workspace mla_front_end needs for B sequences: the float32 q_lat rows
+ * [B, q_lora] (0 bytes when q_lora == 0). Host-only. */
+mla_status mla_front_end_workspace_size(const mla_config* cfg, const mla_proj* pj, int32_t B,
+                                        size_t* bytes);
+
+/* The layer's front end for B sequences (async): the queries mla_decode_attn takes and the
+ * kv_a rows mla_cache_append takes (with w_kva == NULL there).
+ *   x    device [B, D] act_dtype: the layer's normed input (the caller owns that norm).
+ *   q    device [B, H, N+R] act_dtype: q_lora > 0: q_full = W_q_b RMSNorm(W_q_a x) with the
+ *        norm over all q_lora values (x / sqrt(mean(x^2) + q_norm_eps) * q_a_norm_w);
+ *        q_lora == 0: q_full = W_q x. Head h is q_full[h*(N+R) : (h+1)*(N+R)], its q_nope
+ *        first; q_pe is left unrotated (mla_decode_attn rotates it). Rounded once.
+ *   kva  device [B, C+R] float32 = W_kva x, or NULL (then w_kva is not read).
+ * Launches: one kernel computing W_q_a x (or W_q x) and W_kva x together (one read of x),
+ * then, for q_lora > 0, the norm of the q_lat rows and the q_b projection.
+ * Errors: INVALID_ARG (null or misaligned pointer, bad dims, kva without w_kva),
+ * UNSUPPORTED (w_dtype), WORKSPACE, CUDA. No device errors. */
+mla_status mla_front_end(const mla_config* cfg, const mla_proj* pj, const void* x, void* q,
+                         float* kva, int32_t B, void* workspace, size_t ws_bytes,
+                         mla_stream_t stream);
+
+/* o_proj for B sequences (async): y[b] = W_o attn[b], attn [B, H, V] float32 read head after
+ * head (head h's V values at h*V: the layout mla_decode_attn writes), y device [B, D] float32.
+ * Errors: as mla_front_end (w_o must be set). */
+mla_status mla_o_proj(const mla_config* cfg, const mla_proj* pj, const float* attn, float* y,
+                      int32_t B, mla_stream_t stream);
 
 /* ---- device error word ------------------------------------------------------------------ */
 

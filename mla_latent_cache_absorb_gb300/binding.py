@@ -35,6 +35,12 @@ class MlaCache(ctypes.Structure):
     _fields_ = [("rows", c_void_p), ("page_table", c_void_p), ("n_physical_rows", c_int64)]
 
 
+class MlaProj(ctypes.Structure):
+    _fields_ = [("hidden", c_int32), ("q_lora", c_int32), ("w_dtype", c_int32), ("q_norm_eps", c_float),
+                ("w_q_a", c_void_p), ("q_a_norm_w", c_void_p), ("w_q", c_void_p), ("w_kva", c_void_p),
+                ("w_o", c_void_p)]
+
+
 class MlaPlanInfo(ctypes.Structure):
     _fields_ = [("kernel", c_int32), ("heads_per_cta", c_int32), ("head_groups", c_int32),
                 ("splits", c_int32), ("rows_per_split", c_int64), ("capacity", c_int64)]
@@ -46,6 +52,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 _CFG = POINTER(MlaConfig)
 _CACHE = POINTER(MlaCache)
+_PROJ = POINTER(MlaProj)
 _SIGS = {
     "mla_status_string": (c_char_p, [c_int32]),
     "mla_abi_version": (c_int32, []),
@@ -70,6 +77,10 @@ _SIGS = {
     "mla_clear_device_error": (c_int32, [c_void_p, c_void_p]),
     "mla_decode_attn_noalloc": (c_int32, [_CFG, c_void_p, c_void_p, _CACHE, c_void_p, c_void_p, c_void_p,
                                           c_void_p, c_int32, c_void_p, c_void_p]),
+    "mla_front_end_workspace_size": (c_int32, [_CFG, _PROJ, c_int32, POINTER(c_size_t)]),
+    "mla_front_end": (c_int32, [_CFG, _PROJ, c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_size_t,
+                                c_void_p]),
+    "mla_o_proj": (c_int32, [_CFG, _PROJ, c_void_p, c_void_p, c_int32, c_void_p]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -210,3 +221,18 @@ def mla_decode_attn_noalloc(cfg, q, kv_b, cache, seq_lens, positions, out, lse, 
     return _lib.mla_decode_attn_noalloc(ctypes.byref(cfg), _p(q), _p(kv_b), ctypes.byref(cache),
                                         _p(seq_lens), _p(positions), _p(out), _p(lse), B,
                                         _p(device_error), _s(stream))
+
+
+def mla_front_end_workspace_size(cfg, pj, B):
+    n = c_size_t(0)
+    st = _lib.mla_front_end_workspace_size(ctypes.byref(cfg), ctypes.byref(pj), B, ctypes.byref(n))
+    return st, n.value
+
+
+def mla_front_end(cfg, pj, x, q, kva, B, workspace, ws_bytes, stream=None):
+    return _lib.mla_front_end(ctypes.byref(cfg), ctypes.byref(pj), _p(x), _p(q), _p(kva), B, _p(workspace),
+                              ws_bytes, _s(stream))
+
+
+def mla_o_proj(cfg, pj, attn, y, B, stream=None):
+    return _lib.mla_o_proj(ctypes.byref(cfg), ctypes.byref(pj), _p(attn), _p(y), B, _s(stream))

@@ -329,6 +329,11 @@ cudaError_t launch_absorb_tc(const mla_config& cfg, const void* q, const void* k
 cudaError_t launch_combine_tc(const mla_config& cfg, const DecodePlan& plan, const void* kv_b,
                               const int32_t* meta, const float* part_o, const float* part_lse, const void* q_res,
                               float* out, float* lse, int B, WsHeader* hdr, cudaStream_t st);
+// projections (proj.cu): y = W x for one or two weight matrices sharing x [B, K]
+cudaError_t launch_proj(const void* x, bool x_bf16, int K, int B, int w_dtype, const void* w0, int64_t rows0,
+                        void* y0, bool y0_bf16, const void* w1, int64_t rows1, void* y1, bool y1_bf16,
+                        cudaStream_t st);
+cudaError_t launch_rms_norm_rows(float* x, const float* w, int K, int B, float eps, cudaStream_t st);
 cudaError_t launch_combine(const mla_config& cfg, const DecodePlan& plan, const void* kv_b,
                            const int32_t* meta, const float* part_o, const float* part_lse, const void* q_res,
                            float* out, float* lse, int B, cudaStream_t st);

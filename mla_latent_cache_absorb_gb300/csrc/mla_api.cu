@@ -172,6 +172,27 @@ cudaError_t ensure_smem(const void* func, int bytes) {
 
 static mla_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
 
+// A projection's in_dim against its weight dtype: a multiple of 8 (16-byte vectors of x), of 32
+// for Q8_0 blocks, of 64 for the 4-bit groups.
+static bool proj_in_dim_ok(int64_t k, int dt) {
+  if (k < 8 || k > (int64_t(1) << 30) || k % 8 != 0) return false;
+  if (dt == MLA_Q8_0) return k % 32 == 0;
+  if (dt == MLA_Q4_AFFINE) return k % 64 == 0;
+  return dt == MLA_F32 || dt == MLA_BF16;
+}
+
+static mla_status check_proj(const mla_config* cfg, const mla_proj* pj, int B) {
+  mla_status st = check_cfg(cfg);
+  if (st != MLA_OK) return st;
+  if (pj == nullptr || B < 1) return MLA_ERR_INVALID_ARG;
+  if (pj->w_dtype != MLA_F32 && pj->w_dtype != MLA_BF16 && pj->w_dtype != MLA_Q8_0 &&
+      pj->w_dtype != MLA_Q4_AFFINE)
+    return MLA_ERR_UNSUPPORTED;
+  if (!proj_in_dim_ok(pj->hidden, pj->w_dtype) || pj->q_lora < 0) return MLA_ERR_INVALID_ARG;
+  if (pj->q_lora > 0 && !proj_in_dim_ok(pj->q_lora, pj->w_dtype)) return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
+
 static mla_status check_ws(void* ws, size_t ws_bytes, size_t need) {
   if (ws == nullptr || !aligned(ws, 256)) return MLA_ERR_WORKSPACE;
   if (ws_bytes < need) return MLA_ERR_WORKSPACE;
@@ -511,6 +532,63 @@ mla_status mla_get_device_error(const void* workspace, int32_t* seq_out, mla_str
 mla_status mla_clear_device_error(void* workspace, mla_stream_t stream) {
   if (workspace == nullptr) return MLA_ERR_INVALID_ARG;
   return cuda_status(cudaMemsetAsync(workspace, 0, sizeof(WsHeader), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mla_status mla_front_end_workspace_size(const mla_config* cfg, const mla_proj* pj, int32_t B, size_t* bytes) {
+  mla_status st = check_proj(cfg, pj, B);
+  if (st != MLA_OK) return st;
+  if (bytes == nullptr) return MLA_ERR_INVALID_ARG;
+  *bytes = align256((size_t)B * (size_t)pj->q_lora * sizeof(float));
+  return MLA_OK;
+}
+
+mla_status mla_front_end(const mla_config* cfg, const mla_proj* pj, const void* x, void* q, float* kva,
+                         int32_t B, void* workspace, size_t ws_bytes, mla_stream_t stream) {
+  mla_status st = check_proj(cfg, pj, B);
+  if (st != MLA_OK) return st;
+  if (x == nullptr || q == nullptr || pj->w_q == nullptr || !aligned(x, 16) || !aligned(pj->w_q, 16))
+    return MLA_ERR_INVALID_ARG;
+  if (kva != nullptr && (pj->w_kva == nullptr || !aligned(pj->w_kva, 16))) return MLA_ERR_INVALID_ARG;
+  const bool chain = pj->q_lora > 0;
+  if (chain && (pj->w_q_a == nullptr || pj->q_a_norm_w == nullptr || !aligned(pj->w_q_a, 16) ||
+                !(pj->q_norm_eps >= 0.f) || !std::isfinite(pj->q_norm_eps)))
+    return MLA_ERR_INVALID_ARG;
+  size_t need;
+  st = mla_front_end_workspace_size(cfg, pj, B, &need);
+  if (st != MLA_OK) return st;
+  if (chain) {
+    st = check_ws(workspace, ws_bytes, need);
+    if (st != MLA_OK) return st;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool xb = cfg->act_dtype == MLA_BF16;
+  const int64_t q_rows = (int64_t)cfg->n_heads * (cfg->qk_nope + cfg->qk_rope);
+  const int64_t kva_rows = cfg->kv_lora + cfg->qk_rope;
+  const void* w1 = kva != nullptr ? pj->w_kva : nullptr;
+  if (!chain) {
+    return cuda_status(launch_proj(x, xb, pj->hidden, B, pj->w_dtype, pj->w_q, q_rows, q, xb, w1, kva_rows, kva,
+                                   false, s));
+  }
+  float* q_lat = static_cast<float*>(workspace);
+  st = cuda_status(launch_proj(x, xb, pj->hidden, B, pj->w_dtype, pj->w_q_a, pj->q_lora, q_lat, false, w1,
+                               kva_rows, kva, false, s));
+  if (st != MLA_OK) return st;
+  st = cuda_status(launch_rms_norm_rows(q_lat, pj->q_a_norm_w, pj->q_lora, B, pj->q_norm_eps, s));
+  if (st != MLA_OK) return st;
+  return cuda_status(launch_proj(q_lat, false, pj->q_lora, B, pj->w_dtype, pj->w_q, q_rows, q, xb, nullptr, 0,
+                                 nullptr, false, s));
+}
+
+mla_status mla_o_proj(const mla_config* cfg, const mla_proj* pj, const float* attn, float* y, int32_t B,
+                      mla_stream_t stream) {
+  mla_status st = check_proj(cfg, pj, B);
+  if (st != MLA_OK) return st;
+  const int64_t k = (int64_t)cfg->n_heads * cfg->v_head;
+  if (!proj_in_dim_ok(k, pj->w_dtype)) return MLA_ERR_INVALID_ARG;
+  if (attn == nullptr || y == nullptr || pj->w_o == nullptr || !aligned(attn, 16) || !aligned(pj->w_o, 16))
+    return MLA_ERR_INVALID_ARG;
+  return cuda_status(launch_proj(attn, false, (int)k, B, pj->w_dtype, pj->w_o, pj->hidden, y, false, nullptr, 0,
+                                 nullptr, false, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

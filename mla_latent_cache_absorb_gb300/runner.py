@@ -122,3 +122,57 @@ class DeviceStep:
     def pool_host(self) -> np.ndarray:
         a = self.pool.cpu().numpy()
         return a.view(np.uint16) if self.wl.act == "bf16" else a
+
+
+class DeviceProj:
+    """The layer's projections of one problem resident on the GPU: `front_end()` runs
+    mla_front_end (q and the kv_a rows) and `o_proj()` runs mla_o_proj, through the C ABI."""
+
+    def __init__(self, pp, device="cuda:0", stream=None, with_kva=True):
+        wl = pp.wl
+        self.pp, self.wl, self.device = pp, wl, torch.device(device)
+        self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
+        d = self.device
+        cfg = L.MlaConfig()
+        cfg.n_heads, cfg.kv_lora, cfg.qk_nope, cfg.qk_rope, cfg.v_head = wl.H, wl.C, wl.N, wl.R, wl.V
+        cfg.act_dtype = _DT[wl.act]
+        cfg.kv_b_dtype = L.MLA_BF16
+        cfg.softmax_scale = L.mla_softmax_scale(wl.N, wl.R, 1.0)
+        cfg.rms_eps = 1e-6
+        cfg.page_size, cfg.max_pages_per_seq, cfg.rows_per_seq = 0, 0, 1
+        self.cfg = cfg
+        self.x = _dev(pp.x, d)
+        self.w_q_a = _dev(pp.w_q_a, d) if pp.w_q_a is not None else None
+        self.q_a_norm_w = _dev(pp.q_a_norm_w, d) if pp.q_a_norm_w is not None else None
+        self.w_q = _dev(pp.w_q, d)
+        self.w_kva = _dev(pp.w_kva, d)
+        self.w_o = _dev(pp.w_o, d)
+        self.attn = _dev(pp.attn, d)
+        pj = L.MlaProj()
+        pj.hidden, pj.q_lora, pj.w_dtype, pj.q_norm_eps = wl.hidden, wl.q_lora, _DT[wl.w], wl.eps
+        pj.w_q_a = self.w_q_a.data_ptr() if self.w_q_a is not None else None
+        pj.q_a_norm_w = self.q_a_norm_w.data_ptr() if self.q_a_norm_w is not None else None
+        pj.w_q = self.w_q.data_ptr()
+        pj.w_kva = self.w_kva.data_ptr() if with_kva else None
+        pj.w_o = self.w_o.data_ptr()
+        self.pj = pj
+        B = wl.B
+        act = torch.int16 if wl.act == "bf16" else torch.float32
+        self.q = torch.zeros((B, wl.H, wl.N + wl.R), dtype=act, device=d)
+        self.kva = torch.zeros((B, wl.C + wl.R), dtype=torch.float32, device=d) if with_kva else None
+        self.y = torch.zeros((B, wl.hidden), dtype=torch.float32, device=d)
+        st, n = L.mla_front_end_workspace_size(cfg, pj, B)
+        L.check(st, "mla_front_end_workspace_size")
+        self.ws = torch.zeros(max(n, 256), dtype=torch.uint8, device=d)
+
+    def front_end(self):
+        return L.mla_front_end(self.cfg, self.pj, self.x, self.q, self.kva, self.wl.B, self.ws,
+                               self.ws.numel(), self.stream)
+
+    def o_proj(self, attn=None):
+        return L.mla_o_proj(self.cfg, self.pj, self.attn if attn is None else attn, self.y, self.wl.B,
+                            self.stream)
+
+    def q_host(self) -> np.ndarray:
+        q = self.q.cpu().numpy()
+        return q.view(np.uint16) if self.wl.act == "bf16" else q

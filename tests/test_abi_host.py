@@ -164,3 +164,53 @@ def test_q4_affine_kv_b_contract(L):
     assert L.mla_kv_b_bytes(cfg) == size
     cfg.kv_lora = 96
     assert L.mla_kv_b_bytes(cfg) == 0
+
+
+def _proj(L, **kw):
+    pj = L.MlaProj()
+    pj.hidden, pj.q_lora, pj.w_dtype, pj.q_norm_eps = 7168, 1536, L.MLA_BF16, 1e-6
+    pj.w_q_a, pj.q_a_norm_w, pj.w_q, pj.w_kva, pj.w_o = 0x10000, 0x20000, 0x30000, 0x40000, 0x50000
+    for k, v in kw.items():
+        setattr(pj, k, v)
+    return pj
+
+
+def test_front_end_workspace_size(L):
+    st, n = L.mla_front_end_workspace_size(_cfg(L), _proj(L), 64)
+    assert st == 0 and n == 64 * 1536 * 4
+    st, n = L.mla_front_end_workspace_size(_cfg(L), _proj(L, q_lora=0), 64)
+    assert st == 0 and n == 0
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(hidden=7164), "MLA_ERR_INVALID_ARG"),                        # not a multiple of 8
+    (dict(hidden=0), "MLA_ERR_INVALID_ARG"),
+    (dict(q_lora=-1), "MLA_ERR_INVALID_ARG"),
+    (dict(q_lora=1540), "MLA_ERR_INVALID_ARG"),
+    (dict(w_dtype=2, hidden=7168 + 16), "MLA_ERR_INVALID_ARG"),  # Q8_0 blocks need % 32
+    (dict(w_dtype=3, q_lora=1536 + 32), "MLA_ERR_INVALID_ARG"),        # 4-bit groups need % 64
+    (dict(w_dtype=9), "MLA_ERR_UNSUPPORTED"),
+])
+def test_projection_contract_rejected_on_the_host(L, bad, status):
+    st, _ = L.mla_front_end_workspace_size(_cfg(L), _proj(L, **bad), 4)
+    assert st == L.STATUS_CODE[status]
+
+
+def test_front_end_and_o_proj_null_and_misaligned_args(L):
+    # every call below must fail host validation: none of them may reach a kernel launch
+    cfg, pj = _cfg(L), _proj(L)
+    INVALID = L.STATUS_CODE["MLA_ERR_INVALID_ARG"]
+    ws, n = 0x70000, 4 * 1536 * 4
+    assert L.mla_front_end(cfg, pj, None, 0x60000, 0x61000, 4, ws, n) == INVALID
+    assert L.mla_front_end(cfg, pj, 0x60008, 0x60000, 0x61000, 4, ws, n) == INVALID
+    assert L.mla_front_end(cfg, pj, 0x60000, None, 0x61000, 4, ws, n) == INVALID
+    assert L.mla_front_end(cfg, _proj(L, w_kva=None), 0x60000, 0x61000, 0x62000, 4, ws, n) == INVALID
+    assert L.mla_front_end(cfg, _proj(L, q_a_norm_w=None), 0x60000, 0x61000, None, 4, ws, n) == INVALID
+    assert L.mla_front_end(cfg, pj, 0x60000, 0x61000, None, 0, ws, n) == INVALID
+    assert L.mla_front_end(cfg, pj, 0x60000, 0x61000, None, 4, ws, n - 1) == L.STATUS_CODE["MLA_ERR_WORKSPACE"]
+    assert L.mla_o_proj(cfg, _proj(L, w_o=None), 0x60000, 0x61000, 4) == INVALID
+    assert L.mla_o_proj(cfg, pj, 0x60004, 0x61000, 4) == INVALID
+    # o_proj's in_dim is H*V: 3 heads of 8 values (24) is no multiple of the 4-bit group of 64
+    odd = _cfg(L)
+    odd.n_heads, odd.v_head = 3, 8
+    assert L.mla_o_proj(odd, _proj(L, w_dtype=3), 0x60000, 0x61000, 4) == INVALID
