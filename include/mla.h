@@ -317,6 +317,35 @@ mla_status mla_front_end(const mla_config* cfg, const mla_proj* pj, const void* 
 mla_status mla_o_proj(const mla_config* cfg, const mla_proj* pj, const float* attn, float* y,
                       int32_t B, mla_stream_t stream);
 
+/* ---- several query tokens per sequence ----------------------------------------------------
+ * T new tokens of each sequence decoded at once (draft tokens of speculative decoding, a chunk
+ * of a prompt), their rows already in the cache: token i of sequence b sits at position
+ * positions[b] + i and attends the first seq_lens[b] - T + 1 + i rows (itself and every row
+ * before it). The pages have no MLA prefill; this follows the causal decode of one token (moeflux
+ * mla_attn_forward.rs, folded SDPA over cache_len = pos + 1 rows) applied to T stacked query
+ * tokens, as moeflux gpu_matvec.rs's *_n_tokens encoders apply one weight matrix to N stacked
+ * inputs. The T tokens run as T x H heads of one sequence (token-major), so every staged row
+ * tile serves all of them; T = 1 is exactly mla_decode_attn (same kernels, bit-identical).
+ *
+ * Bytes of workspace mla_decode_attn_multi needs for (cfg, T, B); as
+ * mla_decode_workspace_size for T = 1. INVALID_ARG for T < 1, T > 64 or T*H > 65536. */
+mla_status mla_decode_multi_workspace_size(const mla_config* cfg, int32_t tokens, int32_t B,
+                                           size_t* bytes);
+
+/* Multi-token decode for B sequences (async).
+ *   q          device [B, T, H, N+R] act_dtype (token i of sequence b at q[b][i]).
+ *   seq_lens   device [B] int32: rows the last token attends (T <= seq_lens[b] <= capacity);
+ *              the tokens' own rows are the last T of them.
+ *   positions  device [B] int32 RoPE position of each sequence's first token, or NULL when
+ *              q_pe is already rotated.
+ *   out        device [B, T, H, V] float32; lse device [B, T, H] float32 or NULL.
+ * Other arguments, launches and errors as mla_decode_attn; a seq_lens[b] below T is the device
+ * error BAD_SEQ_LEN (that sequence's outputs NaN). */
+mla_status mla_decode_attn_multi(const mla_config* cfg, int32_t tokens, const void* q,
+                                 const void* kv_b, const mla_cache* cache, const int32_t* seq_lens,
+                                 const int32_t* positions, float* out, float* lse, int32_t B,
+                                 void* workspace, size_t ws_bytes, mla_stream_t stream);
+
 /* ---- device error word ------------------------------------------------------------------ */
 
 /* Synchronises `stream`, then reads the workspace's sticky error word: returns the first

@@ -23,7 +23,7 @@ template <int DT>
 __global__ void __launch_bounds__(ABS_THREADS, 4)
 absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const void* __restrict__ kv_b,
               const int32_t* __restrict__ positions, typename Act<DT>::T* __restrict__ q_abs,
-              typename Act<DT>::T* __restrict__ q_res, int B) {
+              typename Act<DT>::T* __restrict__ q_res, int B, int pos_t) {
   // value v goes out as its storage rounding, and (bf16 only) the rounding residual to q_res
   auto put = [&](int64_t i, float v) {
     Act<DT>::store(q_abs, i, v);
@@ -58,7 +58,7 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
     px0 = Act<DT>::load(q, qi);
     px1 = Act<DT>::load(q, qi + 1);
     if (positions != nullptr) {
-      ppos = positions[b];
+      ppos = positions[b / pos_t] + b % pos_t;
       pinv = cfg.rope_inv_freq[p];
     }
   }
@@ -84,7 +84,7 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
       px0 = Act<DT>::load(q, qi);
       px1 = Act<DT>::load(q, qi + 1);
       if (positions != nullptr) {
-        ppos = positions[b];
+        ppos = positions[b / pos_t] + b % pos_t;
         pinv = cfg.rope_inv_freq[p];
       }
     }
@@ -141,7 +141,9 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
 }
 
 cudaError_t launch_absorb(const mla_config& cfg, const void* q, const void* kv_b,
-                          const int32_t* positions, void* q_abs, void* q_res, int B, bool pdl, cudaStream_t st) {
+                          const int32_t* positions, void* q_abs, void* q_res, int B, bool pdl, cudaStream_t st,
+                          int pos_t) {
+  if (pos_t < 1) return cudaErrorInvalidValue;
   dim3 grid(cfg.n_heads, (cfg.kv_lora + ABS_COLS - 1) / ABS_COLS);
   const size_t bchunk = (size_t)(B < ABS_BCHUNK ? B : ABS_BCHUNK);
   const size_t smem = sizeof(float) * ((size_t)cfg.qk_nope * ABS_COLS + bchunk * cfg.qk_nope + 4 * bchunk * ABS_COLS);
@@ -150,13 +152,13 @@ cudaError_t launch_absorb(const mla_config& cfg, const void* q, const void* kv_b
     cudaError_t e = ensure_smem((const void*)k, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_kernel(pdl, k, grid, dim3(ABS_THREADS), smem, st, cfg, static_cast<const uint16_t*>(q), kv_b, positions,
-                      static_cast<uint16_t*>(q_abs), static_cast<uint16_t*>(q_res), B);
+                      static_cast<uint16_t*>(q_abs), static_cast<uint16_t*>(q_res), B, pos_t);
   } else {
     auto k = absorb_kernel<MLA_F32>;
     cudaError_t e = ensure_smem((const void*)k, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_kernel(pdl, k, grid, dim3(ABS_THREADS), smem, st, cfg, static_cast<const float*>(q), kv_b, positions,
-                      static_cast<float*>(q_abs), static_cast<float*>(nullptr), B);
+                      static_cast<float*>(q_abs), static_cast<float*>(nullptr), B, pos_t);
   }
 }
 

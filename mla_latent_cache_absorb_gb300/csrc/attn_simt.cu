@@ -31,6 +31,9 @@ struct SimtArgs {
   int H, C, R, hpb, S;
   int64_t chunk;
   float scale;
+  // query tokens per sequence (heads token-major, kvb_heads per token): head m sees the rows
+  // before L - tokens + 1 + m / kvb_heads
+  int tokens, kvb_heads;
 };
 
 template <int DT>
@@ -44,7 +47,7 @@ __global__ void __launch_bounds__(SIMT_THREADS) attn_simt_kernel(SimtArgs a) {
   const int h0 = g * a.hpb;
   const int nh = min(a.hpb, a.H - h0);
   const int64_t L = a.seq_lens[b];
-  const bool len_ok = (L >= 1 && L <= a.map.capacity());
+  const bool len_ok = (L >= 1 && L >= a.tokens && L <= a.map.capacity());
   if (threadIdx.x == 0 && s == 0 && g == 0) {
     // slots of sequence b for the combine stage: b*S .. b*S + ceil(L/chunk) - 1
     a.meta[2 * b] = b * a.S;
@@ -106,17 +109,20 @@ __global__ void __launch_bounds__(SIMT_THREADS) attn_simt_kernel(SimtArgs a) {
       if (tt < nt)
         for (int k = lane; k < row; k += 32) d = fmaf(q_s[hh * row + k], tile[tt * row + k], d);
       d = warp_sum(d);
-      if (lane == 0) p_s[hh * SIMT_TT + tt] = (tt < nt) ? d * a.scale : -CUDART_INF_F;
+      const bool seen = tt < nt && tb + tt < L - a.tokens + 1 + (h0 + hh) / a.kvb_heads;
+      if (lane == 0) p_s[hh * SIMT_TT + tt] = seen ? d * a.scale : -CUDART_INF_F;
     }
     __syncthreads();
     // online softmax, one thread per head
     for (int hh = threadIdx.x; hh < nh; hh += SIMT_THREADS) {
       float mx = m_s[hh];
       for (int tt = 0; tt < nt; ++tt) mx = fmaxf(mx, p_s[hh * SIMT_TT + tt]);
-      const float alpha = expf(m_s[hh] - mx);   // exp(-inf) = 0 on the first tile
+      // exp(-inf) = 0 on the first tile; a head that sees no row yet keeps its zero sums
+      const float alpha = mx == -CUDART_INF_F ? 1.f : expf(m_s[hh] - mx);
       float sum = 0.f;
       for (int tt = 0; tt < SIMT_TT; ++tt) {
-        const float p = (tt < nt) ? expf(p_s[hh * SIMT_TT + tt] - mx) : 0.f;
+        const float sc = p_s[hh * SIMT_TT + tt];
+        const float p = (tt < nt && sc != -CUDART_INF_F) ? expf(sc - mx) : 0.f;
         p_s[hh * SIMT_TT + tt] = p;
         sum += p;
       }
@@ -142,10 +148,12 @@ __global__ void __launch_bounds__(SIMT_THREADS) attn_simt_kernel(SimtArgs a) {
     const int idx = threadIdx.x + k * SIMT_THREADS;
     if (idx < n_out) {
       const int hh = idx / a.C, c = idx % a.C;
-      po[(int64_t)hh * a.C + c] = acc[k] / l_s[hh];
+      // l = 0: no row of this split is visible to the head: O = 0, lse = -inf (weight 0)
+      po[(int64_t)hh * a.C + c] = l_s[hh] > 0.f ? acc[k] / l_s[hh] : 0.f;
     }
   }
-  for (int hh = threadIdx.x; hh < nh; hh += SIMT_THREADS) pl[hh] = m_s[hh] + logf(l_s[hh]);
+  for (int hh = threadIdx.x; hh < nh; hh += SIMT_THREADS)
+    pl[hh] = l_s[hh] > 0.f ? m_s[hh] + logf(l_s[hh]) : -CUDART_INF_F;
 }
 
 int simt_heads_per_cta(const mla_config& cfg) {
@@ -179,6 +187,9 @@ cudaError_t launch_attn_simt(const mla_config& cfg, const mla_cache& cache, cons
   a.S = plan.splits;
   a.chunk = plan.chunk_rows;
   a.scale = cfg.softmax_scale;
+  a.tokens = plan.tokens;
+  a.kvb_heads = plan.kvb_heads;
+  if (a.tokens < 1 || a.kvb_heads < 1 || a.tokens * a.kvb_heads != cfg.n_heads) return cudaErrorInvalidValue;
   dim3 grid(plan.splits, B, plan.n_groups);
   const size_t smem = simt_smem_bytes(cfg, plan.heads_per_cta);
   cudaError_t e;

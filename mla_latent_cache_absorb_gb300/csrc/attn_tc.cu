@@ -36,6 +36,7 @@
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
+#include <climits>
 #include <cudaTypedefs.h>
 #include <math_constants.h>
 
@@ -96,6 +97,9 @@ struct TcArgs {
   // stream had completed, and writes no cache row; cache rows may then be read before the
   // dependency wait (only the queries wait for it)
   int kv_early;
+  // query tokens per sequence (heads token-major, kvb_heads per token): head m sees the rows
+  // before L - tokens + 1 + m / kvb_heads; one token: every head sees the L rows
+  int tokens, kvb_heads;
 };
 
 struct Smem {
@@ -146,10 +150,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Tiles a sequence contributes (0 for an invalid length).
+// Tiles a sequence contributes (0 for an invalid length: below one row per query token, or
+// past the capacity).
 __device__ __forceinline__ long long seq_tiles(const TcArgs& a, int b) {
   const long long L = a.seq_lens[b];
-  if (L < 1 || L > a.map.capacity()) return 0;
+  if (L < a.tokens || L < 1 || L > a.map.capacity()) return 0;
   return (L + TC_TILE - 1) / TC_TILE;
 }
 
@@ -539,7 +544,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
         const uint32_t s_addr = tmem + lane_base + Cfg<HG>::S_COL + sbuf * HG + h0;
         if (!softmax_wait(s, &s.s_full[sbuf], (uint32_t)((n >> 1) & 1), wg, a.wait_ns)) { ok = false; break; }
         tc::tc_fence_after();
-        const bool valid = (long long)t * TC_TILE + row < L;
+        // Row validity per head: a row at or past L is nobody's; one before L - tokens + 1 is
+        // every head's; in between, head m of the sequence sees it iff m >= hthr (the heads of
+        // the later tokens). Column j of this group is head g * HG + j of the sequence.
+        const long long rg = (long long)t * TC_TILE + row;
+        const long long lim0 = L - a.tokens + 1;
+        const bool valid = rg < L;
+        const int hthr = !valid ? INT_MAX : (rg < lim0 ? 0 : (int)(rg - lim0 + 1) * a.kvb_heads);
+        const int hcol0 = g * HG + h0;   // sequence head of this warpgroup's column 0
         const bool first = (t == tlo);
         // PV of the previous tile has completed (its commit preceded this tile's QK commit);
         // waiting keeps the o_done phases in step for every softmax thread
@@ -552,11 +564,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
           uint32_t r[CW];
           tc::tmem_ld<CW>(s_addr + half * CW, r);
           tc::tmem_wait_ld();
-          if (valid) {
 #pragma unroll
-            for (int j = 0; j < CW; ++j)
+          for (int j = 0; j < CW; ++j)
+            if (hcol0 + half * CW + j >= hthr)
               need |= fmaf(__uint_as_float(r[j]), a.scale_log2, -s.m2[h0 + half * CW + j]) > RESCALE_THRESHOLD;
-          }
         }
         __syncwarp();
         if (softmax_vote_or(need, wg)) {
@@ -567,7 +578,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
             tc::tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < CW; ++j) {
-              float v = valid ? __uint_as_float(r[j]) * a.scale_log2 : -CUDART_INF_F;
+              float v = hcol0 + half * CW + j >= hthr ? __uint_as_float(r[j]) * a.scale_log2 : -CUDART_INF_F;
 #pragma unroll
               for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
               if (lane == 0) s.red[q][h0 + half * CW + j] = v;
@@ -579,7 +590,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
             const float mt = fmaxf(fmaxf(s.red[0][h], s.red[1][h]), fmaxf(s.red[2][h], s.red[3][h]));
             const float mo = s.m2[h];
             const float mn = fmaxf(mo, mt);
-            s.alpha[h] = first ? 0.f : ex2(mo - mn);
+            // a head with no visible row yet keeps its (zero) sums: factor 1, not ex2(-inf + inf)
+            s.alpha[h] = first ? 0.f : (mn == -CUDART_INF_F ? 1.f : ex2(mo - mn));
             s.m2[h] = mn;
           }
           softmax_bar(wg);
@@ -619,10 +631,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
               const int j = c4 * 8 + 2 * e;
               const int h = half * CW + j;
               float p0 = 0.f, p1 = 0.f;
-              if (valid) {
-                p0 = ex2(fmaf(__uint_as_float(r[j]), a.scale_log2, -s.m2[h0 + h]));
-                p1 = ex2(fmaf(__uint_as_float(r[j + 1]), a.scale_log2, -s.m2[h0 + h + 1]));
-              }
+              if (hcol0 + h >= hthr) p0 = ex2(fmaf(__uint_as_float(r[j]), a.scale_log2, -s.m2[h0 + h]));
+              if (hcol0 + h + 1 >= hthr) p1 = ex2(fmaf(__uint_as_float(r[j + 1]), a.scale_log2, -s.m2[h0 + h + 1]));
               lp[h] += p0;
               lp[h + 1] += p1;
               w[e] = pack_bf16x2(p0, p1);
@@ -664,7 +674,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_consta
       if (sidx < HW) {
         const int h = h0 + sidx;
         const float l = s.red[0][h] + s.red[1][h] + s.red[2][h] + s.red[3][h];
-        s.alpha[h] = 1.0f / l;
+        // l = 0: no row of this piece is visible to the head (a later token's row range):
+        // O stays 0 and lse = -inf, weight 0 in the combine
+        s.alpha[h] = l > 0.f ? 1.0f / l : 0.f;
         if (h < nh) {
           const bool bad = *reinterpret_cast<volatile int*>(&s.bad_page[seg & 1][wg]) != 0;
           a.part_lse[(size_t)(g * a.n_slots + slot) * HG + h] =
@@ -764,6 +776,9 @@ cudaError_t launch_attn_tc(const mla_config& cfg, const mla_cache& cache, const 
   a.scale_log2 = cfg.softmax_scale * 1.4426950408889634f;
   a.kv_early = kv_early ? 1 : 0;
   a.wait_ns = wait_limit_ns();
+  a.tokens = plan.tokens;
+  a.kvb_heads = plan.kvb_heads;
+  if (a.tokens < 1 || a.kvb_heads < 1 || a.tokens * a.kvb_heads != cfg.n_heads) return cudaErrorInvalidValue;
   const int grid = plan.n_groups * plan.ctas_per_group;
   cudaError_t e;
   switch (plan.heads_per_cta) {

@@ -38,6 +38,7 @@ struct CombineArgs {
   int H, C, N, V, R, B;
   int hpg, n_slots, max_slots;
   int vper;                 // outputs per CTA (a multiple of CMB_VJ): the merge is done once per CTA
+  int kvb_heads;            // heads of kv_b: head h up-projects through W_UV of head h % kvb_heads
 };
 
 // out[b0 + bb, h, j0 + j] = W_UV row j . vc[bb] for bb < nb <= NBT: one warp per pair of outputs
@@ -105,8 +106,8 @@ __global__ void __launch_bounds__(CMB_THREADS, 2) combine_kernel(CombineArgs a) 
   auto lse_at = [&](int slot) { return ((int64_t)pg * a.n_slots + slot) * a.hpg + hh; };
 
   // W_UV rows of the first 32-output chunk (the rest follow after the merge)
-  const int64_t wrow0 = (int64_t)h * (a.N + a.V) + a.N;
-  const int64_t kv_rows = (int64_t)a.H * (a.N + a.V);
+  const int64_t wrow0 = (int64_t)(h % a.kvb_heads) * (a.N + a.V) + a.N;
+  const int64_t kv_rows = (int64_t)a.kvb_heads * (a.N + a.V);
   stage_kv_b_rows(w_s, 4 * C4, a.kv_b, a.kv_b_dtype, wrow0 + jbeg, min(CMB_VJ, jend - jbeg), 0, C, C, CMB_THREADS,
                   kv_rows);
   pdl_wait();   // the partials and meta come from the attention kernel
@@ -266,6 +267,8 @@ cudaError_t launch_combine(const mla_config& cfg, const DecodePlan& plan, const 
   a.scale = cfg.softmax_scale;
   a.H = cfg.n_heads; a.C = cfg.kv_lora; a.N = cfg.qk_nope; a.V = cfg.v_head; a.R = cfg.qk_rope; a.B = B;
   a.hpg = plan.part_hpg; a.n_slots = plan.n_slots;
+  if (plan.kvb_heads < 1 || plan.kvb_heads * plan.tokens != cfg.n_heads) return cudaErrorInvalidValue;
+  a.kvb_heads = plan.kvb_heads;
   // most slots one sequence can span: splits (CUDA-core path) or CTAs per group (tensor path)
   a.max_slots = plan.path != PATH_SIMT ? plan.ctas_per_group : plan.splits;
   // V-slices per head: enough CTAs to cover the SMs, but every slice merges the partials again

@@ -271,6 +271,10 @@ struct DecodePlan {
   int64_t chunk_rows;    // CUDA-core path: rows per split (a multiple of its row tile)
   int64_t capacity;      // maximum rows a sequence can attend
   int ctas_per_group;    // tensor-core paths: CTAs (pair path: CTA pairs) sharing one tile list
+  // query tokens per sequence: the attention and combine see tokens * kvb_heads heads per
+  // sequence (token-major); head m up-projects through W_UV of head m % kvb_heads and sees the
+  // rows before L - tokens + 1 + m / kvb_heads
+  int tokens, kvb_heads;
   // partials: part_o[g][slot][hh][C], part_lse[g][slot][hh] for part_groups x n_slots slots of
   // part_hpg heads; meta[b] = {first slot, slot count} of sequence b (count 0: invalid length)
   int part_groups, part_hpg, n_slots;
@@ -301,8 +305,10 @@ cudaError_t launch_append_finish(const mla_config& cfg, const mla_cache& cache, 
                                  const float* norm_w, const int32_t* positions,
                                  const int32_t* seq_lens, int B, WsHeader* hdr, bool kva_dep, cudaStream_t st);
 // pdl = false: the absorb starts only after all earlier work on the stream has completed
+// pos_t: query tokens per sequence; the position of query row b is positions[b / pos_t] + b % pos_t
 cudaError_t launch_absorb(const mla_config& cfg, const void* q, const void* kv_b,
-                          const int32_t* positions, void* q_abs, void* q_res, int B, bool pdl, cudaStream_t st);
+                          const int32_t* positions, void* q_abs, void* q_res, int B, bool pdl, cudaStream_t st,
+                          int pos_t = 1);
 cudaError_t launch_attn_simt(const mla_config& cfg, const mla_cache& cache, const DecodePlan& plan,
                              const int32_t* seq_lens, const void* q_abs, const void* q_res, float* part_o,
                              float* part_lse, int32_t* meta, int B, WsHeader* hdr, cudaStream_t st);
@@ -323,7 +329,8 @@ int tc_heads_per_cta(int H);
 bool absorb_tc_supported(const mla_config& cfg, int B);
 bool combine_tc_supported(const mla_config& cfg, int B);
 cudaError_t launch_absorb_tc(const mla_config& cfg, const void* q, const void* kv_b, const int32_t* positions,
-                             void* q_abs, void* q_res, int B, WsHeader* hdr, bool pdl, cudaStream_t st);
+                             void* q_abs, void* q_res, int B, WsHeader* hdr, bool pdl, cudaStream_t st,
+                             int pos_t = 1);
 // q_res != nullptr: the partials came from bf16 latent queries; the combine adds the first-order
 // LSE correction softmax_scale * (vc . q_res[latent]) for the residual the scores did not see.
 cudaError_t launch_combine_tc(const mla_config& cfg, const DecodePlan& plan, const void* kv_b,

@@ -51,6 +51,7 @@ struct AbsorbTcArgs {
   WsHeader* hdr;
   uint64_t wait_ns;
   int B, H, N, R, V, C;
+  int pos_t;                // query tokens per sequence: row b's position is positions[b / pos_t] + b % pos_t
 };
 
 // grid (H, 2 latent halves, batch chunks of 64); 128 threads
@@ -157,7 +158,7 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
       if (i < pe) {
         const int bb = i / hr, p = i - bb * hr;
         xv[m] = *reinterpret_cast<const uint32_t*>(a.q + ((size_t)(b0 + bb) * a.H + h) * qrow + a.N + 2 * p);
-        if (a.positions != nullptr) pv[m] = a.positions[b0 + bb];
+        if (a.positions != nullptr) pv[m] = a.positions[(b0 + bb) / a.pos_t] + (b0 + bb) % a.pos_t;
       }
     }
     auto rotate = [&](int i, uint32_t x, int pos) {
@@ -188,7 +189,7 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
     for (int i = pb + tid + RI * G_THREADS; i < pe; i += G_THREADS) {
       const int bb = i / hr, p = i - bb * hr;
       rotate(i, *reinterpret_cast<const uint32_t*>(a.q + ((size_t)(b0 + bb) * a.H + h) * qrow + a.N + 2 * p),
-             a.positions != nullptr ? a.positions[b0 + bb] : 0);
+             a.positions != nullptr ? a.positions[(b0 + bb) / a.pos_t] + (b0 + bb) % a.pos_t : 0);
     }
   }
   __syncwarp();   // lanes 1-31 of warp 0 wait for lane 0
@@ -266,6 +267,7 @@ struct CombineTcArgs {
   WsHeader* hdr;
   uint64_t wait_ns;
   int H, C, N, V, R, B, hpg, n_slots, max_slots;
+  int kvb_heads;            // heads of kv_b: head h up-projects through W_UV of head h % kvb_heads
 };
 
 // grid (H, batch chunks of 32); 512 threads
@@ -309,7 +311,7 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap w_map, CombineTcArgs a) {
   if (tid == 0) {
     tc::mbar_arrive_expect_tx(&bar_w, 8 * 16384);
     for (int kb = 0; kb < 8; ++kb)
-      tc::tma_load_2d(wu + kb * 16384, &w_map, 64 * kb, h * (a.N + a.V) + a.N, &bar_w);
+      tc::tma_load_2d(wu + kb * 16384, &w_map, 64 * kb, (h % a.kvb_heads) * (a.N + a.V) + a.N, &bar_w);
   }
   pdl_wait();   // the partials and meta come from the attention kernel
   // split weights: 16 lanes per sequence, every sequence of the chunk at once, the first
@@ -519,7 +521,9 @@ bool combine_tc_supported(const mla_config& cfg, int B) {
 }
 
 cudaError_t launch_absorb_tc(const mla_config& cfg, const void* q, const void* kv_b, const int32_t* positions,
-                             void* q_abs, void* q_res, int B, WsHeader* hdr, bool pdl, cudaStream_t st) {
+                             void* q_abs, void* q_res, int B, WsHeader* hdr, bool pdl, cudaStream_t st,
+                             int pos_t) {
+  if (pos_t < 1) return cudaErrorInvalidValue;
   CUtensorMap w_map;
   if (!make_map_2d_bf16(&w_map, kv_b, 512, (uint64_t)cfg.n_heads * (cfg.qk_nope + cfg.v_head), 64, 128))
     return cudaErrorInvalidValue;
@@ -532,6 +536,7 @@ cudaError_t launch_absorb_tc(const mla_config& cfg, const void* q, const void* k
   a.hdr = hdr;
   a.wait_ns = wait_limit_ns();
   a.B = B; a.H = cfg.n_heads; a.N = cfg.qk_nope; a.R = cfg.qk_rope; a.V = cfg.v_head; a.C = cfg.kv_lora;
+  a.pos_t = pos_t;
   cudaError_t e = ensure_smem((const void*)absorb_tc_kernel, ABS_TC_SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(cfg.n_heads, 2, (B + ABS_TC_BCHUNK - 1) / ABS_TC_BCHUNK);
@@ -541,8 +546,10 @@ cudaError_t launch_absorb_tc(const mla_config& cfg, const void* q, const void* k
 cudaError_t launch_combine_tc(const mla_config& cfg, const DecodePlan& plan, const void* kv_b,
                               const int32_t* meta, const float* part_o, const float* part_lse, const void* q_res,
                               float* out, float* lse, int B, WsHeader* hdr, cudaStream_t st) {
+  // cfg.n_heads = plan.tokens query tokens x plan.kvb_heads heads of kv_b
+  if (plan.kvb_heads < 1 || plan.kvb_heads * plan.tokens != cfg.n_heads) return cudaErrorInvalidValue;
   CUtensorMap w_map;
-  if (!make_map_2d_bf16(&w_map, kv_b, 512, (uint64_t)cfg.n_heads * (cfg.qk_nope + cfg.v_head), 64, 128))
+  if (!make_map_2d_bf16(&w_map, kv_b, 512, (uint64_t)plan.kvb_heads * (cfg.qk_nope + cfg.v_head), 64, 128))
     return cudaErrorInvalidValue;
   CombineTcArgs a;
   a.meta = meta; a.part_o = part_o; a.part_lse = part_lse; a.out = out; a.lse = lse; a.hdr = hdr;
@@ -551,6 +558,7 @@ cudaError_t launch_combine_tc(const mla_config& cfg, const DecodePlan& plan, con
   a.wait_ns = wait_limit_ns();
   a.H = cfg.n_heads; a.C = cfg.kv_lora; a.N = cfg.qk_nope; a.V = cfg.v_head; a.R = cfg.qk_rope; a.B = B;
   a.hpg = plan.part_hpg; a.n_slots = plan.n_slots;
+  a.kvb_heads = plan.kvb_heads;
   a.max_slots = plan.path != PATH_SIMT ? plan.ctas_per_group : plan.splits;
   const int smem = CMB_TC_WSMEM + 1024 + CMB_TC_BCHUNK * (64 + a.max_slots) * (int)sizeof(float);
   cudaError_t e = ensure_smem((const void*)combine_tc_kernel, smem);

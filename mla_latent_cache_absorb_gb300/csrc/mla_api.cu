@@ -81,12 +81,17 @@ int simt_heads_per_cta(const mla_config& cfg);
 
 // The split plan: how many row splits per sequence, how many rows each, and where the
 // workspace keeps the fused query rows and the per-split partials.
-static mla_status make_plan(const mla_config& cfg, int B, DecodePlan* p) {
+// tokens > 1: cfg.n_heads counts tokens x (heads of kv_b) per sequence, token-major; the SM-pair
+// kernel (one head per row of its tile, no per-head row limit) is not used then.
+static mla_status make_plan(const mla_config& cfg, int B, DecodePlan* p, int tokens = 1) {
   const int sms = device_sms();
   if (sms <= 0) return MLA_ERR_CUDA;
   std::memset(p, 0, sizeof(*p));
+  if (tokens < 1 || cfg.n_heads % tokens != 0) return MLA_ERR_INVALID_ARG;
+  p->tokens = tokens;
+  p->kvb_heads = cfg.n_heads / tokens;
   p->capacity = cfg.page_size == 0 ? cfg.rows_per_seq : (int64_t)cfg.max_pages_per_seq * cfg.page_size;
-  const int max_pairs = attn_pair_supported(cfg) ? attn_pair_max_pairs() : -1;
+  const int max_pairs = tokens == 1 && attn_pair_supported(cfg) ? attn_pair_max_pairs() : -1;
   if (max_pairs > 0) {
     // 128 heads: one cluster of two CTAs per SM pair, the 64-row tile list split evenly over
     // the pairs that fit on the device at once
@@ -589,6 +594,71 @@ mla_status mla_o_proj(const mla_config* cfg, const mla_proj* pj, const float* at
     return MLA_ERR_INVALID_ARG;
   return cuda_status(launch_proj(attn, false, (int)k, B, pj->w_dtype, pj->w_o, pj->hidden, y, false, nullptr, 0,
                                  nullptr, false, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// ---- several query tokens per sequence -------------------------------------------------------
+// The T tokens of a sequence attend as T x H heads of one sequence (token-major), so every
+// staged row tile serves all of them; the absorb sees B x T query rows of H heads.
+
+static mla_status multi_cfg(const mla_config* cfg, int32_t tokens, mla_config* out) {
+  mla_status st = check_cfg(cfg);
+  if (st != MLA_OK) return st;
+  if (tokens < 1 || tokens > 64 || (int64_t)tokens * cfg->n_heads > 65536) return MLA_ERR_INVALID_ARG;
+  *out = *cfg;
+  out->n_heads = tokens * cfg->n_heads;
+  return MLA_OK;
+}
+
+mla_status mla_decode_multi_workspace_size(const mla_config* cfg, int32_t tokens, int32_t B, size_t* bytes) {
+  if (tokens == 1) return mla_decode_workspace_size(cfg, B, bytes);
+  mla_config vc;
+  mla_status st = multi_cfg(cfg, tokens, &vc);
+  if (st != MLA_OK) return st;
+  if (B < 1 || bytes == nullptr) return MLA_ERR_INVALID_ARG;
+  DecodePlan p;
+  st = make_plan(vc, B, &p, tokens);
+  if (st != MLA_OK) return st;
+  *bytes = p.total;
+  return MLA_OK;
+}
+
+mla_status mla_decode_attn_multi(const mla_config* cfg, int32_t tokens, const void* q, const void* kv_b,
+                                 const mla_cache* cache, const int32_t* seq_lens, const int32_t* positions,
+                                 float* out, float* lse, int32_t B, void* workspace, size_t ws_bytes,
+                                 mla_stream_t stream) {
+  if (tokens == 1)
+    return mla_decode_attn(cfg, q, kv_b, cache, seq_lens, positions, out, lse, B, workspace, ws_bytes, stream);
+  mla_config vc;
+  mla_status st = multi_cfg(cfg, tokens, &vc);
+  if (st != MLA_OK) return st;
+  if (B < 1 || (int64_t)B * tokens >= (int64_t(1) << 31)) return MLA_ERR_INVALID_ARG;
+  DecodePlan plan;
+  st = make_plan(vc, B, &plan, tokens);
+  if (st != MLA_OK) return st;
+  st = check_ws(workspace, ws_bytes, plan.total);
+  if (st != MLA_OK) return st;
+  st = check_absorb_args(cfg, q, kv_b, positions);
+  if (st != MLA_OK) return st;
+  if (seq_lens == nullptr || out == nullptr) return MLA_ERR_INVALID_ARG;
+  st = check_cache(&vc, cache, B);
+  if (st != MLA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t tiles128 = (int64_t)B * ((plan.capacity + 127) / 128);
+  const bool early = plan.path == PATH_TC && tiles128 >= 4 * (int64_t)plan.ctas_per_group;
+  // absorb: B x T query rows of H heads (query row b*T + i sits at positions[b] + i); the fused
+  // rows land as [B][T*H][C+R], the attention's T*H heads per sequence
+  void* q_abs = static_cast<char*>(workspace) + plan.off_qabs;
+  void* q_res = cfg->act_dtype == MLA_BF16 ? static_cast<char*>(workspace) + plan.off_qres : nullptr;
+  const int bq = B * tokens;
+  if (absorb_tc_supported(*cfg, bq))
+    st = cuda_status(launch_absorb_tc(*cfg, q, kv_b, positions, q_abs, q_res, bq, static_cast<WsHeader*>(workspace),
+                                      !early, s, tokens));
+  else
+    st = cuda_status(launch_absorb(*cfg, q, kv_b, positions, q_abs, q_res, bq, !early, s, tokens));
+  if (st != MLA_OK) return st;
+  st = enqueue_partial(&vc, plan, cache, seq_lens, B, workspace, early, s);
+  if (st != MLA_OK) return st;
+  return enqueue_combine(&vc, plan, kv_b, out, lse, B, workspace, s);
 }
 
 }  // extern "C"

@@ -78,11 +78,13 @@ class DeviceStep:
         st, n = L.mla_append_workspace_size(self.cfg, B)
         L.check(st, "mla_append_workspace_size")
         self.ws_append = torch.zeros(n, dtype=torch.uint8, device=d)
-        st, n = L.mla_decode_workspace_size(self.cfg, B)
-        L.check(st, "mla_decode_workspace_size")
+        T = wl.tokens
+        st, n = L.mla_decode_multi_workspace_size(self.cfg, T, B)
+        L.check(st, "mla_decode_multi_workspace_size")
         self.ws_decode = torch.zeros(n, dtype=torch.uint8, device=d)
-        self.out = torch.empty((B, wl.H, wl.V), dtype=torch.float32, device=d)
-        self.lse = torch.empty((B, wl.H), dtype=torch.float32, device=d)
+        tok = () if T == 1 else (T,)
+        self.out = torch.empty((B,) + tok + (wl.H, wl.V), dtype=torch.float32, device=d)
+        self.lse = torch.empty((B,) + tok + (wl.H,), dtype=torch.float32, device=d)
 
     # ---- the two calls ------------------------------------------------------------------
     def append(self, stream=None):
@@ -96,6 +98,13 @@ class DeviceStep:
         return L.mla_decode_attn(self.cfg, self.q, self.kv_b, self.cache, self.seq_lens,
                                  self.positions if positions else None, self.out, self.lse, self.wl.B,
                                  self.ws_decode, self.ws_decode.numel(), s)
+
+    def decode_multi(self, stream=None, positions=True):
+        """mla_decode_attn_multi over the workload's query tokens (every row already cached)."""
+        s = stream if stream is not None else self.stream
+        return L.mla_decode_attn_multi(self.cfg, self.wl.tokens, self.q, self.kv_b, self.cache, self.seq_lens,
+                                       self.positions if positions else None, self.out, self.lse, self.wl.B,
+                                       self.ws_decode, self.ws_decode.numel(), s)
 
     def step(self, stream=None):
         L.check(self.append(stream), "mla_cache_append")

@@ -77,6 +77,10 @@ class Workload:
     yarn_beta_slow: float = 1.0
     rms_eps: float = 1e-6
     seed: int = 0
+    # query tokens per sequence (> 1: multi-token decode; the tokens' own rows are the last
+    # `tokens` of the L_b rows, all pre-filled, q is [B, tokens, H, N+R], positions[b] = L_b -
+    # tokens is the first token's position, and no row is appended)
+    tokens: int = 1
 
     @property
     def row(self) -> int:
@@ -299,10 +303,14 @@ def make_problem(wl: Workload, nan_fill: bool = True) -> Problem:
     B, H, C, N, R = wl.B, wl.H, wl.C, wl.N, wl.R
     row = C + R
     L = lengths_for(wl)
-    positions = (L - 1).astype(np.int32)
+    T = wl.tokens
+    if T > 1 and int(L.min()) < T:
+        raise ValueError("every sequence needs at least one row per query token")
+    positions = (L - T).astype(np.int32)
     norm_w = _rng(wl.seed, "norm_w").uniform(0.5, 1.5, size=C).astype(np.float32)
 
-    q = _rng(wl.seed, "q").standard_normal((B, H, N + R), dtype=np.float32)
+    q_shape = (B, H, N + R) if T == 1 else (B, T, H, N + R)
+    q = _rng(wl.seed, "q").standard_normal(q_shape, dtype=np.float32)
     q = _encode_act(q, wl.act)
 
     # physical placement of logical row (b, t)
@@ -338,7 +346,8 @@ def make_problem(wl: Workload, nan_fill: bool = True) -> Problem:
     rng_pe = _rng(wl.seed, "pe")
     chunk = 1 << 14
     for b in range(B):
-        n_pre = int(positions[b])          # rows 0..P-1 pre-filled; row P is the append slot
+        # rows 0..P-1 pre-filled, row P the append slot; several tokens: every row pre-filled
+        n_pre = int(positions[b]) if T == 1 else int(L[b])
         for t0 in range(0, n_pre, chunk):
             t1 = min(n_pre, t0 + chunk)
             lat = rng_lat.standard_normal((t1 - t0, C), dtype=np.float32) * norm_w[None, :]

@@ -414,6 +414,32 @@ def lse_merge(parts):
 
 
 # ---------------------------------------------------------------------------------------
+# Several query tokens per sequence (speculative / chunked decode)
+# ---------------------------------------------------------------------------------------
+
+def decode_multi_one(q: np.ndarray, W_UK: np.ndarray, W_UV: np.ndarray, rows: np.ndarray,
+                     pos0: Optional[int], inv_freq: np.ndarray, scale: float, kv_lora: int):
+    """T query tokens of one sequence whose own rows are the last T of `rows`: token i sits at
+    position pos0 + i (its q_pe is rotated there; pos0 None: already rotated) and attends the
+    first L - T + 1 + i rows, i.e. itself and every row before it.
+
+    q [T, H, N+R], rows [L, C+R]. Returns out [T, H, V], lse [T, H].
+    Each token is one absorbed decode (decode_one); the tokens share the rows. [moeflux-fwd]
+    folded SDPA over cache_len = pos + 1 rows, applied per stacked token as the `*_n_tokens`
+    batched encoders of moeflux 0.1.0-pre.3, src/riir/backend/gpu/gpu_matvec.rs apply one
+    weight matrix to N stacked inputs.
+    """
+    T, H = q.shape[0], q.shape[1]
+    L = rows.shape[0]
+    out = np.empty((T, H, W_UV.shape[1]))
+    lse = np.empty((T, H))
+    for i in range(T):
+        pos = None if pos0 is None else pos0 + i
+        out[i], lse[i] = decode_one(q[i], W_UK, W_UV, rows[:L - T + 1 + i], pos, inv_freq, scale, kv_lora)
+    return out, lse
+
+
+# ---------------------------------------------------------------------------------------
 # Whole step on decoded inputs
 # ---------------------------------------------------------------------------------------
 

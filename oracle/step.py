@@ -94,6 +94,23 @@ def run_step(prob, seqs=None, heads=None, with_append: bool = True):
     return new, out, lse
 
 
+def run_multi(prob, seqs=None, heads=None):
+    """Multi-token decode of a problem whose workload has tokens > 1 (no append: every row is
+    in the pool). Returns (out [nb, T, nh, V], lse [nb, T, nh]) over the chosen sequences/heads."""
+    wl = prob.wl
+    inv, scale = tables(wl)
+    q = decode_act(prob.q, wl.act)
+    W_UK, W_UV = O.split_kv_b(kv_b_f64(prob), wl.H, wl.N, wl.V)
+    seqs = range(wl.B) if seqs is None else list(seqs)
+    heads = np.arange(wl.H) if heads is None else np.asarray(heads)
+    out = np.empty((len(seqs), wl.tokens, len(heads), wl.V))
+    lse = np.empty((len(seqs), wl.tokens, len(heads)))
+    for i, b in enumerate(seqs):
+        out[i], lse[i] = O.decode_multi_one(q[b][:, heads], W_UK[heads], W_UV[heads], sequence_rows(prob, b),
+                                            int(prob.positions[b]), inv, scale, wl.C)
+    return out, lse
+
+
 def rows_per_second_sample(prob, seconds: float = 10.0, heads=None):
     """Time the oracle on the host over a bounded sample of a workload: whole steps for one
     sequence at a time (all or `heads` of its heads), cycling through the sequences, until

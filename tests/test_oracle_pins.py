@@ -523,3 +523,79 @@ def test_absorbed_layer_equals_mha_on_projected_inputs():
     out, _ = O.decode_one(q[0], W_UK, W_UV, rows, L - 1, inv, 0.3, C)
     ref, _ = O.decode_unabsorbed_one(q[0], W_UK, W_UV, rows, L - 1, inv, 0.3, C)
     np.testing.assert_allclose(O.o_proj(out[None], Wo), O.o_proj(ref[None], Wo), rtol=1e-11, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------------------
+# Several query tokens per sequence
+# ----------------------------------------------------------------------------------------
+
+def _tiny_heads(H=3, C=8, N=4, R=4, V=5):
+    kv_b = RNG.standard_normal((H * (N + V), C))
+    W_UK, W_UV = O.split_kv_b(kv_b, H, N, V)
+    return W_UK, W_UV
+
+
+def test_multi_query_single_token_is_the_plain_decode():
+    W_UK, W_UV = _tiny_heads()
+    rows = RNG.standard_normal((7, 12))
+    q = RNG.standard_normal((1, 3, 8))
+    inv = O.yarn_inv_freq(4, 10000.0, 1.0, 4096, 32.0, 1.0)
+    out, lse = O.decode_multi_one(q, W_UK, W_UV, rows, 6, inv, 0.4, 8)
+    o1, l1 = O.decode_one(q[0], W_UK, W_UV, rows, 6, inv, 0.4, 8)
+    np.testing.assert_array_equal(out[0], o1)
+    np.testing.assert_array_equal(lse[0], l1)
+
+
+def test_multi_query_is_causal():
+    # token i must not see rows past L - T + i: changing them leaves token i alone and moves
+    # the last token
+    W_UK, W_UV = _tiny_heads()
+    L, T = 9, 3
+    rows = RNG.standard_normal((L, 12))
+    q = RNG.standard_normal((T, 3, 8))
+    inv = O.yarn_inv_freq(4, 10000.0, 1.0, 4096, 32.0, 1.0)
+    out, lse = O.decode_multi_one(q, W_UK, W_UV, rows, L - T, inv, 0.4, 8)
+    moved = rows.copy()
+    moved[L - 1] += 5.0
+    out2, lse2 = O.decode_multi_one(q, W_UK, W_UV, moved, L - T, inv, 0.4, 8)
+    np.testing.assert_array_equal(out2[:T - 1], out[:T - 1])
+    assert np.all(np.abs(lse2[T - 1] - lse[T - 1]) > 1e-6)
+
+
+def test_multi_query_identical_rows_count_each_tokens_prefix():
+    # all rows equal: token i averages to W_UV lat and its lse is s + ln(L - T + 1 + i)
+    W_UK, W_UV = _tiny_heads()
+    L, T = 10, 4
+    row = RNG.standard_normal(12)
+    rows = np.tile(row, (L, 1))
+    q = RNG.standard_normal((T, 3, 8))
+    q[:, :, 4:] = 0.0    # no rope part: the score does not depend on the position
+    out, lse = O.decode_multi_one(q, W_UK, W_UV, rows, None, np.zeros(2), 0.4, 8)
+    for i in range(T):
+        for h in range(3):
+            s = 0.4 * float(np.dot(np.einsum("n,nc->c", q[i, h, :4], W_UK[h]), row[:8]))
+            assert abs(lse[i, h] - (s + math.log(L - T + 1 + i))) < 1e-12
+            np.testing.assert_allclose(out[i, h], W_UV[h] @ row[:8], rtol=1e-12, atol=1e-12)
+
+
+def test_multi_query_tokens_sit_at_consecutive_positions():
+    # one rope pair (R = 2, frequency w), no latent: token i at position p0 + i scores row t,
+    # whose pe is k rotated by t*w, as scale |q||k| cos((t - p0 - i) w + phi), phi the angle from
+    # q to k; written out with numpy's cos, apart from the oracle's rotation
+    H, C, N, R, V = 1, 4, 2, 2, 3
+    kv_b = RNG.standard_normal((H * (N + V), C))
+    W_UK, W_UV = O.split_kv_b(kv_b, H, N, V)
+    w, scale, L, T, p0 = 0.37, 0.8, 11, 3, 8
+    qp, k = np.array([0.6, -1.1]), np.array([1.3, 0.4])
+    rows = np.zeros((L, C + R))
+    for t in range(L):
+        c, s_ = math.cos(t * w), math.sin(t * w)
+        rows[t, C:] = [k[0] * c - k[1] * s_, k[0] * s_ + k[1] * c]
+    q = np.zeros((T, H, N + R))
+    q[:, 0, N:] = qp
+    _, lse = O.decode_multi_one(q, W_UK, W_UV, rows, p0, np.array([w]), scale, C)
+    phi = math.atan2(k[1], k[0]) - math.atan2(qp[1], qp[0])
+    mag = math.hypot(*qp) * math.hypot(*k)
+    for i in range(T):
+        sc = [scale * mag * math.cos((t - p0 - i) * w + phi) for t in range(L - T + 1 + i)]
+        assert abs(lse[i, 0] - math.log(sum(math.exp(x) for x in sc))) < 1e-12
