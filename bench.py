@@ -522,6 +522,92 @@ def run_proj(device, name, fmt, K, W):
     return out
 
 
+# multi-token decode sub-records: (workload, query tokens) -> timed calls
+MULTI_BENCH = {("v2lite_b1_t4096", 4): 2000, ("v3_b32_t4096", 2): 200, ("v3_b32_t4096", 4): 100}
+
+
+def run_multi_tokens(device, name, tokens, K, W):
+    """Time mla_decode_attn_multi (T query tokens per sequence over the cached rows) against T
+    one-token mla_decode_attn calls on the same cache: CUDA graphs over R input copies (more than
+    2.2x L2 in all), events around each graph."""
+    import torch
+
+    from mla_latent_cache_absorb_gb300 import binding as L
+    from mla_latent_cache_absorb_gb300 import synth
+    from mla_latent_cache_absorb_gb300.runner import DeviceStep
+
+    wl = synth.WORKLOADS[name].with_(tokens=tokens)
+    prob = synth.make_problem(wl)
+    Lb = prob.seq_lens.astype(np.int64)
+    # rows each token attends, summed (token i of b: L_b - T + 1 + i), and distinct rows read
+    token_rows = int(sum(int(l) * tokens - tokens * (tokens - 1) // 2 for l in Lb))
+    row_bytes = (wl.C + wl.R) * (2 if wl.act == "bf16" else 4)
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 129 * 2 ** 20)
+    per_copy = input_bytes(prob)
+    R = max(1, min(32, math.ceil(2.2 * l2 / per_copy)))
+    stream = torch.cuda.Stream(device=device)
+    copies = [DeviceStep(prob, device=device, stream=stream) for _ in range(R)]
+    G = R * max(1, math.ceil(16 / R))
+
+    def timed(call):
+        with torch.cuda.stream(stream):
+            for i in range(W):
+                L.check(call(copies[i % R], stream), "warm-up")
+            torch.cuda.synchronize(device)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+                s = torch.cuda.current_stream(device)
+                for i in range(G):
+                    L.check(call(copies[i % R], s), "captured call")
+            g.replay()
+            torch.cuda.synchronize(device)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n = max(1, K // G)
+            e0.record(stream)
+            for _ in range(n):
+                g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            return e0.elapsed_time(e1) / (n * G)
+
+    def multi(ds, s):
+        return ds.decode_multi(s)
+
+    def singles(ds, s):
+        # the T tokens one call each (token i: its query, position and length), as without
+        # multi-token decode
+        st = 0
+        for i in range(tokens):
+            st = st or L.mla_decode_attn(ds.cfg, ds.q_tok[i], ds.kv_b, ds.cache, ds.len_tok[i], ds.pos_tok[i],
+                                         ds.out_tok, ds.lse_tok, wl.B, ds.ws_tok, ds.ws_tok.numel(), s)
+        return st
+
+    for ds in copies:
+        ds.q_tok = [ds.q[:, i].contiguous() for i in range(tokens)]
+        ds.len_tok = [(ds.seq_lens - (tokens - 1 - i)).contiguous() for i in range(tokens)]
+        ds.pos_tok = [(ds.positions + i).contiguous() for i in range(tokens)]
+        ds.out_tok = torch.empty((wl.B, wl.H, wl.V), dtype=torch.float32, device=device)
+        ds.lse_tok = torch.empty((wl.B, wl.H), dtype=torch.float32, device=device)
+        st, n = L.mla_decode_workspace_size(ds.cfg, wl.B)
+        L.check(st, "mla_decode_workspace_size")
+        ds.ws_tok = torch.zeros(n, dtype=torch.uint8, device=device)
+    ms_multi = timed(multi)
+    ms_single = timed(singles)
+    st, plan = L.mla_decode_plan(copies[0].cfg, wl.B)
+    del copies
+    torch.cuda.synchronize(device)
+    torch.cuda.empty_cache()
+    hbm = peaks()[0]
+    distinct = int(Lb.sum()) * row_bytes
+    return {"workload": wl.name, "tokens": tokens, "B": wl.B, "H": wl.H, "token_rows_per_call": token_rows,
+            "us_per_call": ms_multi * 1e3, "token_rows_per_s": token_rows / (ms_multi / 1e3),
+            "cache_gbs_distinct_rows": distinct / (ms_multi / 1e3) / 1e9,
+            "cache_hbm_frac": distinct / (ms_multi / 1e3) / 1e9 / hbm,
+            "us_as_one_token_calls": ms_single * 1e3, "speedup_vs_one_token_calls": ms_single / ms_multi,
+            "one_token_attention_kernel": plan.kernel}
+
+
 def run_e2e(torch, L, steps, prob, stream, device, K, W, work):
     """Same metric through the public calls with host buffers: every step copies its inputs
     (query, kv_a rows, positions, lengths) from one pinned host buffer into the step's device
@@ -750,6 +836,8 @@ def main():
     ap.add_argument("--no-also", action="store_true", help="skip the attention sub-records")
     ap.add_argument("--no-proj", action="store_true", help="skip the layer-projection sub-records")
     ap.add_argument("--proj-only", action="store_true", help="print only the layer-projection records")
+    ap.add_argument("--no-multi", action="store_true", help="skip the multi-token decode sub-records")
+    ap.add_argument("--multi-only", action="store_true", help="print only the multi-token decode records")
     ap.add_argument("--proj-filter", default=None,
                     help="with --proj-only: one 'workload:format' record (e.g. v3_proj_b4:bf16)")
     ap.add_argument("--clock-window-s", type=float, default=1.2,
@@ -774,6 +862,10 @@ def main():
         args.steps = 20000 if args.workload == "v2lite_b1_t4096" else 200
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    if args.multi_only:
+        for (name, t), k in MULTI_BENCH.items():
+            print(json.dumps(run_multi_tokens(device, name, t, k, args.warmup)), flush=True)
+        return
     if args.proj_only:
         for (name, fmt), k in PROJ_BENCH.items():
             if args.proj_filter and args.proj_filter != f"{name}:{fmt}":
@@ -804,6 +896,14 @@ def main():
         line["layer_projections"] = {
             "what": "mla_front_end (q chain or q projection + kv_a) and mla_o_proj per call, median of "
                     "in-graph events, weights rotating over copies > 2.2x L2 (not part of value)",
+            "records": recs}
+    if not args.no_multi:
+        recs = [run_multi_tokens(device, name, t, k, args.warmup) for (name, t), k in MULTI_BENCH.items()]
+        for (name, t), r in zip(MULTI_BENCH, recs):
+            line["gpu_launches"] += 3 * (1 + t) * MULTI_BENCH[(name, t)]
+        line["multi_token"] = {
+            "what": "mla_decode_attn_multi (T tokens per sequence, causal) per call vs the same tokens as T "
+                    "one-token calls; CUDA graphs, inputs rotating over copies > 2.2x L2 (not part of value)",
             "records": recs}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from mla_latent_cache_absorb_gb300 import synth
