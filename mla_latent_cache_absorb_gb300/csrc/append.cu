@@ -8,95 +8,11 @@
 // chain, kv_a_layernorm, YaRN RoPE of k_pe, append of row[pos]; PosMismatch / CacheFull guards.
 //
 // Here the finished row is produced in registers (float32) and written once, so the cache
-// never holds a half-finished row and the value is rounded to the cache dtype only once.
+// never holds a half-finished row and the value is rounded to the cache dtype only once. The
+// kv_a projection itself, when asked for, is the layer-projection GEMV of proj.cu.
 #include "common.cuh"
 
 namespace mla {
-
-// ---- kv_a projection: kva[b, r] = sum_k x[b, k] * W[r, k] ------------------------------------
-// Each output row r is shared by GEMV_WPR warps, each taking a contiguous share of the hidden
-// dimension with 16-byte vectors (four in flight per lane) for all B sequences at once; the warp
-// sums are added in a fixed order through shared memory. x is small and stays in L1/L2.
-constexpr int GEMV_RPC = 2;    // rows per CTA
-constexpr int GEMV_WPR = 4;    // warps per row
-constexpr int GEMV_BMAX = 8;   // sequences per register pass
-constexpr int GEMV_UNROLL = 4;
-
-template <int DT>
-__global__ void __launch_bounds__(GEMV_RPC * GEMV_WPR * 32)
-append_gemv_kernel(const typename Act<DT>::T* __restrict__ x, const typename Act<DT>::T* __restrict__ w,
-                   int hidden, int rows, int B, float* __restrict__ kva) {
-  using T = typename Act<DT>::T;
-  pdl_trigger();
-  __shared__ float red[GEMV_RPC][GEMV_WPR][GEMV_BMAX];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rl = warp / GEMV_WPR, wk = warp % GEMV_WPR;
-  const int r = blockIdx.x * GEMV_RPC + rl;
-  constexpr int VEC = 16 / sizeof(T);  // elements per 16-byte load
-  constexpr int STEP = 32 * VEC;
-  // this warp's share of the hidden dimension, in whole vector steps
-  const int share = ((hidden + GEMV_WPR * STEP - 1) / (GEMV_WPR * STEP)) * STEP;
-  const int k_beg = wk * share, k_end = min(hidden, k_beg + share);
-  const T* wr = w + (int64_t)(r < rows ? r : 0) * hidden;
-  for (int b0 = 0; b0 < B; b0 += GEMV_BMAX) {
-    const int nb = min(GEMV_BMAX, B - b0);
-    float acc[GEMV_BMAX];
-#pragma unroll
-    for (int j = 0; j < GEMV_BMAX; ++j) acc[j] = 0.f;
-    if (r < rows) {
-      for (int k0 = k_beg + lane * VEC; k0 < k_end; k0 += STEP * GEMV_UNROLL) {
-        uint4 wv[GEMV_UNROLL];
-#pragma unroll
-        for (int u = 0; u < GEMV_UNROLL; ++u) {
-          const int k = k0 + u * STEP;
-          wv[u] = k < k_end ? *reinterpret_cast<const uint4*>(wr + k) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < GEMV_UNROLL; ++u) {
-          const int k = k0 + u * STEP;
-          if (k >= k_end) break;
-          const T* we = reinterpret_cast<const T*>(&wv[u]);
-#pragma unroll
-          for (int j = 0; j < GEMV_BMAX; ++j) {
-            if (j < nb) {
-              uint4 xv = *reinterpret_cast<const uint4*>(x + (int64_t)(b0 + j) * hidden + k);
-              const T* xe = reinterpret_cast<const T*>(&xv);
-#pragma unroll
-              for (int e = 0; e < VEC; ++e)
-                acc[j] = fmaf(Act<DT>::load(we, e), Act<DT>::load(xe, e), acc[j]);
-            }
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < GEMV_BMAX; ++j) {
-      const float v = warp_sum(acc[j]);
-      if (lane == 0) red[rl][wk][j] = v;
-    }
-    __syncthreads();
-    if (b0 == 0) pdl_wait();   // the previous step's finish kernel may still read kva
-    if (wk == 0 && lane < nb && r < rows) {
-      float v = red[rl][0][lane];
-#pragma unroll
-      for (int q = 1; q < GEMV_WPR; ++q) v += red[rl][q][lane];
-      kva[(int64_t)(b0 + lane) * rows + r] = v;
-    }
-    __syncthreads();
-  }
-}
-
-cudaError_t launch_append_gemv(const mla_config& cfg, const void* x, const void* w, int hidden,
-                               float* kva_out, int B, cudaStream_t st) {
-  const int rows = cfg.kv_lora + cfg.qk_rope;
-  dim3 grid((rows + GEMV_RPC - 1) / GEMV_RPC);
-  dim3 block(GEMV_RPC * GEMV_WPR * 32);
-  if (cfg.act_dtype == MLA_BF16)
-    return launch_pdl(append_gemv_kernel<MLA_BF16>, grid, block, 0, st,
-                      static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(w), hidden, rows, B, kva_out);
-  return launch_pdl(append_gemv_kernel<MLA_F32>, grid, block, 0, st,
-                    static_cast<const float*>(x), static_cast<const float*>(w), hidden, rows, B, kva_out);
-}
 
 // ---- finish: norm + rope + store, one CTA per sequence ---------------------------------------
 constexpr int FIN_THREADS = 128;

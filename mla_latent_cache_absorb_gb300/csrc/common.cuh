@@ -299,8 +299,6 @@ cudaError_t ensure_smem(const void* func, int bytes);
 int device_sms();
 
 // host launchers (defined in the kernel files)
-cudaError_t launch_append_gemv(const mla_config& cfg, const void* x, const void* w, int hidden,
-                               float* kva_out, int B, cudaStream_t st);
 cudaError_t launch_append_finish(const mla_config& cfg, const mla_cache& cache, const float* kva,
                                  const float* norm_w, const int32_t* positions,
                                  const int32_t* seq_lens, int B, WsHeader* hdr, bool kva_dep, cudaStream_t st);

@@ -367,9 +367,7 @@ mla_status mla_cache_append(const mla_config* cfg, const mla_cache* cache, const
   st = check_cache(cfg, cache, B);
   if (st != MLA_OK) return st;
   if (w_kva != nullptr) {
-    const int vec = 16 / (int)act_size(cfg->act_dtype);
-    if (hidden < 1 || hidden % vec != 0 || !aligned(kv_in, 16) || !aligned(w_kva, 16))
-      return MLA_ERR_INVALID_ARG;
+    if (hidden < 8 || hidden % 8 != 0 || !aligned(kv_in, 16) || !aligned(w_kva, 16)) return MLA_ERR_INVALID_ARG;
   }
   size_t need;
   st = mla_append_workspace_size(cfg, B, &need);
@@ -381,7 +379,8 @@ mla_status mla_cache_append(const mla_config* cfg, const mla_cache* cache, const
   const float* kva = static_cast<const float*>(kv_in);
   if (w_kva != nullptr) {
     float* kva_ws = reinterpret_cast<float*>(static_cast<char*>(workspace) + sizeof(WsHeader));
-    st = cuda_status(launch_append_gemv(*cfg, kv_in, w_kva, hidden, kva_ws, B, s));
+    st = cuda_status(launch_proj(kv_in, cfg->act_dtype == MLA_BF16, hidden, B, cfg->act_dtype, w_kva,
+                                 cfg->kv_lora + cfg->qk_rope, kva_ws, false, nullptr, 0, nullptr, false, s));
     if (st != MLA_OK) return st;
     kva = kva_ws;
   }
