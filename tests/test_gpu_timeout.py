@@ -13,7 +13,7 @@ gpu = pytest.mark.gpu
 W = synth.WORKLOADS
 
 CASES = [
-    # 128 heads, eight sequences: tcgen05 absorb, attention (64-head groups) and combine
+    # 128 heads, eight sequences: tcgen05 absorb, SM-pair attention and combine
     ("h128_b8", W["v3_b32_t4096"].with_(B=8, context=("fixed", 300))),
     # 16 heads, one sequence: tcgen05 attention (16-head group) between the CUDA-core kernels
     ("h16_b1", W["v2lite_b1_t4096"].with_(context=("fixed", 1000))),
