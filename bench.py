@@ -495,10 +495,9 @@ def run_proj(device, name, fmt, K, W):
             for i in range(G):
                 dp = copies[i % R]
                 evs[i][0].record(s)
-                L.check(L.mla_front_end(dp.cfg, dp.pj, dp.x, dp.q, dp.kva, wl.B, dp.ws, dp.ws.numel(), s),
-                        "mla_front_end")
+                L.check(dp.front_end(stream=s), "mla_front_end")
                 evs[i][1].record(s)
-                L.check(L.mla_o_proj(dp.cfg, dp.pj, dp.attn, dp.y, wl.B, s), "mla_o_proj")
+                L.check(dp.o_proj(stream=s), "mla_o_proj")
                 evs[i][2].record(s)
         g.replay()
         torch.cuda.synchronize(device)

@@ -290,8 +290,11 @@ typedef struct mla_proj {
   const void* w_o;         /* device [D, H*V], or NULL when mla_o_proj is not used */
 } mla_proj;
 
-/* Bytes of device workspace mla_front_end needs for B sequences: the float32 q_lat rows
- * [B, q_lora] (0 bytes when q_lora == 0). Host-only. */
+/* Bytes of device workspace mla_front_end needs for B sequences. It holds a 256-byte header
+ * (the device error word: clear it once, or zero-fill, before first use; read it with
+ * mla_get_device_error) and, as needed, the float32 q_lat rows, the bf16 halves of the
+ * normalised q_lat and the tensor-core path's split partials. Host-only (the split plan
+ * depends on the device's SM count). */
 mla_status mla_front_end_workspace_size(const mla_config* cfg, const mla_proj* pj, int32_t B,
                                         size_t* bytes);
 
@@ -303,19 +306,29 @@ mla_status mla_front_end_workspace_size(const mla_config* cfg, const mla_proj* p
  *        q_lora == 0: q_full = W_q x. Head h is q_full[h*(N+R) : (h+1)*(N+R)], its q_nope
  *        first; q_pe is left unrotated (mla_decode_attn rotates it). Rounded once.
  *   kva  device [B, C+R] float32 = W_kva x, or NULL (then w_kva is not read).
- * Launches: one kernel computing W_q_a x (or W_q x) and W_kva x together (one read of x),
- * then, for q_lora > 0, the norm of the q_lat rows and the q_b projection.
+ * Launches: one GEMV computing W_q_a x (or W_q x) and W_kva x together (one read of x), then,
+ * for q_lora > 0, the norm of the q_lat rows and the q_b projection. Weights in BF16 with 16
+ * to 128 sequences (256 for a bf16 input) run on the tensor cores: a float32 input as bf16
+ * hi + lo halves (about float32 accuracy), column slices summed in a fixed order. Every
+ * result is run-to-run identical.
  * Errors: INVALID_ARG (null or misaligned pointer, bad dims, kva without w_kva),
- * UNSUPPORTED (w_dtype), WORKSPACE, CUDA. No device errors. */
+ * UNSUPPORTED (w_dtype), WORKSPACE, CUDA; device: TIMEOUT (a bounded wait ran out: that
+ * launch's outputs are NaN). */
 mla_status mla_front_end(const mla_config* cfg, const mla_proj* pj, const void* x, void* q,
                          float* kva, int32_t B, void* workspace, size_t ws_bytes,
                          mla_stream_t stream);
 
+/* Bytes of device workspace mla_o_proj needs for B sequences: the 256-byte header (as for
+ * mla_front_end) and, on the tensor-core path, the bf16 halves of the input and the split
+ * partials. Host-only. */
+mla_status mla_o_proj_workspace_size(const mla_config* cfg, const mla_proj* pj, int32_t B,
+                                     size_t* bytes);
+
 /* o_proj for B sequences (async): y[b] = W_o attn[b], attn [B, H, V] float32 read head after
  * head (head h's V values at h*V: the layout mla_decode_attn writes), y device [B, D] float32.
- * Errors: as mla_front_end (w_o must be set). */
+ * Paths and errors as mla_front_end (w_o must be set). */
 mla_status mla_o_proj(const mla_config* cfg, const mla_proj* pj, const float* attn, float* y,
-                      int32_t B, mla_stream_t stream);
+                      int32_t B, void* workspace, size_t ws_bytes, mla_stream_t stream);
 
 /* ---- several query tokens per sequence ----------------------------------------------------
  * T new tokens of each sequence decoded at once (draft tokens of speculative decoding, a chunk

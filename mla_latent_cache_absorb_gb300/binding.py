@@ -80,7 +80,8 @@ _SIGS = {
     "mla_front_end_workspace_size": (c_int32, [_CFG, _PROJ, c_int32, POINTER(c_size_t)]),
     "mla_front_end": (c_int32, [_CFG, _PROJ, c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_size_t,
                                 c_void_p]),
-    "mla_o_proj": (c_int32, [_CFG, _PROJ, c_void_p, c_void_p, c_int32, c_void_p]),
+    "mla_o_proj_workspace_size": (c_int32, [_CFG, _PROJ, c_int32, POINTER(c_size_t)]),
+    "mla_o_proj": (c_int32, [_CFG, _PROJ, c_void_p, c_void_p, c_int32, c_void_p, c_size_t, c_void_p]),
     "mla_decode_multi_workspace_size": (c_int32, [_CFG, c_int32, c_int32, POINTER(c_size_t)]),
     "mla_decode_attn_multi": (c_int32, [_CFG, c_int32, c_void_p, c_void_p, _CACHE, c_void_p, c_void_p, c_void_p,
                                         c_void_p, c_int32, c_void_p, c_size_t, c_void_p]),
@@ -237,8 +238,15 @@ def mla_front_end(cfg, pj, x, q, kva, B, workspace, ws_bytes, stream=None):
                               ws_bytes, _s(stream))
 
 
-def mla_o_proj(cfg, pj, attn, y, B, stream=None):
-    return _lib.mla_o_proj(ctypes.byref(cfg), ctypes.byref(pj), _p(attn), _p(y), B, _s(stream))
+def mla_o_proj_workspace_size(cfg, pj, B):
+    n = c_size_t(0)
+    st = _lib.mla_o_proj_workspace_size(ctypes.byref(cfg), ctypes.byref(pj), B, ctypes.byref(n))
+    return st, n.value
+
+
+def mla_o_proj(cfg, pj, attn, y, B, workspace, ws_bytes, stream=None):
+    return _lib.mla_o_proj(ctypes.byref(cfg), ctypes.byref(pj), _p(attn), _p(y), B, _p(workspace), ws_bytes,
+                           _s(stream))
 
 
 def mla_decode_multi_workspace_size(cfg, tokens, B):

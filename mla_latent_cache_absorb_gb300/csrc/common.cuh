@@ -338,7 +338,19 @@ cudaError_t launch_combine_tc(const mla_config& cfg, const DecodePlan& plan, con
 cudaError_t launch_proj(const void* x, bool x_bf16, int K, int B, int w_dtype, const void* w0, int64_t rows0,
                         void* y0, bool y0_bf16, const void* w1, int64_t rows1, void* y1, bool y1_bf16,
                         cudaStream_t st);
-cudaError_t launch_rms_norm_rows(float* x, const float* w, int K, int B, float eps, cudaStream_t st);
+cudaError_t launch_rms_norm_rows(float* x, const float* w, int K, int B, float eps, cudaStream_t st,
+                                 uint16_t* hi = nullptr, uint16_t* lo = nullptr);
+// tensor-core projections (bf16 weights, 16 to 128/256 sequences), see proj.cu
+struct ProjTcPlan {
+  bool use;
+  int xsplit, BP, NB, nkb, kb_per_split, splits, stages;
+  int64_t tiles0, tiles1, part_floats;
+};
+ProjTcPlan proj_tc_plan(int64_t rows0, int64_t rows1, int K, int B, bool x_f32, int w_dtype);
+cudaError_t launch_proj_tc(const ProjTcPlan& p, const void* x, const void* x_lo, int K, int B, const void* w0,
+                           int64_t rows0, void* y0, bool y0_bf16, const void* w1, int64_t rows1, void* y1,
+                           bool y1_bf16, float* part, WsHeader* hdr, cudaStream_t st);
+cudaError_t launch_split_hi_lo(const float* x, int64_t n, uint16_t* hi, uint16_t* lo, cudaStream_t st);
 cudaError_t launch_combine(const mla_config& cfg, const DecodePlan& plan, const void* kv_b,
                            const int32_t* meta, const float* part_o, const float* part_lse, const void* q_res,
                            float* out, float* lse, int B, cudaStream_t st);

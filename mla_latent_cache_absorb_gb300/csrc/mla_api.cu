@@ -2,6 +2,7 @@
 // Every entry point validates on the host before enqueueing anything; kernels report what
 // only the GPU can see through the workspace's error word.
 #include <cmath>
+#include <algorithm>
 #include <atomic>
 #include <cstring>
 #include <limits>
@@ -538,11 +539,82 @@ mla_status mla_clear_device_error(void* workspace, mla_stream_t stream) {
   return cuda_status(cudaMemsetAsync(workspace, 0, sizeof(WsHeader), reinterpret_cast<cudaStream_t>(stream)));
 }
 
+}  // extern "C"
+
+namespace {
+
+// The layer projections' workspace: a 256-byte header (the device error word) and, as a call
+// needs them, the float32 q_lat rows, the bf16 hi / lo halves of a float32 input (tensor-core
+// path) and the split partials of the tensor-core GEMMs (reused by the calls of one front end,
+// which run in stream order).
+struct ProjWs {
+  ProjTcPlan pa, pb;            // front end: first launch (q_a or q, with kv_a), q_b; o_proj: pa
+  size_t off_qlat, off_hi, off_lo, off_part, total;
+};
+
+size_t align_up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+mla_status front_end_ws(const mla_config* cfg, const mla_proj* pj, int32_t B, ProjWs* w) {
+  const int64_t q_rows = (int64_t)cfg->n_heads * (cfg->qk_nope + cfg->qk_rope);
+  const int64_t kva_rows = pj->w_kva != nullptr ? cfg->kv_lora + cfg->qk_rope : 0;
+  const bool chain = pj->q_lora > 0;
+  const bool xb = cfg->act_dtype == MLA_BF16;
+  w->pa = proj_tc_plan(chain ? pj->q_lora : q_rows, kva_rows, pj->hidden, B, false, xb ? pj->w_dtype : -1);
+  w->pb = chain ? proj_tc_plan(q_rows, 0, pj->q_lora, B, true, pj->w_dtype) : ProjTcPlan{};
+  size_t off = sizeof(WsHeader);
+  w->off_qlat = off;
+  if (chain) off = align_up256(off + (size_t)B * pj->q_lora * sizeof(float));
+  w->off_hi = off;
+  if (w->pb.use) off = align_up256(off + (size_t)B * pj->q_lora * 2);
+  w->off_lo = off;
+  if (w->pb.use) off = align_up256(off + (size_t)B * pj->q_lora * 2);
+  w->off_part = off;
+  const int64_t part = std::max<int64_t>(w->pa.use ? w->pa.part_floats : 0, w->pb.use ? w->pb.part_floats : 0);
+  off = align_up256(off + (size_t)part * sizeof(float));
+  w->total = off;
+  return MLA_OK;
+}
+
+mla_status o_proj_ws(const mla_config* cfg, const mla_proj* pj, int32_t B, ProjWs* w) {
+  const int64_t k = (int64_t)cfg->n_heads * cfg->v_head;
+  w->pa = proj_tc_plan(pj->hidden, 0, (int)k, B, true, pj->w_dtype);
+  w->pb = ProjTcPlan{};
+  size_t off = sizeof(WsHeader);
+  w->off_qlat = off;
+  w->off_hi = off;
+  if (w->pa.use) off = align_up256(off + (size_t)B * k * 2);
+  w->off_lo = off;
+  if (w->pa.use) off = align_up256(off + (size_t)B * k * 2);
+  w->off_part = off;
+  off = align_up256(off + (size_t)(w->pa.use ? w->pa.part_floats : 0) * sizeof(float));
+  w->total = off;
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 mla_status mla_front_end_workspace_size(const mla_config* cfg, const mla_proj* pj, int32_t B, size_t* bytes) {
   mla_status st = check_proj(cfg, pj, B);
   if (st != MLA_OK) return st;
   if (bytes == nullptr) return MLA_ERR_INVALID_ARG;
-  *bytes = align256((size_t)B * (size_t)pj->q_lora * sizeof(float));
+  ProjWs w;
+  st = front_end_ws(cfg, pj, B, &w);
+  if (st != MLA_OK) return st;
+  *bytes = w.total;
+  return MLA_OK;
+}
+
+mla_status mla_o_proj_workspace_size(const mla_config* cfg, const mla_proj* pj, int32_t B, size_t* bytes) {
+  mla_status st = check_proj(cfg, pj, B);
+  if (st != MLA_OK) return st;
+  if (bytes == nullptr) return MLA_ERR_INVALID_ARG;
+  if (!proj_in_dim_ok((int64_t)cfg->n_heads * cfg->v_head, pj->w_dtype)) return MLA_ERR_INVALID_ARG;
+  ProjWs w;
+  st = o_proj_ws(cfg, pj, B, &w);
+  if (st != MLA_OK) return st;
+  *bytes = w.total;
   return MLA_OK;
 }
 
@@ -557,42 +629,67 @@ mla_status mla_front_end(const mla_config* cfg, const mla_proj* pj, const void* 
   if (chain && (pj->w_q_a == nullptr || pj->q_a_norm_w == nullptr || !aligned(pj->w_q_a, 16) ||
                 !(pj->q_norm_eps >= 0.f) || !std::isfinite(pj->q_norm_eps)))
     return MLA_ERR_INVALID_ARG;
-  size_t need;
-  st = mla_front_end_workspace_size(cfg, pj, B, &need);
+  ProjWs w;
+  st = front_end_ws(cfg, pj, B, &w);
   if (st != MLA_OK) return st;
-  if (chain) {
-    st = check_ws(workspace, ws_bytes, need);
-    if (st != MLA_OK) return st;
-  }
+  st = check_ws(workspace, ws_bytes, w.total);
+  if (st != MLA_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  float* part = reinterpret_cast<float*>(ws + w.off_part);
   const bool xb = cfg->act_dtype == MLA_BF16;
   const int64_t q_rows = (int64_t)cfg->n_heads * (cfg->qk_nope + cfg->qk_rope);
   const int64_t kva_rows = cfg->kv_lora + cfg->qk_rope;
   const void* w1 = kva != nullptr ? pj->w_kva : nullptr;
-  if (!chain) {
-    return cuda_status(launch_proj(x, xb, pj->hidden, B, pj->w_dtype, pj->w_q, q_rows, q, xb, w1, kva_rows, kva,
-                                   false, s));
-  }
-  float* q_lat = static_cast<float*>(workspace);
-  st = cuda_status(launch_proj(x, xb, pj->hidden, B, pj->w_dtype, pj->w_q_a, pj->q_lora, q_lat, false, w1,
-                               kva_rows, kva, false, s));
+  // first launch: q (or q_lat) and kv_a from x, one read of x
+  void* y0 = chain ? static_cast<void*>(ws + w.off_qlat) : q;
+  const int64_t rows0 = chain ? pj->q_lora : q_rows;
+  const bool y0_bf16 = !chain && xb;
+  if (w.pa.use)
+    st = cuda_status(launch_proj_tc(w.pa, x, nullptr, pj->hidden, B, chain ? pj->w_q_a : pj->w_q, rows0, y0, y0_bf16,
+                                    w1, kva_rows, kva, false, part, hdr, s));
+  else
+    st = cuda_status(launch_proj(x, xb, pj->hidden, B, pj->w_dtype, chain ? pj->w_q_a : pj->w_q, rows0, y0, y0_bf16,
+                                 w1, kva_rows, kva, false, s));
+  if (st != MLA_OK || !chain) return st;
+  float* q_lat = reinterpret_cast<float*>(ws + w.off_qlat);
+  uint16_t* hi = reinterpret_cast<uint16_t*>(ws + w.off_hi);
+  uint16_t* lo = reinterpret_cast<uint16_t*>(ws + w.off_lo);
+  st = cuda_status(launch_rms_norm_rows(q_lat, pj->q_a_norm_w, pj->q_lora, B, pj->q_norm_eps, s,
+                                        w.pb.use ? hi : nullptr, w.pb.use ? lo : nullptr));
   if (st != MLA_OK) return st;
-  st = cuda_status(launch_rms_norm_rows(q_lat, pj->q_a_norm_w, pj->q_lora, B, pj->q_norm_eps, s));
-  if (st != MLA_OK) return st;
+  if (w.pb.use)
+    return cuda_status(launch_proj_tc(w.pb, hi, lo, pj->q_lora, B, pj->w_q, q_rows, q, xb, nullptr, 0, nullptr, false,
+                                      part, hdr, s));
   return cuda_status(launch_proj(q_lat, false, pj->q_lora, B, pj->w_dtype, pj->w_q, q_rows, q, xb, nullptr, 0,
                                  nullptr, false, s));
 }
 
 mla_status mla_o_proj(const mla_config* cfg, const mla_proj* pj, const float* attn, float* y, int32_t B,
-                      mla_stream_t stream) {
+                      void* workspace, size_t ws_bytes, mla_stream_t stream) {
   mla_status st = check_proj(cfg, pj, B);
   if (st != MLA_OK) return st;
   const int64_t k = (int64_t)cfg->n_heads * cfg->v_head;
   if (!proj_in_dim_ok(k, pj->w_dtype)) return MLA_ERR_INVALID_ARG;
   if (attn == nullptr || y == nullptr || pj->w_o == nullptr || !aligned(attn, 16) || !aligned(pj->w_o, 16))
     return MLA_ERR_INVALID_ARG;
-  return cuda_status(launch_proj(attn, false, (int)k, B, pj->w_dtype, pj->w_o, pj->hidden, y, false, nullptr, 0,
-                                 nullptr, false, reinterpret_cast<cudaStream_t>(stream)));
+  ProjWs w;
+  st = o_proj_ws(cfg, pj, B, &w);
+  if (st != MLA_OK) return st;
+  st = check_ws(workspace, ws_bytes, w.total);
+  if (st != MLA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  if (!w.pa.use)
+    return cuda_status(launch_proj(attn, false, (int)k, B, pj->w_dtype, pj->w_o, pj->hidden, y, false, nullptr, 0,
+                                   nullptr, false, s));
+  uint16_t* hi = reinterpret_cast<uint16_t*>(ws + w.off_hi);
+  uint16_t* lo = reinterpret_cast<uint16_t*>(ws + w.off_lo);
+  st = cuda_status(launch_split_hi_lo(attn, (int64_t)B * k, hi, lo, s));
+  if (st != MLA_OK) return st;
+  return cuda_status(launch_proj_tc(w.pa, hi, lo, (int)k, B, pj->w_o, pj->hidden, y, false, nullptr, 0, nullptr, false,
+                                    reinterpret_cast<float*>(ws + w.off_part), reinterpret_cast<WsHeader*>(ws), s));
 }
 
 // ---- several query tokens per sequence -------------------------------------------------------

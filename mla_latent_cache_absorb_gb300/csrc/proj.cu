@@ -20,10 +20,19 @@
 // run-to-run identical. One launch can serve two matrices that read the same x (q_a or q, and
 // kv_a): the CTAs past the first matrix's take the second's rows.
 #include "common.cuh"
+#include "tc_ptx.cuh"
+
+#include <math_constants.h>
 
 namespace mla {
 
 namespace {
+
+// bf16 bit pattern of v, round to nearest even
+__device__ __forceinline__ uint16_t pt_bf16_bits(float v) {
+  __nv_bfloat16 h = __float2bfloat16_rn(v);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
 
 constexpr int PJ_WARPS = 8;
 constexpr int PJ_THREADS = 32 * PJ_WARPS;
@@ -521,7 +530,9 @@ constexpr int proj_smem_bytes() { return 2 * PJ_BP * PJ_ROUND * (XBF ? 2 : 4); }
 // In place: x[b, :] = x[b, :] / sqrt(mean(x[b, :]^2) + eps) * w, one CTA per vector; the sum
 // of squares is formed in a fixed order (thread partials, warp butterflies, then the 8 warp
 // sums in warp order).
-__global__ void __launch_bounds__(PJ_THREADS) rms_norm_rows_kernel(float* x, const float* w, int K, float eps) {
+// With hi != nullptr the normalised values go out as bf16 hi and lo [B, K] instead (x unchanged).
+__global__ void __launch_bounds__(PJ_THREADS) rms_norm_rows_kernel(float* x, const float* w, int K, float eps,
+                                                                   uint16_t* hi, uint16_t* lo) {
   __shared__ float part[PJ_WARPS];
   pdl_trigger();
   pdl_wait();
@@ -535,7 +546,17 @@ __global__ void __launch_bounds__(PJ_THREADS) rms_norm_rows_kernel(float* x, con
 #pragma unroll
   for (int i = 0; i < PJ_WARPS; ++i) tot += part[i];
   const float inv = rsqrtf(tot / (float)K + eps);
-  for (int k = threadIdx.x; k < K; k += PJ_THREADS) xb[k] = xb[k] * inv * w[k];
+  for (int k = threadIdx.x; k < K; k += PJ_THREADS) {
+    const float v = xb[k] * inv * w[k];
+    if (hi == nullptr) {
+      xb[k] = v;
+    } else {
+      const int64_t o = (int64_t)blockIdx.x * K + k;
+      const uint16_t h = pt_bf16_bits(v);
+      hi[o] = h;
+      lo[o] = pt_bf16_bits(v - bf16_bits_to_f32(h));
+    }
+  }
 }
 
 template <int WD, bool XBF>
@@ -555,6 +576,223 @@ cudaError_t launch_proj_x(const ProjArgs& a, int64_t blocks, cudaStream_t st) {
 template <int WD>
 cudaError_t launch_proj_dt(const ProjArgs& a, bool x_bf16, int64_t blocks, cudaStream_t st) {
   return x_bf16 ? launch_proj_x<WD, true>(a, blocks, st) : launch_proj_x<WD, false>(a, blocks, st);
+}
+
+// ---- bf16 weights, 16 to 128 sequences: tcgen05 ------------------------------------------------
+// y[b, r] = sum_k W[r, k] x[b, k] as D[r, b] = W_tile . X^T on the tensor cores: a CTA owns 128 rows
+// of W (the M = 128 operand, K-major, 64-column blocks by TMA in the 128-byte swizzle) and one
+// slice of the columns (split-K); the batch is the N operand: the bf16 input rows, or, for a
+// float32 input, its bf16 hi rows then its bf16 lo rows (x = hi + lo to about 2^-16), whose two
+// accumulator halves the epilogue adds. A four-stage ring of (W block, X block) pairs feeds one
+// MMA-issuing thread (two to four stages, as many as keep a CTA within half of the shared
+// memory, so that two CTAs share an SM); the fp32 accumulator [128 rows x N] lives in tensor
+// memory; four warps read it out. With one slice the result goes straight to y; otherwise each slice writes its
+// partial sums and a second kernel adds the slices in order. Warp 0 issues the TMA loads, warp 1
+// owns tensor memory and issues the MMAs, warps 2-5 (one per tensor-memory lane quarter) run
+// the epilogue. Every wait is bounded; on a timeout the CTA records MLA_ERR_TIMEOUT, drains what
+// it issued, frees tensor memory and writes NaN for the outputs it owns.
+constexpr int PT_STAGES = 4;             // at most
+constexpr int PT_SMEM_HALF = 110 * 1024; // stages of one CTA: two CTAs fit an SM
+constexpr uint64_t G_DRAIN_NS = kWaitDrainNs;
+constexpr int PT_THREADS = 192;
+constexpr int PT_A_BYTES = 128 * 128;   // 128 rows x 64 bf16 columns
+
+struct ProjTcArgs {
+  int64_t tiles0;        // 128-row tiles of matrix 0; tiles past it belong to matrix 1
+  int64_t rows[2];
+  void* y[2];            // [B, rows]: float32, or bf16 where y_bf16
+  int y_bf16[2];
+  float* part;           // [splits][B][rows0 + rows1] float32 partial sums (splits > 1)
+  int K, B;
+  int NB;                // MMA N: the padded batch (bf16 input) or twice it (hi ; lo)
+  int BP;                // padded batch: rows of one X half in shared memory
+  int xsplit;            // 1: X is hi and lo (two maps), accumulator halves added
+  int splits, kb_per_split, nkb;
+  int stages;            // ring depth (2 to PT_STAGES)
+  WsHeader* hdr;
+  uint64_t wait_ns;
+};
+
+__global__ void __launch_bounds__(PT_THREADS, 1)
+proj_tc_kernel(const __grid_constant__ CUtensorMap w0_map, const __grid_constant__ CUtensorMap w1_map,
+               const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap xlo_map,
+               const ProjTcArgs a) {
+  extern __shared__ uint8_t pt_raw[];
+  __shared__ uint64_t full[PT_STAGES], empty[PT_STAGES], mma_done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int failed;
+  uint8_t* dyn = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(pt_raw) + 1023) & ~uintptr_t(1023));
+  const int b_bytes = a.NB * 128;
+  const int stage_bytes = PT_A_BYTES + b_bytes;
+  pdl_trigger();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool second = blockIdx.x >= a.tiles0;
+  const int64_t r0 = (second ? blockIdx.x - a.tiles0 : blockIdx.x) * 128;
+  const int64_t rows = second ? a.rows[1] : a.rows[0];
+  const CUtensorMap* wmap = second ? &w1_map : &w0_map;
+  const int split = blockIdx.y;
+  const int kb0 = split * a.kb_per_split, kb1 = min(a.nkb, kb0 + a.kb_per_split);
+  const int nkb = kb1 - kb0;
+  const uint32_t tcols = a.NB <= 64 ? 64 : (a.NB <= 128 ? 128 : 256);
+  const int NS = a.stages;
+  if (tid == 0) {
+    failed = 0;
+    for (int i = 0; i < NS; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], 1);
+    }
+    tc::mbar_init(&mma_done, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&tmem_base, tcols);
+    tc::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::tma_prefetch_desc(wmap);
+    tc::tma_prefetch_desc(&x_map);
+    if (a.xsplit) tc::tma_prefetch_desc(&xlo_map);
+  }
+  tc::tc_fence_before();
+  __syncwarp();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = tmem_base;
+
+  if (warp == 0) {
+    // ======================= TMA producer =======================
+    if (lane == 0) {
+      // the weights are no other kernel's output: the first blocks of W go out before the
+      // dependency wait (their bytes expected without an arrival, so a stage completes only once
+      // its input block, armed with the arrival below, has landed too), the input's after it
+      const int pre = min(nkb, NS);
+      for (int i = 0; i < pre; ++i) {
+        tc::mbar_expect_tx(&full[i], PT_A_BYTES);
+        tc::tma_load_2d(dyn + i * stage_bytes, wmap, 64 * (kb0 + i), (int32_t)r0, &full[i]);
+      }
+      pdl_wait();
+      bool ok = true;
+      int last = -1;
+      for (int i = 0; i < nkb && ok; ++i) {
+        const int st = i % NS;
+        uint8_t* sa = dyn + st * stage_bytes;
+        if (i >= NS) {
+          if (!tc::mbar_wait(&empty[st], (uint32_t)(((i / NS) - 1) & 1), a.wait_ns)) {
+            ok = false;
+            break;
+          }
+          tc::mbar_arrive_expect_tx(&full[st], stage_bytes);
+          tc::tma_load_2d(sa, wmap, 64 * (kb0 + i), (int32_t)r0, &full[st]);
+        } else {
+          tc::mbar_arrive_expect_tx(&full[st], stage_bytes - PT_A_BYTES);
+        }
+        tc::tma_load_2d(sa + PT_A_BYTES, &x_map, 64 * (kb0 + i), 0, &full[st]);
+        if (a.xsplit) tc::tma_load_2d(sa + PT_A_BYTES + a.BP * 128, &xlo_map, 64 * (kb0 + i), 0, &full[st]);
+        last = i;
+      }
+      if (!ok && atomicExch(&failed, 1) == 0) set_error(a.hdr, MLA_ERR_TIMEOUT, 0);
+      // the loads issued must land before the CTA leaves: wait for the stages of the last ones
+      // (every prefetched weight block has its input block issued: no wait precedes those)
+      for (int i = max(0, last - NS + 1); i <= last; ++i)
+        tc::mbar_wait(&full[i % NS], (uint32_t)((i / NS) & 1), G_DRAIN_NS);
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_bf16_f32(128, a.NB, 0, 0);
+      bool ok = true;
+      for (int i = 0; i < nkb; ++i) {
+        const int st = i % NS;
+        if (!tc::mbar_wait(&full[st], (uint32_t)((i / NS) & 1), a.wait_ns) ||
+            *reinterpret_cast<volatile int*>(&failed)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t sa = tc::smem_u32(dyn + st * stage_bytes);
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_f16_ss(tmem, tc::sdesc_sw128(sa + kk * 32, 16, 1024),
+                         tc::sdesc_sw128(sa + PT_A_BYTES + kk * 32, 16, 1024), idesc, (i | kk) != 0);
+        tc::mma_commit(&empty[st]);
+      }
+      if (!ok && atomicExch(&failed, 1) == 0) set_error(a.hdr, MLA_ERR_TIMEOUT, 0);
+      tc::mma_commit(&mma_done);   // arrives once every MMA issued has completed
+    }
+  } else {
+    // ======================= epilogue: warps 2-5, lane quarter warp % 4 =======================
+    const int q = warp & 3;
+    const int64_t r = r0 + 32 * q + lane;
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&mma_done, 0, a.wait_ns + G_DRAIN_NS));
+    ok = ok && !*reinterpret_cast<volatile int*>(&failed);
+    ok = __all_sync(0xffffffffu, ok);
+    tc::tc_fence_after();
+    const int nout = a.xsplit ? a.BP : a.NB;
+    const int y_col = (int)(second ? a.rows[0] : 0);
+    const int64_t rows_all = a.rows[0] + a.rows[1];
+    for (int c0 = 0; c0 < nout; c0 += 32) {
+      uint32_t v[32], w[32];
+      if (ok) {
+        tc::tmem_ld32(tmem + lane_base + c0, v);
+        if (a.xsplit) tc::tmem_ld32(tmem + lane_base + a.BP + c0, w);
+        tc::tmem_wait_ld();
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int b = c0 + j;
+        if (b >= a.B || r >= rows) continue;
+        float val = CUDART_NAN_F;
+        if (ok) val = __uint_as_float(v[j]) + (a.xsplit ? __uint_as_float(w[j]) : 0.f);
+        if (a.splits > 1) {
+          a.part[((int64_t)split * a.B + b) * rows_all + y_col + r] = val;
+        } else {
+          void* Y = second ? a.y[1] : a.y[0];
+          const bool ybf = second ? a.y_bf16[1] != 0 : a.y_bf16[0] != 0;
+          if (ybf) static_cast<uint16_t*>(Y)[(int64_t)b * rows + r] = pt_bf16_bits(val);
+          else static_cast<float*>(Y)[(int64_t)b * rows + r] = val;
+        }
+      }
+    }
+  }
+  __syncwarp();
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, tcols);
+  }
+}
+
+// y[b, r] = sum over the slices, in slice order (one thread per output)
+__global__ void __launch_bounds__(256) proj_reduce_kernel(const float* __restrict__ part, int splits, int B,
+                                                          int64_t rows0, int64_t rows1, void* y0, int y0_bf16,
+                                                          void* y1, int y1_bf16) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t rows_all = rows0 + rows1;
+  const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  if (i >= (int64_t)B * rows_all) return;
+  const int64_t b = i / rows_all, c = i % rows_all;
+  float v = 0.f;
+  for (int s = 0; s < splits; ++s) v += part[((int64_t)s * B + b) * rows_all + c];
+  const bool second = c >= rows0;
+  const int64_t r = second ? c - rows0 : c, rows = second ? rows1 : rows0;
+  void* Y = second ? y1 : y0;
+  if (second ? y1_bf16 : y0_bf16) static_cast<uint16_t*>(Y)[b * rows + r] = pt_bf16_bits(v);
+  else static_cast<float*>(Y)[b * rows + r] = v;
+}
+
+// x [B, K] float32 -> bf16 hi = rn(x) and lo = rn(x - hi), each [B, K] (x = hi + lo to ~2^-16)
+__global__ void __launch_bounds__(256) split_hi_lo_kernel(const float* __restrict__ x, int64_t n,
+                                                          uint16_t* __restrict__ hi, uint16_t* __restrict__ lo) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  if (i >= n) return;
+  const float v = x[i];
+  const uint16_t h = pt_bf16_bits(v);
+  hi[i] = h;
+  lo[i] = pt_bf16_bits(v - bf16_bits_to_f32(h));
 }
 
 }  // namespace
@@ -593,8 +831,104 @@ cudaError_t launch_proj(const void* x, bool x_bf16, int K, int B, int w_dtype, c
   }
 }
 
-cudaError_t launch_rms_norm_rows(float* x, const float* w, int K, int B, float eps, cudaStream_t st) {
-  return launch_pdl(rms_norm_rows_kernel, dim3((unsigned)B), dim3(PJ_THREADS), 0, st, x, w, K, eps);
+cudaError_t launch_rms_norm_rows(float* x, const float* w, int K, int B, float eps, cudaStream_t st,
+                                 uint16_t* hi, uint16_t* lo) {
+  return launch_pdl(rms_norm_rows_kernel, dim3((unsigned)B), dim3(PJ_THREADS), 0, st, x, w, K, eps, hi, lo);
+}
+
+
+ProjTcPlan proj_tc_plan(int64_t rows0, int64_t rows1, int K, int B, bool x_f32, int w_dtype) {
+  ProjTcPlan p = ProjTcPlan{};
+  p.use = w_dtype == MLA_BF16 && B >= 16 && B <= (x_f32 ? 128 : 256) && K >= 64 && K % 8 == 0 &&
+          rows0 + rows1 > 0 && rows0 + rows1 < (int64_t(1) << 31);
+  if (!p.use) return p;
+  p.xsplit = x_f32 ? 1 : 0;
+  p.BP = x_f32 ? ((B + 7) / 8) * 8 : ((B + 15) / 16) * 16;
+  p.NB = x_f32 ? 2 * p.BP : p.BP;
+  p.tiles0 = (rows0 + 127) / 128;
+  p.tiles1 = (rows1 + 127) / 128;
+  p.nkb = (K + 63) / 64;
+  const int stage_bytes = PT_A_BYTES + p.NB * 128;
+  p.stages = PT_SMEM_HALF / stage_bytes;
+  if (p.stages > PT_STAGES) p.stages = PT_STAGES;
+  if (p.stages < 2) p.stages = 2;
+  const int64_t tiles = p.tiles0 + p.tiles1;
+  int sms = device_sms();
+  if (sms <= 0) sms = 152;
+  // Column slices: the CTAs are spread evenly over the SMs, each streams its slice's 64-column
+  // blocks plus a pipeline fill of about eight blocks; more than one slice adds the partial sums'
+  // round trip (8 bytes per output and slice, counted in 16 KB weight blocks per SM). Pick the
+  // count that minimises the busiest SM's load (the fewest slices among equals), each slice at
+  // least four blocks.
+  int64_t best = -1, best_cost = 0;
+  for (int64_t sp = 1; sp <= (p.nkb >= 8 ? p.nkb / 4 : 1); ++sp) {
+    const int64_t kb = (p.nkb + sp - 1) / sp;
+    const int64_t part_blocks = sp > 1 ? (sp * (int64_t)B * (rows0 + rows1) * 8) / (PT_A_BYTES * (int64_t)sms) : 0;
+    const int64_t cost = ((tiles * sp + sms - 1) / sms) * (kb + 8) + part_blocks;
+    if (best < 0 || cost < best_cost) {
+      best = sp;
+      best_cost = cost;
+    }
+  }
+  p.kb_per_split = (int)((p.nkb + best - 1) / best);
+  p.splits = (p.nkb + p.kb_per_split - 1) / p.kb_per_split;
+  p.part_floats = p.splits > 1 ? (int64_t)p.splits * B * (rows0 + rows1) : 0;
+  return p;
+}
+
+cudaError_t launch_proj_tc(const ProjTcPlan& p, const void* x, const void* x_lo, int K, int B, const void* w0,
+                           int64_t rows0, void* y0, bool y0_bf16, const void* w1, int64_t rows1, void* y1,
+                           bool y1_bf16, float* part, WsHeader* hdr, cudaStream_t st) {
+  if (!p.use || (p.splits > 1 && part == nullptr) || (p.xsplit && x_lo == nullptr)) return cudaErrorInvalidValue;
+  if (w1 == nullptr) rows1 = 0;
+  CUtensorMap w0m, w1m, xm, xlm;
+  if (!make_map_2d_bf16(&w0m, w0, (uint64_t)K, (uint64_t)rows0, 64, 128)) return cudaErrorInvalidValue;
+  if (rows1 > 0) {
+    if (!make_map_2d_bf16(&w1m, w1, (uint64_t)K, (uint64_t)rows1, 64, 128)) return cudaErrorInvalidValue;
+  } else {
+    w1m = w0m;
+  }
+  const uint32_t xbox = (uint32_t)(p.xsplit ? p.BP : p.NB);
+  if (!make_map_2d_bf16(&xm, x, (uint64_t)K, (uint64_t)B, 64, xbox)) return cudaErrorInvalidValue;
+  if (p.xsplit) {
+    if (!make_map_2d_bf16(&xlm, x_lo, (uint64_t)K, (uint64_t)B, 64, xbox)) return cudaErrorInvalidValue;
+  } else {
+    xlm = xm;
+  }
+  ProjTcArgs a;
+  a.tiles0 = p.tiles0;
+  a.rows[0] = rows0;
+  a.rows[1] = rows1;
+  a.y[0] = y0;
+  a.y[1] = y1;
+  a.y_bf16[0] = y0_bf16 ? 1 : 0;
+  a.y_bf16[1] = y1_bf16 ? 1 : 0;
+  a.part = part;
+  a.K = K;
+  a.B = B;
+  a.NB = p.NB;
+  a.BP = p.BP;
+  a.xsplit = p.xsplit;
+  a.splits = p.splits;
+  a.kb_per_split = p.kb_per_split;
+  a.nkb = p.nkb;
+  a.stages = p.stages;
+  a.hdr = hdr;
+  a.wait_ns = wait_limit_ns();
+  const int smem = p.stages * (PT_A_BYTES + p.NB * 128) + 1024;
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(proj_tc_kernel), smem);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = p.tiles0 + (rows1 > 0 ? p.tiles1 : 0);
+  e = launch_pdl(proj_tc_kernel, dim3((unsigned)tiles, (unsigned)p.splits), dim3(PT_THREADS), (size_t)smem, st, w0m,
+                 w1m, xm, xlm, a);
+  if (e != cudaSuccess || p.splits == 1) return e;
+  const int64_t n = (int64_t)B * (rows0 + rows1);
+  return launch_pdl(proj_reduce_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, (const float*)part,
+                    p.splits, B, rows0, rows1, y0, y0_bf16 ? 1 : 0, y1, y1_bf16 ? 1 : 0);
+}
+
+cudaError_t launch_split_hi_lo(const float* x, int64_t n, uint16_t* hi, uint16_t* lo, cudaStream_t st) {
+  return launch_pdl(split_hi_lo_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, x, n, hi, lo);
 }
 
 }  // namespace mla

@@ -173,14 +173,17 @@ class DeviceProj:
         st, n = L.mla_front_end_workspace_size(cfg, pj, B)
         L.check(st, "mla_front_end_workspace_size")
         self.ws = torch.zeros(max(n, 256), dtype=torch.uint8, device=d)
+        st, n = L.mla_o_proj_workspace_size(cfg, pj, B)
+        L.check(st, "mla_o_proj_workspace_size")
+        self.ws_o = torch.zeros(max(n, 256), dtype=torch.uint8, device=d)
 
-    def front_end(self):
+    def front_end(self, stream=None):
         return L.mla_front_end(self.cfg, self.pj, self.x, self.q, self.kva, self.wl.B, self.ws,
-                               self.ws.numel(), self.stream)
+                               self.ws.numel(), self.stream if stream is None else stream)
 
-    def o_proj(self, attn=None):
-        return L.mla_o_proj(self.cfg, self.pj, self.attn if attn is None else attn, self.y, self.wl.B,
-                            self.stream)
+    def o_proj(self, attn=None, stream=None):
+        return L.mla_o_proj(self.cfg, self.pj, self.attn if attn is None else attn, self.y, self.wl.B, self.ws_o,
+                            self.ws_o.numel(), self.stream if stream is None else stream)
 
     def q_host(self) -> np.ndarray:
         q = self.q.cpu().numpy()

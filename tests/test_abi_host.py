@@ -175,11 +175,21 @@ def _proj(L, **kw):
     return pj
 
 
-def test_front_end_workspace_size(L):
+def test_projection_workspace_sizes(L):
+    # a 256-byte error-word header, then (Q chain) the float32 q_lat rows, then the tensor-core
+    # path's bf16 halves and split partials; sizes are whole 256-byte blocks
     st, n = L.mla_front_end_workspace_size(_cfg(L), _proj(L), 64)
-    assert st == 0 and n == 64 * 1536 * 4
-    st, n = L.mla_front_end_workspace_size(_cfg(L), _proj(L, q_lora=0), 64)
-    assert st == 0 and n == 0
+    assert st == 0 and n >= 256 + 64 * 1536 * 4 + 2 * 64 * 1536 * 2 and n % 256 == 0
+    st, small = L.mla_front_end_workspace_size(_cfg(L), _proj(L), 4)   # CUDA-core path: q_lat only
+    assert st == 0 and small == 256 + 4 * 1536 * 4
+    st, n = L.mla_front_end_workspace_size(_cfg(L), _proj(L, q_lora=0), 4)
+    assert st == 0 and n == 256
+    st, n = L.mla_o_proj_workspace_size(_cfg(L), _proj(L), 4)
+    assert st == 0 and n == 256
+    st, n = L.mla_o_proj_workspace_size(_cfg(L), _proj(L), 64)
+    assert st == 0 and n >= 256 + 2 * 64 * 16 * 128 * 2 and n % 256 == 0
+    st, n = L.mla_o_proj_workspace_size(_cfg(L), _proj(L, w_dtype=L.MLA_Q8_0), 64)   # CUDA cores
+    assert st == 0 and n == 256
 
 
 @pytest.mark.parametrize("bad,status", [
@@ -208,9 +218,10 @@ def test_front_end_and_o_proj_null_and_misaligned_args(L):
     assert L.mla_front_end(cfg, _proj(L, q_a_norm_w=None), 0x60000, 0x61000, None, 4, ws, n) == INVALID
     assert L.mla_front_end(cfg, pj, 0x60000, 0x61000, None, 0, ws, n) == INVALID
     assert L.mla_front_end(cfg, pj, 0x60000, 0x61000, None, 4, ws, n - 1) == L.STATUS_CODE["MLA_ERR_WORKSPACE"]
-    assert L.mla_o_proj(cfg, _proj(L, w_o=None), 0x60000, 0x61000, 4) == INVALID
-    assert L.mla_o_proj(cfg, pj, 0x60004, 0x61000, 4) == INVALID
+    assert L.mla_o_proj(cfg, _proj(L, w_o=None), 0x60000, 0x61000, 4, ws, n) == INVALID
+    assert L.mla_o_proj(cfg, pj, 0x60004, 0x61000, 4, ws, n) == INVALID
+    assert L.mla_o_proj(cfg, pj, 0x60000, 0x61000, 4, None, 0) == L.STATUS_CODE["MLA_ERR_WORKSPACE"]
     # o_proj's in_dim is H*V: 3 heads of 8 values (24) is no multiple of the 4-bit group of 64
     odd = _cfg(L)
     odd.n_heads, odd.v_head = 3, 8
-    assert L.mla_o_proj(odd, _proj(L, w_dtype=3), 0x60000, 0x61000, 4) == INVALID
+    assert L.mla_o_proj(odd, _proj(L, w_dtype=3), 0x60000, 0x61000, 4, ws, n) == INVALID

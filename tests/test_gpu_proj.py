@@ -26,6 +26,14 @@ CASES = [
     ("v3_b2_q8", PW["v3_proj_b4"].with_(B=2, w="q8_0")),
     ("v3_b3_q4", PW["v3_proj_b4"].with_(B=3, w="q4_affine")),
     ("v3_b17_direct", PW["v3_proj_b4"].with_(B=17, q_lora=0)),
+    # tensor-core path (bf16 weights, 16 or more sequences): the smallest batch, the headline
+    # batch, the largest float32-input batch, one past it (o_proj back on CUDA cores), a direct
+    # q projection with kv_a
+    ("tc_v3_b16", PW["v3_proj_b4"].with_(B=16)),
+    ("tc_v3_b64", PW["v3_proj_b64"]),
+    ("tc_v3_b128", PW["v3_proj_b4"].with_(B=128)),
+    ("tc_v3_b129", PW["v3_proj_b4"].with_(B=129)),
+    ("tc_v2lite_b32_direct", PW["v2lite_proj_b1"].with_(B=32)),
 ]
 
 
@@ -82,6 +90,25 @@ def test_front_end_without_kva_and_repeatability():
 
 
 @gpu
+def test_tensor_core_path_is_repeatable():
+    """The split-K partial sums are added in a fixed order: two runs are bit-identical."""
+    torch = need_gpu()
+    from mla_latent_cache_absorb_gb300 import binding as L
+    from mla_latent_cache_absorb_gb300.runner import DeviceProj
+    dp = DeviceProj(synth.make_proj_problem(PW["v3_proj_b64"].with_(B=48)))
+    outs = []
+    for _ in range(2):
+        L.check(dp.front_end(), "front end")
+        L.check(dp.o_proj(), "o_proj")
+        torch.cuda.synchronize()
+        outs.append((dp.q.clone(), dp.kva.clone(), dp.y.clone()))
+    for u, v in zip(*outs):
+        assert torch.equal(u, v)
+    st, _ = L.mla_get_device_error(dp.ws)
+    assert st == 0
+
+
+@gpu
 def test_front_end_argument_errors():
     need_gpu()
     from mla_latent_cache_absorb_gb300 import binding as L
@@ -94,8 +121,9 @@ def test_front_end_argument_errors():
     dp.pj.w_kva = None
     assert L.mla_front_end(dp.cfg, dp.pj, dp.x, dp.q, dp.kva, dp.wl.B, dp.ws, dp.ws.numel()) == INVALID
     dp.pj.w_kva = saved
+    assert L.mla_o_proj(dp.cfg, dp.pj, dp.attn, dp.y, dp.wl.B, None, 0) == L.STATUS_CODE["MLA_ERR_WORKSPACE"]
     dp.pj.w_o = None
-    assert L.mla_o_proj(dp.cfg, dp.pj, dp.attn, dp.y, dp.wl.B) == INVALID
+    assert L.mla_o_proj(dp.cfg, dp.pj, dp.attn, dp.y, dp.wl.B, dp.ws_o, dp.ws_o.numel()) == INVALID
 
 
 @gpu
