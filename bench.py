@@ -509,7 +509,7 @@ def run_proj(device, name, fmt, K, W):
             o_ms.extend(e[1].elapsed_time(e[2]) for e in evs)
     hbm = peaks()[0]
     out = {"workload": wl.name, "weights": fmt, "B": wl.B, "hidden": wl.hidden, "q_lora": wl.q_lora,
-           "launches_per_step": (1 if wl.q_lora == 0 else 3) + 1, "steps": len(fe_ms)}
+           "launches_per_step": copies[0].launches(), "steps": len(fe_ms)}
     for key, ms in (("front_end", fe_ms), ("o_proj", o_ms)):
         t = statistics.median(ms) / 1e3
         b, f = work[key]

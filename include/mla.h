@@ -307,10 +307,11 @@ mla_status mla_front_end_workspace_size(const mla_config* cfg, const mla_proj* p
  *        first; q_pe is left unrotated (mla_decode_attn rotates it). Rounded once.
  *   kva  device [B, C+R] float32 = W_kva x, or NULL (then w_kva is not read).
  * Launches: one GEMV computing W_q_a x (or W_q x) and W_kva x together (one read of x), then,
- * for q_lora > 0, the norm of the q_lat rows and the q_b projection. Weights in BF16 with 16
- * to 128 sequences (256 for a bf16 input) run on the tensor cores: a float32 input as bf16
- * hi + lo halves (about float32 accuracy), column slices summed in a fixed order. Every
- * result is run-to-run identical.
+ * for q_lora > 0, the norm of the q_lat rows and the q_b projection. Weights in BF16 run on
+ * the tensor cores for 16 to 128 sequences (256 for a bf16 input), and for fewer sequences
+ * when the matrix holds 64 MiB or more: a float32 input as bf16 hi + lo halves (about float32
+ * accuracy), column slices summed in a fixed order. Every result is run-to-run identical and
+ * q does not depend on whether kv_a is computed.
  * Errors: INVALID_ARG (null or misaligned pointer, bad dims, kva without w_kva),
  * UNSUPPORTED (w_dtype), WORKSPACE, CUDA; device: TIMEOUT (a bounded wait ran out: that
  * launch's outputs are NaN). */
@@ -323,6 +324,12 @@ mla_status mla_front_end(const mla_config* cfg, const mla_proj* pj, const void* 
  * partials. Host-only. */
 mla_status mla_o_proj_workspace_size(const mla_config* cfg, const mla_proj* pj, int32_t B,
                                      size_t* bytes);
+
+/* Kernels one mla_front_end call (with or without kv_a) and one mla_o_proj call enqueue for
+ * B sequences (they depend on the path and the column slices chosen). Host-only; either
+ * pointer may be NULL. Errors: as mla_front_end_workspace_size. */
+mla_status mla_proj_launches(const mla_config* cfg, const mla_proj* pj, int32_t B, int32_t* front_end,
+                             int32_t* o_proj);
 
 /* o_proj for B sequences (async): y[b] = W_o attn[b], attn [B, H, V] float32 read head after
  * head (head h's V values at h*V: the layout mla_decode_attn writes), y device [B, D] float32.

@@ -81,6 +81,7 @@ _SIGS = {
     "mla_front_end": (c_int32, [_CFG, _PROJ, c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_size_t,
                                 c_void_p]),
     "mla_o_proj_workspace_size": (c_int32, [_CFG, _PROJ, c_int32, POINTER(c_size_t)]),
+    "mla_proj_launches": (c_int32, [_CFG, _PROJ, c_int32, POINTER(c_int32), POINTER(c_int32)]),
     "mla_o_proj": (c_int32, [_CFG, _PROJ, c_void_p, c_void_p, c_int32, c_void_p, c_size_t, c_void_p]),
     "mla_decode_multi_workspace_size": (c_int32, [_CFG, c_int32, c_int32, POINTER(c_size_t)]),
     "mla_decode_attn_multi": (c_int32, [_CFG, c_int32, c_void_p, c_void_p, _CACHE, c_void_p, c_void_p, c_void_p,
@@ -242,6 +243,13 @@ def mla_o_proj_workspace_size(cfg, pj, B):
     n = c_size_t(0)
     st = _lib.mla_o_proj_workspace_size(ctypes.byref(cfg), ctypes.byref(pj), B, ctypes.byref(n))
     return st, n.value
+
+
+def mla_proj_launches(cfg, pj, B):
+    """(status, kernels of one mla_front_end call, kernels of one mla_o_proj call)."""
+    fe, op = c_int32(0), c_int32(0)
+    st = _lib.mla_proj_launches(ctypes.byref(cfg), ctypes.byref(pj), B, ctypes.byref(fe), ctypes.byref(op))
+    return st, fe.value, op.value
 
 
 def mla_o_proj(cfg, pj, attn, y, B, workspace, ws_bytes, stream=None):

@@ -340,7 +340,7 @@ cudaError_t launch_proj(const void* x, bool x_bf16, int K, int B, int w_dtype, c
                         cudaStream_t st);
 cudaError_t launch_rms_norm_rows(float* x, const float* w, int K, int B, float eps, cudaStream_t st,
                                  uint16_t* hi = nullptr, uint16_t* lo = nullptr);
-// tensor-core projections (bf16 weights, 16 to 128/256 sequences), see proj.cu
+// tensor-core projections (bf16 weights, up to 128/256 sequences), see proj.cu
 struct ProjTcPlan {
   bool use;
   int xsplit, BP, NB, nkb, kb_per_split, splits, stages;

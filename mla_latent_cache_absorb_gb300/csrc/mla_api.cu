@@ -556,7 +556,9 @@ size_t align_up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 mla_status front_end_ws(const mla_config* cfg, const mla_proj* pj, int32_t B, ProjWs* w) {
   const int64_t q_rows = (int64_t)cfg->n_heads * (cfg->qk_nope + cfg->qk_rope);
-  const int64_t kva_rows = pj->w_kva != nullptr ? cfg->kv_lora + cfg->qk_rope : 0;
+  // the kv_a rows count in the plan whether or not they are computed, so that q's column slices
+  // (and so its rounding) do not depend on it
+  const int64_t kva_rows = cfg->kv_lora + cfg->qk_rope;
   const bool chain = pj->q_lora > 0;
   const bool xb = cfg->act_dtype == MLA_BF16;
   w->pa = proj_tc_plan(chain ? pj->q_lora : q_rows, kva_rows, pj->hidden, B, false, xb ? pj->w_dtype : -1);
@@ -615,6 +617,27 @@ mla_status mla_o_proj_workspace_size(const mla_config* cfg, const mla_proj* pj, 
   st = o_proj_ws(cfg, pj, B, &w);
   if (st != MLA_OK) return st;
   *bytes = w.total;
+  return MLA_OK;
+}
+
+mla_status mla_proj_launches(const mla_config* cfg, const mla_proj* pj, int32_t B, int32_t* front_end,
+                             int32_t* o_proj) {
+  mla_status st = check_proj(cfg, pj, B);
+  if (st != MLA_OK) return st;
+  ProjWs w;
+  if (front_end != nullptr) {
+    st = front_end_ws(cfg, pj, B, &w);
+    if (st != MLA_OK) return st;
+    int n = 1 + (w.pa.use && w.pa.splits > 1 ? 1 : 0);                // q_a (or q) with kv_a
+    if (pj->q_lora > 0) n += 2 + (w.pb.use && w.pb.splits > 1 ? 1 : 0);  // norm, q_b
+    *front_end = n;
+  }
+  if (o_proj != nullptr) {
+    if (!proj_in_dim_ok((int64_t)cfg->n_heads * cfg->v_head, pj->w_dtype)) return MLA_ERR_INVALID_ARG;
+    st = o_proj_ws(cfg, pj, B, &w);
+    if (st != MLA_OK) return st;
+    *o_proj = w.pa.use ? 2 + (w.pa.splits > 1 ? 1 : 0) : 1;           // halves, GEMM, reduction
+  }
   return MLA_OK;
 }
 

@@ -578,7 +578,7 @@ cudaError_t launch_proj_dt(const ProjArgs& a, bool x_bf16, int64_t blocks, cudaS
   return x_bf16 ? launch_proj_x<WD, true>(a, blocks, st) : launch_proj_x<WD, false>(a, blocks, st);
 }
 
-// ---- bf16 weights, 16 to 128 sequences: tcgen05 ------------------------------------------------
+// ---- bf16 weights, up to 128 sequences: tcgen05 ------------------------------------------------
 // y[b, r] = sum_k W[r, k] x[b, k] as D[r, b] = W_tile . X^T on the tensor cores: a CTA owns 128 rows
 // of W (the M = 128 operand, K-major, 64-column blocks by TMA in the 128-byte swizzle) and one
 // slice of the columns (split-K); the batch is the N operand: the bf16 input rows, or, for a
@@ -839,8 +839,12 @@ cudaError_t launch_rms_norm_rows(float* x, const float* w, int K, int B, float e
 
 ProjTcPlan proj_tc_plan(int64_t rows0, int64_t rows1, int K, int B, bool x_f32, int w_dtype) {
   ProjTcPlan p = ProjTcPlan{};
-  p.use = w_dtype == MLA_BF16 && B >= 16 && B <= (x_f32 ? 128 : 256) && K >= 64 && K % 8 == 0 &&
-          rows0 + rows1 > 0 && rows0 + rows1 < (int64_t(1) << 31);
+  // Under 16 sequences only a large matrix pays for the extra launches (the input's halves, the
+  // slice reduction) and the fill of the ring: at 4 sequences a 235 MB matrix streams 1.4x faster
+  // than on the CUDA cores, a 30 MB one no faster.
+  const int64_t w_bytes = (rows0 + rows1) * (int64_t)K * 2;
+  p.use = w_dtype == MLA_BF16 && (B >= 16 || w_bytes >= (int64_t(64) << 20)) && B <= (x_f32 ? 128 : 256) &&
+          K >= 64 && K % 8 == 0 && rows0 + rows1 > 0 && rows0 + rows1 < (int64_t(1) << 31);
   if (!p.use) return p;
   p.xsplit = x_f32 ? 1 : 0;
   p.BP = x_f32 ? ((B + 7) / 8) * 8 : ((B + 15) / 16) * 16;

@@ -185,6 +185,12 @@ class DeviceProj:
         return L.mla_o_proj(self.cfg, self.pj, self.attn if attn is None else attn, self.y, self.wl.B, self.ws_o,
                             self.ws_o.numel(), self.stream if stream is None else stream)
 
+    def launches(self) -> int:
+        """Kernels one front_end() plus one o_proj() enqueue."""
+        st, fe, op = L.mla_proj_launches(self.cfg, self.pj, self.wl.B)
+        L.check(st, "mla_proj_launches")
+        return fe + op
+
     def q_host(self) -> np.ndarray:
         q = self.q.cpu().numpy()
         return q.view(np.uint16) if self.wl.act == "bf16" else q

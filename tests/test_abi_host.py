@@ -180,16 +180,35 @@ def test_projection_workspace_sizes(L):
     # path's bf16 halves and split partials; sizes are whole 256-byte blocks
     st, n = L.mla_front_end_workspace_size(_cfg(L), _proj(L), 64)
     assert st == 0 and n >= 256 + 64 * 1536 * 4 + 2 * 64 * 1536 * 2 and n % 256 == 0
-    st, small = L.mla_front_end_workspace_size(_cfg(L), _proj(L), 4)   # CUDA-core path: q_lat only
+    # 4 sequences, 16 heads: every matrix under 64 MiB, CUDA cores: q_lat only
+    st, small = L.mla_front_end_workspace_size(_cfg(L), _proj(L), 4)
     assert st == 0 and small == 256 + 4 * 1536 * 4
     st, n = L.mla_front_end_workspace_size(_cfg(L), _proj(L, q_lora=0), 4)
     assert st == 0 and n == 256
     st, n = L.mla_o_proj_workspace_size(_cfg(L), _proj(L), 4)
     assert st == 0 and n == 256
+    # 4 sequences, 128 heads: q_b (75 MB) and W_o (235 MB) on the tensor cores, q_a + kv_a
+    # (30 MB) on the CUDA cores: q_lat and the halves of the normalised q_lat / of attn
+    st, n = L.mla_front_end_workspace_size(_cfg(L, n_heads=128), _proj(L), 4)
+    assert st == 0 and n >= 256 + 4 * 1536 * 4 + 2 * 4 * 1536 * 2 and n % 256 == 0
+    st, n = L.mla_o_proj_workspace_size(_cfg(L, n_heads=128), _proj(L), 4)
+    assert st == 0 and n >= 256 + 2 * 4 * 128 * 128 * 2 and n % 256 == 0
     st, n = L.mla_o_proj_workspace_size(_cfg(L), _proj(L), 64)
     assert st == 0 and n >= 256 + 2 * 64 * 16 * 128 * 2 and n % 256 == 0
     st, n = L.mla_o_proj_workspace_size(_cfg(L), _proj(L, w_dtype=L.MLA_Q8_0), 64)   # CUDA cores
     assert st == 0 and n == 256
+
+
+def test_projection_launch_counts(L):
+    # 16 heads, 4 sequences: one GEMV each (q_a + kv_a, q_b, o_proj) and the norm
+    assert L.mla_proj_launches(_cfg(L), _proj(L), 4) == (0, 3, 1)
+    assert L.mla_proj_launches(_cfg(L), _proj(L, q_lora=0), 4) == (0, 1, 1)
+    assert L.mla_proj_launches(_cfg(L), _proj(L, w_dtype=L.MLA_Q8_0), 64) == (0, 3, 1)
+    # tensor cores: o_proj adds the halves of attn, and a slice reduction when the columns split
+    st, fe, op = L.mla_proj_launches(_cfg(L, n_heads=128), _proj(L), 64)
+    assert st == 0 and 3 <= fe <= 5 and op in (2, 3)
+    st, _, _ = L.mla_proj_launches(_cfg(L), _proj(L, w_dtype=9), 4)
+    assert st == L.STATUS_CODE["MLA_ERR_UNSUPPORTED"]
 
 
 @pytest.mark.parametrize("bad,status", [

@@ -26,9 +26,9 @@ CASES = [
     ("v3_b2_q8", PW["v3_proj_b4"].with_(B=2, w="q8_0")),
     ("v3_b3_q4", PW["v3_proj_b4"].with_(B=3, w="q4_affine")),
     ("v3_b17_direct", PW["v3_proj_b4"].with_(B=17, q_lora=0)),
-    # tensor-core path (bf16 weights, 16 or more sequences): the smallest batch, the headline
-    # batch, the largest float32-input batch, one past it (o_proj back on CUDA cores), a direct
-    # q projection with kv_a
+    # tensor-core path (bf16 weights, 16 or more sequences, or a matrix of 64 MiB or more, as
+    # q_b and W_o in v3_b4 above): the smallest batch, the headline batch, the largest
+    # float32-input batch, one past it (o_proj back on CUDA cores), a direct q projection with kv_a
     ("tc_v3_b16", PW["v3_proj_b4"].with_(B=16)),
     ("tc_v3_b64", PW["v3_proj_b64"]),
     ("tc_v3_b128", PW["v3_proj_b4"].with_(B=128)),
