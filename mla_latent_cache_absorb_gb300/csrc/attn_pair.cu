@@ -430,11 +430,13 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
         if (!defer_q && !load_q()) { ok = false; break; }
         for (int t = tlo; t < thi && ok; ++t) {
           const int st = (int)(n % AP_STAGES);
+          // the row lookup (a page-table read) goes before the wait for a free stage, which
+          // lies on the loop from PV of tile n - 3 to QK^T of tile n
+          int64_t pr = a.map.phys(sb, (int64_t)t * AP_TILE);
           if (n >= AP_STAGES && !wait_bar(s, &s.empty[st], (uint32_t)(((n / AP_STAGES) - 1) & 1), a.wait_ns)) {
             ok = false;
             break;
           }
-          int64_t pr = a.map.phys(sb, (int64_t)t * AP_TILE);
           if (pr < 0) {   // out-of-range page id: load a valid row, flag the segment
             atomicExch(&s.bad_page[seg & 3], 1);
             set_error(a.hdr, MLA_ERR_BAD_PAGE, sb);
