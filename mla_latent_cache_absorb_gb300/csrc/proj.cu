@@ -161,6 +161,10 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem) : "memory");
 }
+__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d), "l"(gmem) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
@@ -322,9 +326,18 @@ __global__ void __launch_bounds__(PJ_THREADS, 2) proj_gemv_kernel(const __grid_c
 // flight per warp. x goes through one shared buffer per round (16 KB: 1024 bf16 or 512 float32
 // columns of 8 sequences), loaded into registers a round ahead and stored between the
 // round's two barriers.
+// Quantised weights (Q8_0, 4-bit affine) go through the same ring as raw bytes, when K is a
+// multiple of 256 (whole steps; every run below starts on a 16- or 8-byte boundary): a step of
+// a row is 8 Q8_0 blocks (8 x 34 = 272 bytes, 17 pieces of 16 bytes), or 128 bytes of 4-bit
+// codes plus the row's 4 bf16 scales and 4 bf16 biases (two 8-byte pieces). The warp's pieces
+// are shared out over its lanes, so a lane decodes bytes other lanes copied: a __syncwarp after
+// the wait makes them visible, and one after the step's use frees the slot for reuse.
+// SLOT: bytes of one step of the warp's 4 rows; D: steps in flight per warp.
 template <int WD> struct Ring;
-template <> struct Ring<MLA_BF16> { static constexpr int D = 4, LB = 16; };
-template <> struct Ring<MLA_F32> { static constexpr int D = 2, LB = 32; };
+template <> struct Ring<MLA_BF16> { static constexpr int D = 4, LB = 16, SLOT = PJ_RW * 32 * 16; };
+template <> struct Ring<MLA_F32> { static constexpr int D = 2, LB = 32, SLOT = PJ_RW * 32 * 32; };
+template <> struct Ring<MLA_Q8_0> { static constexpr int D = 8, LB = 0, SLOT = PJ_RW * 272; };
+template <> struct Ring<MLA_Q4_AFFINE> { static constexpr int D = 8, LB = 0, SLOT = PJ_RW * (128 + 16); };
 
 template <bool XBF> struct XRound {
   static constexpr int EB = XBF ? 2 : 4;
@@ -338,18 +351,19 @@ template <bool XBF> struct XRound {
 
 template <int WD, bool XBF>
 constexpr int ring_smem_bytes() {
-  return XRound<XBF>::BYTES + PJ_WARPS * Ring<WD>::D * PJ_RW * 32 * Ring<WD>::LB;
+  return XRound<XBF>::BYTES + PJ_WARPS * Ring<WD>::D * Ring<WD>::SLOT;
 }
 
 template <int WD, bool XBF>
 __global__ void __launch_bounds__(PJ_THREADS, 2) proj_gemv_ring_kernel(const __grid_constant__ ProjArgs a) {
   using XR = XRound<XBF>;
-  constexpr int D = Ring<WD>::D, LB = Ring<WD>::LB, EW = WD == MLA_BF16 ? 2 : 4;
+  constexpr int D = Ring<WD>::D, LB = Ring<WD>::LB, SLOT = Ring<WD>::SLOT, EW = WD == MLA_BF16 ? 2 : 4;
+  constexpr bool QUANT = WD == MLA_Q8_0 || WD == MLA_Q4_AFFINE;
   extern __shared__ __align__(16) uint8_t sm[];
   __shared__ float red[PJ_WARPS][32];
   uint8_t* xs = sm;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint8_t* ring = sm + XR::BYTES + warp * (D * PJ_RW * 32 * LB);
+  uint8_t* ring = sm + XR::BYTES + warp * (D * SLOT);
   pdl_trigger();
   const int S = a.ksplit, g = warp / S, s = warp % S;
   const bool second = blockIdx.x >= a.ctas0;
@@ -371,8 +385,12 @@ __global__ void __launch_bounds__(PJ_THREADS, 2) proj_gemv_ring_kernel(const __g
 #pragma unroll
   for (int r = 0; r < PJ_RW; ++r) {
     row_ok[r] = r0 + r < rows;
-    wrow[r] = W + (row_ok[r] ? (r0 + r) * (int64_t)K * EW : 0) + lane * 8 * EW;
+    const int64_t rr = row_ok[r] ? r0 + r : 0;
+    wrow[r] = W + rr * (int64_t)K * EW + lane * 8 * EW;   // bf16 / float32
   }
+  // 4-bit: the scales and the biases of all rows follow the codes
+  const uint8_t* q4_sc = W + rows * (int64_t)(K / 2);
+  const uint8_t* q4_bi = q4_sc + rows * (int64_t)(K / 64) * 2;
   auto step_col = [&](int n) {
     return (n >> lg_spr) * XR::COLS + ((s + ((n & (spr - 1)) << lg_s)) * PJ_STEP) + lane * 8;
   };
@@ -382,13 +400,40 @@ __global__ void __launch_bounds__(PJ_THREADS, 2) proj_gemv_ring_kernel(const __g
     if (n < nsteps) {
       const int k = step_col(n);
       if (k < K) {
-        uint8_t* slot = ring + (n % D) * (PJ_RW * 32 * LB) + lane * LB;
-        const int koff = (k - lane * 8) * EW;
+        if constexpr (WD == MLA_Q8_0) {
+          // 68 pieces: piece i = (row i / 17, 16-byte piece i % 17), lane i % 32
+          uint8_t* slot = ring + (n % D) * SLOT;
+          const int64_t boff = (int64_t)((k - lane * 8) / 32) * 34;
 #pragma unroll
-        for (int r = 0; r < PJ_RW; ++r) {
-          if (row_ok[r]) {
+          for (int u = 0; u < 3; ++u) {
+            const int i = lane + 32 * u;
+            const int r = i / 17, pc = i % 17;   // lane-dependent row: addressed directly
+            if (i < PJ_RW * 17 && r0 + r < rows)
+              cp_async16(slot + r * 272 + 16 * pc, W + (r0 + r) * (int64_t)(K / 32) * 34 + boff + 16 * pc);
+          }
+        } else if constexpr (WD == MLA_Q4_AFFINE) {
+          // codes: lane l copies piece l % 8 of row l / 8; lanes 0-7 also the scales (rows
+          // 0-3) or the biases (rows 0-3) of the step's four 64-column groups
+          uint8_t* slot = ring + (n % D) * SLOT;
+          const int k0 = k - lane * 8;
+          const int r = lane >> 3, pc = lane & 7;   // lane-dependent row: addressed directly
+          if (r0 + r < rows) cp_async16(slot + r * 128 + 16 * pc, W + (r0 + r) * (int64_t)(K / 2) + k0 / 2 + 16 * pc);
+          if (lane < 8) {
+            const int rr = lane & 3;
+            if (r0 + rr < rows) {
+              const int64_t g = (r0 + rr) * (int64_t)(K / 64) + k0 / 64;
+              cp_async8(slot + PJ_RW * 128 + (lane >> 2) * 32 + rr * 8, (lane < 4 ? q4_sc : q4_bi) + g * 2);
+            }
+          }
+        } else {
+          uint8_t* slot = ring + (n % D) * SLOT + lane * LB;
+          const int koff = (k - lane * 8) * EW;
 #pragma unroll
-            for (int h = 0; h < LB / 16; ++h) cp_async16(slot + r * 32 * LB + 16 * h, wrow[r] + koff + 16 * h);
+          for (int r = 0; r < PJ_RW; ++r) {
+            if (row_ok[r]) {
+#pragma unroll
+              for (int h = 0; h < LB / 16; ++h) cp_async16(slot + r * 32 * LB + 16 * h, wrow[r] + koff + 16 * h);
+            }
           }
         }
       }
@@ -447,13 +492,37 @@ __global__ void __launch_bounds__(PJ_THREADS, 2) proj_gemv_ring_kernel(const __g
       for (int q = 0; q < spr; ++q, ++n) {
         issue(n + D - 1);
         cp_async_wait<D - 1>();
+        if constexpr (QUANT) __syncwarp();   // the other lanes' pieces of this step have landed
         const int k = step_col(n);
         if (k < K) {
-          const uint8_t* slot = ring + (n % D) * (PJ_RW * 32 * LB);
+          const uint8_t* slot = ring + (n % D) * SLOT;
           float w[PJ_RW][8];
 #pragma unroll
           for (int r = 0; r < PJ_RW; ++r) {
-            if (WD == MLA_BF16) {
+            if constexpr (WD == MLA_Q8_0) {
+              // lane l: block l / 4 of the step, codes 8 (l % 4) .. +7, as 16-bit-aligned bytes
+              const uint8_t* blk = slot + r * 272 + (lane >> 2) * 34;
+              const float d = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(blk)));
+              const uint32_t o = (uint32_t)(blk - slot) + 2 + 8 * (lane & 3);   // even
+              const uint32_t* wp = reinterpret_cast<const uint32_t*>(slot + (o & ~3u));
+              const uint32_t sh = (o & 3u) * 8;                                  // 0 or 16
+              // the third word only when the codes straddle it (the last block's last lane
+              // would otherwise read past the row)
+              const uint32_t w0 = wp[0], w1 = wp[1], w2 = sh ? wp[2] : 0u;
+              const uint32_t c01 = __funnelshift_r(w0, w1, sh), c23 = __funnelshift_r(w1, w2, sh);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                w[r][e] = d * (float)(int8_t)(c01 >> (8 * e));
+                w[r][4 + e] = d * (float)(int8_t)(c23 >> (8 * e));
+              }
+            } else if constexpr (WD == MLA_Q4_AFFINE) {
+              const uint32_t cw = *reinterpret_cast<const uint32_t*>(slot + r * 128 + lane * 4);
+              const uint16_t* sb = reinterpret_cast<const uint16_t*>(slot + PJ_RW * 128);
+              const float sc = bf16_bits_to_f32(sb[r * 4 + (lane >> 3)]);
+              const float bi = bf16_bits_to_f32(sb[16 + r * 4 + (lane >> 3)]);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) w[r][e] = fmaf(sc, (float)((cw >> (4 * e)) & 15u), bi);
+            } else if constexpr (WD == MLA_BF16) {
               const uint4 u = *reinterpret_cast<const uint4*>(slot + (r * 32 + lane) * LB);
               const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -495,6 +564,7 @@ __global__ void __launch_bounds__(PJ_THREADS, 2) proj_gemv_ring_kernel(const __g
             }
           }
         }
+        if constexpr (QUANT) __syncwarp();   // every lane is done with this slot before it is refilled
       }
       __syncthreads();   // every warp is done with this round's x
       if (t + 1 < nrounds) {
@@ -559,9 +629,14 @@ __global__ void __launch_bounds__(PJ_THREADS) rms_norm_rows_kernel(float* x, con
   }
 }
 
+// bf16 / float32 weights always take the ring; quantised ones when their steps are whole
+constexpr bool proj_uses_ring(int wd, int K) {
+  return wd == MLA_BF16 || wd == MLA_F32 || ((wd == MLA_Q8_0 || wd == MLA_Q4_AFFINE) && K % 256 == 0);
+}
+
 template <int WD, bool XBF>
 cudaError_t launch_proj_x(const ProjArgs& a, int64_t blocks, cudaStream_t st) {
-  if constexpr (WD == MLA_BF16 || WD == MLA_F32) {
+  if (proj_uses_ring(WD, a.K)) {
     constexpr int bytes = ring_smem_bytes<WD, XBF>();
     const cudaError_t e = ensure_smem(reinterpret_cast<const void*>(proj_gemv_ring_kernel<WD, XBF>), bytes);
     if (e != cudaSuccess) return e;
@@ -806,10 +881,10 @@ cudaError_t launch_proj(const void* x, bool x_bf16, int K, int B, int w_dtype, c
   a.x = x;
   a.K = K;
   a.B = B;
-  // Split the columns among more warps (at most the steps of a round: 4, or 2 for float32 x
-  // under bf16 / float32 weights) only while the grid stays under two CTAs per SM.
+  // Split the columns among more warps (at most the steps of a round: 4, or 2 for float32 x on
+  // the ring kernel) only while the grid stays under two CTAs per SM.
   const int64_t target = 2 * (int64_t)device_sms();
-  const int s_max = (!x_bf16 && (w_dtype == MLA_BF16 || w_dtype == MLA_F32)) ? 2 : 4;
+  const int s_max = (!x_bf16 && proj_uses_ring(w_dtype, K)) ? 2 : 4;
   int S = 1;
   while (S < s_max) {
     const int64_t rows_per_cta = (int64_t)(PJ_WARPS / S) * PJ_RW;

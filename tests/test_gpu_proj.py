@@ -25,6 +25,9 @@ CASES = [
     ("v3_b4", PW["v3_proj_b4"]),
     ("v3_b2_q8", PW["v3_proj_b4"].with_(B=2, w="q8_0")),
     ("v3_b3_q4", PW["v3_proj_b4"].with_(B=3, w="q4_affine")),
+    # in_dim not a multiple of 256: the quantised GEMV without the ring (hidden 2112)
+    ("v2lite_b3_q8_k2112", PW["v2lite_proj_b1"].with_(B=3, w="q8_0", hidden=2112)),
+    ("v2lite_b3_q4_k2112", PW["v2lite_proj_b1"].with_(B=3, w="q4_affine", hidden=2112)),
     ("v3_b17_direct", PW["v3_proj_b4"].with_(B=17, q_lora=0)),
     # tensor-core path (bf16 weights, 16 or more sequences, or a matrix of 64 MiB or more, as
     # q_b and W_o in v3_b4 above): the smallest batch, the headline batch, the largest
