@@ -509,19 +509,25 @@ __global__ void __launch_bounds__(PJ_THREADS, 2) proj_gemv_ring_kernel(const __g
               // the third word only when the codes straddle it (the last block's last lane
               // would otherwise read past the row)
               const uint32_t w0 = wp[0], w1 = wp[1], w2 = sh ? wp[2] : 0u;
-              const uint32_t c01 = __funnelshift_r(w0, w1, sh), c23 = __funnelshift_r(w1, w2, sh);
+              // the sign bit of every code flipped, then each byte placed in the mantissa of
+              // 2^23 (one byte permute) and 2^23 + 128 taken off: exactly the signed code, with
+              // no int-to-float conversion (those issue at a quarter of the FMA rate)
+              const uint32_t c01 = __funnelshift_r(w0, w1, sh) ^ 0x80808080u;
+              const uint32_t c23 = __funnelshift_r(w1, w2, sh) ^ 0x80808080u;
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                w[r][e] = d * (float)(int8_t)(c01 >> (8 * e));
-                w[r][4 + e] = d * (float)(int8_t)(c23 >> (8 * e));
+                w[r][e] = d * (__uint_as_float(__byte_perm(c01, 0x4B000000u, 0x7650u | e)) - 8388736.0f);
+                w[r][4 + e] = d * (__uint_as_float(__byte_perm(c23, 0x4B000000u, 0x7650u | e)) - 8388736.0f);
               }
             } else if constexpr (WD == MLA_Q4_AFFINE) {
               const uint32_t cw = *reinterpret_cast<const uint32_t*>(slot + r * 128 + lane * 4);
               const uint16_t* sb = reinterpret_cast<const uint16_t*>(slot + PJ_RW * 128);
               const float sc = bf16_bits_to_f32(sb[r * 4 + (lane >> 3)]);
               const float bi = bf16_bits_to_f32(sb[16 + r * 4 + (lane >> 3)]);
+              // each code in the mantissa of 2^23 and 2^23 taken off (exact, no conversion)
 #pragma unroll
-              for (int e = 0; e < 8; ++e) w[r][e] = fmaf(sc, (float)((cw >> (4 * e)) & 15u), bi);
+              for (int e = 0; e < 8; ++e)
+                w[r][e] = fmaf(sc, __uint_as_float(((cw >> (4 * e)) & 15u) | 0x4B000000u) - 8388608.0f, bi);
             } else if constexpr (WD == MLA_BF16) {
               const uint4 u = *reinterpret_cast<const uint4*>(slot + (r * 32 + lane) * LB);
               const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
