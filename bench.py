@@ -79,8 +79,15 @@ def step_work(prob):
         byts += (C + R) * wl.hidden * e + B * wl.hidden * e
     else:
         byts += B * (C + R) * 4
+    decode_flops, decode_bytes = flops, byts   # mla_decode_attn alone (kernel 3 runs it in one launch)
+    if wl.append == "gemv":
+        flops += B * 2 * (C + R) * wl.hidden
+        byts += (C + R) * wl.hidden * e + B * wl.hidden * e
+    else:
+        byts += B * (C + R) * 4
     byts += B * (C + R) * e  # the appended rows
-    return dict(rows=rows, flops=flops, bytes=byts, attn_flops=attn_flops, attn_bytes=attn_bytes)
+    return dict(rows=rows, flops=flops, bytes=byts, attn_flops=attn_flops, attn_bytes=attn_bytes,
+                decode_flops=decode_flops, decode_bytes=decode_bytes)
 
 
 def input_bytes(prob):
@@ -218,7 +225,7 @@ def peaks():
 
 
 # attention kernel of a plan (mla_plan_info.kernel) -> its source file and kernel name
-KERNEL_FILE = {0: "attn_simt", 1: "attn_tc", 2: "attn_pair"}
+KERNEL_FILE = {0: "attn_simt", 1: "attn_tc", 2: "attn_pair", 3: "decode_small"}
 
 
 def kernel_source_sha(kernel: int) -> str:
@@ -281,7 +288,7 @@ def run_ours(args, rank, world, device, workload, K, W, with_e2e=True, with_cloc
         steps.append(DeviceStep(prob, device=device, stream=stream))
     st, plan = L.mla_decode_plan(steps[0].cfg, wl.B)
     L.check(st, "mla_decode_plan")
-    launches_per_step = (2 if wl.append == "gemv" else 1) + 3
+    launches_per_step = (2 if wl.append == "gemv" else 1) + (1 if plan.kernel == 3 else 3)
 
     def one_step(ds, s, ev=None):
         # the user's calls: mla_cache_append, then mla_decode_attn; a step whose attention is
@@ -289,6 +296,11 @@ def run_ours(args, rank, world, device, workload, K, W, with_e2e=True, with_cloc
         L.check(ds.append(s), "mla_cache_append")
         if ev is None:
             L.check(ds.decode(s), "mla_decode_attn")
+            return
+        if plan.kernel == 3:   # one launch: the whole decode is the bracketed kernel
+            ev[0].record(s)
+            L.check(ds.decode(s), "mla_decode_attn")
+            ev[1].record(s)
             return
         L.check(ds.absorb(s), "mla_decode_absorb")
         ev[0].record(s)
@@ -397,7 +409,11 @@ def run_ours(args, rank, world, device, workload, K, W, with_e2e=True, with_cloc
     ms_per_step = tmax / K
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
     hbm, tf_burst, tf_sust, src = peaks()
-    attn_gbs = work["attn_bytes"] / (attn_avg_ms / 1e3) / 1e9
+    # the bracketed kernel's algorithmic work: the attention (kernels 0-2), or the whole decode
+    # (kernel 3: absorb, attention, merge and W_UV in one launch)
+    k_bytes = work["decode_bytes"] if plan.kernel == 3 else work["attn_bytes"]
+    k_flops = work["decode_flops"] if plan.kernel == 3 else work["attn_flops"]
+    attn_gbs = k_bytes / (attn_avg_ms / 1e3) / 1e9
     step_s = ms_per_step / 1e3
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K, "warmup": W,
@@ -411,7 +427,8 @@ def run_ours(args, rank, world, device, workload, K, W, with_e2e=True, with_cloc
                       f"by in-graph events",
             "gpus": f"replicas x{world}" if world > 1 else "single GPU",
             "attention_kernel": {0: "cuda-core", 1: "tcgen05, one CTA per head group",
-                                 2: "tcgen05, SM pairs (clusters of two CTAs)"}[plan.kernel],
+                                 2: "tcgen05, SM pairs (clusters of two CTAs)",
+                                 3: "one launch: absorb, attention, merge and W_UV (CUDA cores)"}[plan.kernel],
             "heads_per_cta": plan.heads_per_cta, "splits": plan.splits,
             "rows_per_split": plan.rows_per_split,
         },
@@ -419,12 +436,13 @@ def run_ours(args, rank, world, device, workload, K, W, with_e2e=True, with_cloc
         "hbm_gbs": work["bytes"] / step_s / 1e9,
         "step_roofline_frac": max(work["flops"] / (tf_burst * 1e12), work["bytes"] / (hbm * 1e9)) / step_s,
         "roofline": {
-            "kernel": f"{KERNEL_FILE[plan.kernel]} (split attention)",
+            "kernel": f"{KERNEL_FILE[plan.kernel]} ({'whole decode' if plan.kernel == 3 else 'split attention'})",
             "bound": "hbm", "achieved": attn_gbs, "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm,
             "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback",
-            "bytes_per_launch": work["attn_bytes"], "avg_launch_us": attn_avg_ms * 1e3,
+            "bytes_per_launch": k_bytes, "avg_launch_us": attn_avg_ms * 1e3,
             "traffic": ncu_traffic(plan.kernel, wl.name),
-            "tensor_tflops": work["attn_flops"] / (attn_avg_ms / 1e3) / 1e12,
+            "tensor_tflops": k_flops / (attn_avg_ms / 1e3) / 1e12 if plan.kernel in (1, 2) else None,
+            "kernel_tflops": k_flops / (attn_avg_ms / 1e3) / 1e12,
         },
         "gpu_launches": launches_per_step * K,
         "clocks": clocks,
@@ -881,7 +899,8 @@ def main():
             if wname == args.workload:
                 continue
             sub = run_ours(args, rank, world, device, wname, k, args.warmup, with_e2e=False, with_clocks=False)
-            also[wname] = {"roofline_frac": sub["roofline"]["frac"], "avg_launch_us": sub["roofline"]["avg_launch_us"],
+            also[wname] = {"kernel": sub["roofline"]["kernel"],
+                           "roofline_frac": sub["roofline"]["frac"], "avg_launch_us": sub["roofline"]["avg_launch_us"],
                            "attn_gbs": sub["roofline"]["achieved"], "ms_per_step": sub["ms_per_step"],
                            "rows_per_s": sub["value"], "steps": k, "heads_per_cta": sub["run"]["heads_per_cta"]}
             line["gpu_launches"] += sub["gpu_launches"]

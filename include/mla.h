@@ -171,7 +171,11 @@ typedef struct mla_plan_info {
                               per SM and head group, 128-row tiles,
                               2 = tcgen05 on SM pairs (bf16 rows of 576, exactly 128 heads):
                               a cluster of two CTAs shares each 64-row tile, one latent half
-                              each; `splits` then counts CTA pairs */
+                              each; `splits` then counts CTA pairs,
+                              3 = one launch for tiny batches (bf16, one query row per
+                              sequence, B * H <= 64, H <= 32): absorb, attention over 32-row
+                              chunks, merge and W_UV in a single grid separated by grid-wide
+                              barriers; `splits` then counts the grid's CTAs */
   int32_t heads_per_cta;   /* heads that share each staged row tile (kernel 2: per CTA pair) */
   int32_t head_groups;     /* ceil(H / heads_per_cta) */
   int32_t splits;          /* row splits per sequence (partials kept in the workspace) */
@@ -239,7 +243,13 @@ mla_status mla_cache_append(const mla_config* cfg, const mla_cache* cache,
  * after it streams cache rows while the absorb still runs, waiting only for the fused
  * queries. Otherwise every kernel is launched as described at the top. The three step calls
  * below always keep every kernel's wait in place; the results are bit-identical either way.
- * Device errors: BAD_SEQ_LEN, BAD_PAGE (that sequence's out/lse become NaN). */
+ * Tiny batches (mla_decode_plan reports kernel 3) run instead as one launch (absorb,
+ * attention over 32-row chunks, merge and W_UV in one grid, float32 throughout): its results
+ * agree with the three step calls within rounding, not bit for bit, and are the same from run
+ * to run and for a sequence whatever the rest of the batch. It uses the workspace's header for
+ * its barrier counters (left zero when it returns).
+ * Device errors: BAD_SEQ_LEN, BAD_PAGE (that sequence's out/lse become NaN), TIMEOUT (one
+ * launch: a grid-wide wait ran out; the outputs that CTA owns become NaN). */
 mla_status mla_decode_attn(const mla_config* cfg, const void* q, const void* kv_b,
                            const mla_cache* cache, const int32_t* seq_lens,
                            const int32_t* positions, float* out, float* lse, int32_t B,

@@ -280,8 +280,23 @@ struct DecodePlan {
   int part_groups, part_hpg, n_slots;
   // q_res: bf16 rounding residual of the fused query rows (bf16 activations only)
   size_t off_qabs, off_qres, off_po, off_plse, off_meta, total;
+  // one-launch decode for tiny batches (decode_small.cu), used by mla_decode_attn when set;
+  // its float32 queries, chunk partials, slice shares of out and per-head counters follow the
+  // staged layout
+  int small;
+  size_t off_sq, off_sp, off_sw, off_sc;
 };
 enum { PATH_SIMT = 0, PATH_TC = 1, PATH_PAIR = 2 };
+
+// one-launch decode for tiny batches: absorb, attention over 32-row chunks, merge and W_UV in
+// one grid with bounded grid-wide barriers (decode_small.cu)
+bool decode_small_supported(const mla_config& cfg, int B, int tokens);
+int64_t decode_small_max_chunks(const mla_config& cfg);
+int decode_small_grid(const mla_config& cfg, int B);
+cudaError_t launch_decode_small(const mla_config& cfg, const mla_cache& cache, const void* q, const void* kv_b,
+                                const int32_t* seq_lens, const int32_t* positions, float* out, float* lse, int B,
+                                float* qf, float* part, float* wshare, unsigned int* head_cnt, WsHeader* hdr,
+                                cudaStream_t st);
 
 // True when the CUDA driver's tensor-map encoder could be found (looked up once per process).
 bool tma_encoder_available();

@@ -1,0 +1,601 @@
+// One-launch decode for tiny batches: absorb, split attention and LSE-merge combine with the
+// W_UV up-projection in a single grid, phases separated by grid-wide barriers, all in float32
+// on the CUDA cores.
+//
+// moeflux 0.1.0-pre.3, src/riir/attn/mla_attn_forward.rs, folded SDPA chain (q_prime from the
+// nope rows of kv_b, SDPA over the compressed rows, out_per_head through the v rows of kv_b);
+// turbospark-runtime 0.3.0, src/families/deepseek2/attn.rs, absorb -> MQA attention over the
+// compressed rows [kv_lat ; k_pe] -> v-combine.
+//
+// For a handful of query rows (B x H <= 64, H <= 32) the staged path is four dependent kernels whose
+// boundaries and set-up cost more than their work. Here the grid (one CTA per SM at most) runs:
+//   1. absorb: q'[b,h,c] = sum_n q_nope[b,h,n] W_UK,h[n,c] in float32, 64 latent columns per
+//      item, and the RoPE of q_pe; W_UK is read into registers before the dependency wait, and
+//      the rows of the CTA's first chunk are already on their way (bulk copies).
+//   2. attention: each sequence is cut into 32-row chunks (boundaries fixed by the sequence's
+//      own length, so a sequence's result does not depend on the rest of the batch); a CTA
+//      takes chunks g, g + G, ... and writes, per chunk and head, the chunk's maximum, sum and
+//      unnormalised output row. A warp serves heads w, w + 8, ...; lanes own 16-byte column
+//      pieces of the rows, the scores of 8 rows come together in a transpose-reduce, and the
+//      products run as packed float pairs.
+//   3. merge and W_UV: per (sequence, head, 64 latent columns) the chunks' partials in chunk
+//      order, and that slice's share of out = W_UV o (W_UV read before the dependency wait);
+//      the last slice of a head to finish adds the shares in slice order and writes out, lse.
+// The two barriers count arrivals in the workspace header (zero before a call; the last CTA
+// out resets them). Every wait is bounded: a CTA whose wait runs out records MLA_ERR_TIMEOUT
+// and writes NaN for the outputs it owns.
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int SM_THREADS = 256;
+constexpr int SM_WARPS = SM_THREADS / 32;
+constexpr int SM_CHUNK = 32;            // rows per attention chunk (one per lane)
+constexpr int SM_MAX_HPW = 4;           // heads per warp at most (H <= 32)
+constexpr int SM_MAX_CHUNKS = 256;     // 32-row chunks of a sequence at most (capacity <= 8192)
+constexpr int SM_MAX_CPL = 16;          // latent columns per lane at most (two 8-column pieces: C <= 512)
+
+struct SmallArgs {
+  const uint16_t* q;        // [B][H][N + R] bf16
+  const uint16_t* kv_b;     // [H][N + V][C] bf16
+  const uint16_t* rows;     // cache rows [n_phys][C + R] bf16
+  RowMap map;
+  const int32_t* seq_lens;
+  const int32_t* positions; // or nullptr
+  const double* inv_freq;
+  float* out;               // [B][H][V]
+  float* lse;               // [B][H] or nullptr
+  float* qf;                // [B][H][C + R] float32 fused queries
+  float* wshare;            // [B][H][C / 64][V]: each latent slice's share of out
+  unsigned int* head_cnt;   // [B * H] finished slices per head (zeroed in phase 1)
+  float* part;              // [B][max_chunks][H][C + 4]: output row, max (log2 units), sum, 2 zeros
+                            // (rows of C + 4 floats keep every float4 access 16-byte aligned)
+  WsHeader* hdr;
+  int B, H, C, R, N, V, max_chunks;
+  float scale_log2;
+  uint64_t wait_ns;
+};
+
+// Arrival counters of the two barriers and of the exit, in the header's spare words.
+__device__ __forceinline__ unsigned int* sm_counter(WsHeader* hdr, int i) {
+  return reinterpret_cast<unsigned int*>(&hdr->pad[8 + i]);
+}
+
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide barrier of the G CTAs: every thread's writes before it are visible to every thread
+// after it. False (for the whole CTA) when the wait ran out.
+__device__ bool grid_barrier(unsigned int* ctr, unsigned int G, uint64_t limit_ns, int* flag_s) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // release: the CTA's writes (ordered before this thread by the block barrier) are visible to
+    // every CTA that acquires the count
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+    const uint64_t t0 = tc::global_ns();
+    int ok = 1;
+    while (ld_acquire_gpu(ctr) < G) {
+      if (tc::global_ns() - t0 > limit_ns) {
+        ok = 0;
+        break;
+      }
+    }
+    *flag_s = ok;
+  }
+  __syncthreads();
+  return *flag_s != 0;
+}
+
+__device__ __forceinline__ float bf16f(uint16_t u) { return __uint_as_float((uint32_t)u << 16); }
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// The share of a cache row that a lane owns, as float pairs: x[0..3] latent piece `lane`,
+// x[4..7] piece lane + 32, x[8] RoPE pair `lane`; zeros where the lane owns nothing (or the flag
+// is off). A bf16 pair (lo, hi) of a 32-bit word becomes (lo << 16, hi with the low half cleared).
+__device__ __forceinline__ void load_row_share(const uint8_t* row, int lane, int C, bool own0, bool own1, bool ownr,
+                                               float2 x[9]) {
+  uint4 u0 = make_uint4(0u, 0u, 0u, 0u), u1 = u0;
+  uint32_t ur = 0u;
+  if (own0) u0 = *reinterpret_cast<const uint4*>(row + 16 * lane);
+  if (own1) u1 = *reinterpret_cast<const uint4*>(row + 16 * (lane + 32));
+  if (ownr) ur = *reinterpret_cast<const uint32_t*>(row + 2 * C + 4 * lane);
+  const uint32_t w[9] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w, ur};
+#pragma unroll
+  for (int i = 0; i < 9; ++i) x[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+}
+
+// Sum over the warp of v[i] for i = lane & 7: a transpose-reduce (lanes trade half of their
+// values with the lane at distance 4, then 2, then 1, keeping the rows whose index bits match
+// their own), then an all-reduce over the four groups of eight lanes. A fixed order, so every
+// call with the same inputs gives the same bits.
+__device__ __forceinline__ float transpose_sum8(const float v[8], int lane) {
+  const bool c = (lane & 4) != 0, d = (lane & 2) != 0, e = (lane & 1) != 0;
+  float w[4], y[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = c ? v[i] : v[i + 4];
+    w[i] = (c ? v[i + 4] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = d ? w[i] : w[i + 2];
+    y[i] = (d ? w[i + 2] : w[i]) + __shfl_xor_sync(0xffffffffu, send, 2);
+  }
+  float z = (e ? y[1] : y[0]) + __shfl_xor_sync(0xffffffffu, e ? y[0] : y[1], 1);
+  z += __shfl_xor_sync(0xffffffffu, z, 8);
+  z += __shfl_xor_sync(0xffffffffu, z, 16);
+  return z;
+}
+
+// Global -> shared bulk copy completing on an mbarrier of this CTA (both addresses and the size
+// multiples of 16 bytes).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   tc::smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
+               : "memory");
+}
+
+// Chunks of sequence b (0 when its length is out of range).
+__device__ __forceinline__ int seq_chunks(const SmallArgs& a, int b) {
+  const long long L = a.seq_lens[b];
+  if (L < 1 || L > a.map.capacity()) return 0;
+  return (int)((L + SM_CHUNK - 1) / SM_CHUNK);
+}
+
+// Warp 0: the rows of chunk k into rows_s ([32][C + R] bf16). Lane r maps row r of the chunk;
+// each run of consecutive physical rows goes in one bulk copy (a contiguous cache or a page
+// gives one copy per chunk), all completing on `bar`. *bad_s says whether a row lay outside
+// the pool (not copied).
+__device__ __forceinline__ void issue_chunk_rows(const SmallArgs& a, const int* cfirst, int k, uint8_t* rows_s,
+                                                 uint64_t* bar, int* bad_s) {
+  const int lane = threadIdx.x & 31;
+  int b = 0;
+  while (b + 1 < a.B && cfirst[b + 1] <= k) ++b;
+  const int t0 = (k - cfirst[b]) * SM_CHUNK;
+  const int nr = (int)min((long long)SM_CHUNK, (long long)a.seq_lens[b] - t0);
+  const int64_t pr = lane < nr ? a.map.phys(b, (int64_t)t0 + lane) : -1;
+  const int64_t prev = __shfl_up_sync(0xffffffffu, pr, 1);
+  const bool good = pr >= 0;
+  const bool start = good && (lane == 0 || prev < 0 || prev + 1 != pr);
+  const unsigned int goodm = __ballot_sync(0xffffffffu, good), startm = __ballot_sync(0xffffffffu, start);
+  const unsigned int want = nr >= 32 ? 0xffffffffu : ((1u << nr) - 1u);
+  const uint32_t bytes = (uint32_t)(a.C + a.R) * 2u;
+  if (lane == 0) {
+    *bad_s = goodm != want;
+    tc::mbar_arrive_expect_tx(bar, (uint32_t)__popc(goodm) * bytes);
+  }
+  __syncwarp();
+  if (start) {   // the run ends at the next start or at the first row without a physical row
+    const unsigned int above = lane == 31 ? 0u : (0xffffffffu << (lane + 1));
+    const unsigned int stops = (startm | ~goodm) & above;
+    const int end = stops ? __ffs(stops) - 1 : 32;
+    bulk_g2s(rows_s + (size_t)lane * bytes, a.rows + pr * (a.C + a.R), (uint32_t)(end - lane) * bytes, bar);
+  }
+}
+
+template <int HPW>   // heads per warp: ceil(H / 8)
+__global__ void __launch_bounds__(SM_THREADS, 1) decode_small_kernel(const __grid_constant__ SmallArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];   // the chunk's rows [32][C + R] bf16
+  __shared__ float w_s[SM_MAX_CHUNKS];               // merge: chunk weights
+  __shared__ float ol_s[64];                         //        merged latent slice
+  __shared__ int flag_s;
+  __shared__ int cfirst_s[65];          // chunk prefix over the sequences (B <= 64)
+  __shared__ float red_s[4][64];
+  __shared__ float wred_s[SM_WARPS];
+  __shared__ uint64_t rows_bar;
+  __shared__ int rows_bad_s;
+  pdl_trigger();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const unsigned int G = gridDim.x;
+  const int g = blockIdx.x;
+  const int B = a.B, H = a.H, C = a.C, R = a.R, N = a.N, V = a.V;
+  const int CR = C + R, NV = N + V;
+  const int row_bytes = CR * 2;         // a warp reads one row at a time, 16 bytes a lane
+  uint8_t* rows_s = smem;
+  bool ok = true;
+
+  // ---- before the dependency wait: chunk layout and weights (no earlier kernel writes them) ----
+  if (tid == 0) {
+    int acc = 0;
+    for (int b = 0; b < B; ++b) {
+      cfirst_s[b] = acc;
+      acc += seq_chunks(a, b);
+    }
+    cfirst_s[B] = acc;
+    tc::mbar_init(&rows_bar, 1);
+    tc::fence_mbar_init();
+  }
+  const int n_items1 = B * H * (C / 64);   // absorb and merge items: (sequence, head, 64 latent columns)
+  // the first absorb item's W_UK slice: column cc * 64 + (tid & 63), nope rows of quarter tid >> 6
+  const int nq = N / 4;
+  float wuk[32];
+  if (g < n_items1) {
+    const int h = (g / (C / 64)) % H, cc = g % (C / 64);
+    const int c = cc * 64 + (tid & 63), n0 = (tid >> 6) * nq;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      wuk[i] = i < nq ? bf16f(a.kv_b[((int64_t)h * NV + n0 + i) * C + c]) : 0.f;
+  }
+  // the first merge item's W_UV slice: row tid >> 1, latent columns cc * 64 + (tid & 1) * 32 .. + 31
+  uint32_t wuv[16];
+  if (g < n_items1) {
+    const int h = (g / (C / 64)) % H, cc = g % (C / 64), v = tid >> 1;
+    const uint4* src = reinterpret_cast<const uint4*>(a.kv_b + ((int64_t)h * NV + N + v) * C + cc * 64 + (tid & 1) * 32);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 u = v < V ? src[i] : make_uint4(0, 0, 0, 0);
+      wuv[4 * i] = u.x; wuv[4 * i + 1] = u.y; wuv[4 * i + 2] = u.z; wuv[4 * i + 3] = u.w;
+    }
+  }
+  pdl_wait();   // q and the appended cache row come from earlier kernels; the workspace and out
+                // may still be read by them
+  __syncthreads();
+  const int total_chunks = cfirst_s[B];
+  // the rows of this CTA's first chunk land while the absorb runs
+  uint32_t rows_par = 0;
+  bool rows_pending = g < total_chunks;
+  if (rows_pending && warp == 0) issue_chunk_rows(a, cfirst_s, g, rows_s, &rows_bar, &rows_bad_s);
+  if (g == 0) {   // lengths out of range: that sequence's outputs come out NaN (no chunks)
+    for (int b = tid; b < B; b += SM_THREADS)
+      if (cfirst_s[b + 1] == cfirst_s[b]) set_error(a.hdr, MLA_ERR_BAD_SEQ_LEN, b);
+    for (int i = tid; i < B * H; i += SM_THREADS) a.head_cnt[i] = 0u;   // used after two barriers
+  }
+
+  // ================================ 1. absorb ================================
+  for (int it = g; it < n_items1; it += G) {
+    const int b = it / (H * (C / 64)), h = (it / (C / 64)) % H, cc = it % (C / 64);
+    const int c = cc * 64 + (tid & 63), n0 = (tid >> 6) * nq;
+    const uint16_t* qn = a.q + ((int64_t)b * H + h) * (N + R);
+    float acc = 0.f;
+    if (it == g) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < nq) acc = fmaf(bf16f(qn[n0 + i]), wuk[i], acc);
+    } else {
+      for (int i = 0; i < nq; ++i) acc = fmaf(bf16f(qn[n0 + i]), bf16f(a.kv_b[((int64_t)h * NV + n0 + i) * C + c]), acc);
+    }
+    red_s[tid >> 6][tid & 63] = acc;
+    __syncthreads();
+    float* qf = a.qf + ((int64_t)b * H + h) * CR;
+    if (tid < 64) qf[cc * 64 + tid] = ((red_s[0][tid] + red_s[1][tid]) + red_s[2][tid]) + red_s[3][tid];
+    if (cc == 0 && tid >= 64 && tid < 64 + R / 2) {
+      const int p = tid - 64;
+      const float x0 = bf16f(qn[N + 2 * p]), x1 = bf16f(qn[N + 2 * p + 1]);
+      if (a.positions != nullptr) {
+        float cv, sv;
+        rope_cs_value(a.inv_freq[p], a.positions[b], &cv, &sv);
+        qf[C + 2 * p] = x0 * cv - x1 * sv;
+        qf[C + 2 * p + 1] = x0 * sv + x1 * cv;
+      } else {
+        qf[C + 2 * p] = x0;
+        qf[C + 2 * p + 1] = x1;
+      }
+    }
+    __syncthreads();
+  }
+  ok = grid_barrier(sm_counter(a.hdr, 0), G, a.wait_ns, &flag_s);
+
+  // ================================ 2. attention over 32-row chunks ================================
+  // A warp serves heads w, w + 8, ... (HPW of them). Lane l owns the latent 16-byte pieces l and
+  // l + 32 (columns 8l .. 8l + 7 and 256 + 8l ..) and the RoPE pair l of every row, so a warp
+  // reads a row of shared memory without bank conflicts and keeps its heads' queries in
+  // registers. Scores: each lane forms its share of (row, head) for 8 rows at a time, and a
+  // transpose-reduce leaves the score of row r of the chunk in lane r.
+  const int np = C / 8;                       // latent pieces of a row
+  const bool own0 = lane < np, own1 = lane + 32 < np, ownr = 2 * lane < R;
+  for (int k = g; ok && k < total_chunks; k += G) {
+    int b = 0;
+    while (b + 1 < B && cfirst_s[b + 1] <= k) ++b;
+    const int j = k - cfirst_s[b];
+    const int nr = (int)min((long long)SM_CHUNK, (long long)a.seq_lens[b] - j * SM_CHUNK);
+    float* part = a.part + ((int64_t)b * a.max_chunks + j) * H * (C + 4);
+    // the warp's queries (written by other CTAs before the barrier: read from L2)
+    float2 q[HPW][9];
+#pragma unroll
+    for (int jj = 0; jj < HPW; ++jj) {
+      const int h = warp + SM_WARPS * jj;
+      const float4* qh = reinterpret_cast<const float4*>(a.qf + ((int64_t)b * H + h) * CR);
+      float4 t0 = make_float4(0.f, 0.f, 0.f, 0.f), t1 = t0, t2 = t0, t3 = t0;
+      float2 tr = make_float2(0.f, 0.f);
+      if (h < H) {
+        if (own0) {
+          t0 = __ldcg(qh + 2 * lane);
+          t1 = __ldcg(qh + 2 * lane + 1);
+        }
+        if (own1) {
+          t2 = __ldcg(qh + 2 * (lane + 32));
+          t3 = __ldcg(qh + 2 * (lane + 32) + 1);
+        }
+        if (ownr) tr = __ldcg(reinterpret_cast<const float2*>(a.qf + ((int64_t)b * H + h) * CR + C) + lane);
+      }
+      q[jj][0] = make_float2(t0.x, t0.y); q[jj][1] = make_float2(t0.z, t0.w);
+      q[jj][2] = make_float2(t1.x, t1.y); q[jj][3] = make_float2(t1.z, t1.w);
+      q[jj][4] = make_float2(t2.x, t2.y); q[jj][5] = make_float2(t2.z, t2.w);
+      q[jj][6] = make_float2(t3.x, t3.y); q[jj][7] = make_float2(t3.z, t3.w);
+      q[jj][8] = tr;
+    }
+    const bool landed = tc::mbar_wait(&rows_bar, rows_par, a.wait_ns);
+    if (!__syncthreads_and(landed)) {
+      ok = false;
+      break;
+    }
+    rows_pending = false;
+    rows_par ^= 1u;
+    if (rows_bad_s) {   // a row outside the pool: the merge of the sequence's heads comes out NaN
+      if (tid == 0) set_error(a.hdr, MLA_ERR_BAD_PAGE, b);
+      for (int i = tid; i < H; i += SM_THREADS) {
+        part[(int64_t)i * (C + 4) + C] = 0.f;
+        part[(int64_t)i * (C + 4) + C + 1] = CUDART_NAN_F;
+      }
+    } else {
+      float s[HPW];
+#pragma unroll
+      for (int jj = 0; jj < HPW; ++jj) s[jj] = 0.f;
+      for (int g8 = 0; g8 * 8 < nr; ++g8) {
+        float sp[HPW][8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = g8 * 8 + i;
+          float2 x[9];
+          load_row_share(rows_s + r * row_bytes, lane, C, own0 && r < nr, own1 && r < nr, ownr && r < nr, x);
+#pragma unroll
+          for (int jj = 0; jj < HPW; ++jj) {   // even and odd columns in the two halves of a pair
+            float2 d = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < 9; ++e) d = __ffma2_rn(q[jj][e], x[e], d);
+            sp[jj][i] = d.x + d.y;
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < HPW; ++jj) {
+          const float t = transpose_sum8(sp[jj], lane);   // row g8 * 8 + (lane & 7)
+          if ((lane >> 3) == g8) s[jj] = t;
+        }
+      }
+      float p[HPW], m[HPW], l[HPW];
+#pragma unroll
+      for (int jj = 0; jj < HPW; ++jj) {
+        const float sc = lane < nr ? s[jj] * a.scale_log2 : -CUDART_INF_F;
+        m[jj] = warp_max(sc);
+        p[jj] = lane < nr ? ex2(sc - m[jj]) : 0.f;
+        l[jj] = warp_sum(p[jj]);
+      }
+      // output: lane accumulates its two latent pieces of the warp's heads, rows in order
+      float2 o[HPW][8];
+#pragma unroll
+      for (int jj = 0; jj < HPW; ++jj)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[jj][e] = make_float2(0.f, 0.f);
+#pragma unroll 2
+      for (int r = 0; r < nr; ++r) {
+        float2 v[9];
+        load_row_share(rows_s + r * row_bytes, lane, C, own0, own1, false, v);
+#pragma unroll
+        for (int jj = 0; jj < HPW; ++jj) {
+          const float pr = __shfl_sync(0xffffffffu, p[jj], r);
+          const float2 pr2 = make_float2(pr, pr);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[jj][e] = __ffma2_rn(pr2, v[e], o[jj][e]);
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < HPW; ++jj) {
+        const int h = warp + SM_WARPS * jj;
+        if (h < H) {
+          float4* ph = reinterpret_cast<float4*>(part + (int64_t)h * (C + 4));
+          if (own0) {
+            ph[2 * lane] = make_float4(o[jj][0].x, o[jj][0].y, o[jj][1].x, o[jj][1].y);
+            ph[2 * lane + 1] = make_float4(o[jj][2].x, o[jj][2].y, o[jj][3].x, o[jj][3].y);
+          }
+          if (own1) {
+            ph[2 * (lane + 32)] = make_float4(o[jj][4].x, o[jj][4].y, o[jj][5].x, o[jj][5].y);
+            ph[2 * (lane + 32) + 1] = make_float4(o[jj][6].x, o[jj][6].y, o[jj][7].x, o[jj][7].y);
+          }
+          if (lane == 0) ph[C / 4] = make_float4(m[jj], l[jj], 0.f, 0.f);
+        }
+      }
+    }
+    __syncthreads();   // rows_s is free: the next chunk of this CTA goes in
+    if (k + G < total_chunks) {
+      if (warp == 0) issue_chunk_rows(a, cfirst_s, k + (int)G, rows_s, &rows_bar, &rows_bad_s);
+      rows_pending = true;
+    }
+  }
+  if (ok) ok = grid_barrier(sm_counter(a.hdr, 1), G, a.wait_ns, &flag_s);
+
+  // ================================ 3. merge and W_UV ================================
+  // Item (sequence, head, 64 latent columns): the chunks' partials merged in chunk order, then
+  // that slice's share of out[b,h,:] = W_UV,h o (W_UV of the first item read before the
+  // dependency wait). The last of a head's C/64 items to finish (a counter per head) adds the
+  // shares in slice order and writes out and lse: no further barrier.
+  __shared__ __align__(16) float colred_s[16][64];
+  __shared__ int last_s;
+  for (int it = g; it < n_items1; it += G) {
+    const int b = it / (H * (C / 64)), h = (it / (C / 64)) % H, cc = it % (C / 64);
+    const int nch = cfirst_s[b + 1] - cfirst_s[b];
+    float* share = a.wshare + ((int64_t)(b * H + h) * (C / 64) + cc) * V;
+    float M = CUDART_NAN_F, Ls = CUDART_NAN_F;
+    if (!ok) {   // a CTA whose wait ran out: its shares are NaN
+      for (int v = tid; v < V; v += SM_THREADS) share[v] = CUDART_NAN_F;
+    } else {
+      const float* pb = a.part + (int64_t)b * a.max_chunks * H * (C + 4) + (int64_t)h * (C + 4);
+      const int64_t cstride = (int64_t)H * (C + 4);   // between chunks
+      // every load at once: the maximum and sum of chunk tid, columns 4 * (tid & 15) .. + 3 of
+      // chunks (tid >> 4) + 16 i
+      float2 ml = make_float2(-CUDART_INF_F, 0.f);
+      if (tid < nch) ml = __ldcg(reinterpret_cast<const float2*>(pb + tid * cstride + C));
+      const int quad = tid & 15, grp = tid >> 4;
+      float4 t[SM_MAX_CHUNKS / 16];
+#pragma unroll
+      for (int i = 0; i < SM_MAX_CHUNKS / 16; ++i) {
+        const int kk = grp + 16 * i;
+        t[i] = kk < nch ? __ldcg(reinterpret_cast<const float4*>(pb + kk * cstride + cc * 64) + quad)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      const float mx = warp_max(ml.x);
+      if (lane == 0) wred_s[warp] = mx;
+      __syncthreads();
+      M = wred_s[0];
+      for (int w = 1; w < SM_WARPS; ++w) M = fmaxf(M, wred_s[w]);
+      __syncthreads();
+      const float wk = tid < nch ? ex2(ml.x - M) : 0.f;
+      if (tid < nch) w_s[tid] = wk;
+      const float pl = warp_sum(wk * ml.y);
+      if (lane == 0) wred_s[warp] = pl;
+      __syncthreads();
+      Ls = 0.f;
+      for (int w = 0; w < SM_WARPS; ++w) Ls += wred_s[w];
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < SM_MAX_CHUNKS / 16; ++i) {
+        const int kk = grp + 16 * i;
+        if (kk < nch) {
+          const float w = w_s[kk];
+          acc.x = fmaf(w, t[i].x, acc.x); acc.y = fmaf(w, t[i].y, acc.y);
+          acc.z = fmaf(w, t[i].z, acc.z); acc.w = fmaf(w, t[i].w, acc.w);
+        }
+      }
+      reinterpret_cast<float4*>(colred_s[grp])[quad] = acc;
+      __syncthreads();
+      if (tid < 64) {
+        float sum = 0.f;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) sum += colred_s[q][tid];
+        ol_s[tid] = sum / Ls;
+      }
+      __syncthreads();
+      // the slice's share of out: row tid >> 1, half tid & 1 of the 64 columns
+      const int v = tid >> 1;
+      uint32_t wv[16];
+      if (it == g) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) wv[i] = wuv[i];
+      } else {
+        const uint4* wsrc =
+            reinterpret_cast<const uint4*>(a.kv_b + ((int64_t)h * NV + N + v) * C + cc * 64 + (tid & 1) * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 u = v < V ? wsrc[i] : make_uint4(0, 0, 0, 0);
+          wv[4 * i] = u.x; wv[4 * i + 1] = u.y; wv[4 * i + 2] = u.z; wv[4 * i + 3] = u.w;
+        }
+      }
+      const float* o = ol_s + (tid & 1) * 32;
+      float y = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        y = fmaf(__uint_as_float(wv[i] << 16), o[2 * i], y);
+        y = fmaf(__uint_as_float(wv[i] & 0xFFFF0000u), o[2 * i + 1], y);
+      }
+      y += __shfl_xor_sync(0xffffffffu, y, 1);
+      if ((tid & 1) == 0 && v < V) share[v] = y;
+    }
+    // the last of the head's slices adds the shares
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      last_s = atomicAdd(&a.head_cnt[b * H + h], 1u) == (unsigned int)(C / 64 - 1);
+      __threadfence();
+    }
+    __syncthreads();
+    if (last_s) {
+      const float* sh0 = a.wshare + (int64_t)(b * H + h) * (C / 64) * V;
+      const bool valid = nch > 0;   // a length out of range: NaN
+      for (int v = tid; v < V; v += SM_THREADS) {
+        float y = 0.f;
+        for (int s2 = 0; s2 < C / 64; ++s2) y += __ldcg(sh0 + s2 * V + v);
+        a.out[((int64_t)b * H + h) * V + v] = valid ? y : CUDART_NAN_F;
+      }
+      if (tid == 0 && a.lse != nullptr)
+        a.lse[(int64_t)b * H + h] = valid ? (M + __log2f(Ls)) * 0.69314718055994530942f : CUDART_NAN_F;
+    }
+    __syncthreads();   // w_s, ol_s, colred_s, wred_s and last_s are reused by the next item
+  }
+  if (!ok && tid == 0) set_error(a.hdr, MLA_ERR_TIMEOUT, 0);
+
+  // ---- leave: a row copy still in flight (a wait that ran out) gets one more bounded wait ----
+  if (rows_pending && tid == 0) tc::mbar_wait(&rows_bar, rows_par, kWaitDrainNs);
+  // ---- the last CTA out resets the counters for the next call ----
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(sm_counter(a.hdr, 2), 1u) == G - 1) {
+      for (int i = 0; i < 3; ++i) atomicExch(sm_counter(a.hdr, i), 0u);
+      __threadfence();
+    }
+  }
+}
+
+}  // namespace
+
+bool decode_small_supported(const mla_config& cfg, int B, int tokens) {
+  const int64_t cap = cfg.page_size == 0 ? cfg.rows_per_seq : (int64_t)cfg.max_pages_per_seq * cfg.page_size;
+  return tokens == 1 && cfg.act_dtype == MLA_BF16 && cfg.kv_b_dtype == MLA_BF16 && B >= 1 &&
+         (int64_t)B * cfg.n_heads <= 64 && cfg.n_heads <= SM_WARPS * SM_MAX_HPW && cfg.kv_lora % 128 == 0 &&
+         cfg.kv_lora <= 32 * SM_MAX_CPL && (cfg.kv_lora + cfg.qk_rope) % 8 == 0 && cfg.qk_rope % 2 == 0 &&
+         cfg.qk_rope <= 64 && cfg.qk_nope % 4 == 0 && cfg.qk_nope <= 128 &&
+         cfg.v_head % 16 == 0 && cfg.v_head <= 128 && cap >= 1 && cap <= (int64_t)SM_CHUNK * SM_MAX_CHUNKS;
+}
+
+int64_t decode_small_max_chunks(const mla_config& cfg) {
+  const int64_t cap = cfg.page_size == 0 ? cfg.rows_per_seq : (int64_t)cfg.max_pages_per_seq * cfg.page_size;
+  return (cap + SM_CHUNK - 1) / SM_CHUNK;
+}
+
+// CTAs of the grid: one per chunk of the longest batch, at most one per SM.
+int decode_small_grid(const mla_config& cfg, int B) {
+  const int sms = device_sms();
+  const int64_t chunks = (int64_t)B * decode_small_max_chunks(cfg);
+  return (int)(chunks < sms ? chunks : sms);
+}
+
+cudaError_t launch_decode_small(const mla_config& cfg, const mla_cache& cache, const void* q, const void* kv_b,
+                                const int32_t* seq_lens, const int32_t* positions, float* out, float* lse, int B,
+                                float* qf, float* part, float* wshare, unsigned int* head_cnt, WsHeader* hdr,
+                                cudaStream_t st) {
+  SmallArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.kv_b = static_cast<const uint16_t*>(kv_b);
+  a.rows = static_cast<const uint16_t*>(cache.rows);
+  a.map = RowMap{cache.page_table, cfg.page_size, cfg.max_pages_per_seq, cfg.rows_per_seq, cache.n_physical_rows};
+  a.seq_lens = seq_lens;
+  a.positions = positions;
+  a.inv_freq = cfg.rope_inv_freq;
+  a.out = out;
+  a.lse = lse;
+  a.qf = qf;
+  a.part = part;
+  a.wshare = wshare;
+  a.head_cnt = head_cnt;
+  a.hdr = hdr;
+  a.B = B;
+  a.H = cfg.n_heads;
+  a.C = cfg.kv_lora;
+  a.R = cfg.qk_rope;
+  a.N = cfg.qk_nope;
+  a.V = cfg.v_head;
+  a.max_chunks = (int)decode_small_max_chunks(cfg);
+  a.scale_log2 = cfg.softmax_scale * 1.4426950408889634f;
+  a.wait_ns = wait_limit_ns();
+  const int smem = SM_CHUNK * (cfg.kv_lora + cfg.qk_rope) * 2;   // the chunk's rows
+  const int hpw = (cfg.n_heads + SM_WARPS - 1) / SM_WARPS;
+  void (*kern)(SmallArgs) = hpw == 1 ? decode_small_kernel<1> : hpw == 2 ? decode_small_kernel<2> : decode_small_kernel<4>;
+  cudaError_t e = ensure_smem((const void*)kern, smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, dim3((unsigned)decode_small_grid(cfg, B)), dim3(SM_THREADS), (size_t)smem, st, a);
+}
+
+}  // namespace mla

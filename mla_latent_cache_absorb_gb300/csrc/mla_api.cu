@@ -154,6 +154,18 @@ static mla_status make_plan(const mla_config& cfg, int B, DecodePlan* p, int tok
   off = align256(off + n_part * sizeof(float));
   p->off_meta = off;
   off = align256(off + (size_t)B * 2 * sizeof(int32_t));
+  p->small = decode_small_supported(cfg, B, tokens) ? 1 : 0;
+  if (p->small) {
+    const size_t rows_q = (size_t)B * cfg.n_heads;
+    p->off_sq = off;
+    off = align256(off + rows_q * row * sizeof(float));
+    p->off_sp = off;
+    off = align256(off + rows_q * (size_t)decode_small_max_chunks(cfg) * (cfg.kv_lora + 4) * sizeof(float));
+    p->off_sw = off;
+    off = align256(off + rows_q * (size_t)(cfg.kv_lora / 64) * cfg.v_head * sizeof(float));
+    p->off_sc = off;
+    off = align256(off + rows_q * sizeof(uint32_t));
+  }
   p->total = off;
   return MLA_OK;
 }
@@ -354,6 +366,13 @@ mla_status mla_decode_plan(const mla_config* cfg, int32_t B, mla_plan_info* info
   info->splits = p.splits;
   info->rows_per_split = p.chunk_rows;   // 0: tiles are balanced across CTAs instead
   info->capacity = p.capacity;
+  if (p.small) {   // mla_decode_attn runs the one-launch path
+    info->kernel = 3;
+    info->heads_per_cta = cfg->n_heads;
+    info->head_groups = 1;
+    info->splits = decode_small_grid(*cfg, B);
+    info->rows_per_split = 32;
+  }
   return MLA_OK;
 }
 
@@ -508,6 +527,16 @@ mla_status mla_decode_attn(const mla_config* cfg, const void* q, const void* kv_
   st = check_cache(cfg, cache, B);
   if (st != MLA_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (plan.small) {
+    // tiny batches: the whole decode in one launch
+    char* ws = static_cast<char*>(workspace);
+    return cuda_status(launch_decode_small(*cfg, *cache, q, kv_b, seq_lens, positions, out, lse, B,
+                                           reinterpret_cast<float*>(ws + plan.off_sq),
+                                           reinterpret_cast<float*>(ws + plan.off_sp),
+                                           reinterpret_cast<float*>(ws + plan.off_sw),
+                                           reinterpret_cast<unsigned int*>(ws + plan.off_sc),
+                                           reinterpret_cast<WsHeader*>(ws), s));
+  }
   // Long attentions (at the cache's capacity, at least four 128-row tiles per CTA, or eight
   // 64-row tiles per CTA pair): the absorb starts once everything before it on the stream, the
   // cache append above all, has completed, and the attention then streams cache rows while the

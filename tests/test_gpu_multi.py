@@ -87,8 +87,11 @@ def test_tokens_share_the_last_token_view():
     d1 = DeviceStep(single)
     L.check(d1.decode(), "decode")
     torch.cuda.synchronize()
+    # a wrong row view would differ at O(1); the one-token call runs in float32 here (the
+    # one-launch path for tiny batches) and the T-token call from bf16 latent queries, so they
+    # agree to the oracle's output tolerance rather than to bf16 rounding of the same sums
     r = max_rel(ds.out[:, -1].cpu().numpy(), d1.out.cpu().numpy())
-    assert r <= 1e-3, r
+    assert r <= OUT_TOL, r
 
 
 @gpu

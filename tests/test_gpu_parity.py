@@ -219,11 +219,15 @@ STEP_CASES = [
 def test_fused_call_equals_the_three_step_calls(name, wl):
     # for long attentions mla_decode_attn launches its absorb in plain stream order and lets
     # the attention read cache rows before waiting for it; the three step calls keep every wait
-    # in place. Same kernels, same split plan: the results agree bit for bit.
+    # in place. Same kernels, same split plan: the results agree bit for bit. For tiny batches
+    # (plan kernel 3) mla_decode_attn is one float32 launch instead: it agrees with the step
+    # calls within the oracle's tolerances and is run-to-run identical.
     torch = need_gpu()
     from mla_latent_cache_absorb_gb300 import binding as L
     from mla_latent_cache_absorb_gb300.runner import DeviceStep
     ds = DeviceStep(synth.make_problem(wl))
+    st, plan = L.mla_decode_plan(ds.cfg, wl.B)
+    L.check(st, "plan")
     L.check(ds.append(), "mla_cache_append")
     L.check(ds.absorb(), "mla_decode_absorb")
     L.check(ds.partial(), "mla_decode_partial")
@@ -233,9 +237,18 @@ def test_fused_call_equals_the_three_step_calls(name, wl):
     assert torch.isfinite(o_steps).all()
     ds.out.fill_(float("nan"))
     ds.lse.fill_(float("nan"))
+    first = None
     for _ in range(2):   # twice: the second call follows the first call's combine, not an append
         L.check(ds.decode(), "mla_decode_attn")
         torch.cuda.synchronize()
-        assert torch.equal(ds.out, o_steps) and torch.equal(ds.lse, l_steps)
+        if plan.kernel == 3:
+            assert max_rel(ds.out.cpu().numpy(), o_steps.cpu().numpy()) <= OUT_TOL
+            assert float((ds.lse - l_steps).abs().max()) <= LSE_TOL
+            if first is None:
+                first = (ds.out.clone(), ds.lse.clone())
+            else:
+                assert torch.equal(ds.out, first[0]) and torch.equal(ds.lse, first[1])
+        else:
+            assert torch.equal(ds.out, o_steps) and torch.equal(ds.lse, l_steps)
     e, seq = L.mla_get_device_error(ds.ws_decode, ds.stream)
     assert e == 0, (e, seq)

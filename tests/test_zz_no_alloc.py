@@ -38,17 +38,18 @@ def _noalloc(ds, out, lse, err, seq_lens=None):
 
 
 CASES = [
-    ("tiny_f32", {}),                                                  # CUDA-core attention
-    ("v2lite_b1_t4096", dict(B=3, context=("uniform", 100, 900))),     # tcgen05, 16 heads
-    ("v3_b32_t4096", dict(B=5, context=("uniform", 200, 1500))),       # tcgen05, 128 heads
-    ("ragged_paged_b64", dict(B=6, context=("uniform", 64, 2000))),   # paged cache
+    ("tiny_f32", "tiny_f32", {}),                                               # CUDA-core attention
+    ("v2lite_tc", "v2lite_b1_t4096", dict(B=5, context=("uniform", 100, 900))),   # tcgen05, 16 heads
+    ("v2lite_one_launch", "v2lite_b1_t4096", dict(B=2, context=("uniform", 100, 900))),  # tiny batch
+    ("v3", "v3_b32_t4096", dict(B=5, context=("uniform", 200, 1500))),          # tcgen05, 128 heads
+    ("ragged_paged", "ragged_paged_b64", dict(B=6, context=("uniform", 64, 2000))),  # paged cache
     # a long attention: the absorb launched in plain stream order, cache rows read early
-    ("v3_b32_t4096", dict(B=16, context=("uniform", 1500, 2500))),
+    ("v3_long", "v3_b32_t4096", dict(B=16, context=("uniform", 1500, 2500))),
 ]
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("name,kw", CASES, ids=[c[0] + ("_long" if c[1].get("B") == 16 else "") for c in CASES])
+@pytest.mark.parametrize("name,kw", [c[1:] for c in CASES], ids=[c[0] for c in CASES])
 def test_noalloc_matches_decode_attn_twice_in_a_row(name, kw):
     import torch
     from mla_latent_cache_absorb_gb300 import binding as L
