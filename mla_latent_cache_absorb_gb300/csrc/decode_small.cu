@@ -72,14 +72,17 @@ __device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
   return v;
 }
 
-// Grid-wide barrier of the G CTAs: every thread's writes before it are visible to every thread
-// after it. False (for the whole CTA) when the wait ran out.
-__device__ bool grid_barrier(unsigned int* ctr, unsigned int G, uint64_t limit_ns, int* flag_s) {
+// Grid-wide barrier of the G CTAs in two halves: every thread's writes before grid_arrive are
+// visible to every thread after the matching grid_wait; work in between overlaps the wait.
+__device__ __forceinline__ void grid_arrive(unsigned int* ctr) {
   __syncthreads();
+  // release: the CTA's writes (ordered before this thread by the block barrier) become visible
+  // to every CTA that acquires the count
+  if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+}
+// False (for the whole CTA) when the wait ran out.
+__device__ bool grid_wait(unsigned int* ctr, unsigned int G, uint64_t limit_ns, int* flag_s) {
   if (threadIdx.x == 0) {
-    // release: the CTA's writes (ordered before this thread by the block barrier) are visible to
-    // every CTA that acquires the count
-    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
     const uint64_t t0 = tc::global_ns();
     int ok = 1;
     while (ld_acquire_gpu(ctr) < G) {
@@ -93,6 +96,10 @@ __device__ bool grid_barrier(unsigned int* ctr, unsigned int G, uint64_t limit_n
   __syncthreads();
   return *flag_s != 0;
 }
+__device__ __forceinline__ bool grid_barrier(unsigned int* ctr, unsigned int G, uint64_t limit_ns, int* flag_s) {
+  grid_arrive(ctr);
+  return grid_wait(ctr, G, limit_ns, flag_s);
+}
 
 __device__ __forceinline__ float bf16f(uint16_t u) { return __uint_as_float((uint32_t)u << 16); }
 
@@ -102,42 +109,32 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// The share of a cache row that a lane owns, as float pairs: x[0..3] latent piece `lane`,
-// x[4..7] piece lane + 32, x[8] RoPE pair `lane`; zeros where the lane owns nothing (or the flag
-// is off). A bf16 pair (lo, hi) of a 32-bit word becomes (lo << 16, hi with the low half cleared).
-__device__ __forceinline__ void load_row_share(const uint8_t* row, int lane, int C, bool own0, bool own1, bool ownr,
-                                               float2 x[9]) {
-  uint4 u0 = make_uint4(0u, 0u, 0u, 0u), u1 = u0;
-  uint32_t ur = 0u;
-  if (own0) u0 = *reinterpret_cast<const uint4*>(row + 16 * lane);
-  if (own1) u1 = *reinterpret_cast<const uint4*>(row + 16 * (lane + 32));
-  if (ownr) ur = *reinterpret_cast<const uint32_t*>(row + 2 * C + 4 * lane);
-  const uint32_t w[9] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w, ur};
-#pragma unroll
-  for (int i = 0; i < 9; ++i) x[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+// Warp-level bf16 tensor-core steps (m16n8k16, float32 accumulate) and the shared-memory
+// fragment loads that feed them (four 8x8 bf16 matrices; lane l gives the row address of
+// matrix l / 8).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t r[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t r[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void mma_bf16(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+               "{%0, %1, %2, %3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Sum over the warp of v[i] for i = lane & 7: a transpose-reduce (lanes trade half of their
-// values with the lane at distance 4, then 2, then 1, keeping the rows whose index bits match
-// their own), then an all-reduce over the four groups of eight lanes. A fixed order, so every
-// call with the same inputs gives the same bits.
-__device__ __forceinline__ float transpose_sum8(const float v[8], int lane) {
-  const bool c = (lane & 4) != 0, d = (lane & 2) != 0, e = (lane & 1) != 0;
-  float w[4], y[2];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float send = c ? v[i] : v[i + 4];
-    w[i] = (c ? v[i + 4] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 4);
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const float send = d ? w[i] : w[i + 2];
-    y[i] = (d ? w[i + 2] : w[i]) + __shfl_xor_sync(0xffffffffu, send, 2);
-  }
-  float z = (e ? y[1] : y[0]) + __shfl_xor_sync(0xffffffffu, e ? y[0] : y[1], 1);
-  z += __shfl_xor_sync(0xffffffffu, z, 8);
-  z += __shfl_xor_sync(0xffffffffu, z, 16);
-  return z;
+// x = hi + lo with hi = bf16(x) and lo = bf16(x - hi): the pair carries 16 significant bits.
+__device__ __forceinline__ void split_bf16(float x, __nv_bfloat16* hi, __nv_bfloat16* lo) {
+  *hi = __float2bfloat16_rn(x);
+  *lo = __float2bfloat16_rn(x - __bfloat162float(*hi));
 }
 
 // Global -> shared bulk copy completing on an mbarrier of this CTA (both addresses and the size
@@ -149,24 +146,23 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                : "memory");
 }
 
-// Chunks of sequence b (0 when its length is out of range).
-__device__ __forceinline__ int seq_chunks(const SmallArgs& a, int b) {
-  const long long L = a.seq_lens[b];
+// Chunks of a sequence of length L (0 when the length is out of range).
+__device__ __forceinline__ int seq_chunks(const SmallArgs& a, int L) {
   if (L < 1 || L > a.map.capacity()) return 0;
-  return (int)((L + SM_CHUNK - 1) / SM_CHUNK);
+  return (L + SM_CHUNK - 1) / SM_CHUNK;
 }
 
 // Warp 0: the rows of chunk k into rows_s ([32][C + R] bf16). Lane r maps row r of the chunk;
 // each run of consecutive physical rows goes in one bulk copy (a contiguous cache or a page
 // gives one copy per chunk), all completing on `bar`. *bad_s says whether a row lay outside
 // the pool (not copied).
-__device__ __forceinline__ void issue_chunk_rows(const SmallArgs& a, const int* cfirst, int k, uint8_t* rows_s,
-                                                 uint64_t* bar, int* bad_s) {
+__device__ __forceinline__ void issue_chunk_rows(const SmallArgs& a, const int* cfirst, const int* len, int k,
+                                                 uint8_t* rows_s, uint64_t* bar, int* bad_s) {
   const int lane = threadIdx.x & 31;
   int b = 0;
   while (b + 1 < a.B && cfirst[b + 1] <= k) ++b;
   const int t0 = (k - cfirst[b]) * SM_CHUNK;
-  const int nr = (int)min((long long)SM_CHUNK, (long long)a.seq_lens[b] - t0);
+  const int nr = min(SM_CHUNK, len[b] - t0);
   const int64_t pr = lane < nr ? a.map.phys(b, (int64_t)t0 + lane) : -1;
   const int64_t prev = __shfl_up_sync(0xffffffffu, pr, 1);
   const bool good = pr >= 0;
@@ -187,13 +183,35 @@ __device__ __forceinline__ void issue_chunk_rows(const SmallArgs& a, const int* 
   }
 }
 
+// The landed rows of a chunk (raw [32][C + R]) into the padded tile (row pitch C + R + 8, so
+// the eight row addresses of a fragment load fall in distinct banks); rows at or past nr are
+// zero, so they add nothing to P V.
+__device__ __forceinline__ void relayout_rows(const uint8_t* raw, uint8_t* tile, int CR, int nr) {
+  const int pieces = CR / 8;
+  for (int i = threadIdx.x; i < SM_CHUNK * pieces; i += SM_THREADS) {
+    const int r = i / pieces, pc = i - r * pieces;
+    const uint4 v = r < nr ? *reinterpret_cast<const uint4*>(raw + (size_t)(r * CR + pc * 8) * 2) : make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(tile + (size_t)(r * (CR + 8) + pc * 8) * 2) = v;
+  }
+}
+
+// rows of chunk k of the batch (k < the chunk total), its sequence and index in the sequence
+__device__ __forceinline__ int chunk_rows(int B, const int* cfirst, const int* len, int k, int* b_out, int* j_out) {
+  int b = 0;
+  while (b + 1 < B && cfirst[b + 1] <= k) ++b;
+  *b_out = b;
+  *j_out = k - cfirst[b];
+  return min(SM_CHUNK, len[b] - (k - cfirst[b]) * SM_CHUNK);
+}
+
 template <int HPW>   // heads per warp: ceil(H / 8)
 __global__ void __launch_bounds__(SM_THREADS, 1) decode_small_kernel(const __grid_constant__ SmallArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];   // the chunk's rows [32][C + R] bf16
+  extern __shared__ __align__(16) uint8_t smem[];   // chunk rows (raw and padded), queries, scores, P
   __shared__ float w_s[SM_MAX_CHUNKS];               // merge: chunk weights
   __shared__ float ol_s[64];                         //        merged latent slice
   __shared__ int flag_s;
   __shared__ int cfirst_s[65];          // chunk prefix over the sequences (B <= 64)
+  __shared__ int len_s[64];             // their lengths
   __shared__ float red_s[4][64];
   __shared__ float wred_s[SM_WARPS];
   __shared__ uint64_t rows_bar;
@@ -204,20 +222,37 @@ __global__ void __launch_bounds__(SM_THREADS, 1) decode_small_kernel(const __gri
   const int g = blockIdx.x;
   const int B = a.B, H = a.H, C = a.C, R = a.R, N = a.N, V = a.V;
   const int CR = C + R, NV = N + V;
-  const int row_bytes = CR * 2;         // a warp reads one row at a time, 16 bytes a lane
-  uint8_t* rows_s = smem;
+  constexpr int MT = HPW > 2 ? 2 : 1;   // 16-head tiles of the tensor-core steps
+  constexpr int HM = 16 * MT;
+  const int CRP = CR + 8;               // padded row pitch (elements) of the tile, queries
+  uint8_t* rows_s = smem;                                                        // raw [32][CR]
+  __nv_bfloat16* tile_s = reinterpret_cast<__nv_bfloat16*>(smem + SM_CHUNK * CR * 2);   // [32][CRP]
+  __nv_bfloat16* q_s = tile_s + SM_CHUNK * CRP;                                  // [2][HM][CRP] hi, lo
+  float* sc_s = reinterpret_cast<float*>(q_s + 2 * HM * CRP);                    // [8][HM][32] column parts
+  __nv_bfloat16* p_s = reinterpret_cast<__nv_bfloat16*>(sc_s + SM_WARPS * HM * SM_CHUNK);  // [2][HM][40]
+  constexpr int PP = SM_CHUNK + 8;      // P row pitch
   bool ok = true;
 
   // ---- before the dependency wait: chunk layout and weights (no earlier kernel writes them) ----
   if (tid == 0) {
     int acc = 0;
     for (int b = 0; b < B; ++b) {
+      const int L = a.seq_lens[b];
+      len_s[b] = L;
       cfirst_s[b] = acc;
-      acc += seq_chunks(a, b);
+      acc += seq_chunks(a, L);
     }
     cfirst_s[B] = acc;
     tc::mbar_init(&rows_bar, 1);
     tc::fence_mbar_init();
+  }
+  for (int i = tid; i < (HM - H) * CRP; i += SM_THREADS) {   // padding heads: zero queries and P
+    q_s[H * CRP + i] = __float2bfloat16_rn(0.f);
+    q_s[(HM + H) * CRP + i] = __float2bfloat16_rn(0.f);
+  }
+  for (int i = tid; i < (HM - H) * PP; i += SM_THREADS) {
+    p_s[H * PP + i] = __float2bfloat16_rn(0.f);
+    p_s[(HM + H) * PP + i] = __float2bfloat16_rn(0.f);
   }
   const int n_items1 = B * H * (C / 64);   // absorb and merge items: (sequence, head, 64 latent columns)
   // the first absorb item's W_UK slice: column cc * 64 + (tid & 63), nope rows of quarter tid >> 6
@@ -248,7 +283,7 @@ __global__ void __launch_bounds__(SM_THREADS, 1) decode_small_kernel(const __gri
   // the rows of this CTA's first chunk land while the absorb runs
   uint32_t rows_par = 0;
   bool rows_pending = g < total_chunks;
-  if (rows_pending && warp == 0) issue_chunk_rows(a, cfirst_s, g, rows_s, &rows_bar, &rows_bad_s);
+  if (rows_pending && warp == 0) issue_chunk_rows(a, cfirst_s, len_s, g, rows_s, &rows_bar, &rows_bad_s);
   if (g == 0) {   // lengths out of range: that sequence's outputs come out NaN (no chunks)
     for (int b = tid; b < B; b += SM_THREADS)
       if (cfirst_s[b + 1] == cfirst_s[b]) set_error(a.hdr, MLA_ERR_BAD_SEQ_LEN, b);
@@ -287,133 +322,191 @@ __global__ void __launch_bounds__(SM_THREADS, 1) decode_small_kernel(const __gri
     }
     __syncthreads();
   }
-  ok = grid_barrier(sm_counter(a.hdr, 0), G, a.wait_ns, &flag_s);
+  grid_arrive(sm_counter(a.hdr, 0));
+  // while the other CTAs finish their absorb: the first chunk's rows into the padded tile, and
+  // the next chunk's copy issued into the raw buffer
+  bool cur_bad = false;
+  if (rows_pending) {
+    const bool landed = tc::mbar_wait(&rows_bar, rows_par, a.wait_ns);
+    if (__syncthreads_and(landed)) {
+      rows_pending = false;
+      rows_par ^= 1u;
+      cur_bad = rows_bad_s != 0;
+      int b0, j0;
+      relayout_rows(rows_s, reinterpret_cast<uint8_t*>(tile_s), CR, chunk_rows(B, cfirst_s, len_s, g, &b0, &j0));
+      __syncthreads();
+      if (g + (int)G < total_chunks) {
+        if (warp == 0) issue_chunk_rows(a, cfirst_s, len_s, g + (int)G, rows_s, &rows_bar, &rows_bad_s);
+        rows_pending = true;
+      }
+    } else {
+      ok = false;
+    }
+  }
+  ok = grid_wait(sm_counter(a.hdr, 0), G, a.wait_ns, &flag_s) && ok;
 
   // ================================ 2. attention over 32-row chunks ================================
-  // A warp serves heads w, w + 8, ... (HPW of them). Lane l owns the latent 16-byte pieces l and
-  // l + 32 (columns 8l .. 8l + 7 and 256 + 8l ..) and the RoPE pair l of every row, so a warp
-  // reads a row of shared memory without bank conflicts and keeps its heads' queries in
-  // registers. Scores: each lane forms its share of (row, head) for 8 rows at a time, and a
-  // transpose-reduce leaves the score of row r of the chunk in lane r.
-  const int np = C / 8;                       // latent pieces of a row
-  const bool own0 = lane < np, own1 = lane + 32 < np, ownr = 2 * lane < R;
+  // On the tensor cores, warp-level bf16 steps with float32 accumulation. The float32 queries
+  // and probabilities each go in as two bf16 operands (hi + lo), the cache rows exactly.
+  //   scores: S[h, r] = q'_h . row_r; warp w takes an eighth of the (C + R) / 16 column steps
+  //           for all 32 rows; the eight parts meet in shared memory.
+  //   softmax: warp w, heads w, w + 8, ...: lane r holds row r; max, probabilities, sum.
+  //   output: O[h, c] = sum_r P[h, r] row_r[c]; warp w takes latent columns w C/8 .. + C/8.
+  const uint32_t tile_a = tc::smem_u32(tile_s), q_a = tc::smem_u32(q_s), p_a = tc::smem_u32(p_s);
+  const int grp = lane >> 2, tig = lane & 3;
+  const int KS = CR / 16;
+  int q_seq = -1;
   for (int k = g; ok && k < total_chunks; k += G) {
-    int b = 0;
-    while (b + 1 < B && cfirst_s[b + 1] <= k) ++b;
-    const int j = k - cfirst_s[b];
-    const int nr = (int)min((long long)SM_CHUNK, (long long)a.seq_lens[b] - j * SM_CHUNK);
+    int b, j;
+    const int nr = chunk_rows(B, cfirst_s, len_s, k, &b, &j);
     float* part = a.part + ((int64_t)b * a.max_chunks + j) * H * (C + 4);
-    // the warp's queries (written by other CTAs before the barrier: read from L2)
-    float2 q[HPW][9];
-#pragma unroll
-    for (int jj = 0; jj < HPW; ++jj) {
-      const int h = warp + SM_WARPS * jj;
-      const float4* qh = reinterpret_cast<const float4*>(a.qf + ((int64_t)b * H + h) * CR);
-      float4 t0 = make_float4(0.f, 0.f, 0.f, 0.f), t1 = t0, t2 = t0, t3 = t0;
-      float2 tr = make_float2(0.f, 0.f);
-      if (h < H) {
-        if (own0) {
-          t0 = __ldcg(qh + 2 * lane);
-          t1 = __ldcg(qh + 2 * lane + 1);
-        }
-        if (own1) {
-          t2 = __ldcg(qh + 2 * (lane + 32));
-          t3 = __ldcg(qh + 2 * (lane + 32) + 1);
-        }
-        if (ownr) tr = __ldcg(reinterpret_cast<const float2*>(a.qf + ((int64_t)b * H + h) * CR + C) + lane);
+    if (k != g) {   // a later chunk: its copy was issued when the previous tile was made
+      const bool landed = tc::mbar_wait(&rows_bar, rows_par, a.wait_ns);
+      if (!__syncthreads_and(landed)) {
+        ok = false;
+        break;
       }
-      q[jj][0] = make_float2(t0.x, t0.y); q[jj][1] = make_float2(t0.z, t0.w);
-      q[jj][2] = make_float2(t1.x, t1.y); q[jj][3] = make_float2(t1.z, t1.w);
-      q[jj][4] = make_float2(t2.x, t2.y); q[jj][5] = make_float2(t2.z, t2.w);
-      q[jj][6] = make_float2(t3.x, t3.y); q[jj][7] = make_float2(t3.z, t3.w);
-      q[jj][8] = tr;
+      rows_pending = false;
+      rows_par ^= 1u;
+      cur_bad = rows_bad_s != 0;
+      relayout_rows(rows_s, reinterpret_cast<uint8_t*>(tile_s), CR, nr);
+      __syncthreads();
+      if (k + (int)G < total_chunks) {
+        if (warp == 0) issue_chunk_rows(a, cfirst_s, len_s, k + (int)G, rows_s, &rows_bar, &rows_bad_s);
+        rows_pending = true;
+      }
     }
-    const bool landed = tc::mbar_wait(&rows_bar, rows_par, a.wait_ns);
-    if (!__syncthreads_and(landed)) {
-      ok = false;
-      break;
+    if (b != q_seq) {   // this sequence's fused queries (written by other CTAs before the barrier)
+      const float4* src = reinterpret_cast<const float4*>(a.qf + (int64_t)b * H * CR);
+      const int n4 = CR / 4;
+      for (int i = tid; i < H * n4; i += SM_THREADS) {
+        const int h = i / n4, c4 = i - h * n4;
+        const float4 v = __ldcg(src + i);
+        __nv_bfloat16 hi[4], lo[4];
+        split_bf16(v.x, &hi[0], &lo[0]);
+        split_bf16(v.y, &hi[1], &lo[1]);
+        split_bf16(v.z, &hi[2], &lo[2]);
+        split_bf16(v.w, &hi[3], &lo[3]);
+        *reinterpret_cast<uint2*>(q_s + h * CRP + 4 * c4) = *reinterpret_cast<const uint2*>(hi);
+        *reinterpret_cast<uint2*>(q_s + (HM + h) * CRP + 4 * c4) = *reinterpret_cast<const uint2*>(lo);
+      }
+      q_seq = b;
     }
-    rows_pending = false;
-    rows_par ^= 1u;
-    if (rows_bad_s) {   // a row outside the pool: the merge of the sequence's heads comes out NaN
+    __syncthreads();
+    if (cur_bad) {   // a row outside the pool: the merge of the sequence's heads comes out NaN
       if (tid == 0) set_error(a.hdr, MLA_ERR_BAD_PAGE, b);
       for (int i = tid; i < H; i += SM_THREADS) {
         part[(int64_t)i * (C + 4) + C] = 0.f;
         part[(int64_t)i * (C + 4) + C + 1] = CUDART_NAN_F;
       }
     } else {
-      float s[HPW];
+      // ---- scores: warp w takes column steps w KS/8 .. (w+1) KS/8 - 1 of all 32 rows ----
+      {
+        const int ks0 = warp * KS / SM_WARPS, ks1 = (warp + 1) * KS / SM_WARPS;
+        float acc[2][4][MT][4];   // [hi, lo][8-row tile][head tile]
 #pragma unroll
-      for (int jj = 0; jj < HPW; ++jj) s[jj] = 0.f;
-      for (int g8 = 0; g8 * 8 < nr; ++g8) {
-        float sp[HPW][8];
+        for (int x = 0; x < 2; ++x)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int r = g8 * 8 + i;
-          float2 x[9];
-          load_row_share(rows_s + r * row_bytes, lane, C, own0 && r < nr, own1 && r < nr, ownr && r < nr, x);
+          for (int y = 0; y < 4; ++y)
 #pragma unroll
-          for (int jj = 0; jj < HPW; ++jj) {   // even and odd columns in the two halves of a pair
-            float2 d = make_float2(0.f, 0.f);
+            for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-            for (int e = 0; e < 9; ++e) d = __ffma2_rn(q[jj][e], x[e], d);
-            sp[jj][i] = d.x + d.y;
+              for (int e = 0; e < 4; ++e) acc[x][y][mt][e] = 0.f;
+        // B (two tiles per load): rows 8 (2 i + lane / 16) + (lane & 7), columns ks*16 + 8 (lane / 8 & 1);
+        // A: head row (lane & 7) + 8 (lane / 8 & 1), columns ks*16 + 8 (lane / 16)
+        const uint32_t b_lane = tile_a + (uint32_t)((((lane >> 4) * 8 + (lane & 7)) * CRP + 8 * ((lane >> 3) & 1)) * 2);
+        const uint32_t a_lane = q_a + (uint32_t)((((lane & 7) + 8 * ((lane >> 3) & 1)) * CRP + 8 * (lane >> 4)) * 2);
+        for (int ks = ks0; ks < ks1; ++ks) {
+          uint32_t bf[2][4];
+          ldsm_x4(b_lane + ks * 32, bf[0]);                              // row tiles 0, 1
+          ldsm_x4(b_lane + (uint32_t)(16 * CRP * 2) + ks * 32, bf[1]);   // row tiles 2, 3
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            uint32_t ah[4], al[4];
+            ldsm_x4(a_lane + (uint32_t)((mt * 16 * CRP + ks * 16) * 2), ah);
+            ldsm_x4(a_lane + (uint32_t)(((HM + mt * 16) * CRP + ks * 16) * 2), al);
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+              const uint32_t b0 = bf[nt >> 1][2 * (nt & 1)], b1 = bf[nt >> 1][2 * (nt & 1) + 1];
+              mma_bf16(acc[0][nt][mt], ah, b0, b1);
+              mma_bf16(acc[1][nt][mt], al, b0, b1);
+            }
           }
         }
 #pragma unroll
-        for (int jj = 0; jj < HPW; ++jj) {
-          const float t = transpose_sum8(sp[jj], lane);   // row g8 * 8 + (lane & 7)
-          if ((lane >> 3) == g8) s[jj] = t;
-        }
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            float* s0 = sc_s + (warp * HM + mt * 16 + grp) * SM_CHUNK + nt * 8 + 2 * tig;
+            *reinterpret_cast<float2*>(s0) =
+                make_float2(acc[0][nt][mt][0] + acc[1][nt][mt][0], acc[0][nt][mt][1] + acc[1][nt][mt][1]);
+            *reinterpret_cast<float2*>(s0 + 8 * SM_CHUNK) =
+                make_float2(acc[0][nt][mt][2] + acc[1][nt][mt][2], acc[0][nt][mt][3] + acc[1][nt][mt][3]);
+          }
       }
-      float p[HPW], m[HPW], l[HPW];
-#pragma unroll
-      for (int jj = 0; jj < HPW; ++jj) {
-        const float sc = lane < nr ? s[jj] * a.scale_log2 : -CUDART_INF_F;
-        m[jj] = warp_max(sc);
-        p[jj] = lane < nr ? ex2(sc - m[jj]) : 0.f;
-        l[jj] = warp_sum(p[jj]);
-      }
-      // output: lane accumulates its two latent pieces of the warp's heads, rows in order
-      float2 o[HPW][8];
-#pragma unroll
-      for (int jj = 0; jj < HPW; ++jj)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[jj][e] = make_float2(0.f, 0.f);
-#pragma unroll 2
-      for (int r = 0; r < nr; ++r) {
-        float2 v[9];
-        load_row_share(rows_s + r * row_bytes, lane, C, own0, own1, false, v);
-#pragma unroll
-        for (int jj = 0; jj < HPW; ++jj) {
-          const float pr = __shfl_sync(0xffffffffu, p[jj], r);
-          const float2 pr2 = make_float2(pr, pr);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o[jj][e] = __ffma2_rn(pr2, v[e], o[jj][e]);
-        }
-      }
+      __syncthreads();
+      // ---- softmax over the chunk's rows, per head ----
 #pragma unroll
       for (int jj = 0; jj < HPW; ++jj) {
         const int h = warp + SM_WARPS * jj;
         if (h < H) {
-          float4* ph = reinterpret_cast<float4*>(part + (int64_t)h * (C + 4));
-          if (own0) {
-            ph[2 * lane] = make_float4(o[jj][0].x, o[jj][0].y, o[jj][1].x, o[jj][1].y);
-            ph[2 * lane + 1] = make_float4(o[jj][2].x, o[jj][2].y, o[jj][3].x, o[jj][3].y);
+          float sum = 0.f;   // the eight column parts, in order
+#pragma unroll
+          for (int w = 0; w < SM_WARPS; ++w) sum += sc_s[(w * HM + h) * SM_CHUNK + lane];
+          const float sc = lane < nr ? sum * a.scale_log2 : -CUDART_INF_F;
+          const float m = warp_max(sc);
+          const float pv = lane < nr ? ex2(sc - m) : 0.f;
+          const float l = warp_sum(pv);
+          split_bf16(pv, &p_s[h * PP + lane], &p_s[(HM + h) * PP + lane]);
+          if (lane == 0) reinterpret_cast<float4*>(part + (int64_t)h * (C + 4))[C / 4] = make_float4(m, l, 0.f, 0.f);
+        }
+      }
+      __syncthreads();
+      // ---- output rows: latent columns of this warp ----
+      {
+        const int tpw = C / 64;   // 8-column tiles per warp
+        uint32_t pf[2][2][MT][4];   // [column step][hi, lo][head tile]
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+          for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+              ldsm_x4(p_a + (uint32_t)((((hl * HM + mt * 16) + (lane & 7) + 8 * ((lane >> 3) & 1)) * PP + ks * 16 +
+                                        8 * (lane >> 4)) * 2),
+                      pf[ks][hl][mt]);
+#pragma unroll 2
+        for (int jt = 0; jt < tpw; ++jt) {
+          const int n0 = (warp * tpw + jt) * 8;
+          uint32_t bv[4];   // rows 0-7, 8-15, 16-23, 24-31 of columns n0 .. n0 + 7, transposed
+          ldsm_x4_trans(tile_a + (uint32_t)((lane * CRP + n0) * 2), bv);
+          float acc[2][MT][4];
+#pragma unroll
+          for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) acc[hl][mt][e] = 0.f;
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+            for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+              for (int mt = 0; mt < MT; ++mt) mma_bf16(acc[hl][mt], pf[ks][hl][mt], bv[2 * ks], bv[2 * ks + 1]);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            const int h = mt * 16 + grp;
+            if (h < H)
+              *reinterpret_cast<float2*>(part + (int64_t)h * (C + 4) + n0 + 2 * tig) =
+                  make_float2(acc[0][mt][0] + acc[1][mt][0], acc[0][mt][1] + acc[1][mt][1]);
+            if (h + 8 < H)
+              *reinterpret_cast<float2*>(part + (int64_t)(h + 8) * (C + 4) + n0 + 2 * tig) =
+                  make_float2(acc[0][mt][2] + acc[1][mt][2], acc[0][mt][3] + acc[1][mt][3]);
           }
-          if (own1) {
-            ph[2 * (lane + 32)] = make_float4(o[jj][4].x, o[jj][4].y, o[jj][5].x, o[jj][5].y);
-            ph[2 * (lane + 32) + 1] = make_float4(o[jj][6].x, o[jj][6].y, o[jj][7].x, o[jj][7].y);
-          }
-          if (lane == 0) ph[C / 4] = make_float4(m[jj], l[jj], 0.f, 0.f);
         }
       }
     }
-    __syncthreads();   // rows_s is free: the next chunk of this CTA goes in
-    if (k + G < total_chunks) {
-      if (warp == 0) issue_chunk_rows(a, cfirst_s, k + (int)G, rows_s, &rows_bar, &rows_bad_s);
-      rows_pending = true;
-    }
+    __syncthreads();   // the tile, scores and P are reused by the next chunk
   }
   if (ok) ok = grid_barrier(sm_counter(a.hdr, 1), G, a.wait_ns, &flag_s);
 
@@ -546,7 +639,7 @@ bool decode_small_supported(const mla_config& cfg, int B, int tokens) {
   return tokens == 1 && cfg.act_dtype == MLA_BF16 && cfg.kv_b_dtype == MLA_BF16 && B >= 1 &&
          (int64_t)B * cfg.n_heads <= 64 && cfg.n_heads <= SM_WARPS * SM_MAX_HPW && cfg.kv_lora % 128 == 0 &&
          cfg.kv_lora <= 32 * SM_MAX_CPL && (cfg.kv_lora + cfg.qk_rope) % 8 == 0 && cfg.qk_rope % 2 == 0 &&
-         cfg.qk_rope <= 64 && cfg.qk_nope % 4 == 0 && cfg.qk_nope <= 128 &&
+         cfg.qk_rope <= 64 && cfg.qk_rope % 16 == 0 && cfg.qk_nope % 4 == 0 && cfg.qk_nope <= 128 &&
          cfg.v_head % 16 == 0 && cfg.v_head <= 128 && cap >= 1 && cap <= (int64_t)SM_CHUNK * SM_MAX_CHUNKS;
 }
 
@@ -590,8 +683,11 @@ cudaError_t launch_decode_small(const mla_config& cfg, const mla_cache& cache, c
   a.max_chunks = (int)decode_small_max_chunks(cfg);
   a.scale_log2 = cfg.softmax_scale * 1.4426950408889634f;
   a.wait_ns = wait_limit_ns();
-  const int smem = SM_CHUNK * (cfg.kv_lora + cfg.qk_rope) * 2;   // the chunk's rows
   const int hpw = (cfg.n_heads + SM_WARPS - 1) / SM_WARPS;
+  const int CR = cfg.kv_lora + cfg.qk_rope, hm = hpw > 2 ? 32 : 16;
+  // raw rows, padded tile, queries (hi, lo), the scores' eight column parts, P (hi, lo)
+  const int smem = SM_CHUNK * CR * 2 + SM_CHUNK * (CR + 8) * 2 + 2 * hm * (CR + 8) * 2 + SM_WARPS * hm * SM_CHUNK * 4 +
+                   2 * hm * (SM_CHUNK + 8) * 2;
   void (*kern)(SmallArgs) = hpw == 1 ? decode_small_kernel<1> : hpw == 2 ? decode_small_kernel<2> : decode_small_kernel<4>;
   cudaError_t e = ensure_smem((const void*)kern, smem);
   if (e != cudaSuccess) return e;
