@@ -428,7 +428,7 @@ def run_ours(args, rank, world, device, workload, K, W, with_e2e=True, with_cloc
             "gpus": f"replicas x{world}" if world > 1 else "single GPU",
             "attention_kernel": {0: "cuda-core", 1: "tcgen05, one CTA per head group",
                                  2: "tcgen05, SM pairs (clusters of two CTAs)",
-                                 3: "one launch: absorb, attention, merge and W_UV (CUDA cores)"}[plan.kernel],
+                                 3: "one launch: absorb and merge with W_UV on the CUDA cores, chunk attention on warp-level bf16 tensor-core steps"}[plan.kernel],
             "heads_per_cta": plan.heads_per_cta, "splits": plan.splits,
             "rows_per_split": plan.rows_per_split,
         },

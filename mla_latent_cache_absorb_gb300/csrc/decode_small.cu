@@ -276,6 +276,10 @@ __global__ void __launch_bounds__(SM_THREADS, 1) decode_small_kernel(const __gri
       wuv[4 * i] = u.x; wuv[4 * i + 1] = u.y; wuv[4 * i + 2] = u.z; wuv[4 * i + 3] = u.w;
     }
   }
+  // the first absorb item's RoPE angle (positions and frequencies are inputs, read before the wait)
+  float cos0 = 1.f, sin0 = 0.f;
+  if (g < n_items1 && g % (C / 64) == 0 && tid >= 64 && tid < 64 + R / 2 && a.positions != nullptr)
+    rope_cs_value(a.inv_freq[tid - 64], a.positions[g / (H * (C / 64))], &cos0, &sin0);
   pdl_wait();   // q and the appended cache row come from earlier kernels; the workspace and out
                 // may still be read by them
   __syncthreads();
@@ -311,8 +315,8 @@ __global__ void __launch_bounds__(SM_THREADS, 1) decode_small_kernel(const __gri
       const int p = tid - 64;
       const float x0 = bf16f(qn[N + 2 * p]), x1 = bf16f(qn[N + 2 * p + 1]);
       if (a.positions != nullptr) {
-        float cv, sv;
-        rope_cs_value(a.inv_freq[p], a.positions[b], &cv, &sv);
+        float cv = cos0, sv = sin0;
+        if (it != g) rope_cs_value(a.inv_freq[p], a.positions[b], &cv, &sv);
         qf[C + 2 * p] = x0 * cv - x1 * sv;
         qf[C + 2 * p + 1] = x0 * sv + x1 * cv;
       } else {
@@ -598,10 +602,10 @@ __global__ void __launch_bounds__(SM_THREADS, 1) decode_small_kernel(const __gri
     }
     // the last of the head's slices adds the shares
     __syncthreads();
-    if (tid == 0) {
-      __threadfence();
-      last_s = atomicAdd(&a.head_cnt[b * H + h], 1u) == (unsigned int)(C / 64 - 1);
-      __threadfence();
+    if (tid == 0) {   // acquire-release: the shares written before are seen by the last slice
+      unsigned int prev;
+      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(&a.head_cnt[b * H + h]) : "memory");
+      last_s = prev == (unsigned int)(C / 64 - 1);
     }
     __syncthreads();
     if (last_s) {

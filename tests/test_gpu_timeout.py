@@ -1,6 +1,6 @@
 """The timeout path of the bounded device waits, driven on purpose and without a fault: the
 main-loop wait limit is set far below what a copy or an MMA takes (mla_set_wait_limit_ns), so
-the tensor-core kernels' waits run out. Each such CTA records MLA_ERR_TIMEOUT, drains what it
+the tensor-core kernels' waits (and the one-launch path's grid-wide barriers) run out. Each such CTA records MLA_ERR_TIMEOUT, drains what it
 issued, frees its tensor memory and writes NaN for the outputs it owns; the context stays
 usable and the next call with the normal limit is bit-identical to a clean run."""
 import numpy as np
@@ -15,8 +15,10 @@ W = synth.WORKLOADS
 CASES = [
     # 128 heads, eight sequences: tcgen05 absorb, SM-pair attention and combine
     ("h128_b8", W["v3_b32_t4096"].with_(B=8, context=("fixed", 300))),
-    # 16 heads, one sequence: tcgen05 attention (16-head group) between the CUDA-core kernels
-    ("h16_b1", W["v2lite_b1_t4096"].with_(context=("fixed", 1000))),
+    # 16 heads, five sequences: tcgen05 attention (16-head group) between the CUDA-core kernels
+    ("h16_b5", W["v2lite_b1_t4096"].with_(B=5, context=("fixed", 1000))),
+    # 16 heads, one sequence: the one-launch path (its grid-wide barriers and row copies)
+    ("h16_b1_one_launch", W["v2lite_b1_t4096"].with_(context=("fixed", 1000))),
 ]
 
 
