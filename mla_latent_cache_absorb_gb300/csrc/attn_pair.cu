@@ -444,9 +444,8 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
           }
           uint8_t* dst = stages + st * AP_STAGE;
           tc::mbar_arrive_expect_tx(&s.full[st], AP_STAGE);
-          for (int j = 0; j < 4; ++j)
-            tc::tma_load_2d_hint(dst + j * AP_BLK, &rows_map, 256 * (int)c + 64 * j, (int32_t)pr, &s.full[st],
-                                 kv_policy);
+          // this CTA's four 64-column latent blocks in one copy (four [64 rows][64] tiles)
+          tc::tma_load_3d_hint(dst, &rows_map, 0, (int32_t)pr, 4 * (int)c, &s.full[st], kv_policy);
           tc::tma_load_2d_hint(dst + 4 * AP_BLK, &rope_map, 512 + 32 * (int)c, (int32_t)pr, &s.full[st], kv_policy);
           last_n[st] = n;
           if (defer_q && t == tlo) {
@@ -1005,7 +1004,7 @@ cudaError_t launch_attn_pair(const mla_config& cfg, const mla_cache& cache, cons
     return cudaErrorInvalidValue;
   if (q_res == nullptr) return cudaErrorInvalidValue;
   CUtensorMap rows_map, rope_map, qrope_map, qres_map;
-  if (!make_map_2d_bf16(&rows_map, cache.rows, 576, (uint64_t)cache.n_physical_rows, 64, AP_TILE) ||
+  if (!make_map_row_blocks_bf16(&rows_map, cache.rows, 576, (uint64_t)cache.n_physical_rows, 8, AP_TILE, 4) ||
       !make_map_2d_bf16(&rope_map, cache.rows, 576, (uint64_t)cache.n_physical_rows, 32, AP_TILE, 64) ||
       !make_map_2d_bf16(&qrope_map, q_abs, 576, (uint64_t)B * cfg.n_heads, 32, AP_HEADS, 64) ||
       !make_map_2d_bf16(&qres_map, q_res, 576, (uint64_t)B * cfg.n_heads, 32, AP_HEADS, 64))

@@ -306,6 +306,8 @@ bool tma_encoder_available();
 // is rejected.
 bool make_map_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
                       uint32_t box_rows, int swizzle_bytes = 128);
+bool make_map_row_blocks_bf16(CUtensorMap* m, const void* base, uint64_t row_elems, uint64_t rows,
+                              uint32_t n_blocks, uint32_t box_rows, uint32_t box_blocks);
 
 // Raise a kernel's dynamic shared memory limit once per (kernel, device), so that repeated
 // launches (and launches under stream capture) make no attribute calls.
