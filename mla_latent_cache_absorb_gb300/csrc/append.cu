@@ -34,7 +34,6 @@ append_finish_kernel(mla_config cfg, RowMap map, typename Act<DT>::T* __restrict
   const float* src = kva + (int64_t)b * row;
   const bool has_pair = threadIdx.x < R / 2;
   float x0 = 0.f, x1 = 0.f;
-  double inv = 0.0;
   auto load_row = [&]() {
 #pragma unroll
     for (int k = 0; k < FIN_MAX_PER_THREAD; ++k) {
@@ -52,9 +51,16 @@ append_finish_kernel(mla_config cfg, RowMap map, typename Act<DT>::T* __restrict
     const int i = threadIdx.x + k * FIN_THREADS;
     wn[k] = (i < C) ? norm_w[i] : 0.f;
   }
-  if (has_pair) inv = cfg.rope_inv_freq[threadIdx.x];
   const int pos = positions[b];
   const int len = seq_lens != nullptr ? seq_lens[b] : pos;
+  // this thread's RoPE angle, before the wait (float64 arithmetic is slow on this GPU: the
+  // frequency is split into a float pair once and the angle formed in float where that holds)
+  float rc = 1.f, rs = 0.f;
+  if (has_pair) {
+    float fh, fl;
+    rope_freq_split(cfg.rope_inv_freq, threadIdx.x, &fh, &fl);
+    rope_cs_split(cfg.rope_inv_freq, fh, fl, threadIdx.x, pos, &rc, &rs);
+  }
   pdl_wait();   // the cache row may still be read by the previous step's attention
   if (kva_dep) load_row();
   if (len != pos) {
@@ -94,10 +100,8 @@ append_finish_kernel(mla_config cfg, RowMap map, typename Act<DT>::T* __restrict
   }
   // RoPE over the pe tail: one thread per pair (2i, 2i+1)
   if (has_pair) {
-    float c, s;
-    rope_cs_value(inv, pos, &c, &s);
-    Act<DT>::store(dst, C + 2 * threadIdx.x, x0 * c - x1 * s);
-    Act<DT>::store(dst, C + 2 * threadIdx.x + 1, x0 * s + x1 * c);
+    Act<DT>::store(dst, C + 2 * threadIdx.x, x0 * rc - x1 * rs);
+    Act<DT>::store(dst, C + 2 * threadIdx.x + 1, x0 * rs + x1 * rc);
   }
   for (int i = threadIdx.x + FIN_THREADS; i < R / 2; i += FIN_THREADS) {   // R / 2 > 128 only
     float c, s;

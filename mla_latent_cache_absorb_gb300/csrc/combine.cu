@@ -257,6 +257,189 @@ __global__ void __launch_bounds__(CMB_THREADS, 2) combine_kernel(CombineArgs a) 
   }
 }
 
+// ---- small batches (B <= 8), bf16 or Q8_0 kv_b: one CTA per head ----
+// Before the dependency wait every thread issues its share of the head's W_UV rows as raw
+// 16-byte cp.async pieces (the whole [V][row] slice in flight at once). After it: one warp per
+// sequence forms the slot weights; each thread merges one (sequence, 4 latent columns) item
+// with all its slots' loads in flight (sixteen at a time, summed in slot order); one warp per
+// output row then decodes its W_UV row from shared memory (lane l: columns 16 l .. 16 l + 15)
+// against the merged rows it holds in registers, with fixed-order warp sums.
+constexpr int CMB_S_THREADS = 512;
+constexpr int CMB_S_BMAX = 8;
+constexpr int CMB_S_U = 16;
+
+template <int WDT, int BT>
+__global__ void __launch_bounds__(CMB_S_THREADS, 1) combine_small_kernel(CombineArgs a) {
+  extern __shared__ __align__(16) uint8_t sm_raw[];
+  pdl_trigger();
+  const int h = blockIdx.x;
+  const int B = a.B, C = a.C, V = a.V;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int RB = WDT == MLA_Q8_0 ? C / 32 * 34 : C * 2;   // raw bytes of a W_UV row
+  uint8_t* w_s = sm_raw;                                                       // [V][RB]
+  float* vc_s = reinterpret_cast<float*>(sm_raw + (((size_t)V * RB + 15) & ~(size_t)15));   // [BT][C]
+  float* wt_s = vc_s + BT * C;                                                 // [BT][max_slots]
+  float* lse_s = wt_s + BT * a.max_slots;                                      // [BT]
+  int* first_s = reinterpret_cast<int*>(lse_s + BT);                           // [BT]
+  int* cnt_s = first_s + BT;                                                   // [BT]
+  const int pg = h / a.hpg, hh = h % a.hpg;
+  auto lse_at = [&](int slot) { return ((int64_t)pg * a.n_slots + slot) * a.hpg + hh; };
+
+  {   // W_UV rows of head h % kvb_heads, raw
+    const uint8_t* src0 = static_cast<const uint8_t*>(a.kv_b) + ((int64_t)(h % a.kvb_heads) * (a.N + V) + a.N) * RB;
+    const int ppr = RB / 16;
+    for (int i = tid; i < V * ppr; i += CMB_S_THREADS) {
+      const int r = i / ppr, pc = i - r * ppr;
+      const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(w_s + r * RB + pc * 16));
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src0 + (int64_t)r * RB + pc * 16)
+                   : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  pdl_wait();   // the partials and meta come from the attention kernel
+
+  // slot weights exp(lse_s - lse): one warp per sequence
+  if (warp < BT) {
+    int first = 0, ns = 0;
+    if (warp < B) {
+      first = a.meta[2 * warp];
+      ns = min(a.meta[2 * warp + 1], a.max_slots);
+    }
+    float mx = -CUDART_INF_F;
+    for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, a.part_lse[lse_at(first + s)]);
+    mx = warp_max(mx);
+    float tot = 0.f;
+    for (int s = lane; s < ns; s += 32) tot += expf(a.part_lse[lse_at(first + s)] - mx);
+    tot = warp_sum(tot);
+    const float l = (ns > 0) ? mx + logf(tot) : CUDART_NAN_F;
+    for (int s = lane; s < ns; s += 32) wt_s[warp * a.max_slots + s] = expf(a.part_lse[lse_at(first + s)] - l);
+    if (lane == 0) {
+      lse_s[warp] = l;
+      first_s[warp] = first;
+      cnt_s[warp] = ns;
+    }
+  }
+  __syncthreads();
+
+  // vc[b][4 g .. 4 g + 3] = sum_s w_s O_s, slots in order
+  const int C4 = C / 4;
+  for (int item = tid; item < B * C4; item += CMB_S_THREADS) {
+    const int b = item / C4, g = item - b * C4;
+    const int ns = cnt_s[b], first = first_s[b];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < ns; s0 += CMB_S_U) {
+      float4 x[CMB_S_U];
+#pragma unroll
+      for (int u = 0; u < CMB_S_U; ++u)
+        x[u] = s0 + u < ns ? __ldcg(reinterpret_cast<const float4*>(a.part_o + lse_at(first + s0 + u) * C) + g)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < CMB_S_U; ++u) {
+        const float w = s0 + u < ns ? wt_s[b * a.max_slots + s0 + u] : 0.f;
+        if (w != 0.f) {   // empty slots carry weight 0 and unwritten data: skip, never 0 * x
+          acc.x = fmaf(w, x[u].x, acc.x);
+          acc.y = fmaf(w, x[u].y, acc.y);
+          acc.z = fmaf(w, x[u].z, acc.z);
+          acc.w = fmaf(w, x[u].w, acc.w);
+        }
+      }
+    }
+    if (isnan(lse_s[b])) acc = make_float4(CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F);
+    reinterpret_cast<float4*>(vc_s)[b * C4 + g] = acc;
+  }
+  for (int i = B * C4 + tid; i < BT * C4; i += CMB_S_THREADS)   // sequences past B: zero
+    reinterpret_cast<float4*>(vc_s)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+
+  // lse, one warp per sequence; with bf16 latent queries q_hi = q' - res the exact log-sum-exp
+  // is, to first order, lse + scale * vc . res
+  if (a.lse != nullptr && warp < B) {
+    float l = lse_s[warp];
+    if (a.q_res != nullptr) {
+      const uint16_t* res = a.q_res + ((int64_t)warp * a.H + h) * (C + a.R);
+      float d = 0.f;
+      for (int c = lane; c < C; c += 32) d = fmaf(vc_s[warp * C + c], bf16_bits_to_f32(res[c]), d);
+      d = warp_sum(d);
+      l += a.scale * d;
+    }
+    if (lane == 0) a.lse[(int64_t)warp * a.H + h] = l;
+  }
+
+  // out[b, h, v]: warp per row v, lane l over latent columns 16 l .. 16 l + 15 (C = 512; fewer
+  // lanes for narrower rows), merged rows of every sequence held in registers
+  const int cpl = C / 32;   // columns per lane: 8 or 16
+  constexpr int BG = BT < 4 ? BT : 4;   // sequences per pass over the rows
+#pragma unroll 1
+  for (int b0 = 0; b0 < BT; b0 += BG) {
+    float vr[BG][16];
+#pragma unroll
+    for (int b = 0; b < BG; ++b)
+#pragma unroll
+      for (int e = 0; e < 16; ++e) vr[b][e] = e < cpl ? vc_s[(b0 + b) * C + cpl * lane + e] : 0.f;
+    for (int v = warp; v < V; v += CMB_S_THREADS / 32) {
+      float w[16];
+      if (WDT == MLA_Q8_0) {
+        // the lane's columns lie in block (cpl lane) / 32, from element (cpl lane) % 32
+        const int c0 = cpl * lane;
+        const uint8_t* blk = w_s + v * RB + (c0 >> 5) * 34;
+        const float d = __half2float(*reinterpret_cast<const __half*>(blk));
+        const uint16_t* c16 = reinterpret_cast<const uint16_t*>(blk + 2 + (c0 & 31));
+#pragma unroll
+        for (int e2 = 0; e2 < 8; ++e2) {
+          const uint16_t cc = e2 * 2 < cpl ? c16[e2] : 0;
+          w[2 * e2] = d * (float)(int8_t)(cc & 0xFF);
+          w[2 * e2 + 1] = d * (float)(int8_t)(cc >> 8);
+        }
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(w_s + v * RB + 2 * cpl * lane);
+#pragma unroll
+        for (int q4 = 0; q4 < 2; ++q4) {
+          const uint4 u = q4 * 8 < cpl ? src[q4] : make_uint4(0, 0, 0, 0);
+          const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            w[8 * q4 + 2 * e] = __uint_as_float(uw[e] << 16);
+            w[8 * q4 + 2 * e + 1] = __uint_as_float(uw[e] & 0xFFFF0000u);
+          }
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < BG; ++b) {
+        float y = 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) y = fmaf(w[e], vr[b][e], y);
+        y = warp_sum(y);
+        if (lane == 0 && b0 + b < B) a.out[((int64_t)(b0 + b) * a.H + h) * V + v] = y;
+      }
+    }
+  }
+}
+
+static bool combine_small_fits(const mla_config& cfg, int B, int max_slots) {
+  return B >= 1 && B <= CMB_S_BMAX && (cfg.kv_b_dtype == MLA_BF16 || cfg.kv_b_dtype == MLA_Q8_0) &&
+         (cfg.kv_lora == 256 || cfg.kv_lora == 512) && cfg.v_head <= 512 && max_slots >= 1 && max_slots <= 1024;
+}
+
+template <int WDT, int BT>
+static cudaError_t launch_combine_small_bt(const CombineArgs& a, cudaStream_t st) {
+  const int RB = WDT == MLA_Q8_0 ? a.C / 32 * 34 : a.C * 2;
+  const size_t smem = (((size_t)a.V * RB + 15) & ~(size_t)15) +
+                      sizeof(float) * ((size_t)BT * a.C + (size_t)BT * a.max_slots + 3 * BT);
+  auto k = combine_small_kernel<WDT, BT>;
+  cudaError_t e = ensure_smem((const void*)k, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k, dim3(a.H), dim3(CMB_S_THREADS), smem, st, a);
+}
+
+template <int WDT>
+static cudaError_t launch_combine_small(const CombineArgs& a, cudaStream_t st) {
+  if (a.B <= 1) return launch_combine_small_bt<WDT, 1>(a, st);
+  if (a.B <= 2) return launch_combine_small_bt<WDT, 2>(a, st);
+  if (a.B <= 4) return launch_combine_small_bt<WDT, 4>(a, st);
+  return launch_combine_small_bt<WDT, 8>(a, st);
+}
+
 cudaError_t launch_combine(const mla_config& cfg, const DecodePlan& plan, const void* kv_b,
                            const int32_t* meta, const float* part_o, const float* part_lse, const void* q_res,
                            float* out, float* lse, int B, cudaStream_t st) {
@@ -271,6 +454,14 @@ cudaError_t launch_combine(const mla_config& cfg, const DecodePlan& plan, const 
   a.kvb_heads = plan.kvb_heads;
   // most slots one sequence can span: splits (CUDA-core path) or CTAs per group (tensor path)
   a.max_slots = plan.path != PATH_SIMT ? plan.ctas_per_group : plan.splits;
+  if (combine_small_fits(cfg, B, a.max_slots)) {
+    const int RB = cfg.kv_b_dtype == MLA_Q8_0 ? cfg.kv_lora / 32 * 34 : cfg.kv_lora * 2;
+    const int bt = B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : 8;
+    const size_t smem = (((size_t)cfg.v_head * RB + 15) & ~(size_t)15) +
+                        sizeof(float) * ((size_t)bt * cfg.kv_lora + (size_t)bt * a.max_slots + 3 * bt);
+    if (smem <= 227 * 1024)
+      return cfg.kv_b_dtype == MLA_Q8_0 ? launch_combine_small<MLA_Q8_0>(a, st) : launch_combine_small<MLA_BF16>(a, st);
+  }
   // V-slices per head: enough CTAs to cover the SMs, but every slice merges the partials again
   const int chunks = (cfg.v_head + CMB_VJ - 1) / CMB_VJ;
   const int64_t base_ctas = (int64_t)cfg.n_heads * ((B + CMB_BC - 1) / CMB_BC);

@@ -262,6 +262,24 @@ __device__ __forceinline__ void rope_cs_f32(float inv_hi, float inv_lo, int pos,
   __sincosf(r + a_lo, s, c);
 }
 
+// The frequency of pair i as an unevaluated float sum hi + lo (two float64 operations, done once
+// per pair in a kernel's prologue: float64 arithmetic is slow on this GPU).
+__device__ __forceinline__ void rope_freq_split(const double* inv_freq, int i, float* hi, float* lo) {
+  const double inv = inv_freq[i];
+  const float h = __double2float_rn(inv);
+  *hi = h;
+  *lo = __double2float_rn(inv - static_cast<double>(h));
+}
+// The RoPE angle of pair i at pos: in float arithmetic from (hi, lo) where that form holds
+// (0 < hi <= 1, 0 <= pos < ROPE_F32_MAX_POS), else in float64 from inv_freq.
+__device__ __forceinline__ void rope_cs_split(const double* inv_freq, float hi, float lo, int i, int pos, float* c,
+                                              float* s) {
+  if (pos >= 0 && pos < ROPE_F32_MAX_POS && hi > 0.f && hi <= 1.f)
+    rope_cs_f32(hi, lo, pos, c, s);
+  else
+    rope_cs(inv_freq, i, pos, c, s);
+}
+
 // ---- decode plan: how the rows of a sequence are split, and the workspace layout -------------
 struct DecodePlan {
   int path;              // PATH_SIMT or PATH_TC

@@ -276,10 +276,9 @@ __global__ void __launch_bounds__(SM_THREADS, 1) decode_small_kernel(const __gri
       wuv[4 * i] = u.x; wuv[4 * i + 1] = u.y; wuv[4 * i + 2] = u.z; wuv[4 * i + 3] = u.w;
     }
   }
-  // the first absorb item's RoPE angle (positions and frequencies are inputs, read before the wait)
-  float cos0 = 1.f, sin0 = 0.f;
-  if (g < n_items1 && g % (C / 64) == 0 && tid >= 64 && tid < 64 + R / 2 && a.positions != nullptr)
-    rope_cs_value(a.inv_freq[tid - 64], a.positions[g / (H * (C / 64))], &cos0, &sin0);
+  // the RoPE frequencies as float pairs (inputs, read before the wait)
+  __shared__ float f_hi[32], f_lo[32];   // R <= 64
+  if (a.positions != nullptr && tid < R / 2) rope_freq_split(a.inv_freq, tid, &f_hi[tid], &f_lo[tid]);
   pdl_wait();   // q and the appended cache row come from earlier kernels; the workspace and out
                 // may still be read by them
   __syncthreads();
@@ -315,8 +314,8 @@ __global__ void __launch_bounds__(SM_THREADS, 1) decode_small_kernel(const __gri
       const int p = tid - 64;
       const float x0 = bf16f(qn[N + 2 * p]), x1 = bf16f(qn[N + 2 * p + 1]);
       if (a.positions != nullptr) {
-        float cv = cos0, sv = sin0;
-        if (it != g) rope_cs_value(a.inv_freq[p], a.positions[b], &cv, &sv);
+        float cv, sv;
+        rope_cs_split(a.inv_freq, f_hi[p], f_lo[p], p, a.positions[b], &cv, &sv);
         qf[C + 2 * p] = x0 * cv - x1 * sv;
         qf[C + 2 * p + 1] = x0 * sv + x1 * cv;
       } else {
