@@ -267,6 +267,8 @@ __global__ void __launch_bounds__(CMB_THREADS, 2) combine_kernel(CombineArgs a) 
 constexpr int CMB_S_THREADS = 512;
 constexpr int CMB_S_BMAX = 8;
 constexpr int CMB_S_U = 16;
+constexpr int CMB_S_MAXS = 256;
+constexpr int CMB_S_VP = 18;       // lane pitch of the merged rows in shared memory (floats)   // slots a sequence may span at most (weights from registers)
 
 template <int WDT, int BT>
 __global__ void __launch_bounds__(CMB_S_THREADS, 1) combine_small_kernel(CombineArgs a) {
@@ -277,8 +279,10 @@ __global__ void __launch_bounds__(CMB_S_THREADS, 1) combine_small_kernel(Combine
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int RB = WDT == MLA_Q8_0 ? C / 32 * 34 : C * 2;   // raw bytes of a W_UV row
   uint8_t* w_s = sm_raw;                                                       // [V][RB]
-  float* vc_s = reinterpret_cast<float*>(sm_raw + (((size_t)V * RB + 15) & ~(size_t)15));   // [BT][C]
-  float* wt_s = vc_s + BT * C;                                                 // [BT][max_slots]
+  // merged rows, lane-major for the output phase: [BT][32 lanes][18] (lane l's columns
+  // C/32 l .. at 18 l: a row of 64-bit loads across the lanes hits distinct bank pairs)
+  float* vc_s = reinterpret_cast<float*>(sm_raw + (((size_t)V * RB + 15) & ~(size_t)15));
+  float* wt_s = vc_s + BT * 32 * CMB_S_VP;                                     // [BT][max_slots]
   float* lse_s = wt_s + BT * a.max_slots;                                      // [BT]
   int* first_s = reinterpret_cast<int*>(lse_s + BT);                           // [BT]
   int* cnt_s = first_s + BT;                                                   // [BT]
@@ -297,42 +301,64 @@ __global__ void __launch_bounds__(CMB_S_THREADS, 1) combine_small_kernel(Combine
     asm volatile("cp.async.commit_group;" ::: "memory");
   }
   pdl_wait();   // the partials and meta come from the attention kernel
-
-  // slot weights exp(lse_s - lse): one warp per sequence
-  if (warp < BT) {
-    int first = 0, ns = 0;
-    if (warp < B) {
-      first = a.meta[2 * warp];
-      ns = min(a.meta[2 * warp + 1], a.max_slots);
-    }
-    float mx = -CUDART_INF_F;
-    for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, a.part_lse[lse_at(first + s)]);
-    mx = warp_max(mx);
-    float tot = 0.f;
-    for (int s = lane; s < ns; s += 32) tot += expf(a.part_lse[lse_at(first + s)] - mx);
-    tot = warp_sum(tot);
-    const float l = (ns > 0) ? mx + logf(tot) : CUDART_NAN_F;
-    for (int s = lane; s < ns; s += 32) wt_s[warp * a.max_slots + s] = expf(a.part_lse[lse_at(first + s)] - l);
-    if (lane == 0) {
-      lse_s[warp] = l;
-      first_s[warp] = first;
-      cnt_s[warp] = ns;
-    }
+  __shared__ float dres_s[CMB_S_BMAX][4];   // per sequence: vc . residual, by 32-item group
+  if (tid < B) {
+    first_s[tid] = a.meta[2 * tid];
+    cnt_s[tid] = min(a.meta[2 * tid + 1], a.max_slots);
   }
   __syncthreads();
 
-  // vc[b][4 g .. 4 g + 3] = sum_s w_s O_s, slots in order
+  // vc[b][4 g .. 4 g + 3] = sum_s w_s O_s (slots in order), item (b, g) = it. The first batch of a
+  // thread's slot loads (and its query residual) goes out before the slot weights are formed.
   const int C4 = C / 4;
-  for (int item = tid; item < B * C4; item += CMB_S_THREADS) {
-    const int b = item / C4, g = item - b * C4;
-    const int ns = cnt_s[b], first = first_s[b];
+  const bool use_res = a.q_res != nullptr;
+  for (int it0 = 0; it0 < BT * C4; it0 += CMB_S_THREADS) {
+    const int it = it0 + tid;
+    const bool live = it < B * C4;
+    const int b = live ? it / C4 : 0, g = it - b * C4;
+    const int ns = live ? cnt_s[b] : 0, first = first_s[b];
+    float4 x[CMB_S_U];
+#pragma unroll
+    for (int u = 0; u < CMB_S_U; ++u)
+      x[u] = u < ns ? __ldcg(reinterpret_cast<const float4*>(a.part_o + lse_at(first + u) * C) + g)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    uint2 res = make_uint2(0u, 0u);
+    if (live && use_res)
+      res = *reinterpret_cast<const uint2*>(a.q_res + ((int64_t)b * a.H + h) * (C + a.R) + 4 * g);
+    if (it0 == 0) {
+      // slot weights exp(lse_s - lse): one warp per sequence, every LSE loaded once
+      if (warp < B) {
+        const int wn = cnt_s[warp], wf = first_s[warp];
+        float lv[CMB_S_MAXS / 32];
+        float mx = -CUDART_INF_F;
+#pragma unroll
+        for (int k = 0; k < CMB_S_MAXS / 32; ++k) {
+          const int sl = lane + 32 * k;
+          lv[k] = sl < wn ? a.part_lse[lse_at(wf + sl)] : -CUDART_INF_F;
+          mx = fmaxf(mx, lv[k]);
+        }
+        mx = warp_max(mx);
+        float tot = 0.f;
+#pragma unroll
+        for (int k = 0; k < CMB_S_MAXS / 32; ++k)
+          if (lane + 32 * k < wn) tot += expf(lv[k] - mx);
+        tot = warp_sum(tot);
+        const float l = (wn > 0) ? mx + logf(tot) : CUDART_NAN_F;
+#pragma unroll
+        for (int k = 0; k < CMB_S_MAXS / 32; ++k)
+          if (lane + 32 * k < wn) wt_s[warp * a.max_slots + lane + 32 * k] = expf(lv[k] - l);
+        if (lane == 0) lse_s[warp] = l;
+      }
+      __syncthreads();
+    }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = 0; s0 < ns; s0 += CMB_S_U) {
-      float4 x[CMB_S_U];
+      if (s0 > 0) {
 #pragma unroll
-      for (int u = 0; u < CMB_S_U; ++u)
-        x[u] = s0 + u < ns ? __ldcg(reinterpret_cast<const float4*>(a.part_o + lse_at(first + s0 + u) * C) + g)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int u = 0; u < CMB_S_U; ++u)
+          x[u] = s0 + u < ns ? __ldcg(reinterpret_cast<const float4*>(a.part_o + lse_at(first + s0 + u) * C) + g)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
 #pragma unroll
       for (int u = 0; u < CMB_S_U; ++u) {
         const float w = s0 + u < ns ? wt_s[b * a.max_slots + s0 + u] : 0.f;
@@ -344,52 +370,68 @@ __global__ void __launch_bounds__(CMB_S_THREADS, 1) combine_small_kernel(Combine
         }
       }
     }
-    if (isnan(lse_s[b])) acc = make_float4(CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F);
-    reinterpret_cast<float4*>(vc_s)[b * C4 + g] = acc;
+    if (it < BT * C4) {
+      if (!live) acc = make_float4(0.f, 0.f, 0.f, 0.f);   // sequences past B
+      else if (isnan(lse_s[b])) acc = make_float4(CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F);
+      const int bb = it / C4, col = 4 * (it - bb * C4), cpl = C / 32;
+      float* dst = vc_s + (bb * 32 + col / cpl) * CMB_S_VP + col % cpl;
+      *reinterpret_cast<float2*>(dst) = make_float2(acc.x, acc.y);
+      *reinterpret_cast<float2*>(dst + 2) = make_float2(acc.z, acc.w);
+    }
+    // vc . residual of this item, summed over the warp's 32 items (all of sequence b: C4 is a
+    // multiple of 32), in a fixed order
+    float d = 0.f;
+    if (live && use_res)
+      d = ((acc.x * __uint_as_float(res.x << 16) + acc.y * __uint_as_float(res.x & 0xFFFF0000u)) +
+           acc.z * __uint_as_float(res.y << 16)) + acc.w * __uint_as_float(res.y & 0xFFFF0000u);
+    d = warp_sum(d);
+    if (lane == 0 && live) dres_s[b][(g >> 5) & 3] = d;
   }
-  for (int i = B * C4 + tid; i < BT * C4; i += CMB_S_THREADS)   // sequences past B: zero
-    reinterpret_cast<float4*>(vc_s)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
 
-  // lse, one warp per sequence; with bf16 latent queries q_hi = q' - res the exact log-sum-exp
-  // is, to first order, lse + scale * vc . res
-  if (a.lse != nullptr && warp < B) {
-    float l = lse_s[warp];
-    if (a.q_res != nullptr) {
-      const uint16_t* res = a.q_res + ((int64_t)warp * a.H + h) * (C + a.R);
+  // lse: with bf16 latent queries q_hi = q' - res the exact log-sum-exp is, to first order,
+  // lse + scale * vc . res
+  if (a.lse != nullptr && tid < B) {
+    float l = lse_s[tid];
+    if (use_res) {
       float d = 0.f;
-      for (int c = lane; c < C; c += 32) d = fmaf(vc_s[warp * C + c], bf16_bits_to_f32(res[c]), d);
-      d = warp_sum(d);
+      for (int k = 0; k < C4 / 32; ++k) d += dres_s[tid][k];
       l += a.scale * d;
     }
-    if (lane == 0) a.lse[(int64_t)warp * a.H + h] = l;
+    a.lse[(int64_t)tid * a.H + h] = l;
   }
 
-  // out[b, h, v]: warp per row v, lane l over latent columns 16 l .. 16 l + 15 (C = 512; fewer
-  // lanes for narrower rows), merged rows of every sequence held in registers
+  // out[b, h, v]: warp per row v, lane l over latent columns cpl l .. cpl l + cpl - 1, the
+  // sequences' merged rows held in registers four at a time; the four sums meet in a
+  // transpose-reduce (lanes trade halves at distances 16 and 8, then add at 4, 2, 1)
   const int cpl = C / 32;   // columns per lane: 8 or 16
-  constexpr int BG = BT < 4 ? BT : 4;   // sequences per pass over the rows
 #pragma unroll 1
-  for (int b0 = 0; b0 < BT; b0 += BG) {
-    float vr[BG][16];
+  for (int b0 = 0; b0 < BT; b0 += 4) {
+    float2 vr[4][8];
 #pragma unroll
-    for (int b = 0; b < BG; ++b)
+    for (int b = 0; b < 4; ++b)
 #pragma unroll
-      for (int e = 0; e < 16; ++e) vr[b][e] = e < cpl ? vc_s[(b0 + b) * C + cpl * lane + e] : 0.f;
+      for (int e = 0; e < 8; ++e)
+        vr[b][e] = (b0 + b < BT && 2 * e < cpl)
+                       ? *reinterpret_cast<const float2*>(vc_s + ((b0 + b) * 32 + lane) * CMB_S_VP + 2 * e)
+                       : make_float2(0.f, 0.f);
     for (int v = warp; v < V; v += CMB_S_THREADS / 32) {
-      float w[16];
+      float2 w[8];
       if (WDT == MLA_Q8_0) {
         // the lane's columns lie in block (cpl lane) / 32, from element (cpl lane) % 32
         const int c0 = cpl * lane;
         const uint8_t* blk = w_s + v * RB + (c0 >> 5) * 34;
         const float d = __half2float(*reinterpret_cast<const __half*>(blk));
+        const float2 dd = make_float2(d, d), bias = make_float2(-8388736.0f, -8388736.0f);
         const uint16_t* c16 = reinterpret_cast<const uint16_t*>(blk + 2 + (c0 & 31));
 #pragma unroll
-        for (int e2 = 0; e2 < 8; ++e2) {
-          const uint16_t cc = e2 * 2 < cpl ? c16[e2] : 0;
-          w[2 * e2] = d * (float)(int8_t)(cc & 0xFF);
-          w[2 * e2 + 1] = d * (float)(int8_t)(cc >> 8);
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t cc = (2 * e < cpl ? (uint32_t)c16[e] : 0u) ^ 0x8080u;   // absent columns: code 0
+          w[e] = __fmul2_rn(__fadd2_rn(make_float2(__uint_as_float(__byte_perm(cc, 0x4B000000u, 0x7650u)),
+                                                   __uint_as_float(__byte_perm(cc, 0x4B000000u, 0x7651u))),
+                                       bias),
+                            dd);
         }
       } else {
         const uint4* src = reinterpret_cast<const uint4*>(w_s + v * RB + 2 * cpl * lane);
@@ -398,34 +440,40 @@ __global__ void __launch_bounds__(CMB_S_THREADS, 1) combine_small_kernel(Combine
           const uint4 u = q4 * 8 < cpl ? src[q4] : make_uint4(0, 0, 0, 0);
           const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            w[8 * q4 + 2 * e] = __uint_as_float(uw[e] << 16);
-            w[8 * q4 + 2 * e + 1] = __uint_as_float(uw[e] & 0xFFFF0000u);
-          }
+          for (int e = 0; e < 4; ++e) w[4 * q4 + e] = make_float2(__uint_as_float(uw[e] << 16), __uint_as_float(uw[e] & 0xFFFF0000u));
         }
       }
+      float y[4];
 #pragma unroll
-      for (int b = 0; b < BG; ++b) {
-        float y = 0.f;
+      for (int b = 0; b < 4; ++b) {
+        float2 y2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) y = fmaf(w[e], vr[b][e], y);
-        y = warp_sum(y);
-        if (lane == 0 && b0 + b < B) a.out[((int64_t)(b0 + b) * a.H + h) * V + v] = y;
+        for (int e = 0; e < 8; ++e) y2 = __ffma2_rn(w[e], vr[b][e], y2);
+        y[b] = y2.x + y2.y;
       }
+      const bool c = (lane & 16) != 0, dd8 = (lane & 8) != 0;
+      const float w0 = (c ? y[2] : y[0]) + __shfl_xor_sync(0xffffffffu, c ? y[0] : y[2], 16);
+      const float w1 = (c ? y[3] : y[1]) + __shfl_xor_sync(0xffffffffu, c ? y[1] : y[3], 16);
+      float z = (dd8 ? w1 : w0) + __shfl_xor_sync(0xffffffffu, dd8 ? w0 : w1, 8);
+      z += __shfl_xor_sync(0xffffffffu, z, 4);
+      z += __shfl_xor_sync(0xffffffffu, z, 2);
+      z += __shfl_xor_sync(0xffffffffu, z, 1);
+      const int bb = b0 + 2 * (int)c + (int)dd8;   // the sequence this lane's sum belongs to
+      if ((lane & 7) == 0 && bb < B) a.out[((int64_t)bb * a.H + h) * V + v] = z;
     }
   }
 }
 
 static bool combine_small_fits(const mla_config& cfg, int B, int max_slots) {
   return B >= 1 && B <= CMB_S_BMAX && (cfg.kv_b_dtype == MLA_BF16 || cfg.kv_b_dtype == MLA_Q8_0) &&
-         (cfg.kv_lora == 256 || cfg.kv_lora == 512) && cfg.v_head <= 512 && max_slots >= 1 && max_slots <= 1024;
+         (cfg.kv_lora == 256 || cfg.kv_lora == 512) && cfg.v_head <= 512 && max_slots >= 1 && max_slots <= CMB_S_MAXS;
 }
 
 template <int WDT, int BT>
 static cudaError_t launch_combine_small_bt(const CombineArgs& a, cudaStream_t st) {
   const int RB = WDT == MLA_Q8_0 ? a.C / 32 * 34 : a.C * 2;
   const size_t smem = (((size_t)a.V * RB + 15) & ~(size_t)15) +
-                      sizeof(float) * ((size_t)BT * a.C + (size_t)BT * a.max_slots + 3 * BT);
+                      sizeof(float) * ((size_t)BT * 32 * CMB_S_VP + (size_t)BT * a.max_slots + 3 * BT);
   auto k = combine_small_kernel<WDT, BT>;
   cudaError_t e = ensure_smem((const void*)k, (int)smem);
   if (e != cudaSuccess) return e;
@@ -458,7 +506,7 @@ cudaError_t launch_combine(const mla_config& cfg, const DecodePlan& plan, const 
     const int RB = cfg.kv_b_dtype == MLA_Q8_0 ? cfg.kv_lora / 32 * 34 : cfg.kv_lora * 2;
     const int bt = B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : 8;
     const size_t smem = (((size_t)cfg.v_head * RB + 15) & ~(size_t)15) +
-                        sizeof(float) * ((size_t)bt * cfg.kv_lora + (size_t)bt * a.max_slots + 3 * bt);
+                        sizeof(float) * ((size_t)bt * 32 * CMB_S_VP + (size_t)bt * a.max_slots + 3 * bt);
     if (smem <= 227 * 1024)
       return cfg.kv_b_dtype == MLA_Q8_0 ? launch_combine_small<MLA_Q8_0>(a, st) : launch_combine_small<MLA_BF16>(a, st);
   }
