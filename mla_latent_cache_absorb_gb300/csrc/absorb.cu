@@ -43,26 +43,33 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
   float* red_s = q_s + bchunk * N;          // [4][bchunk][ABS_COLS] partial sums over nope quarters
   const int tid = threadIdx.x;
 
-  // Loads of the first pass go out together: this thread's q_pe pair (the head's B*R/2 pairs
-  // are shared out over the CTAs of the head), its q_nope elements of the first sequence chunk,
-  // then the W_UK slice; nothing waits for a load before all of them are in flight.
+  // The W_UK slice is staged before the dependency wait; after it, this thread's q_pe pair (the
+  // head's B*R/2 pairs are shared out over the CTAs of the head) and its q_nope elements of the
+  // first sequence chunk go out together.
   const int n_pairs = B * (R / 2);
   const int pair0 = blockIdx.y * ABS_THREADS + tid;
   const int pair_stride = gridDim.y * ABS_THREADS;
   float px0 = 0.f, px1 = 0.f;
   int ppos = 0;
   double pinv = 0.0;
+  if (pair0 < n_pairs && positions != nullptr) {
+    const int b = pair0 / (R / 2), p = pair0 % (R / 2);
+    ppos = positions[b / pos_t] + b % pos_t;
+    pinv = cfg.rope_inv_freq[p];
+  }
+  const int64_t wrow0 = (int64_t)h * (N + V);
+  stage_kv_b_rows(w_s, ABS_COLS, kv_b, cfg.kv_b_dtype, wrow0, N, c0, min(ABS_COLS, C - c0), C, ABS_THREADS,
+                  (int64_t)cfg.n_heads * (cfg.qk_nope + cfg.v_head));
+  // q may be written by a kernel two or more launches back (the front end): every read of it
+  // comes after the wait for the previous kernel, which completes only after that one's own wait
+  pdl_wait();
   if (pair0 < n_pairs) {
     const int b = pair0 / (R / 2), p = pair0 % (R / 2);
     const int64_t qi = ((int64_t)b * H + h) * qrow + N + 2 * p;
     px0 = Act<DT>::load(q, qi);
     px1 = Act<DT>::load(q, qi + 1);
-    if (positions != nullptr) {
-      ppos = positions[b / pos_t] + b % pos_t;
-      pinv = cfg.rope_inv_freq[p];
-    }
   }
-  constexpr int QPRE = 16;                  // q_nope elements prefetched per thread
+  constexpr int QPRE = 16;                  // q_nope elements loaded together per thread
   const int nb0 = min(ABS_BCHUNK, B);
   float qv[QPRE];
 #pragma unroll
@@ -71,10 +78,6 @@ absorb_kernel(mla_config cfg, const typename Act<DT>::T* __restrict__ q, const v
     qv[u] = 0.f;
     if (i < nb0 * N) qv[u] = Act<DT>::load(q, ((int64_t)(i / N) * H + h) * qrow + i % N);
   }
-  const int64_t wrow0 = (int64_t)h * (N + V);
-  stage_kv_b_rows(w_s, ABS_COLS, kv_b, cfg.kv_b_dtype, wrow0, N, c0, min(ABS_COLS, C - c0), C, ABS_THREADS,
-                  (int64_t)cfg.n_heads * (cfg.qk_nope + cfg.v_head));
-  pdl_wait();   // the fused query rows may still be read by the previous step's attention
 
   // q_pe: rotate at positions[b] (or copy when positions == NULL) into the row's tail
   for (int i = pair0; i < n_pairs; i += pair_stride) {

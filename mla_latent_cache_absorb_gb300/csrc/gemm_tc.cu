@@ -99,6 +99,9 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
     for (int cb = 0; cb < 4; ++cb)
       tc::tma_load_2d(ws + cb * 16384, &w_map, 256 * lh + 64 * cb, h * (a.N + a.V), &bar_w);
   }
+  // q may be written by a kernel two or more launches back (the front end): every read of it
+  // comes after the wait for the previous kernel, which completes only after that one's own wait
+  pdl_wait();
   // q_nope rows of this batch chunk, 128-byte swizzled, zero rows past the batch (all of a
   // thread's loads are issued before its first store)
   {
@@ -139,7 +142,6 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap w_map, AbsorbTcArgs a) {
     }
     tc::mma_commit(&bar_mma);   // arrives once every MMA issued above has completed
   }
-  pdl_wait();   // the fused query rows may still be read by the previous step's attention
   // rotated q_pe into the row's tail, while the MMAs run: the batch chunk's pairs are shared
   // by the CTAs of the two latent halves; a thread loads all of its pairs (and positions)
   // before using any
