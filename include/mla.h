@@ -173,9 +173,11 @@ typedef struct mla_plan_info {
                               a cluster of two CTAs shares each 64-row tile, one latent half
                               each; `splits` then counts CTA pairs,
                               3 = one launch for tiny batches (bf16, one query row per
-                              sequence, B * H <= 64, H <= 32): absorb, attention over 32-row
-                              chunks, merge and W_UV in a single grid separated by grid-wide
-                              barriers; `splits` then counts the grid's CTAs */
+                              sequence, B * H <= 64, H <= 32, capacity <= 8192, and few
+                              enough chunks and heads that the grid takes them in about one
+                              round): absorb, attention over 32-row chunks, merge and W_UV
+                              in a single grid separated by grid-wide barriers; `splits`
+                              then counts the grid's CTAs */
   int32_t heads_per_cta;   /* heads that share each staged row tile (kernel 2: per CTA pair) */
   int32_t head_groups;     /* ceil(H / heads_per_cta) */
   int32_t splits;          /* row splits per sequence (partials kept in the workspace) */

@@ -637,25 +637,42 @@ __global__ void __launch_bounds__(SM_THREADS, 1) decode_small_kernel(const __gri
 
 }  // namespace
 
-bool decode_small_supported(const mla_config& cfg, int B, int tokens) {
-  const int64_t cap = cfg.page_size == 0 ? cfg.rows_per_seq : (int64_t)cfg.max_pages_per_seq * cfg.page_size;
-  return tokens == 1 && cfg.act_dtype == MLA_BF16 && cfg.kv_b_dtype == MLA_BF16 && B >= 1 &&
-         (int64_t)B * cfg.n_heads <= 64 && cfg.n_heads <= SM_WARPS * SM_MAX_HPW && cfg.kv_lora % 128 == 0 &&
-         cfg.kv_lora <= 32 * SM_MAX_CPL && (cfg.kv_lora + cfg.qk_rope) % 8 == 0 && cfg.qk_rope % 2 == 0 &&
-         cfg.qk_rope <= 64 && cfg.qk_rope % 16 == 0 && cfg.qk_nope % 4 == 0 && cfg.qk_nope <= 128 &&
-         cfg.v_head % 16 == 0 && cfg.v_head <= 128 && cap >= 1 && cap <= (int64_t)SM_CHUNK * SM_MAX_CHUNKS;
-}
-
 int64_t decode_small_max_chunks(const mla_config& cfg) {
   const int64_t cap = cfg.page_size == 0 ? cfg.rows_per_seq : (int64_t)cfg.max_pages_per_seq * cfg.page_size;
   return (cap + SM_CHUNK - 1) / SM_CHUNK;
 }
 
-// CTAs of the grid: one per chunk of the longest batch, at most one per SM.
+// CTAs of the grid: one per chunk of the longest batch or per absorb / merge item (sequence, head,
+// 64 latent columns), whichever is more, at most one per SM.
 int decode_small_grid(const mla_config& cfg, int B) {
   const int sms = device_sms();
   const int64_t chunks = (int64_t)B * decode_small_max_chunks(cfg);
-  return (int)(chunks < sms ? chunks : sms);
+  const int64_t items = (int64_t)B * cfg.n_heads * (cfg.kv_lora / 64);
+  const int64_t want = chunks > items ? chunks : items;
+  return (int)(want < sms ? want : sms);
+}
+
+bool decode_small_supported(const mla_config& cfg, int B, int tokens) {
+  const int64_t cap = cfg.page_size == 0 ? cfg.rows_per_seq : (int64_t)cfg.max_pages_per_seq * cfg.page_size;
+  const bool dims = tokens == 1 && cfg.act_dtype == MLA_BF16 && cfg.kv_b_dtype == MLA_BF16 && B >= 1 &&
+                    (int64_t)B * cfg.n_heads <= 64 && cfg.n_heads <= SM_WARPS * SM_MAX_HPW &&
+                    cfg.kv_lora % 128 == 0 && cfg.kv_lora <= 32 * SM_MAX_CPL &&
+                    (cfg.kv_lora + cfg.qk_rope) % 8 == 0 && cfg.qk_rope <= 64 && cfg.qk_rope % 16 == 0 &&
+                    cfg.qk_nope % 4 == 0 && cfg.qk_nope <= 128 && cfg.v_head % 16 == 0 && cfg.v_head <= 128 &&
+                    cap >= 1 && cap <= (int64_t)SM_CHUNK * SM_MAX_CHUNKS;
+  if (!dims) return false;
+  const int G = decode_small_grid(cfg, B);
+  if (G < 1) return false;
+  // Against the staged kernels with the tensor-core attention (rows of 512 + 64), the one launch
+  // wins while its CTAs take few rounds: measured on one GB300 it takes ~14.6 us with one round
+  // of absorb / merge items and one of 32-row chunks, ~4.6 us more per further round of items and
+  // ~3.3 us per further round of chunks, against ~21-25 us staged. Otherwise (the staged path's
+  // CUDA-core attention) it is always the faster.
+  const int64_t items = (int64_t)B * cfg.n_heads * (cfg.kv_lora / 64);
+  const int64_t chunks = (int64_t)B * decode_small_max_chunks(cfg);
+  const int64_t rounds = (items + G - 1) / G + (chunks + G - 1) / G;
+  const bool staged_tc = cfg.kv_lora == 512 && cfg.qk_rope == 64;
+  return !staged_tc || rounds <= 3;
 }
 
 cudaError_t launch_decode_small(const mla_config& cfg, const mla_cache& cache, const void* q, const void* kv_b,

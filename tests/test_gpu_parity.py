@@ -181,8 +181,12 @@ def test_identity_page_table_equals_contiguous():
 @gpu
 def test_batched_slice_equals_single_sequence():
     # each sequence of a batch of identical sequences matches the same sequence run alone
-    # (the split plan depends on B, so agreement is to float32 reassociation, not bits)
+    # (the split plan depends on B, so agreement is to float32 reassociation, not bits; when the
+    # planner hands the single sequence to the one-launch path and the batch to the staged
+    # kernels, agreement is to the two paths' parity tolerance)
     need_gpu()
+    from mla_latent_cache_absorb_gb300 import binding as L
+    from mla_latent_cache_absorb_gb300.runner import DeviceStep
     wl = W["v2lite_b1_t4096"].with_(B=1, context=("fixed", 500))
     prob1 = synth.make_problem(wl)
     _, o1, l1, _ = run_gpu(prob1)
@@ -196,8 +200,11 @@ def test_batched_slice_equals_single_sequence():
     prob3.seq_lens = np.repeat(prob1.seq_lens, 3)
     prob3.kva_rows = np.concatenate([prob1.kva_rows] * 3, axis=0)
     _, o3, l3, _ = run_gpu(prob3)
+    k1 = L.mla_decode_plan(DeviceStep(prob1).cfg, 1)[1].kernel
+    k3 = L.mla_decode_plan(DeviceStep(prob3).cfg, 3)[1].kernel
+    to, tl = (1e-5, 1e-5) if (k1 == 3) == (k3 == 3) else (OUT_TOL, LSE_TOL)
     for b in range(3):
-        assert max_rel(o3[b], o1[0]) <= 1e-5 and np.max(np.abs(l3[b] - l1[0])) <= 1e-5
+        assert max_rel(o3[b], o1[0]) <= to and np.max(np.abs(l3[b] - l1[0])) <= tl
     assert np.array_equal(o3[0], o3[1]) and np.array_equal(o3[1], o3[2])
 
 

@@ -1,8 +1,9 @@
 """The one-launch decode for tiny batches (plan kernel 3: absorb, attention over 32-row chunks,
 merge and W_UV in one grid with grid-wide barriers) against the fp64 oracle: ragged lengths
-(chunks with fewer than 32 rows, one-row sequences), several sequences sharing the grid,
-B x H at its limit, 32 heads (four heads per warp), paged caches, and the pre-rotated q_pe
-path. The full-size one-sequence workload runs through it in test_gpu_parity."""
+(chunks with fewer than 32 rows, one-row sequences), several sequences sharing the grid, CTAs
+that take two chunks or two absorb / merge items, 32 heads (four heads per warp, two 16-head
+tensor-core tiles), a 256-wide latent, paged caches. The full-size one-sequence workload runs
+through it in test_gpu_parity. Each case is one the planner hands to the one-launch path."""
 import numpy as np
 import pytest
 
@@ -14,12 +15,13 @@ W = synth.WORKLOADS
 V2 = W["v2lite_b1_t4096"]
 
 CASES = [
-    ("b2_ragged", V2.with_(B=2, context=("uniform", 1, 700))),
-    ("b4_limit", V2.with_(B=4, context=("uniform", 30, 2000))),          # B x H = 64
+    ("b2_ragged", V2.with_(B=2, context=("uniform", 1, 700))),            # two rounds of items
+    ("b4_h4", V2.with_(B=4, H=4, context=("uniform", 30, 2000))),         # two rounds of chunks
     ("one_row", V2.with_(B=1, context=("fixed", 0))),                     # L = 1: one short chunk
     ("exact_chunks", V2.with_(B=1, context=("fixed", 255))),              # L = 256: 8 full chunks
-    ("h32_b2", W["v3_b32_t4096"].with_(B=2, H=32, context=("fixed", 1000))),
-    ("paged_b3", W["ragged_paged_b64"].with_(B=3, H=16, context=("uniform", 1, 900))),
+    ("h32", W["v3_b32_t4096"].with_(B=1, H=32, context=("fixed", 1000))),
+    ("h32_c256", V2.with_(B=1, H=32, C=256, context=("fixed", 700))),
+    ("paged_b3", W["ragged_paged_b64"].with_(B=3, H=8, context=("uniform", 1, 900))),
 ]
 
 
@@ -48,7 +50,7 @@ def test_one_launch_batch_slice_equals_single_sequence():
     for bit."""
     need_gpu()
     from mla_latent_cache_absorb_gb300.runner import DeviceStep
-    wl = V2.with_(B=1, context=("fixed", 777))
+    wl = V2.with_(B=1, H=8, context=("fixed", 777))
     prob1 = synth.make_problem(wl)
     assert _plan(DeviceStep(prob1), 1).kernel == 3
     _, o1, l1, _ = run_gpu(prob1)
