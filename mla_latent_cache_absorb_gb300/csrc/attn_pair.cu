@@ -25,7 +25,7 @@
 //
 // Softmax: two threads per head (heads are the MMA rows; each thread holds 32 of the tile's 64
 // scores of its head), log2 domain, with a running maximum that is only raised when a score
-// exceeds it by more than 2^8; then the output rows of that head are rescaled in both CTAs (the
+// exceeds it by more than 2^16; then the output rows of that head are rescaled in both CTAs (the
 // rescale factor travels with the probabilities).
 //
 // Work split: the 64-row tiles of all sequences form one list; pair k takes the k-th equal share
@@ -81,7 +81,10 @@ constexpr uint32_t AP_S_COL = 0;     // S: two buffers of 64 columns
 constexpr uint32_t AP_Q_COL = 128;   // latent queries: 128 columns of bf16 pairs (256 latent)
 constexpr uint32_t AP_O_COL = 256;   // O: 256 columns
 constexpr uint32_t AP_TMEM_COLS = 512;
-constexpr float AP_RESCALE = 8.0f;   // log2 units: p may reach 2^8 before a rescale
+// log2 units: p may reach 2^16 before a rescale (bf16 P and the float32 sums hold that with room
+// to spare: at most 2^16 x 2^17 rows x |v| per sum); at 2^8 the YaRN-scaled scores of the long
+// Q8_0 workload crossed it on a tenth of the tiles, each costing a wait for PV and an O rescale
+constexpr float AP_RESCALE = 16.0f;
 constexpr uint64_t AP_DRAIN = kWaitDrainNs;
 // named barriers: own-head softmax threads (128), score senders (64), factor receivers (64)
 constexpr int AP_BAR_OWN = 1, AP_BAR_SEND = 2, AP_BAR_RECV = 3;

@@ -18,7 +18,7 @@
 //
 // Softmax: one thread per tile row in each of one or two warpgroups (HG = 64: two, each owning
 // 32 heads, so two warps share every SM sub-partition), log2 domain, with a per-head running
-// maximum that is only raised when a score exceeds it by more than 2^8: the exact column max
+// maximum that is only raised when a score exceeds it by more than 2^16: the exact column max
 // (a cross-thread reduction) and the rescale of O^T in TMEM happen on the first tile of a
 // segment and on those rare tiles only. Each thread keeps per-head partial sums of p; they are
 // reduced once per segment.
@@ -81,7 +81,7 @@ struct Cfg {
   }
 };
 constexpr int TC_HG_MAX = 64;
-constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: p may reach 2^8 before a rescale
+constexpr float RESCALE_THRESHOLD = 16.0f;  // log2 units: p may reach 2^16 before a rescale
 
 struct TcArgs {
   RowMap map;
