@@ -233,22 +233,28 @@ __device__ __forceinline__ uint32_t swz(uint32_t hl, uint32_t k, uint32_t row_by
 
 // Latent queries of head lane `h` of sequence `sb`: latent columns [col0, col0 + 64 nblk) of this
 // CTA's half into tensor-memory columns t_q + col0 / 2 onwards (bf16 pairs, 32 columns a store).
-// Warp-collective (tcgen05.st).
+// Two 64-column blocks (256 bytes) per thread are in flight at once, so the whole load costs one
+// memory round trip per pair of blocks (nblk even). Warp-collective (tcgen05.st).
 __device__ __forceinline__ void load_q_lat(const PairArgs& a, uint32_t c, int sb, int h, int col0, int nblk,
                                            uint32_t t_q) {
   const uint4* src =
       reinterpret_cast<const uint4*>(a.q_abs + ((size_t)sb * AP_HEADS + h) * 576 + 256 * c + col0);
-  for (int bi = 0; bi < nblk; ++bi) {
-    uint32_t r[32];
+  for (int bi = 0; bi < nblk; bi += 2) {
+    uint4 v[16];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint4 v = src[8 * bi + i];
-      r[4 * i] = v.x;
-      r[4 * i + 1] = v.y;
-      r[4 * i + 2] = v.z;
-      r[4 * i + 3] = v.w;
+    for (int i = 0; i < 16; ++i) v[i] = src[8 * bi + i];
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+      uint32_t r[32];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        r[4 * i] = v[8 * hb + i].x;
+        r[4 * i + 1] = v[8 * hb + i].y;
+        r[4 * i + 2] = v[8 * hb + i].z;
+        r[4 * i + 3] = v[8 * hb + i].w;
+      }
+      tc::tmem_st32(t_q + (uint32_t)(col0 / 2 + 32 * (bi + hb)), r);
     }
-    tc::tmem_st32(t_q + (uint32_t)(col0 / 2 + 32 * bi), r);
   }
 }
 
@@ -618,11 +624,13 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
         uint32_t r[32];
         tc::tmem_ld32(t_o + cb, r);
         tc::tmem_wait_ld();
+        // a lane writes its own head's row: one 32-byte sector per store
 #pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          *reinterpret_cast<float4*>(po + cb + j) =
-              make_float4(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv,
-                          __uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv);
+        for (int j = 0; j < 32; j += 8)
+          tc::st_global_v8(po + cb + j, __uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv,
+                           __uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv,
+                           __uint_as_float(r[j + 4]) * inv, __uint_as_float(r[j + 5]) * inv,
+                           __uint_as_float(r[j + 6]) * inv, __uint_as_float(r[j + 7]) * inv);
       }
     };
     // this thread's share of the latent queries of sequence qb (own heads: half of the 256
@@ -673,12 +681,6 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
           tc::tmem_wait_ld();
           tc::tc_fence_before();
           tc::mbar_arrive(&s.s_free[b]);
-          if (last) {
-            // QK^T of the segment is complete: its latent queries may be replaced by the next one's
-            PairSegIter pk = it;
-            int qb, x0, x1;
-            if (pk.next(a, &qb, &x0, &x1)) queries(qb);
-          }
           if (nvalid < AP_TILE) {
             // rows past the sequence: zero this CTA's latent columns of them, so that
             // 0 * (stale or NaN) cannot reach O (QK^T of the tile has completed: s_full above)
@@ -766,6 +768,12 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
           tc::tc_fence_before();
           tc::mbar_arrive(&s.pv_ready[b]);
           if (last) {
+            // QK^T of the segment completed before its last scores were read: the latent queries
+            // may be replaced by the next segment's, off the path of this tile's probabilities and
+            // overlapping the wait for its PV
+            PairSegIter pk = it;
+            int qb, x0, x1;
+            if (pk.next(a, &qb, &x0, &x1)) queries(qb);
             // ---- epilogue of the segment: this head's lse and its half of O ----
             s.xch[k][hl] = l;
             group_bar(AP_BAR_OWN, AP_N_OWN);
@@ -827,11 +835,6 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
           tc::tmem_wait_ld();
           tc::tc_fence_before();
           tc::mbar_arrive(&s.s_free[b]);
-          if (t + 1 == thi) {
-            PairSegIter pk = it;
-            int qb, x0, x1;
-            if (pk.next(a, &qb, &x0, &x1)) queries(qb);
-          }
           // the peer has read what we sent into this buffer two tiles ago (and so the bulk copy
           // out of our staging buffer b has completed)
           if (n >= 2 && !group_wait(s, &s.srecv_grant[b], (uint32_t)(((n >> 1) - 1) & 1), AP_BAR_SEND, AP_N_SEND,
@@ -853,6 +856,13 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
           if (hl == 0)
             tc::bulk_s2s(pr_srecv + b * AP_SBUF, tc::smem_u32(sbuf), AP_SBUF, pr_srecv_full + 8 * b);
           ++n_sent;
+          if (t + 1 == thi) {
+            // the segment's QK^T is complete (its last scores are read): load the next one's
+            // queries once this tile's scores are on their way to the peer
+            PairSegIter pk = it;
+            int qb, x0, x1;
+            if (pk.next(a, &qb, &x0, &x1)) queries(qb);
+          }
         }
         if (!ok) break;
         ++seg;
