@@ -312,8 +312,9 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
         tc::mbar_init(&s.full[i], 1);
         tc::mbar_init(&s.empty[i], 1);
       }
-      // the latent queries from the own-head and score-sender threads, the rope queries by TMA
-      tc::mbar_init(&s.q_full, AP_N_OWN + AP_N_SEND + 1);
+      // the latent queries from the own-head, score-sender and receiver threads, the rope queries
+      // by TMA
+      tc::mbar_init(&s.q_full, AP_N_OWN + AP_N_SEND + AP_N_RECV + 1);
       tc::mbar_init(&s.q_empty, 1);
       for (int i = 0; i < 2; ++i) {
         tc::mbar_init(&s.s_full[i], 1);
@@ -435,8 +436,10 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
       };
       while (ok && it.next(a, &sb, &tlo, &thi)) {
         fail_b = sb;
-        const bool defer_q = a.kv_early && seg == 0;
-        if (!defer_q && !load_q()) { ok = false; break; }
+        // A segment's rope queries replace the previous segment's once its last QK^T is done
+        // (q_empty); that wait comes after the segment's first tile is on its way, so that the
+        // tile's load overlaps the end of the previous segment instead of following it.
+        bool q_pending = true;
         for (int t = tlo; t < thi && ok; ++t) {
           const int st = (int)(n % AP_STAGES);
           // the row lookup (a page-table read) goes before the wait for a free stage, which
@@ -457,8 +460,9 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
           tc::tma_load_3d_hint(dst, &rows_map, 0, (int32_t)pr, 4 * (int)c, &s.full[st], kv_policy);
           tc::tma_load_2d_hint(dst + 4 * AP_BLK, &rope_map, 512 + 32 * (int)c, (int32_t)pr, &s.full[st], kv_policy);
           last_n[st] = n;
-          if (defer_q && t == tlo) {
-            pdl_wait();
+          if (q_pending) {
+            q_pending = false;
+            if (a.kv_early && seg == 0) pdl_wait();
             if (!load_q()) ok = false;
           }
           if (ok) ++n;
@@ -633,14 +637,22 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
                            __uint_as_float(r[j + 6]) * inv, __uint_as_float(r[j + 7]) * inv);
       }
     };
-    // this thread's share of the latent queries of sequence qb (own heads: half of the 256
-    // columns each; score senders: all of them), then arrival on q_full
+    // The next segment's latent queries of this thread into L2 while this segment runs (the
+    // lines that `queries` below loads at its end).
+    auto prefetch_next = [&]() {
+      PairSegIter pk = it;
+      int qb, x0, x1;
+      if (!pk.next(a, &qb, &x0, &x1)) return;
+      const char* p = reinterpret_cast<const char*>(a.q_abs + ((size_t)qb * AP_HEADS + h) * 576 + 256 * c + 128 * set);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p + 128));
+    };
+    // this thread's share of the latent queries of sequence qb, then arrival on q_full: half of
+    // its head's 256 columns (the two warps on each lane quarter split them by `set`)
     auto queries = [&](int qb) {
       __syncwarp();
-      if (own)
-        load_q_lat(a, c, qb, h, 128 * set, 2, t_q);
-      else
-        load_q_lat(a, c, qb, h, 0, 4, t_q);
+      tc::tc_fence_after();
+      load_q_lat(a, c, qb, h, 128 * set, 2, t_q);
       tc::tmem_wait_st();
       tc::tc_fence_before();
       tc::mbar_arrive(&s.q_full);
@@ -667,6 +679,7 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
         const long long L = a.seq_lens[sb];
         m = -CUDART_INF_F;
         l = 0.f;
+        prefetch_next();
         for (int t = tlo; t < thi; ++t, ++n) {
           const bool first = t == tlo, last = t + 1 == thi;
           const int b = (int)(n & 1);
@@ -822,6 +835,7 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
       }
       while (ok && it.next(a, &sb, &tlo, &thi)) {
         fail_b = sb;
+        prefetch_next();
         for (int t = tlo; t < thi; ++t, ++n) {
           const int b = (int)(n & 1);
           if (!group_wait(s, &s.s_full[b], (uint32_t)((n >> 1) & 1), AP_BAR_SEND, AP_N_SEND, a.wait_ns)) {
@@ -872,8 +886,14 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
     } else {
       // ---------------- the peer's head h: its rescale factors, epilogue ----------------
       int n_got = 0, l_got = 0;
+      {
+        PairSegIter pk = it;
+        int qb, x0, x1;
+        if (pk.next(a, &qb, &x0, &x1)) queries(qb);
+      }
       while (ok && it.next(a, &sb, &tlo, &thi)) {
         fail_b = sb;
+        prefetch_next();
         for (int t = tlo; t < thi; ++t, ++n) {
           const bool last = t + 1 == thi;
           const int b = (int)(n & 1);
@@ -900,6 +920,11 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
           tc::tc_fence_before();
           tc::mbar_arrive(&s.pv_ready[b]);
           if (last) {
+            // The peer's probabilities of this tile came from this CTA's scores of it, so the
+            // segment's QK^T has completed: the second half of the next segment's queries.
+            PairSegIter pk = it;
+            int qb, x0, x1;
+            if (pk.next(a, &qb, &x0, &x1)) queries(qb);
             // ---- epilogue of the segment for the peer's head: its 1/l comes from the peer ----
             if (!group_wait(s, &s.o_full, (uint32_t)(seg & 1), AP_BAR_RECV, AP_N_RECV, a.wait_ns)) {
               ok = false;
