@@ -28,8 +28,8 @@
 // exceeds it by more than 2^16; then the output rows of that head are rescaled in both CTAs (the
 // rescale factor travels with the probabilities).
 //
-// Work split: the 64-row tiles of all sequences form one list; pair k takes the k-th equal share
-// of it, crossing sequence boundaries. Each (pair, sequence) piece writes a partial (O normalised,
+// Work split: the 64-row tiles of all sequences form one list, with a few units of switch cost
+// ahead of each sequence; pair k takes the k-th equal share of it, crossing sequence boundaries. Each (pair, sequence) piece writes a partial (O normalised,
 // lse) into slot k + b; CTA c writes latent columns [256c, 256c + 256) of every head and the lse
 // of its own heads.
 //
@@ -201,7 +201,19 @@ __device__ __forceinline__ long long seq_tiles(const PairArgs& a, int b) {
   return (L + AP_TILE - 1) / AP_TILE;
 }
 
-// Segment iterator over the (sequence, tile range) pieces of a pair's share.
+// The work list the pairs share is measured in tiles, plus AP_SEG_COST units ahead of each
+// sequence: a pair that starts a new sequence within its share pays for the switch (the next
+// queries, the previous segment's epilogue, a cold exchange chain: ~5 us, ~3 tiles' time), so
+// it takes that many fewer tiles and the pairs end closer together. Sequence b occupies
+// [v_b, v_b + AP_SEG_COST + n_b) of the list, its tiles the last n_b units of that.
+constexpr long long AP_SEG_COST = 3;
+__device__ __forceinline__ long long seq_width(const PairArgs& a, int b) {
+  const long long n = seq_tiles(a, b);
+  return n > 0 ? n + AP_SEG_COST : 0;
+}
+
+// Segment iterator over the (sequence, tile range) pieces of a pair's share [r0, r1) of the
+// work list; p is the list position where sequence b starts.
 struct PairSegIter {
   int b;
   long long p;
@@ -209,15 +221,15 @@ struct PairSegIter {
   __device__ bool next(const PairArgs& a, int* sb, int* t_lo, int* t_hi) {
     while (b < a.B && p < r1) {
       const long long n = seq_tiles(a, b);
-      const long long lo = max(r0, p), hi = min(r1, p + n);
+      const long long p_t = p + AP_SEG_COST;   // list position of the sequence's first tile
+      const long long lo = max(r0, p_t), hi = min(r1, p_t + n);
       const int cur = b;
-      const long long pb = p;
       ++b;
-      p += n;
+      p += n > 0 ? n + AP_SEG_COST : 0;
       if (hi > lo) {
         *sb = cur;
-        *t_lo = (int)(lo - pb);
-        *t_hi = (int)(hi - pb);
+        *t_lo = (int)(lo - p_t);
+        *t_hi = (int)(hi - p_t);
         return true;
       }
     }
@@ -277,11 +289,11 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
   const uint32_t peer = c ^ 1u;
   const int pair = blockIdx.x >> 1;
 
-  // ---- total tile count (block scan over per-thread chunks of sequences) ----
+  // ---- length of the work list (block scan over per-thread chunks of sequences) ----
   const int chunk = (a.B + AP_THREADS - 1) / AP_THREADS;
   const int cb0 = min(a.B, tid * chunk), cb1 = min(a.B, cb0 + chunk);
   long long mine = 0;
-  for (int b = cb0; b < cb1; ++b) mine += seq_tiles(a, b);
+  for (int b = cb0; b < cb1; ++b) mine += seq_width(a, b);
   long long incl = mine;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -350,11 +362,11 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
       tc::tma_prefetch_desc(&qres_map);
     }
   }
-  // the thread whose chunk holds tile r0 finds the first sequence of the pair's share
+  // the thread whose chunk holds list position r0 finds the first sequence of the pair's share
   if (r0 < r1 && before <= r0 && r0 < before + mine) {
     long long p = before;
     for (int b = cb0; b < cb1; ++b) {
-      const long long n = seq_tiles(a, b);
+      const long long n = seq_width(a, b);
       if (r0 < p + n) {
         s.seg_b0 = b;
         s.seg_p0 = p;
@@ -364,15 +376,18 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
     }
   }
   if (!a.kv_early) pdl_wait();
-  // CTA 0 of pair 0 publishes, per sequence, which partial slots the combine must merge
+  // CTA 0 of pair 0 publishes, per sequence, which partial slots the combine must merge: those
+  // of the pairs whose shares hold the sequence's first tile (list position x) to its last
+  // (x + n - 1); pair k holds [T k / n_pairs, T (k + 1) / n_pairs)
   if (blockIdx.x == 0) {
     long long p = before;
     for (int b = cb0; b < cb1; ++b) {
       const long long n = seq_tiles(a, b);
       int first = 0, count = 0;
       if (n > 0) {
-        const long long kf = ((p + 1) * a.n_pairs + T - 1) / T - 1;
-        const long long kl = ((p + n) * a.n_pairs + T - 1) / T - 1;
+        const long long x = p + AP_SEG_COST;
+        const long long kf = ((x + 1) * a.n_pairs + T - 1) / T - 1;
+        const long long kl = ((x + n) * a.n_pairs + T - 1) / T - 1;
         first = (int)(kf + b);
         count = (int)(kl - kf + 1);
       } else {
@@ -380,7 +395,7 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
       }
       a.meta[2 * b] = first;
       a.meta[2 * b + 1] = count;
-      p += n;
+      p += seq_width(a, b);
     }
   }
   if (r0 >= r1) {
@@ -390,9 +405,10 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
     if (c == 0 && before <= r0 && r0 < before + mine) {
       long long p = before;
       for (int b = cb0; b < cb1; ++b) {
-        const long long n = seq_tiles(a, b);
+        const long long n = seq_width(a, b);
         if (r0 < p + n) {
-          if (p < r0) {
+          // an empty share strictly inside the sequence's tiles lies in its slot interval
+          if (p + AP_SEG_COST < r0) {
             float* pl = a.part_lse + (size_t)(pair + b) * AP_HEADS;
             for (int h = 0; h < AP_HEADS; ++h) pl[h] = -CUDART_INF_F;
           }
