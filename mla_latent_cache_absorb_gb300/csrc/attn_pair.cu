@@ -203,10 +203,11 @@ __device__ __forceinline__ long long seq_tiles(const PairArgs& a, int b) {
 
 // The work list the pairs share is measured in tiles, plus AP_SEG_COST units ahead of each
 // sequence: a pair that starts a new sequence within its share pays for the switch (the next
-// queries, the previous segment's epilogue, a cold exchange chain: ~5 us, ~3 tiles' time), so
-// it takes that many fewer tiles and the pairs end closer together. Sequence b occupies
+// queries, the previous segment's epilogue, a cold exchange chain: ~5-7 us), so it takes that
+// many fewer tiles and the pairs end closer together (3, 4 and 5 units measured: 4 was best).
+// Sequence b occupies
 // [v_b, v_b + AP_SEG_COST + n_b) of the list, its tiles the last n_b units of that.
-constexpr long long AP_SEG_COST = 3;
+constexpr long long AP_SEG_COST = 4;
 __device__ __forceinline__ long long seq_width(const PairArgs& a, int b) {
   const long long n = seq_tiles(a, b);
   return n > 0 ? n + AP_SEG_COST : 0;
