@@ -205,8 +205,7 @@ __device__ __forceinline__ long long seq_tiles(const PairArgs& a, int b) {
 // sequence: a pair that starts a new sequence within its share pays for the switch (the next
 // queries, the previous segment's epilogue, a cold exchange chain: ~5-7 us), so it takes that
 // many fewer tiles and the pairs end closer together (3, 4 and 5 units measured: 4 was best).
-// Sequence b occupies
-// [v_b, v_b + AP_SEG_COST + n_b) of the list, its tiles the last n_b units of that.
+// Sequence b occupies [v_b, v_b + AP_SEG_COST + n_b) of the list, its tiles the last n_b units.
 constexpr long long AP_SEG_COST = 4;
 __device__ __forceinline__ long long seq_width(const PairArgs& a, int b) {
   const long long n = seq_tiles(a, b);
