@@ -29,21 +29,21 @@
 // rescale factor travels with the probabilities).
 //
 // Work split: the 64-row tiles of all sequences form one list, with a few units of switch cost
-// ahead of each sequence; pair k takes the k-th equal share of it, crossing sequence boundaries. Each (pair, sequence) piece writes a partial (O normalised,
-// lse) into slot k + b; CTA c writes latent columns [256c, 256c + 256) of every head and the lse
-// of its own heads.
+// ahead of each sequence; pair k takes the k-th equal share of it, crossing sequence boundaries.
+// Each (pair, sequence) piece writes a partial (O normalised, lse) into slot k + b; CTA c writes
+// latent columns [256c, 256c + 256) of every head and the lse of its own heads.
 //
 // Roles (384 threads). Warps 0-7 access tensor memory, warp w the lane quarter w mod 4 (32 heads):
 // on this CTA's own heads, warps of both sets run the softmax (one half of the tile's rows each)
 // and the epilogue of those heads; on the peer's heads, warps 0-3 send this CTA's partial scores
 // and warps 4-7 take the peer's rescale factors, rescale those heads' output rows and write their
-// epilogue. The own-head warps and the score senders also load each segment's latent queries
-// into tensor memory. Of warps 8-11, one issues the TMA loads and one owns tensor memory and
+// epilogue. All eight warps also load each segment's latent queries into tensor memory (half of
+// a head's columns each). Of warps 8-11, one issues the TMA loads and one owns tensor memory and
 // issues the MMAs (one thread), polling and issuing whichever of the next QK^T and the next PV is
 // ready; both sit on the sub-partitions of the peer-head warps. A third forwards the score grants
-// to the peer, so that no softmax thread waits on a remote arrival. Every wait is bounded; on a timeout the CTA records MLA_ERR_TIMEOUT and tells
-// its peer, every role stops, transfers in flight in both directions are drained, and tensor
-// memory is freed.
+// to the peer, so that no softmax thread waits on a remote arrival. Every wait is bounded; on a
+// timeout the CTA records MLA_ERR_TIMEOUT and tells its peer, every role stops, transfers in
+// flight in both directions are drained, and tensor memory is freed.
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -243,30 +243,27 @@ __device__ __forceinline__ uint32_t swz(uint32_t hl, uint32_t k, uint32_t row_by
   return hl * row_bytes + ((k ^ (hl & 7u)) << 4);
 }
 
-// Latent queries of head lane `h` of sequence `sb`: latent columns [col0, col0 + 64 nblk) of this
+// Latent queries of head lane `h` of sequence `sb`: latent columns [col0, col0 + 128) of this
 // CTA's half into tensor-memory columns t_q + col0 / 2 onwards (bf16 pairs, 32 columns a store).
-// Two 64-column blocks (256 bytes) per thread are in flight at once, so the whole load costs one
-// memory round trip per pair of blocks (nblk even). Warp-collective (tcgen05.st).
-__device__ __forceinline__ void load_q_lat(const PairArgs& a, uint32_t c, int sb, int h, int col0, int nblk,
-                                           uint32_t t_q) {
+// All 256 bytes are requested at once, so the load costs one memory round trip. Warp-collective
+// (tcgen05.st).
+__device__ __forceinline__ void load_q_lat(const PairArgs& a, uint32_t c, int sb, int h, int col0, uint32_t t_q) {
   const uint4* src =
       reinterpret_cast<const uint4*>(a.q_abs + ((size_t)sb * AP_HEADS + h) * 576 + 256 * c + col0);
-  for (int bi = 0; bi < nblk; bi += 2) {
-    uint4 v[16];
+  uint4 v[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = src[8 * bi + i];
+  for (int i = 0; i < 16; ++i) v[i] = src[i];
 #pragma unroll
-    for (int hb = 0; hb < 2; ++hb) {
-      uint32_t r[32];
+  for (int hb = 0; hb < 2; ++hb) {
+    uint32_t r[32];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        r[4 * i] = v[8 * hb + i].x;
-        r[4 * i + 1] = v[8 * hb + i].y;
-        r[4 * i + 2] = v[8 * hb + i].z;
-        r[4 * i + 3] = v[8 * hb + i].w;
-      }
-      tc::tmem_st32(t_q + (uint32_t)(col0 / 2 + 32 * (bi + hb)), r);
+    for (int i = 0; i < 8; ++i) {
+      r[4 * i] = v[8 * hb + i].x;
+      r[4 * i + 1] = v[8 * hb + i].y;
+      r[4 * i + 2] = v[8 * hb + i].z;
+      r[4 * i + 3] = v[8 * hb + i].w;
     }
+    tc::tmem_st32(t_q + (uint32_t)(col0 / 2 + 32 * hb), r);
   }
 }
 
@@ -659,7 +656,8 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
       PairSegIter pk = it;
       int qb, x0, x1;
       if (!pk.next(a, &qb, &x0, &x1)) return;
-      const char* p = reinterpret_cast<const char*>(a.q_abs + ((size_t)qb * AP_HEADS + h) * 576 + 256 * c + 128 * set);
+      const char* p =
+          reinterpret_cast<const char*>(a.q_abs + ((size_t)qb * AP_HEADS + h) * 576 + 256 * c + 128 * set);
       asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
       asm volatile("prefetch.global.L2 [%0];" ::"l"(p + 128));
     };
@@ -668,7 +666,7 @@ attn_pair_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_cons
     auto queries = [&](int qb) {
       __syncwarp();
       tc::tc_fence_after();
-      load_q_lat(a, c, qb, h, 128 * set, 2, t_q);
+      load_q_lat(a, c, qb, h, 128 * set, t_q);
       tc::tmem_wait_st();
       tc::tc_fence_before();
       tc::mbar_arrive(&s.q_full);
